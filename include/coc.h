@@ -1,0 +1,240 @@
+/*
+ * coc.h — fused tensor-parallel matmul + collective operators for GB300 (sm_103a).
+ *
+ * The operators are those of the MindSpeed developer guide page on
+ * compute-communication parallelism (CoC), section 融合算子实现
+ * ("fused-operator implementation"):
+ *
+ *   MATMUL_ALL_REDUCE (and its deterministic form)      coc_matmul_all_reduce
+ *   MATMUL_REDUCE_SCATTER (and its deterministic form)  coc_matmul_reduce_scatter
+ *   ALL_GATHER_MATMUL                                   coc_all_gather_matmul
+ *   ALL_GATHER_MATMUL_V2 (also returns the gather)      coc_all_gather_matmul_v2
+ *   w8A16 pseudo-quantised MATMUL_ALL_REDUCE, fp16,
+ *     per tensor / per channel / per group scales       coc_matmul_all_reduce_w8a16
+ *
+ * The same page's section 问题分析 ("problem analysis") places them in the
+ * Megatron ColumnParallelLinear / RowParallelLinear layers: the matmul is
+ * followed by AllReduce without sequence parallelism, by AllGather or
+ * ReduceScatter with it.
+ *
+ * One GPU, R emulated ranks.  Each tensor-parallel rank is a separate set of
+ * caller-owned device buffers ("shards"), so every collective is carried out
+ * inside one persistent CUDA kernel: AllReduce becomes a cross-shard
+ * reduction in the tensor-core accumulator whose result is stored to all R
+ * rank outputs, ReduceScatter routes each row block to its owning rank, and
+ * AllGather routes each operand tile from the shard that holds its rows.
+ *
+ * Chunking.  Following the page's CoC idea (section 解决思路: split compute
+ * and communication into smaller sub-tasks and pipeline them; the left
+ * matmul operand is split along m into 2/4/8 parts and m must be a multiple
+ * of the split count), `chunks` in {1, 2, 4, 8} splits the output rows into
+ * equal chunks processed in chunk order; one chunk's reduce/scatter/gather
+ * epilogue overlaps the next chunk's matmul mainloop.  chunks = 1 means no
+ * chunking.  The result never depends on `chunks`.
+ *
+ * Deterministic mode (same section: "及其确定性计算").  With deterministic != 0
+ * the output is bitwise reproducible for identical inputs on the same GPU and
+ * library build, across runs and across chunk counts: each output element is
+ * accumulated in fp32 in the fixed order rank 0..R-1, k ascending, with no
+ * split-K, atomics or arrival-order reduction, and rounded once
+ * (round-to-nearest-even) to the output type.  The current kernels use this
+ * order in both modes, so deterministic = 0 gives the same bits.
+ *
+ * Conventions for every entry point:
+ *   - All matrices are row-major and densely packed, in device memory the
+ *     caller owns (allocated through PyTorch or cudaMalloc).  Base pointers
+ *     must be 16-byte aligned and every row must span a multiple of 16 bytes
+ *     (TMA requirement), see the per-call alignment notes.
+ *   - Array-of-pointer arguments (`x`, `w`, `out`, ...) are HOST arrays of R
+ *     device pointers, read before the call returns.
+ *   - The library allocates nothing per call.  On the first call on a device
+ *     it allocates a small status buffer (a few words) that coc_shutdown()
+ *     frees.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream).  Outputs must not alias inputs or each other.
+ *   - Argument errors are detected on the host before any CUDA call and are
+ *     returned as status codes; nothing is thrown across the ABI and no
+ *     output is touched when a call is rejected.
+ *   - A launch failure returns COC_ERR_CUDA.  Every wait inside the kernel is
+ *     bounded (about one second); a wait that runs out stops the kernel
+ *     cleanly and records COC_ERR_TIMEOUT in the status buffer, which
+ *     coc_sync_status() reports.  Results of a call that timed out are
+ *     undefined.
+ */
+#ifndef COC_H_
+#define COC_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define COC_MAX_RANKS 8
+
+typedef enum {
+    COC_OK = 0,
+    COC_ERR_INVALID_ARG = 1,   /* null pointer, bad enum, R or chunks not in {1,2,4,8} */
+    COC_ERR_SHAPE = 2,         /* sizes that do not fit together or exceed the limits */
+    COC_ERR_ALIGN = 3,         /* base pointer or row pitch not 16-byte aligned */
+    COC_ERR_UNSUPPORTED = 4,   /* device is not sm_103 / feature not built */
+    COC_ERR_CUDA = 5,          /* a CUDA runtime call or the kernel launch failed */
+    COC_ERR_TIMEOUT = 6        /* a bounded device-side wait ran out (see coc_sync_status) */
+} coc_status_t;
+
+typedef enum { COC_FP16 = 0, COC_BF16 = 1 } coc_dtype_t;
+
+typedef enum {
+    COC_SCALE_TENSOR = 0,      /* one scale for the whole weight */
+    COC_SCALE_CHANNEL = 1,     /* one scale per output column j */
+    COC_SCALE_GROUP = 2        /* one scale per (group of group_size rows of K, column j) */
+} coc_scale_t;
+
+/* Opaque CUDA stream handle; identical to cudaStream_t / CUstream. */
+typedef struct CUstream_st* coc_stream_t;
+
+/*
+ * MATMUL_ALL_REDUCE — row-parallel linear followed by AllReduce
+ * (CoC page, 融合算子实现, first bullet; 问题分析 for the layer).
+ *
+ *   Y = sum_{r=0}^{R-1} X_r @ W_r          (fp32 accumulation)
+ *   out[r] = round_rne(Y)  for every r     (all R copies bit-identical)
+ *
+ * R        ranks, in {1, 2, 4, 8}
+ * m, n     output rows / columns; k_shard = contraction length held by each rank
+ *          (the full contraction is K = R * k_shard)
+ * x[r]     m x k_shard,   dtype `dt`, row pitch k_shard elements
+ * w[r]     k_shard x n,   dtype `dt`, row pitch n elements
+ * out[r]   m x n,         dtype `dt`, row pitch n elements
+ * chunks   in {1, 2, 4, 8}; m % chunks == 0 (COC_ERR_SHAPE otherwise)
+ * Alignment: k_shard % 8 == 0 and n % 8 == 0 (16-byte rows), pointers 16-byte
+ * aligned.  m, n, k_shard in [0, 2^31); m == 0 or n == 0 is a no-op and
+ * k_shard == 0 writes zeros.
+ */
+coc_status_t coc_matmul_all_reduce(int R, int64_t m, int64_t n, int64_t k_shard,
+                                   const void* const* x, const void* const* w,
+                                   void* const* out, coc_dtype_t dt,
+                                   int chunks, int deterministic, coc_stream_t stream);
+
+/*
+ * MATMUL_REDUCE_SCATTER — row-parallel linear followed by ReduceScatter along
+ * the rows (sequence parallelism) (CoC page, 融合算子实现, second bullet).
+ *
+ *   Y = sum_r X_r @ W_r;   out[r] = round_rne(Y[r*m/R : (r+1)*m/R, :])
+ *
+ * Rank r always owns the contiguous row block [r*m/R, (r+1)*m/R), whatever
+ * `chunks` is.  Arguments as coc_matmul_all_reduce, except
+ * out[r]   (m/R) x n.
+ * Shape:   m % R == 0, (m/R) % 8 == 0, m % chunks == 0.
+ */
+coc_status_t coc_matmul_reduce_scatter(int R, int64_t m, int64_t n, int64_t k_shard,
+                                       const void* const* x, const void* const* w,
+                                       void* const* out, coc_dtype_t dt,
+                                       int chunks, int deterministic, coc_stream_t stream);
+
+/*
+ * ALL_GATHER_MATMUL — AllGather of the sequence-parallel input followed by a
+ * column-parallel linear (CoC page, 融合算子实现, third bullet).
+ *
+ *   Xg = [X_0; X_1; ...; X_{R-1}]   (rows stacked in rank order, R*m_shard x k)
+ *   out[r] = round_rne(Xg @ W_r)
+ *
+ * x[r]     m_shard x k,          row pitch k
+ * w[r]     k x n_shard,          row pitch n_shard
+ * out[r]   (R*m_shard) x n_shard, row pitch n_shard
+ * Shape:   m_shard % 8 == 0, (R*m_shard) % chunks == 0; chunks split the
+ *          gathered rows.  k % 8 == 0, n_shard % 8 == 0.
+ * `deterministic` is accepted; there is no cross-rank sum, so results are
+ * always reproducible.
+ */
+coc_status_t coc_all_gather_matmul(int R, int64_t m_shard, int64_t n_shard, int64_t k,
+                                   const void* const* x, const void* const* w,
+                                   void* const* out, coc_dtype_t dt,
+                                   int chunks, int deterministic, coc_stream_t stream);
+
+/*
+ * ALL_GATHER_MATMUL_V2 — as coc_all_gather_matmul, and the AllGather
+ * intermediate is also returned (CoC page, 融合算子实现, third bullet: "V2
+ * supports obtaining the ALL_GATHER intermediate result").
+ *
+ * gathered[r]  (R*m_shard) x k, row pitch k: receives a bit-exact copy of Xg.
+ *              Entries may be NULL to skip that rank's copy; `gathered`
+ *              itself must not be NULL.
+ * Shape:   as coc_all_gather_matmul, and n_shard > 0.
+ */
+coc_status_t coc_all_gather_matmul_v2(int R, int64_t m_shard, int64_t n_shard, int64_t k,
+                                      const void* const* x, const void* const* w,
+                                      void* const* out, void* const* gathered,
+                                      coc_dtype_t dt, int chunks, int deterministic,
+                                      coc_stream_t stream);
+
+/*
+ * w8A16 MATMUL_ALL_REDUCE — fp16 activations, int8 weights dequantised in the
+ * kernel (CoC page, 融合算子实现, last bullet: "pseudo-quantisation, fp16,
+ * per tensor / per channel / per group").
+ *
+ *   Wd_r[t, j] = fp16_rne( float(Wq_r[t, j]) * s_r(t, j) )   (exact product, one rounding)
+ *   Y = sum_r X_r @ Wd_r;  out[r] = fp16_rne(Y) for every r
+ *
+ * x[r]      m x k_shard fp16
+ * w[r]      k_shard x n int8 (symmetric; no zero point)
+ * scale[r]  fp16 scales as seen by rank r:
+ *             COC_SCALE_TENSOR:  1 value
+ *             COC_SCALE_CHANNEL: n values, s(t, j) = scale[r][j]
+ *             COC_SCALE_GROUP:   (k_shard/group_size) x n, row-major,
+ *                                s(t, j) = scale[r][(t / group_size) * n + j]
+ *                                (rank r's rows of the full (K/group_size) x n table)
+ * group_size  used for COC_SCALE_GROUP only: a multiple of 64 dividing k_shard.
+ * out[r]    m x n fp16
+ * Alignment: k_shard % 8 == 0, n % 16 == 0 (16-byte int8 rows).
+ */
+coc_status_t coc_matmul_all_reduce_w8a16(int R, int64_t m, int64_t n, int64_t k_shard,
+                                         const void* const* x, const void* const* w,
+                                         const void* const* scale, coc_scale_t gran,
+                                         int64_t group_size, void* const* out,
+                                         int chunks, int deterministic, coc_stream_t stream);
+
+/*
+ * Plain sharded contraction with a single output: out = round_rne(sum_r X_r @ W_r).
+ * The same kernel as coc_matmul_all_reduce with a plain one-buffer epilogue;
+ * it is the denominator of the fused-overhead measurement (the pages have no
+ * counterpart of their own).  Arguments as coc_matmul_all_reduce, `out` a
+ * single m x n buffer.
+ */
+coc_status_t coc_matmul(int R, int64_t m, int64_t n, int64_t k_shard,
+                        const void* const* x, const void* const* w, void* out,
+                        coc_dtype_t dt, coc_stream_t stream);
+
+/*
+ * Waits for `stream`, then returns and clears the device-side status of
+ * this library on the current device: COC_ERR_TIMEOUT if a kernel's bounded
+ * wait ran out since the last check, COC_ERR_CUDA if the stream reports an
+ * error, COC_OK otherwise.
+ */
+coc_status_t coc_sync_status(coc_stream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char* coc_status_string(coc_status_t status);
+
+/* Details of the most recent error on this thread (static per-thread buffer). */
+const char* coc_last_error(void);
+
+/* Library ABI version: (major << 16) | minor. */
+int coc_version(void);
+
+/*
+ * Test hook: while `enable` is non-zero, kernels launched afterwards make
+ * their epilogue wait on a barrier nothing arrives at, so the bounded waits
+ * run out and the kernel stops with COC_ERR_TIMEOUT.  For fault-handling
+ * tests only.
+ */
+coc_status_t coc_debug_inject_timeout(int enable);
+
+/* Frees the per-device status buffers.  Further calls re-create them. */
+coc_status_t coc_shutdown(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* COC_H_ */

@@ -1,0 +1,275 @@
+"""Python binding of the C ABI in include/coc.h (ctypes; argument marshalling only).
+
+Every operator runs in the library's CUDA kernels.  PyTorch is used for device
+memory (tensors, optional output allocation) and for the current stream.  If
+libcoc.so is missing or cannot be loaded the binding raises: there is no
+fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libcoc.so")
+
+OK, ERR_INVALID_ARG, ERR_SHAPE, ERR_ALIGN, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = range(7)
+FP16, BF16 = 0, 1
+SCALE_TENSOR, SCALE_CHANNEL, SCALE_GROUP = 0, 1, 2
+_GRAN = {"tensor": SCALE_TENSOR, "channel": SCALE_CHANNEL, "group": SCALE_GROUP}
+MAX_RANKS = 8
+
+# Every symbol include/coc.h declares (checked by the CPU test suite).
+EXPORTS = (
+    "coc_matmul_all_reduce", "coc_matmul_reduce_scatter", "coc_all_gather_matmul",
+    "coc_all_gather_matmul_v2", "coc_matmul_all_reduce_w8a16", "coc_matmul",
+    "coc_sync_status", "coc_status_string", "coc_last_error", "coc_version",
+    "coc_debug_inject_timeout", "coc_shutdown",
+)
+
+
+class CocError(RuntimeError):
+    def __init__(self, status: int, name: str, detail: str):
+        super().__init__(f"{name}: {detail}" if detail else name)
+        self.status = status
+        self.name = name
+        self.detail = detail
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libcoc.so (built by __graft_entry__.build() or build.py)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                                   "`python -c 'import __graft_entry__ as g; g.build()'`")
+            L = ctypes.CDLL(LIB_PATH)
+            i64, i32, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
+            pp = ctypes.POINTER(ctypes.c_void_p)
+            row = [i32, i64, i64, i64, pp, pp, pp, i32, i32, i32, vp]
+            for name in ("coc_matmul_all_reduce", "coc_matmul_reduce_scatter", "coc_all_gather_matmul"):
+                getattr(L, name).argtypes = row
+                getattr(L, name).restype = i32
+            L.coc_all_gather_matmul_v2.argtypes = [i32, i64, i64, i64, pp, pp, pp, pp, i32, i32, i32, vp]
+            L.coc_all_gather_matmul_v2.restype = i32
+            L.coc_matmul_all_reduce_w8a16.argtypes = [i32, i64, i64, i64, pp, pp, pp, i32, i64, pp, i32, i32, vp]
+            L.coc_matmul_all_reduce_w8a16.restype = i32
+            L.coc_matmul.argtypes = [i32, i64, i64, i64, pp, pp, vp, i32, vp]
+            L.coc_matmul.restype = i32
+            L.coc_sync_status.argtypes = [vp]
+            L.coc_sync_status.restype = i32
+            L.coc_status_string.argtypes = [i32]
+            L.coc_status_string.restype = ctypes.c_char_p
+            L.coc_last_error.argtypes = []
+            L.coc_last_error.restype = ctypes.c_char_p
+            L.coc_version.restype = i32
+            L.coc_debug_inject_timeout.argtypes = [i32]
+            L.coc_debug_inject_timeout.restype = i32
+            L.coc_shutdown.restype = i32
+            _lib = L
+    return _lib
+
+
+def _check(status: int) -> None:
+    if status != OK:
+        L = lib()
+        raise CocError(status, L.coc_status_string(status).decode(), L.coc_last_error().decode())
+
+
+def _ptrs(ts) -> ctypes.Array:
+    arr = (ctypes.c_void_p * len(ts))()
+    for i, t in enumerate(ts):
+        arr[i] = None if t is None else t.data_ptr()
+    return arr
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.float16:
+        return FP16
+    if dt == torch.bfloat16:
+        return BF16
+    raise TypeError(f"unsupported dtype {dt}; expected float16 or bfloat16")
+
+
+def _check_list(ts, name, shape, dtype, device):
+    if not isinstance(ts, (list, tuple)) or len(ts) == 0:
+        raise ValueError(f"{name} must be a non-empty list of tensors")
+    for i, t in enumerate(ts):
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name}[{i}] is not a tensor")
+        if t.device != device:
+            raise ValueError(f"{name}[{i}] is on {t.device}, expected {device}")
+        if t.dtype != dtype:
+            raise TypeError(f"{name}[{i}] has dtype {t.dtype}, expected {dtype}")
+        if tuple(t.shape) != tuple(shape):
+            raise ValueError(f"{name}[{i}] has shape {tuple(t.shape)}, expected {tuple(shape)}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name}[{i}] is not contiguous")
+
+
+def _prep(xs, ws):
+    if not xs or not ws or len(xs) != len(ws):
+        raise ValueError("xs and ws must be lists of equal length (one tensor per rank)")
+    R = len(xs)
+    if R > MAX_RANKS:
+        raise ValueError(f"at most {MAX_RANKS} ranks")
+    x0, w0 = xs[0], ws[0]
+    if x0.dim() != 2 or w0.dim() != 2:
+        raise ValueError("X and W shards must be 2-D")
+    if x0.device.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    return R, x0, w0
+
+
+def _outs(outs, R, shape, dtype, device):
+    if outs is None:
+        return [torch.empty(shape, dtype=dtype, device=device) for _ in range(R)]
+    _check_list(outs, "outs", shape, dtype, device)
+    if len(outs) != R:
+        raise ValueError("need one output per rank")
+    return list(outs)
+
+
+def matmul_all_reduce(xs, ws, outs=None, chunks: int = 1, deterministic: bool = False, stream=None):
+    """MATMUL_ALL_REDUCE: outs[r] = sum_q xs[q] @ ws[q] for every rank r."""
+    R, x0, w0 = _prep(xs, ws)
+    m, ks = x0.shape
+    n = w0.shape[1]
+    _check_list(xs, "xs", (m, ks), x0.dtype, x0.device)
+    _check_list(ws, "ws", (ks, n), x0.dtype, x0.device)
+    outs = _outs(outs, R, (m, n), x0.dtype, x0.device)
+    _check(lib().coc_matmul_all_reduce(R, m, n, ks, _ptrs(xs), _ptrs(ws), _ptrs(outs), _dtype_code(x0.dtype),
+                                       int(chunks), int(bool(deterministic)), _stream(stream)))
+    return outs
+
+
+def matmul_reduce_scatter(xs, ws, outs=None, chunks: int = 1, deterministic: bool = False, stream=None):
+    """MATMUL_REDUCE_SCATTER: outs[r] = rows [r*m/R, (r+1)*m/R) of sum_q xs[q] @ ws[q]."""
+    R, x0, w0 = _prep(xs, ws)
+    m, ks = x0.shape
+    n = w0.shape[1]
+    _check_list(xs, "xs", (m, ks), x0.dtype, x0.device)
+    _check_list(ws, "ws", (ks, n), x0.dtype, x0.device)
+    if m % R:
+        raise CocError(ERR_SHAPE, "COC_ERR_SHAPE", f"m = {m} is not a multiple of R = {R}")
+    outs = _outs(outs, R, (m // R, n), x0.dtype, x0.device)
+    _check(lib().coc_matmul_reduce_scatter(R, m, n, ks, _ptrs(xs), _ptrs(ws), _ptrs(outs), _dtype_code(x0.dtype),
+                                           int(chunks), int(bool(deterministic)), _stream(stream)))
+    return outs
+
+
+def _ag_common(xs, ws, outs):
+    R, x0, w0 = _prep(xs, ws)
+    ms, k = x0.shape
+    ns = w0.shape[1]
+    _check_list(xs, "xs", (ms, k), x0.dtype, x0.device)
+    _check_list(ws, "ws", (k, ns), x0.dtype, x0.device)
+    outs = _outs(outs, R, (R * ms, ns), x0.dtype, x0.device)
+    return R, x0, ms, k, ns, outs
+
+
+def all_gather_matmul(xs, ws, outs=None, chunks: int = 1, deterministic: bool = False, stream=None):
+    """ALL_GATHER_MATMUL: outs[r] = cat(xs, dim=0) @ ws[r]."""
+    R, x0, ms, k, ns, outs = _ag_common(xs, ws, outs)
+    _check(lib().coc_all_gather_matmul(R, ms, ns, k, _ptrs(xs), _ptrs(ws), _ptrs(outs), _dtype_code(x0.dtype),
+                                       int(chunks), int(bool(deterministic)), _stream(stream)))
+    return outs
+
+
+def all_gather_matmul_v2(xs, ws, outs=None, gathered=None, chunks: int = 1, deterministic: bool = False,
+                         stream=None):
+    """ALL_GATHER_MATMUL_V2: as all_gather_matmul, and gathered[r] = cat(xs, dim=0).
+
+    `gathered` entries may be None to skip that rank's copy."""
+    R, x0, ms, k, ns, outs = _ag_common(xs, ws, outs)
+    if gathered is None:
+        gathered = [torch.empty((R * ms, k), dtype=x0.dtype, device=x0.device) for _ in range(R)]
+    else:
+        if len(gathered) != R:
+            raise ValueError("need one gathered entry per rank (None to skip)")
+        present = [g for g in gathered if g is not None]
+        if present:
+            _check_list(present, "gathered", (R * ms, k), x0.dtype, x0.device)
+    _check(lib().coc_all_gather_matmul_v2(R, ms, ns, k, _ptrs(xs), _ptrs(ws), _ptrs(outs), _ptrs(gathered),
+                                          _dtype_code(x0.dtype), int(chunks), int(bool(deterministic)),
+                                          _stream(stream)))
+    return outs, gathered
+
+
+def matmul_all_reduce_w8a16(xs, wqs, scales, gran, group_size: int = 0, outs=None, chunks: int = 1,
+                            deterministic: bool = False, stream=None):
+    """w8A16 MATMUL_ALL_REDUCE: outs[r] = sum_q xs[q] @ fp16(wqs[q] * s_q) for every r.
+
+    gran: "tensor" | "channel" | "group" (or the SCALE_* codes); scales[q] is
+    rank q's view of the fp16 scale tensor."""
+    R, x0, w0 = _prep(xs, wqs)
+    gcode = _GRAN[gran] if isinstance(gran, str) else int(gran)
+    m, ks = x0.shape
+    n = w0.shape[1]
+    _check_list(xs, "xs", (m, ks), torch.float16, x0.device)
+    _check_list(wqs, "wqs", (ks, n), torch.int8, x0.device)
+    if len(scales) != R:
+        raise ValueError("need one scale view per rank")
+    for i, s in enumerate(scales):
+        if s.dtype != torch.float16 or s.device != x0.device or not s.is_contiguous():
+            raise ValueError(f"scales[{i}] must be a contiguous fp16 tensor on {x0.device}")
+        need = 1 if gcode == SCALE_TENSOR else n if gcode == SCALE_CHANNEL else \
+            (ks // group_size) * n if group_size > 0 else 0
+        if s.numel() < need:
+            raise ValueError(f"scales[{i}] has {s.numel()} values, needs {need}")
+    outs = _outs(outs, R, (m, n), torch.float16, x0.device)
+    _check(lib().coc_matmul_all_reduce_w8a16(R, m, n, ks, _ptrs(xs), _ptrs(wqs), _ptrs(scales), gcode,
+                                             int(group_size), _ptrs(outs), int(chunks), int(bool(deterministic)),
+                                             _stream(stream)))
+    return outs
+
+
+def matmul(xs, ws, out=None, stream=None):
+    """Plain sharded contraction into one buffer (the fused-overhead baseline)."""
+    R, x0, w0 = _prep(xs, ws)
+    m, ks = x0.shape
+    n = w0.shape[1]
+    _check_list(xs, "xs", (m, ks), x0.dtype, x0.device)
+    _check_list(ws, "ws", (ks, n), x0.dtype, x0.device)
+    if out is None:
+        out = torch.empty((m, n), dtype=x0.dtype, device=x0.device)
+    else:
+        _check_list([out], "out", (m, n), x0.dtype, x0.device)
+    _check(lib().coc_matmul(R, m, n, ks, _ptrs(xs), _ptrs(ws), out.data_ptr(), _dtype_code(x0.dtype),
+                            _stream(stream)))
+    return out
+
+
+def sync_status(stream=None) -> None:
+    """Wait for the stream and raise CocError if a kernel's bounded wait ran out."""
+    _check(lib().coc_sync_status(_stream(stream)))
+
+
+def inject_timeout(enable: bool) -> None:
+    """Test hook: make subsequently launched kernels stop with COC_ERR_TIMEOUT."""
+    _check(lib().coc_debug_inject_timeout(int(bool(enable))))
+
+
+def shutdown() -> None:
+    _check(lib().coc_shutdown())
+
+
+def version() -> tuple:
+    v = lib().coc_version()
+    return (v >> 16, v & 0xFFFF)

@@ -1,0 +1,417 @@
+// Host side of the C ABI declared in include/coc.h: argument validation
+// (before any CUDA call), TMA descriptor encoding, launch of the persistent
+// fused kernel, and the device status buffer used by the bounded waits.
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <unordered_map>
+
+#include <cudaTypedefs.h>
+
+#include "coc_internal.h"
+
+namespace coc {
+namespace {
+
+thread_local char g_err[512] = "";
+
+coc_status_t fail(coc_status_t st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    std::vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+coc_status_t cuda_fail(cudaError_t e, const char* what) {
+    return fail(COC_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+std::atomic<int> g_inject{0};
+
+struct DeviceState {
+    int sm_count = 0;
+    int cc_major = 0, cc_minor = 0;
+    unsigned* status = nullptr;
+};
+
+std::mutex g_mu;
+std::unordered_map<int, DeviceState> g_dev;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+coc_status_t device_state(DeviceState** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_encode == nullptr) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
+            return fail(COC_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    DeviceState& st = g_dev[dev];
+    if (st.status == nullptr) {
+        if ((e = cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&st.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&st.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute");
+        if (st.cc_major != 10 || st.cc_minor != 3)
+            return fail(COC_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a", dev,
+                        st.cc_major, st.cc_minor);
+        void* p = nullptr;
+        if ((e = cudaMalloc(&p, STATUS_WORDS * sizeof(unsigned))) != cudaSuccess) return cuda_fail(e, "cudaMalloc(status)");
+        if ((e = cudaMemset(p, 0, STATUS_WORDS * sizeof(unsigned))) != cudaSuccess) {
+            cudaFree(p);
+            return cuda_fail(e, "cudaMemset(status)");
+        }
+        st.status = static_cast<unsigned*>(p);
+    }
+    *out = &st;
+    return COC_OK;
+}
+
+// 2-D row-major tensor map: inner dimension `cols` (contiguous), `rows` rows of
+// `pitch_bytes`, box of box_cols x box_rows.
+coc_status_t encode(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t cols, uint64_t rows,
+                    uint64_t pitch_bytes, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw) {
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {pitch_bytes};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(COC_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for %llu x %llu, pitch %llu", static_cast<int>(r),
+                    static_cast<unsigned long long>(rows), static_cast<unsigned long long>(cols),
+                    static_cast<unsigned long long>(pitch_bytes));
+    return COC_OK;
+}
+
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1024;
+
+bool pow2_rank(int v) { return v == 1 || v == 2 || v == 4 || v == 8; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+coc_status_t check_common(int R, int chunks, coc_dtype_t dt, int deterministic) {
+    (void)deterministic;
+    if (!pow2_rank(R)) return fail(COC_ERR_INVALID_ARG, "R = %d; must be 1, 2, 4 or 8", R);
+    if (!pow2_rank(chunks)) return fail(COC_ERR_INVALID_ARG, "chunks = %d; must be 1, 2, 4 or 8", chunks);
+    if (dt != COC_FP16 && dt != COC_BF16) return fail(COC_ERR_INVALID_ARG, "unknown dtype %d", static_cast<int>(dt));
+    return COC_OK;
+}
+
+coc_status_t check_dims(int64_t a, int64_t b, int64_t c) {
+    if (a < 0 || b < 0 || c < 0) return fail(COC_ERR_SHAPE, "negative size");
+    if (a > kMaxDim || b > kMaxDim || c > kMaxDim) return fail(COC_ERR_SHAPE, "size above 2^31 - 1024");
+    return COC_OK;
+}
+
+// R device pointers; all non-null and 16-byte aligned when `needed`.
+coc_status_t check_ptrs(const void* const* arr, int R, bool needed, const char* name, bool allow_null_entries = false) {
+    if (arr == nullptr) return fail(COC_ERR_INVALID_ARG, "%s is NULL", name);
+    if (!needed) return COC_OK;
+    for (int r = 0; r < R; ++r) {
+        if (arr[r] == nullptr) {
+            if (allow_null_entries) continue;
+            return fail(COC_ERR_INVALID_ARG, "%s[%d] is NULL", name, r);
+        }
+        if (!aligned16(arr[r])) return fail(COC_ERR_ALIGN, "%s[%d] is not 16-byte aligned", name, r);
+    }
+    return COC_OK;
+}
+
+int chunk_m_tiles(int64_t m, int chunks) {
+    const int64_t rows = m / chunks;
+    return (rows > 0 && rows % BM == 0) ? static_cast<int>(rows / BM) : 0;
+}
+
+int largest_pow2_divisor_le(int64_t v, int cap) {
+    int b = cap;
+    while (b > 8 && v % b != 0) b >>= 1;
+    return b;
+}
+
+CUtensorMapDataType tma_dtype(coc_dtype_t dt) {
+    return dt == COC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+}
+
+coc_status_t launch_checked(int op, bool bf16, KParams& p, DeviceState* ds, cudaStream_t stream) {
+    p.status = ds->status;
+    p.inject_timeout = g_inject.load();
+    const int grid = p.units < ds->sm_count ? p.units : ds->sm_count;
+    cudaError_t e = launch(op, bf16, p, grid, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+    return COC_OK;
+}
+
+// ---- row-parallel family: AR, RS, W8, plain ----------------------------------
+coc_status_t row_parallel(int op, int R, int64_t m, int64_t n, int64_t ks, const void* const* x,
+                          const void* const* w, void* const* out, int n_out, coc_dtype_t dt, int chunks,
+                          const void* const* scale, coc_scale_t gran, int64_t group, cudaStream_t stream) {
+    KParams p;
+    std::memset(&p, 0, sizeof p);
+    p.R = R;
+    p.n_out = n_out;
+    p.m = static_cast<int>(m);
+    p.n = static_cast<int>(n);
+    p.k = static_cast<int>(ks);
+    p.num_kshards = R;
+    p.kblocks = static_cast<int>((ks + BK - 1) / BK);
+    p.m_tiles = static_cast<int>((m + BM - 1) / BM);
+    p.n_tiles = static_cast<int>((n + BN - 1) / BN);
+    p.units = p.m_tiles * p.n_tiles;
+    p.chunk_mt = chunk_m_tiles(m, chunks);
+    p.rows_per_rank = static_cast<int>(m / R);
+    p.store_rows = 32;
+    p.a_box_rows = BM;
+    p.gran = static_cast<int>(gran);
+    p.group = static_cast<int>(group);
+    if (op == OP_RS) p.store_rows = largest_pow2_divisor_le(p.rows_per_rank, 32);
+
+    DeviceState* ds = nullptr;
+    coc_status_t st = device_state(&ds);
+    if (st != COC_OK) return st;
+
+    const bool w8 = (op == OP_W8);
+    const CUtensorMapDataType adt = w8 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : tma_dtype(dt);
+    if (ks > 0) {
+        for (int r = 0; r < R; ++r) {
+            if ((st = encode(&p.tm_a[r], adt, x[r], ks, m, ks * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B)) != COC_OK) return st;
+            if (w8) {
+                st = encode(&p.tm_b[r], CU_TENSOR_MAP_DATA_TYPE_UINT8, w[r], n, ks, n, BN, BK, CU_TENSOR_MAP_SWIZZLE_NONE);
+            } else {
+                st = encode(&p.tm_b[r], adt, w[r], n, ks, n * 2, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B);
+            }
+            if (st != COC_OK) return st;
+        }
+    }
+    const int64_t out_rows = (op == OP_RS) ? m / R : m;
+    for (int o = 0; o < n_out; ++o) {
+        if ((st = encode(&p.tm_out[o], adt, out[o], n, out_rows, n * 2, EPI_COLS, p.store_rows, CU_TENSOR_MAP_SWIZZLE_128B)) != COC_OK)
+            return st;
+    }
+    if (w8)
+        for (int r = 0; r < R; ++r) p.scale[r] = static_cast<const uint16_t*>(scale[r]);
+    return launch_checked(op, dt == COC_BF16 && !w8, p, ds, stream);
+}
+
+coc_status_t validate_row_parallel(int R, int64_t m, int64_t n, int64_t ks, const void* const* x, const void* const* w,
+                                   const void* const* out, int n_out, coc_dtype_t dt, int chunks, int det,
+                                   int w_elem_bytes) {
+    coc_status_t st;
+    if ((st = check_common(R, chunks, dt, det)) != COC_OK) return st;
+    if ((st = check_dims(m, n, ks)) != COC_OK) return st;
+    const bool empty = (m == 0 || n == 0);
+    if ((st = check_ptrs(x, R, !empty && ks > 0, "x")) != COC_OK) return st;
+    if ((st = check_ptrs(w, R, !empty && ks > 0, "w")) != COC_OK) return st;
+    if ((st = check_ptrs(out, n_out, !empty, "out")) != COC_OK) return st;
+    if (m % chunks != 0) return fail(COC_ERR_SHAPE, "m = %lld is not a multiple of chunks = %d", (long long)m, chunks);
+    if ((ks * 2) % 16 != 0) return fail(COC_ERR_ALIGN, "k_shard = %lld: rows of X must span a multiple of 16 bytes", (long long)ks);
+    if ((n * 2) % 16 != 0 || (n * w_elem_bytes) % 16 != 0)
+        return fail(COC_ERR_ALIGN, "n = %lld: rows of W and of the output must span a multiple of 16 bytes", (long long)n);
+    return COC_OK;
+}
+
+}  // namespace
+}  // namespace coc
+
+using namespace coc;
+
+#define COC_API extern "C" __attribute__((visibility("default")))
+
+COC_API coc_status_t coc_matmul_all_reduce(int R, int64_t m, int64_t n, int64_t k_shard, const void* const* x,
+                                           const void* const* w, void* const* out, coc_dtype_t dt, int chunks,
+                                           int deterministic, coc_stream_t stream) {
+    coc_status_t st = validate_row_parallel(R, m, n, k_shard, x, w, out, R, dt, chunks, deterministic, 2);
+    if (st != COC_OK || m == 0 || n == 0) return st;
+    return row_parallel(OP_AR, R, m, n, k_shard, x, w, out, R, dt, chunks, nullptr, COC_SCALE_TENSOR, 0,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+COC_API coc_status_t coc_matmul(int R, int64_t m, int64_t n, int64_t k_shard, const void* const* x, const void* const* w,
+                                void* out, coc_dtype_t dt, coc_stream_t stream) {
+    void* outs[1] = {out};
+    coc_status_t st = validate_row_parallel(R, m, n, k_shard, x, w, outs, 1, dt, 1, 1, 2);
+    if (st != COC_OK || m == 0 || n == 0) return st;
+    return row_parallel(OP_AR, R, m, n, k_shard, x, w, outs, 1, dt, 1, nullptr, COC_SCALE_TENSOR, 0,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+COC_API coc_status_t coc_matmul_reduce_scatter(int R, int64_t m, int64_t n, int64_t k_shard, const void* const* x,
+                                               const void* const* w, void* const* out, coc_dtype_t dt, int chunks,
+                                               int deterministic, coc_stream_t stream) {
+    coc_status_t st = validate_row_parallel(R, m, n, k_shard, x, w, out, R, dt, chunks, deterministic, 2);
+    if (st != COC_OK) return st;
+    if (m % R != 0) return fail(COC_ERR_SHAPE, "ReduceScatter: m = %lld is not a multiple of R = %d", (long long)m, R);
+    if ((m / R) % 8 != 0) return fail(COC_ERR_SHAPE, "ReduceScatter: m / R = %lld is not a multiple of 8", (long long)(m / R));
+    if (m == 0 || n == 0) return COC_OK;
+    return row_parallel(OP_RS, R, m, n, k_shard, x, w, out, R, dt, chunks, nullptr, COC_SCALE_TENSOR, 0,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+COC_API coc_status_t coc_matmul_all_reduce_w8a16(int R, int64_t m, int64_t n, int64_t k_shard, const void* const* x,
+                                                 const void* const* w, const void* const* scale, coc_scale_t gran,
+                                                 int64_t group_size, void* const* out, int chunks, int deterministic,
+                                                 coc_stream_t stream) {
+    coc_status_t st = validate_row_parallel(R, m, n, k_shard, x, w, out, R, COC_FP16, chunks, deterministic, 1);
+    if (st != COC_OK) return st;
+    if (gran != COC_SCALE_TENSOR && gran != COC_SCALE_CHANNEL && gran != COC_SCALE_GROUP)
+        return fail(COC_ERR_INVALID_ARG, "unknown scale granularity %d", static_cast<int>(gran));
+    if (scale == nullptr) return fail(COC_ERR_INVALID_ARG, "scale is NULL");
+    const bool empty = (m == 0 || n == 0);
+    for (int r = 0; r < R && !empty; ++r) {
+        if (scale[r] == nullptr) return fail(COC_ERR_INVALID_ARG, "scale[%d] is NULL", r);
+        if (gran != COC_SCALE_TENSOR && !aligned16(scale[r]))
+            return fail(COC_ERR_ALIGN, "scale[%d] is not 16-byte aligned", r);
+        if (gran == COC_SCALE_TENSOR && (reinterpret_cast<uintptr_t>(scale[r]) & 1u))
+            return fail(COC_ERR_ALIGN, "scale[%d] is not 2-byte aligned", r);
+    }
+    if (gran == COC_SCALE_GROUP) {
+        if (group_size <= 0 || group_size % BK != 0)
+            return fail(COC_ERR_SHAPE, "group_size = %lld must be a positive multiple of %d", (long long)group_size, BK);
+        if (k_shard % group_size != 0)
+            return fail(COC_ERR_SHAPE, "k_shard = %lld is not a multiple of group_size = %lld", (long long)k_shard,
+                        (long long)group_size);
+    }
+    if (empty) return COC_OK;
+    return row_parallel(OP_W8, R, m, n, k_shard, x, w, out, R, COC_FP16, chunks, scale, gran, group_size,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+namespace coc {
+namespace {
+
+coc_status_t all_gather(int R, int64_t ms, int64_t ns, int64_t k, const void* const* x, const void* const* w,
+                        void* const* out, void* const* gathered, bool v2, coc_dtype_t dt, int chunks, int det,
+                        cudaStream_t stream) {
+    coc_status_t st;
+    if ((st = check_common(R, chunks, dt, det)) != COC_OK) return st;
+    if ((st = check_dims(ms, ns, k)) != COC_OK) return st;
+    const int64_t m = static_cast<int64_t>(R) * ms;
+    if (m > kMaxDim) return fail(COC_ERR_SHAPE, "gathered rows R * m_shard above 2^31 - 1024");
+    if (v2 && gathered == nullptr) return fail(COC_ERR_INVALID_ARG, "gathered is NULL");
+    const bool empty = (ms == 0 || ns == 0);
+    if ((st = check_ptrs(x, R, ms > 0 && k > 0 && (ns > 0 || v2), "x")) != COC_OK) return st;
+    if ((st = check_ptrs(w, R, !empty && k > 0, "w")) != COC_OK) return st;
+    if ((st = check_ptrs(out, R, !empty, "out")) != COC_OK) return st;
+    if (v2 && (st = check_ptrs(const_cast<const void* const*>(gathered), R, ms > 0 && k > 0, "gathered", true)) != COC_OK)
+        return st;
+    if (ms % 8 != 0) return fail(COC_ERR_SHAPE, "m_shard = %lld is not a multiple of 8", (long long)ms);
+    if (m % chunks != 0) return fail(COC_ERR_SHAPE, "gathered m = %lld is not a multiple of chunks = %d", (long long)m, chunks);
+    if ((k * 2) % 16 != 0) return fail(COC_ERR_ALIGN, "k = %lld: rows must span a multiple of 16 bytes", (long long)k);
+    if ((ns * 2) % 16 != 0) return fail(COC_ERR_ALIGN, "n_shard = %lld: rows must span a multiple of 16 bytes", (long long)ns);
+    if (v2 && ns == 0 && ms > 0) return fail(COC_ERR_SHAPE, "ALL_GATHER_MATMUL_V2 needs n_shard > 0");
+    if (empty) return COC_OK;
+
+    KParams p;
+    std::memset(&p, 0, sizeof p);
+    p.R = R;
+    p.n_out = R;
+    p.m = static_cast<int>(m);
+    p.n = static_cast<int>(ns);
+    p.k = static_cast<int>(k);
+    p.num_kshards = 1;
+    p.kblocks = static_cast<int>((k + BK - 1) / BK);
+    p.m_tiles = static_cast<int>((m + BM - 1) / BM);
+    p.n_tiles = static_cast<int>((ns + BN - 1) / BN);
+    p.units = R * p.m_tiles * p.n_tiles;
+    p.chunk_mt = chunk_m_tiles(m, chunks);
+    p.rows_per_rank = static_cast<int>(ms);
+    p.a_box_rows = largest_pow2_divisor_le(ms, BM);
+    p.store_rows = 32;
+    p.has_gather = (v2 && k > 0) ? 1 : 0;
+
+    DeviceState* ds = nullptr;
+    if ((st = device_state(&ds)) != COC_OK) return st;
+    const CUtensorMapDataType tdt = tma_dtype(dt);
+    for (int r = 0; r < R; ++r) {
+        if (k > 0) {
+            if ((st = encode(&p.tm_a[r], tdt, x[r], k, ms, k * 2, BK, p.a_box_rows, CU_TENSOR_MAP_SWIZZLE_128B)) != COC_OK) return st;
+            if ((st = encode(&p.tm_b[r], tdt, w[r], ns, k, ns * 2, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B)) != COC_OK) return st;
+        }
+        if ((st = encode(&p.tm_out[r], tdt, out[r], ns, m, ns * 2, EPI_COLS, p.store_rows, CU_TENSOR_MAP_SWIZZLE_128B)) != COC_OK)
+            return st;
+        p.gsrc[r] = static_cast<const uint16_t*>(x[r]);
+        p.gdst[r] = v2 ? static_cast<uint16_t*>(gathered[r]) : nullptr;
+    }
+    return launch_checked(OP_AG, dt == COC_BF16, p, ds, stream);
+}
+
+}  // namespace
+}  // namespace coc
+
+COC_API coc_status_t coc_all_gather_matmul(int R, int64_t m_shard, int64_t n_shard, int64_t k, const void* const* x,
+                                           const void* const* w, void* const* out, coc_dtype_t dt, int chunks,
+                                           int deterministic, coc_stream_t stream) {
+    return all_gather(R, m_shard, n_shard, k, x, w, out, nullptr, false, dt, chunks, deterministic,
+                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+COC_API coc_status_t coc_all_gather_matmul_v2(int R, int64_t m_shard, int64_t n_shard, int64_t k, const void* const* x,
+                                              const void* const* w, void* const* out, void* const* gathered,
+                                              coc_dtype_t dt, int chunks, int deterministic, coc_stream_t stream) {
+    return all_gather(R, m_shard, n_shard, k, x, w, out, gathered, true, dt, chunks, deterministic,
+                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+COC_API coc_status_t coc_sync_status(coc_stream_t stream) {
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    DeviceState* ds = nullptr;
+    coc_status_t st = device_state(&ds);
+    if (st != COC_OK) return st;
+    unsigned words[STATUS_WORDS] = {0};
+    if ((e = cudaMemcpy(words, ds->status, sizeof words, cudaMemcpyDeviceToHost)) != cudaSuccess)
+        return cuda_fail(e, "cudaMemcpy(status)");
+    if (words[0] != 0) {
+        if ((e = cudaMemset(ds->status, 0, sizeof words)) != cudaSuccess) return cuda_fail(e, "cudaMemset(status)");
+        return fail(COC_ERR_TIMEOUT, "device wait timed out (flags 0x%x, first wait site 0x%x, block %u)", words[0],
+                    words[1], words[2] ? words[2] - 1 : 0);
+    }
+    return COC_OK;
+}
+
+COC_API const char* coc_status_string(coc_status_t s) {
+    switch (s) {
+        case COC_OK: return "COC_OK";
+        case COC_ERR_INVALID_ARG: return "COC_ERR_INVALID_ARG";
+        case COC_ERR_SHAPE: return "COC_ERR_SHAPE";
+        case COC_ERR_ALIGN: return "COC_ERR_ALIGN";
+        case COC_ERR_UNSUPPORTED: return "COC_ERR_UNSUPPORTED";
+        case COC_ERR_CUDA: return "COC_ERR_CUDA";
+        case COC_ERR_TIMEOUT: return "COC_ERR_TIMEOUT";
+        default: return "COC_ERR_UNKNOWN";
+    }
+}
+
+COC_API const char* coc_last_error(void) { return g_err; }
+
+COC_API int coc_version(void) { return (1 << 16) | 0; }
+
+COC_API coc_status_t coc_debug_inject_timeout(int enable) {
+    g_inject.store(enable ? 1 : 0);
+    return COC_OK;
+}
+
+COC_API coc_status_t coc_shutdown(void) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    int cur = 0;
+    const bool have_cur = cudaGetDevice(&cur) == cudaSuccess;
+    coc_status_t st = COC_OK;
+    for (auto& kv : g_dev) {
+        if (kv.second.status != nullptr) {
+            if (cudaSetDevice(kv.first) == cudaSuccess && cudaFree(kv.second.status) == cudaSuccess)
+                kv.second.status = nullptr;
+            else
+                st = fail(COC_ERR_CUDA, "could not free the status buffer of device %d", kv.first);
+        }
+    }
+    if (have_cur) cudaSetDevice(cur);
+    g_dev.clear();
+    return st;
+}

@@ -1,0 +1,68 @@
+// Internal interface between the host API (coc_api.cu) and the persistent
+// kernel (coc_kernel.cu).  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>            // CUtensorMap (types only; the driver is reached
+                             // through cudaGetDriverEntryPointByVersion)
+#include <cuda_runtime_api.h>
+#include <stdint.h>
+
+#include "../../include/coc.h"
+
+namespace coc {
+
+// ---- tile geometry (one CTA, one tcgen05 MMA of 128 x 256 per k-step) ----
+constexpr int BM = 128;         // tile rows   (TMEM lanes)
+constexpr int BN = 256;         // tile cols   (TMEM fp32 columns per accumulator)
+constexpr int BK = 64;          // k per stage (one 128-byte swizzle row of 16-bit data)
+constexpr int UMMA_K = 16;      // k per tcgen05.mma kind::f16
+constexpr int EPI_COLS = 64;    // epilogue sub-tile width (one 128-byte swizzle row)
+constexpr int NUM_EPI_WARPS = 4;
+constexpr int NUM_XFORM_WARPS = 4;   // w8A16 dequant warps
+
+constexpr int A_STAGE_BYTES = BM * BK * 2;        // 16 KiB
+constexpr int B_STAGE_BYTES = BN * BK * 2;        // 32 KiB
+constexpr int RAW_STAGE_BYTES = BN * BK;          // 16 KiB int8 (w8A16)
+constexpr int EPI_BUF_BYTES = 32 * EPI_COLS * 2;  // 4 KiB per warp per buffer
+
+enum OpKind : int { OP_AR = 0, OP_RS = 1, OP_AG = 2, OP_W8 = 3 };
+
+// Device status words (per device, zero when healthy).
+enum : unsigned { DEV_ERR_TIMEOUT = 1u };
+constexpr int STATUS_WORDS = 8;   // [0] error bits, [1] first "where" code, [2] block
+
+struct KParams {
+    CUtensorMap tm_a[COC_MAX_RANKS];    // A operand (X shards), K-major, 128B swizzle
+    CUtensorMap tm_b[COC_MAX_RANKS];    // B operand (W shards), MN-major, 128B swizzle (int8: no swizzle)
+    CUtensorMap tm_out[COC_MAX_RANKS];  // outputs, 128B swizzle, box 64 x store_rows
+
+    const uint16_t* gsrc[COC_MAX_RANKS];  // AG-V2: X shards (gather source)
+    uint16_t* gdst[COC_MAX_RANKS];        // AG-V2: gathered outputs (NULL = skip)
+    const uint16_t* scale[COC_MAX_RANKS]; // w8A16 scales (rank views)
+    unsigned* status;                     // STATUS_WORDS device words
+
+    int R;             // ranks
+    int n_out;         // output maps written by an AR tile (R, or 1 for the plain GEMM)
+    int m;             // output rows (AG: gathered rows R * m_shard)
+    int n;             // output columns per buffer (AG: n_shard)
+    int k;             // contraction length per shard (AG: full k)
+    int num_kshards;   // shards summed per tile (AR/RS/W8: R; AG: 1)
+    int kblocks;       // ceil(k / BK)
+    int m_tiles, n_tiles;
+    int units;         // work units (tiles; AG: R * tiles)
+    int chunk_mt;      // m-tiles per chunk for chunk-major order; 0 = row order
+    int rows_per_rank; // RS: m/R; AG: m_shard
+    int a_box_rows;    // AG: rows per A TMA box (divides m_shard and BM)
+    int store_rows;    // rows per output TMA store box (divides 32)
+    int gran;          // w8A16 scale granularity
+    int group;         // w8A16 group size (rows of K)
+    int inject_timeout;
+    int has_gather;    // AG-V2
+};
+
+// Host-side launch helpers implemented in coc_kernel.cu.
+cudaError_t launch(int op, bool bf16, const KParams& p, int grid, cudaStream_t stream);
+size_t smem_bytes(int op);
+int block_threads(int op);
+
+}  // namespace coc

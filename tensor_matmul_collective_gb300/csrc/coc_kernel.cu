@@ -1,0 +1,661 @@
+// Persistent fused matmul + collective kernel for GB300 (sm_103a).
+//
+// One kernel computes every operator of the CoC page's "fused-operator
+// implementation" section (MindSpeed developer guide, compute-communication
+// parallelism): MATMUL_ALL_REDUCE, MATMUL_REDUCE_SCATTER, ALL_GATHER_MATMUL
+// (+V2) and the w8A16 MATMUL_ALL_REDUCE.  With the R tensor-parallel ranks held
+// as R shard buffers on one GPU, the collective becomes part of the tile
+// pipeline:
+//
+//   AllReduce      the contraction runs over all R shards into one TMEM
+//                  accumulator (rank 0..R-1, k ascending) and the epilogue
+//                  stores the rounded tile to all R rank outputs;
+//   ReduceScatter  same accumulator, the epilogue routes each 8..32-row block
+//                  to the rank that owns those rows;
+//   AllGather      the producer routes each A tile from the shard holding its
+//                  rows; V2 also copies the gathered rows out, spread over all
+//                  work units;
+//   w8A16          int8 weight tiles are dequantised in shared memory by
+//                  dedicated warps and fed to the fp16 MMA.
+//
+// CoC chunking (page section 解决思路: split compute and communication into
+// smaller sub-tasks and pipeline them) is the work-unit order: units are
+// issued chunk by chunk along m, and the double-buffered TMEM accumulator lets
+// one tile's epilogue (the "communication") run while the next tile's
+// mainloop runs.
+//
+// Warp roles (one CTA per SM, persistent over work units):
+//   warp 0      TMA producer: A/B tiles into a STAGES-deep smem ring
+//   warp 1      TMEM owner + MMA issuer: tcgen05.mma 128x256x16, fp32 in TMEM
+//   warps 2-5   epilogue: tcgen05.ld -> round -> swizzled smem -> TMA store(s)
+//   warps 6-9   (w8A16 only) int8 -> fp16 dequantisation into the B stage
+//
+// Every mbarrier wait is bounded (COC_WAIT_NS); a wait that runs out sets a
+// CTA-wide abort flag and the device status word, every role leaves its loop,
+// in-flight copies and MMAs are drained (again with bounded waits), TMEM is
+// freed and the kernel returns.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "coc_internal.h"
+
+namespace coc {
+namespace {
+
+#ifndef COC_WAIT_NS
+#define COC_WAIT_NS 1000000000ull   // one second
+#endif
+constexpr unsigned long long kDrainNs = 20000000ull;  // 20 ms for post-abort drains
+
+// ------------------------------------------------------------ PTX helpers ---
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(c0), "r"(c1), "r"(src)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ---- tcgen05 ----
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                           uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+
+// 32 lanes x 32 consecutive fp32 columns: thread t receives lane (base + t).
+__device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+          "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
+          "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
+          "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Instruction descriptor, kind::f16: D fp32, A/B both fp16 or both bf16,
+// A K-major, B MN-major ("transposed"), N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t make_idesc(bool bf16, int M, int N) {
+    return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | (0u << 15) | (1u << 16) |
+           (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Shared-memory matrix descriptor: start >> 4 [0,14), LBO >> 4 [16,30),
+// SBO >> 4 [32,46), fixed 0b001 at [46,49), swizzle mode 2 (128-byte) at [61,64).
+__device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(lbo >> 4) << 16) |
+           (static_cast<uint64_t>(sbo >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// ------------------------------------------------------------ bounded waits ---
+
+struct Ctl {
+    volatile uint32_t* abort_flag;   // shared memory, CTA-wide
+    unsigned* status;                // global status words
+};
+
+__device__ __noinline__ void raise_timeout(const Ctl& c, unsigned where) {
+    *c.abort_flag = 1u;
+    atomicOr(c.status, DEV_ERR_TIMEOUT);
+    atomicCAS(c.status + 1, 0u, where);
+    atomicCAS(c.status + 2, 0u, blockIdx.x + 1u);
+}
+
+// Wait for phase `parity` of `bar`.  False if the CTA is aborting or the wait
+// ran out (which starts the abort).
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const Ctl& c,
+                                             unsigned where, unsigned long long limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*c.abort_flag) return false;
+        if (globaltimer() - t0 > limit_ns) {
+            raise_timeout(c, where);
+            return false;
+        }
+    }
+    return true;
+}
+
+// Post-abort drain: wait for a phase that is known to complete (an issued
+// copy or MMA) regardless of the abort flag, for at most limit_ns.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
+    if (mbar_try_wait(bar, parity)) return;
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer() - t0 > limit_ns) return;
+    }
+}
+
+// Whole-warp wait with a warp-uniform outcome.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const Ctl& c, unsigned where) {
+    const bool ok = wait_bounded(bar, parity, c, where, COC_WAIT_NS);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// ------------------------------------------------------------ scheduling ---
+
+// Work unit -> (rank r for AllGather, m-tile, n-tile).  Units go chunk by
+// chunk; inside a chunk the m-tiles of one (rank, n-tile) column are adjacent
+// so concurrently running CTAs share their B tiles in L2.
+template <int OP>
+__device__ __forceinline__ void decode_unit(const KParams& p, int u, int& r, int& mt, int& nt) {
+    const int rg = (OP == OP_AG) ? p.R : 1;
+    if (p.chunk_mt > 0) {
+        const int per_chunk = p.chunk_mt * p.n_tiles * rg;
+        const int c = u / per_chunk;
+        int v = u - c * per_chunk;
+        const int mi = v % p.chunk_mt;
+        v /= p.chunk_mt;
+        nt = v % p.n_tiles;
+        r = v / p.n_tiles;
+        mt = c * p.chunk_mt + mi;
+    } else {
+        const int per_row = p.n_tiles * rg;
+        mt = u / per_row;
+        const int v = u - mt * per_row;
+        nt = v % p.n_tiles;
+        r = v / p.n_tiles;
+    }
+}
+
+// ------------------------------------------------------------ conversions ---
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(uint32_t lo_bits, uint32_t hi_bits) {
+    const float lo = __uint_as_float(lo_bits), hi = __uint_as_float(hi_bits);
+    if constexpr (BF16) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&h);
+    } else {
+        __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+}
+
+// Four signed int8 values (bytes of w) -> two half2 holding them exactly.
+// Published bias trick (Kim et al., "Who Says Elephants Can't Run", 2022):
+// flip the sign bits so each byte is u = q + 128, place it under the binary16
+// exponent pattern 0x64 (value 1024 + u), subtract 1152.
+__device__ __forceinline__ void i8x4_to_h2x2(uint32_t w, __half2& h01, __half2& h23) {
+    const uint32_t u = w ^ 0x80808080u;
+    uint32_t a, b;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(a) : "r"(u), "r"(0x64646464u), "r"(0x4140u));
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(b) : "r"(u), "r"(0x64646464u), "r"(0x4342u));
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
+    h01 = __hsub2(*reinterpret_cast<__half2*>(&a), bias);
+    h23 = __hsub2(*reinterpret_cast<__half2*>(&b), bias);
+}
+
+// ------------------------------------------------------------ the kernel ---
+
+template <int OP>
+struct Cfg {
+    static constexpr int STAGES = (OP == OP_W8) ? 3 : 4;
+    static constexpr int WARPS = 2 + NUM_EPI_WARPS + ((OP == OP_W8) ? NUM_XFORM_WARPS : 0);
+    static constexpr int THREADS = WARPS * 32;
+    static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES + ((OP == OP_W8) ? RAW_STAGE_BYTES : 0);
+    static constexpr int EPI_BYTES = NUM_EPI_WARPS * 2 * EPI_BUF_BYTES;
+    static constexpr int BAR_BYTES = 256;
+    static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
+};
+
+template <int OP, bool BF16>
+__global__ void __launch_bounds__(Cfg<OP>::THREADS, 1) coc_fused_kernel(const __grid_constant__ KParams p) {
+    using C = Cfg<OP>;
+    constexpr int S = C::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+    uint8_t* a_st = smem;                                  // S x 16 KiB
+    uint8_t* b_st = a_st + S * A_STAGE_BYTES;              // S x 32 KiB
+    uint8_t* raw_st = b_st + S * B_STAGE_BYTES;            // S x 16 KiB (w8A16)
+    uint8_t* epi = raw_st + ((OP == OP_W8) ? S * RAW_STAGE_BYTES : 0);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(epi + C::EPI_BYTES);
+    uint64_t* full = bars;             // [S]  stage ready for the MMA
+    uint64_t* empty = bars + S;        // [S]  stage consumed by the MMA
+    uint64_t* rawfull = bars + 2 * S;  // [S]  w8A16: raw int8 + A tile landed
+    uint64_t* accf = bars + 3 * S;     // [2]  accumulator ready for the epilogue
+    uint64_t* acce = accf + 2;         // [2]  accumulator drained by the epilogue
+    uint64_t* never = acce + 2;        // [1]  nothing arrives here (fault-injection test)
+    uint64_t* drain = never + 1;       // [1]  MMA drain before TMEM release
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint32_t* abort_word = tmem_slot + 1;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const Ctl ctl{abort_word, p.status};
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(smem_u32(&full[s]), (OP == OP_W8) ? NUM_XFORM_WARPS : 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+            mbar_init(smem_u32(&rawfull[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&accf[b]), 1);
+            mbar_init(smem_u32(&acce[b]), NUM_EPI_WARPS);
+        }
+        mbar_init(smem_u32(never), 1);
+        mbar_init(smem_u32(drain), 1);
+        *abort_word = 0u;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        fence_proxy_async_smem();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), 2 * BN);   // two 128 x 256 fp32 accumulators = all 512 columns
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int total_kb = p.num_kshards * p.kblocks;
+
+    if (warp == 0) {
+        // ================================================= TMA producer ===
+        if (lane == 0) {
+            for (int i = 0; i < p.num_kshards && i < COC_MAX_RANKS; ++i) prefetch_tmap(&p.tm_a[i]);
+        }
+        uint32_t stage = 0, phase = 0;
+        uint32_t filled = 0, fill_parity = 0;   // per-stage bit masks of the last fill
+        bool ok = true;
+        for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+            int r, mt, nt;
+            decode_unit<OP>(p, u, r, mt, nt);
+            for (int ks = 0; ok && ks < p.num_kshards; ++ks) {
+                for (int kb = 0; kb < p.kblocks; ++kb) {
+                    ok = warp_wait(smem_u32(&empty[stage]), phase ^ 1u, ctl, 0x100u + stage);
+                    if (!ok) break;
+                    if (lane == 0) {
+                        const uint32_t fb = smem_u32((OP == OP_W8) ? &rawfull[stage] : &full[stage]);
+                        const uint32_t a_dst = smem_u32(a_st + stage * A_STAGE_BYTES);
+                        const int kc = kb * BK;
+                        if constexpr (OP == OP_W8) {
+                            mbar_expect_tx(fb, A_STAGE_BYTES + RAW_STAGE_BYTES);
+                        } else {
+                            mbar_expect_tx(fb, A_STAGE_BYTES + B_STAGE_BYTES);
+                        }
+                        if constexpr (OP == OP_AG) {
+                            // gathered rows -> (shard, local row); rows past the
+                            // end read beyond the last shard and are zero-filled
+                            for (int rb = 0; rb < BM; rb += p.a_box_rows) {
+                                const int g = mt * BM + rb;
+                                int s = g / p.rows_per_rank;
+                                if (s > p.R - 1) s = p.R - 1;
+                                tma_load_2d(a_dst + rb * 128, &p.tm_a[s], kc, g - s * p.rows_per_rank, fb);
+                            }
+                        } else {
+                            tma_load_2d(a_dst, &p.tm_a[ks], kc, mt * BM, fb);
+                        }
+                        const CUtensorMap* bm = &p.tm_b[(OP == OP_AG) ? r : ks];
+                        if constexpr (OP == OP_W8) {
+                            tma_load_2d(smem_u32(raw_st + stage * RAW_STAGE_BYTES), bm, nt * BN, kc, fb);
+                        } else {
+                            const uint32_t b_dst = smem_u32(b_st + stage * B_STAGE_BYTES);
+#pragma unroll
+                            for (int j = 0; j < BN / 64; ++j)
+                                tma_load_2d(b_dst + j * (64 * BK * 2), bm, nt * BN + j * 64, kc, fb);
+                        }
+                        filled |= 1u << stage;
+                        fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
+                    }
+                    __syncwarp();
+                    if (++stage == S) { stage = 0; phase ^= 1u; }
+                }
+            }
+        }
+        if (!ok && lane == 0) {
+            // leave no TMA load in flight into shared memory
+            for (int s = 0; s < S; ++s) {
+                if (filled & (1u << s)) {
+                    const uint32_t fb = smem_u32((OP == OP_W8) ? &rawfull[s] : &full[s]);
+                    drain_wait(fb, (fill_parity >> s) & 1u, kDrainNs);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ================================================= MMA issuer ===
+        constexpr uint32_t idesc = make_idesc(BF16, BM, BN);
+        uint32_t stage = 0, phase = 0;
+        int acc_i = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+            const int buf = acc_i & 1;
+            const uint32_t aph = (acc_i >> 1) & 1;
+            ok = warp_wait(smem_u32(&acce[buf]), aph ^ 1u, ctl, 0x200u + buf);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + buf * BN;
+            for (int i = 0; i < total_kb; ++i) {
+                ok = warp_wait(smem_u32(&full[stage]), phase, ctl, 0x210u + stage);
+                if (!ok) break;
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint64_t ad = make_sdesc(smem_u32(a_st + stage * A_STAGE_BYTES), 16, 1024);
+                    const uint64_t bd = make_sdesc(smem_u32(b_st + stage * B_STAGE_BYTES), 64 * BK * 2, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                        // A: +32 bytes per 16-element k step inside the 128-byte swizzle row
+                        // B: +2 eight-row groups (2 KiB) per 16-element k step
+                        tc_mma_f16(d_tmem, ad + static_cast<uint64_t>(kk * 2), bd + static_cast<uint64_t>(kk * 128),
+                                   idesc, (i > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    tc_commit(smem_u32(&empty[stage]));
+                }
+                __syncwarp();
+                if (++stage == S) { stage = 0; phase ^= 1u; }
+            }
+            if (!ok) break;
+            if (lane == 0) tc_commit(smem_u32(&accf[buf]));
+            __syncwarp();
+            ++acc_i;
+        }
+        // every issued MMA must finish before TMEM is released
+        if (lane == 0) {
+            tc_commit(smem_u32(drain));
+            drain_wait(smem_u32(drain), 0, kDrainNs);
+        }
+        __syncwarp();
+    } else if (warp < 2 + NUM_EPI_WARPS) {
+        // ================================================= epilogue ===
+        const int q = warp & 3;                 // TMEM lane quadrant this warp may read
+        const int et = (warp - 2) * 32 + lane;  // 0..127 among epilogue threads
+        uint8_t* my_epi = epi + (warp - 2) * 2 * EPI_BUF_BYTES;
+        int acc_i = 0, sb_i = 0;
+        bool ok = true;
+        if (p.inject_timeout) ok = warp_wait(smem_u32(never), 0, ctl, 0x300u);
+        for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+            int r, mt, nt;
+            decode_unit<OP>(p, u, r, mt, nt);
+            const int buf = acc_i & 1;
+            const uint32_t aph = (acc_i >> 1) & 1;
+            ok = warp_wait(smem_u32(&accf[buf]), aph, ctl, 0x310u + buf);
+            if (!ok) break;
+            tc_fence_after();
+            const int row0 = mt * BM + 32 * q;
+            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + buf * BN;
+            for (int sub = 0; sub < BN / EPI_COLS; ++sub) {
+                uint32_t va[32], vb[32];
+                if (total_kb > 0) {
+                    tmem_ld_32cols(t_row + sub * EPI_COLS, va);
+                    tmem_ld_32cols(t_row + sub * EPI_COLS + 32, vb);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) { va[i] = 0u; vb[i] = 0u; }
+                }
+                if (sub == BN / EPI_COLS - 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&acce[buf]));
+                }
+                const int col = nt * BN + sub * EPI_COLS;
+                if (col >= p.n || row0 >= p.m) continue;   // sub-tile entirely outside the output
+                uint8_t* sbuf = my_epi + (sb_i & 1) * EPI_BUF_BYTES;
+                ++sb_i;
+                if (lane == 0) bulk_wait_read<1>();   // the store that last read this buffer is done
+                __syncwarp();
+                uint8_t* rowp = sbuf + lane * 128;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint32_t* v = (j < 4) ? (va + 8 * j) : (vb + 8 * (j - 4));
+                    uint4 w4;
+                    w4.x = pack2<BF16>(v[0], v[1]);
+                    w4.y = pack2<BF16>(v[2], v[3]);
+                    w4.z = pack2<BF16>(v[4], v[5]);
+                    w4.w = pack2<BF16>(v[6], v[7]);
+                    *reinterpret_cast<uint4*>(rowp + ((j ^ (lane & 7)) << 4)) = w4;
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    const uint32_t src = smem_u32(sbuf);
+                    if constexpr (OP == OP_RS) {
+                        for (int rb = 0; rb < 32; rb += p.store_rows) {
+                            const int g = row0 + rb;
+                            if (g >= p.m) break;
+                            const int dst = g / p.rows_per_rank;
+                            tma_store_2d(&p.tm_out[dst], src + rb * 128, col, g - dst * p.rows_per_rank);
+                        }
+                    } else if constexpr (OP == OP_AG) {
+                        tma_store_2d(&p.tm_out[r], src, col, row0);
+                    } else {
+                        for (int o = 0; o < p.n_out; ++o) tma_store_2d(&p.tm_out[o], src, col, row0);
+                    }
+                    bulk_commit();
+                }
+                __syncwarp();
+            }
+            ++acc_i;
+            if constexpr (OP == OP_AG) {
+                if (p.has_gather) {
+                    // V2: this unit's share of the m-tile's gathered rows.  The
+                    // tile's rows are one contiguous run of the gathered
+                    // matrix; it is cut into R * n_tiles equal pieces, one per
+                    // unit that works on this m-tile.
+                    const int rows = min(BM, p.m - mt * BM);
+                    const long long vpr = p.k / 8;              // 16-byte vectors per row
+                    const long long total = rows * vpr;
+                    const long long Q = static_cast<long long>(p.R) * p.n_tiles;
+                    const long long qi = static_cast<long long>(r) * p.n_tiles + nt;
+                    const long long v0 = total * qi / Q, v1 = total * (qi + 1) / Q;
+                    for (long long vv = v0 + et; vv < v1; vv += 32 * NUM_EPI_WARPS) {
+                        const int lr = static_cast<int>(vv / vpr);
+                        const long long c = vv - lr * vpr;
+                        const int g = mt * BM + lr;
+                        const int s = g / p.rows_per_rank;
+                        const int l = g - s * p.rows_per_rank;
+                        const uint4 val = __ldg(reinterpret_cast<const uint4*>(p.gsrc[s] + (static_cast<long long>(l) * p.k) + c * 8));
+                        const long long off = static_cast<long long>(g) * p.k + c * 8;
+                        for (int d = 0; d < p.R; ++d)
+                            if (p.gdst[d] != nullptr) __stcs(reinterpret_cast<uint4*>(p.gdst[d] + off), val);
+                    }
+                }
+            }
+        }
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
+    } else if constexpr (OP == OP_W8) {
+        // ================================================= w8A16 dequant ===
+        // Thread tt owns 8 consecutive columns (cc) of the 256-wide tile and
+        // rows kr0, kr0 + 4, ..., of the 64-row k-block.
+        const int tt = (warp - 2 - NUM_EPI_WARPS) * 32 + lane;
+        const int cc = tt & 31;
+        const int kr0 = tt >> 5;
+        uint32_t stage = 0, phase = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+            int r, mt, nt;
+            decode_unit<OP>(p, u, r, mt, nt);
+            const int j0 = nt * BN + cc * 8;   // first global column of this thread
+            for (int ks = 0; ok && ks < p.num_kshards; ++ks) {
+                const __half* sc = reinterpret_cast<const __half*>(p.scale[ks]);
+                for (int kb = 0; kb < p.kblocks; ++kb) {
+                    __half2 s2[4];
+                    if (p.gran == COC_SCALE_TENSOR) {
+                        const __half s = sc[0];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) s2[e] = __halves2half2(s, s);
+                    } else {
+                        const __half* row = sc + ((p.gran == COC_SCALE_GROUP)
+                                                      ? static_cast<long long>((kb * BK) / p.group) * p.n
+                                                      : 0LL);
+                        if (j0 + 8 <= p.n) {
+                            const uint4 s8 = __ldg(reinterpret_cast<const uint4*>(row + j0));
+                            s2[0] = *reinterpret_cast<const __half2*>(&s8.x);
+                            s2[1] = *reinterpret_cast<const __half2*>(&s8.y);
+                            s2[2] = *reinterpret_cast<const __half2*>(&s8.z);
+                            s2[3] = *reinterpret_cast<const __half2*>(&s8.w);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) s2[e] = __float2half2_rn(0.f);   // columns past n
+                        }
+                    }
+                    ok = warp_wait(smem_u32(&rawfull[stage]), phase, ctl, 0x400u + stage);
+                    if (!ok) break;
+                    const uint8_t* raw = raw_st + stage * RAW_STAGE_BYTES;
+                    uint8_t* bst = b_st + stage * B_STAGE_BYTES;
+#pragma unroll 4
+                    for (int i = 0; i < BK / 4; ++i) {
+                        const int kk = kr0 + 4 * i;
+                        const uint2 q8 = *reinterpret_cast<const uint2*>(raw + kk * BN + cc * 8);
+                        __half2 h[4];
+                        i8x4_to_h2x2(q8.x, h[0], h[1]);
+                        i8x4_to_h2x2(q8.y, h[2], h[3]);
+                        uint4 o;
+                        __half2 m0 = __hmul2_rn(h[0], s2[0]), m1 = __hmul2_rn(h[1], s2[1]);
+                        __half2 m2 = __hmul2_rn(h[2], s2[2]), m3 = __hmul2_rn(h[3], s2[3]);
+                        o.x = *reinterpret_cast<uint32_t*>(&m0);
+                        o.y = *reinterpret_cast<uint32_t*>(&m1);
+                        o.z = *reinterpret_cast<uint32_t*>(&m2);
+                        o.w = *reinterpret_cast<uint32_t*>(&m3);
+                        // MN-major 128-byte-swizzled B layout: 64-column blocks of
+                        // 64 rows x 128 bytes, 16-byte chunks XOR-ed with row % 8
+                        const int blk = cc >> 3, c16 = cc & 7;
+                        *reinterpret_cast<uint4*>(bst + blk * (64 * BK * 2) + kk * 128 + ((c16 ^ (kk & 7)) << 4)) = o;
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&full[stage]));
+                    if (++stage == S) { stage = 0; phase ^= 1u; }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, 2 * BN);
+    }
+}
+
+template <int OP, bool BF16>
+cudaError_t launch_t(const KParams& p, int grid, cudaStream_t stream) {
+    auto kern = coc_fused_kernel<OP, BF16>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<OP>::SMEM);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(Cfg<OP>::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Cfg<OP>::SMEM;
+    cfg.stream = stream;
+    cfg.attrs = nullptr;
+    cfg.numAttrs = 0;
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+}  // namespace
+
+cudaError_t launch(int op, bool bf16, const KParams& p, int grid, cudaStream_t stream) {
+    switch (op) {
+        case OP_AR: return bf16 ? launch_t<OP_AR, true>(p, grid, stream) : launch_t<OP_AR, false>(p, grid, stream);
+        case OP_RS: return bf16 ? launch_t<OP_RS, true>(p, grid, stream) : launch_t<OP_RS, false>(p, grid, stream);
+        case OP_AG: return bf16 ? launch_t<OP_AG, true>(p, grid, stream) : launch_t<OP_AG, false>(p, grid, stream);
+        case OP_W8: return launch_t<OP_W8, false>(p, grid, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+size_t smem_bytes(int op) { return op == OP_W8 ? Cfg<OP_W8>::SMEM : Cfg<OP_AR>::SMEM; }
+int block_threads(int op) { return op == OP_W8 ? Cfg<OP_W8>::THREADS : Cfg<OP_AR>::THREADS; }
+
+}  // namespace coc
