@@ -100,14 +100,17 @@ def test_zero_k_writes_zeros():
     assert all(torch.count_nonzero(o).item() == 0 for o in outs)
 
 
-def test_small_integers_bitwise():
-    # |x|, |w| <= 4, K = 512: every partial sum is an integer < 256 -> exact in bf16
+@pytest.mark.parametrize("dt,lim", [(F16, 4), (BF16, 1)])
+def test_small_integers_bitwise(dt, lim):
+    # Integer inputs with K = 512: every partial sum is an integer far below
+    # 2^24 (exact in fp32) and the results stay inside the range where the
+    # output type holds every integer (2048 for fp16, 256 for bf16).
     g = torch.Generator().manual_seed(5)
     R, m, n, ks = 4, 160, 264, 128
-    xs = [torch.randint(-4, 5, (m, ks), generator=g).to(BF16) for _ in range(R)]
-    ws = [torch.randint(-4, 5, (ks, n), generator=g).to(BF16) for _ in range(R)]
-    ref = orc.matmul_all_reduce(orc.BF16, bits(xs), bits(ws))
-    assert np.abs(ref).max() < 256
+    xs = [torch.randint(-lim, lim + 1, (m, ks), generator=g).to(dt) for _ in range(R)]
+    ws = [torch.randint(-lim, lim + 1, (ks, n), generator=g).to(dt) for _ in range(R)]
+    ref = orc.matmul_all_reduce(CODE[dt], bits(xs), bits(ws))
+    assert np.abs(ref).max() < (2048 if dt == F16 else 256)
     outs = coc.matmul_all_reduce(to_dev(xs), to_dev(ws))
     coc.sync_status()
     for o in outs:
