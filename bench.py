@@ -1,0 +1,588 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused tensor-parallel matmul + collective operators.
+
+One step = one pass over every fused operator on its TP8 layer shape (8
+emulated ranks), i.e. every step of the hot path:
+
+  bloom7b_ar          MATMUL_ALL_REDUCE   m 2048, K 16384 (8 x 2048), n 4096, bf16, chunks 4
+  llama70b_ag_v2      ALL_GATHER_MATMUL_V2  8 x (512 x 8192) gathered, W 8192 x (8 x 7168), bf16
+  llama70b_rs         MATMUL_REDUCE_SCATTER  m 4096, K 28672 (8 x 3584), n 8192, bf16
+  w8a16_ar_{tensor,channel,group}  w8A16 MATMUL_ALL_REDUCE  m 4096, K 8192 (8 x 1024), n 8192, fp16 x int8
+  bloom176b_det_ar    deterministic MATMUL_ALL_REDUCE  m 2048, K 57344 (8 x 7168), n 14336, bf16
+  bloom176b_det_rs    deterministic MATMUL_REDUCE_SCATTER, same shapes
+
+value = algorithmic FLOPs (2 m n K per operator) of all steps on all ranks /
+wall time of the timed steps (CUDA events, max over ranks), in TFLOP/s.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs the whole suite on its own GPU
+(replicas; the path has no cross-GPU exchange), rank 0 prints the line.
+--impl reference times the fp64 CPU oracle on a bounded sample of the same
+workload instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused matmul+AR/RS/AG TFLOP/s and % of GB300 dense bf16 peak, 8 emulated TP shards"
+UNIT = "TFLOP/s"
+WORKLOAD = ("tp8_suite: bloom7b_ar + llama70b_ag_v2 + llama70b_rs + w8a16_ar x {tensor,channel,group} "
+            "+ bloom176b_det_ar + bloom176b_det_rs (8 emulated TP ranks each)")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-context", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("coc_kernel.cu", "coc_internal.h"):
+        h.update(open(os.path.join(ROOT, "tensor_matmul_collective_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:12]
+
+
+def load_traffic(op: str):
+    """DRAM bytes per launch of `op` from the committed ncu summary, if it was
+    taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    want = kernel_source_hash()
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 3 and not line.startswith("#") and parts[0] == op and parts[2] == want:
+            return float(parts[1])
+    return None
+
+
+# ------------------------------------------------------------------ clocks ---
+
+class ClockSampler:
+    FIELDS = ("pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id: str | None):
+        self.bus = (bus_id or "").lower()
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=10)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [[c.strip() for c in ln.split(",")] for ln in out.splitlines() if ln.count(",") >= 8]
+        if self.bus:
+            mine = [r for r in rows if self.bus in r[0].lower()]
+            rows = mine or rows
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        power = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(power) if power else None}
+
+
+# ------------------------------------------------------------------- suite ---
+
+class Op:
+    def __init__(self, name, kind, flops, run, inputs, outputs, shape, gran=None):
+        self.name, self.kind, self.flops, self.run = name, kind, flops, run
+        self.inputs, self.outputs, self.shape, self.gran = inputs, outputs, shape, gran
+        self.shares_prev_inputs = False   # reads the inputs uploaded for the operator before it
+
+
+def build_suite(dev):
+    """Device inputs/outputs for every operator of one step (inputs drawn on
+    the host from the seeded generators, uploaded once)."""
+    import torch
+
+    from tensor_matmul_collective_gb300 import coc
+    from tensor_matmul_collective_gb300 import workloads as wl
+
+    ops, host = [], {}
+
+    def up(ts):
+        return [t.to(dev) for t in ts]
+
+    s = wl.BLOOM7B_AR
+    xs, ws = s.make()
+    host["bloom7b"] = (xs, ws)
+    dx, dw = up(xs), up(ws)
+    out7 = [torch.empty(s.m, s.n, dtype=s.dtype, device=dev) for _ in range(s.R)]
+    ops.append(Op("bloom7b_ar", "ar", s.flops(), lambda dx=dx, dw=dw, o=out7: coc.matmul_all_reduce(dx, dw, o, chunks=4),
+                  dx + dw, out7, s))
+
+    s = wl.LLAMA70B_AG
+    xs, ws = s.make()
+    host["llama_ag"] = (xs, ws)
+    dx, dw = up(xs), up(ws)
+    outg = [torch.empty(s.m, s.n_shard, dtype=s.dtype, device=dev) for _ in range(s.R)]
+    gat = [torch.empty(s.m, s.k, dtype=s.dtype, device=dev) for _ in range(s.R)]
+    ops.append(Op("llama70b_ag_v2", "ag_v2", s.flops(),
+                  lambda dx=dx, dw=dw, o=outg, g=gat: coc.all_gather_matmul_v2(dx, dw, o, g, chunks=4),
+                  dx + dw, outg + gat, s))
+
+    s = wl.LLAMA70B_RS
+    xs, ws = s.make()
+    host["llama_rs"] = (xs, ws)
+    dx, dw = up(xs), up(ws)
+    outr = [torch.empty(s.m // s.R, s.n, dtype=s.dtype, device=dev) for _ in range(s.R)]
+    ops.append(Op("llama70b_rs", "rs", s.flops(),
+                  lambda dx=dx, dw=dw, o=outr: coc.matmul_reduce_scatter(dx, dw, o, chunks=4), dx + dw, outr, s))
+
+    s = wl.W8A16_AR
+    xs8 = wqs = None
+    for gran in wl.SCALE_GRANS:
+        x_, w_, scales = s.make(gran)
+        if xs8 is None:
+            xs8, wqs = x_, w_
+            dx8, dwq = up(xs8), up(wqs)
+        host[f"w8_{gran}"] = (xs8, wqs, scales)
+        if gran == "group":
+            dsc = up(scales)
+            uniq = dsc
+        else:                       # one scale tensor shared by every rank
+            d0 = scales[0].to(dev)
+            dsc, uniq = [d0] * s.R, [d0]
+        out8 = [torch.empty(s.m, s.n, dtype=torch.float16, device=dev) for _ in range(s.R)]
+        op = Op(f"w8a16_ar_{gran}", "w8a16_ar", s.flops(),
+                lambda dx=dx8, dw=dwq, sc=dsc, o=out8, g=gran, grp=s.group: coc.matmul_all_reduce_w8a16(
+                    dx, dw, sc, g, grp, o, chunks=4),
+                (dx8 + dwq if gran == "tensor" else []) + uniq, out8, s, gran)
+        op.shares_prev_inputs = gran != "tensor"
+        ops.append(op)
+
+    s = wl.BLOOM176B
+    xs, ws = s.make()
+    host["bloom176b"] = (xs, ws)
+    dx, dw = up(xs), up(ws)
+    outa = [torch.empty(s.m, s.n, dtype=s.dtype, device=dev) for _ in range(s.R)]
+    outs = [torch.empty(s.m // s.R, s.n, dtype=s.dtype, device=dev) for _ in range(s.R)]
+    ops.append(Op("bloom176b_det_ar", "ar", s.flops(),
+                  lambda dx=dx, dw=dw, o=outa: coc.matmul_all_reduce(dx, dw, o, chunks=4, deterministic=True),
+                  dx + dw, outa, s))
+    op = Op("bloom176b_det_rs", "rs", s.flops(),
+            lambda dx=dx, dw=dw, o=outs: coc.matmul_reduce_scatter(dx, dw, o, chunks=4, deterministic=True),
+            [], outs, s)
+    op.shares_prev_inputs = True
+    ops.append(op)
+    return ops, host
+
+
+def time_device(ops, steps, warmup, dist, sampler):
+    import torch
+    from tensor_matmul_collective_gb300 import coc
+
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        for op in ops:
+            op.run()
+    torch.cuda.synchronize()
+    coc.sync_status()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ops) + 1)] for _ in range(steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for s in range(steps):
+        ev[s][0].record(stream)
+        for i, op in enumerate(ops):
+            op.run()
+            ev[s][i + 1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if dist is not None:
+        dist.barrier()
+    coc.sync_status()
+    total_ms = t_start.elapsed_time(t_end)
+    per_op = [statistics.mean(ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(steps)) for i in range(len(ops))]
+    return total_ms, per_op, clocks
+
+
+def time_e2e(ops, steps, dev):
+    """Same suite through the public API from pinned host buffers: each step
+    copies every operator's inputs host->device, runs it and copies its
+    outputs device->host.  Copies run on their own streams so one operator's
+    transfers overlap another's compute."""
+    import torch
+
+    from tensor_matmul_collective_gb300 import coc
+
+    h_in = [[t.to("cpu").pin_memory() for t in op.inputs] for op in ops]
+    h_out = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in op.outputs] for op in ops]
+    comp = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    n = len(ops)
+    in_ready = [torch.cuda.Event() for _ in range(n)]
+    done = [torch.cuda.Event() for _ in range(n)]
+    out_done = [torch.cuda.Event() for _ in range(n)]
+    h2d = sum(t.numel() * t.element_size() for hs in h_in for t in hs)
+    d2h = sum(t.numel() * t.element_size() for hs in h_out for t in hs)
+
+    # the last operator of each run of operators that read the same inputs
+    last_reader = list(range(n))
+    for i in range(n - 1, 0, -1):
+        if ops[i].shares_prev_inputs:
+            last_reader[i - 1] = last_reader[i]
+
+    def step(first):
+        for i, op in enumerate(ops):
+            with torch.cuda.stream(s_in):
+                if not first and op.inputs:
+                    s_in.wait_event(done[last_reader[i]])   # previous step finished reading these inputs
+                for d, h in zip(op.inputs, h_in[i]):
+                    d.copy_(h, non_blocking=True)
+                in_ready[i].record(s_in)
+            comp.wait_event(in_ready[i])
+            if i > 0:
+                comp.wait_event(in_ready[i - 1])
+            if not first:
+                comp.wait_event(out_done[i])          # previous step's outputs are back on the host
+            op.run()
+            done[i].record(comp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(done[i])
+                for h, d in zip(h_out[i], op.outputs):
+                    h.copy_(d, non_blocking=True)
+                out_done[i].record(s_out)
+
+    step(True)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step(False)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    coc.sync_status()
+    del h_in, h_out
+    return wall, h2d, d2h
+
+
+def time_context(ops, dev):
+    """Context numbers measured outside the timed region: the same contraction
+    with a plain one-buffer epilogue (fused overhead) and the unfused torch
+    sequence (per-shard torch.matmul, then a separate reduction/copy)."""
+    import torch
+
+    from tensor_matmul_collective_gb300 import coc
+
+    def t(fn, it=10):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(it):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / it
+
+    out = {}
+    for op in ops:
+        if op.kind not in ("ar", "rs"):
+            continue
+        s = op.shape
+        dx, dw = op.inputs[:s.R], op.inputs[s.R:2 * s.R]
+        if not dx:   # bloom176b_det_rs shares the AR inputs
+            prev = [o for o in ops if o.name == "bloom176b_det_ar"][0]
+            dx, dw = prev.inputs[:s.R], prev.inputs[s.R:2 * s.R]
+        plain = torch.empty(s.m, s.n, dtype=s.dtype, device=dev)
+        tf = t(op.run)
+        tp = t(lambda: coc.matmul(dx, dw, plain))
+
+        def unfused(dx=dx, dw=dw, R=s.R, kind=op.kind, m=s.m):
+            acc = torch.stack([torch.matmul(a, b) for a, b in zip(dx, dw)]).sum(0, dtype=torch.float32).to(dx[0].dtype)
+            if kind == "ar":
+                return [acc.clone() for _ in range(R)]
+            return [acc[r * (m // R):(r + 1) * (m // R)].clone() for r in range(R)]
+        tu = t(unfused, 3)
+        out[op.name] = {"fused_ms": round(tf, 4), "plain_epilogue_ms": round(tp, 4),
+                        "fused_overhead": round(tf / tp - 1.0, 4), "torch_unfused_ms": round(tu, 4)}
+    ag = [o for o in ops if o.kind == "ag_v2"]
+    if ag:
+        op = ag[0]
+        s = op.shape
+        dx, dw = op.inputs[:s.R], op.inputs[s.R:]
+        outs = op.outputs[:s.R]
+        xg = op.outputs[s.R]
+        tf = t(op.run)
+        t_ag = t(lambda: coc.all_gather_matmul(dx, dw, outs, chunks=4))
+        t_plain = t(lambda: [coc.matmul([xg], [dw[r]], outs[r]) for r in range(s.R)])
+        tu = t(lambda: [torch.matmul(torch.cat(dx, 0), dw[r]) for r in range(s.R)], 3)
+        out[op.name] = {"fused_ms": round(tf, 4), "all_gather_matmul_ms": round(t_ag, 4),
+                        "plain_epilogue_ms": round(t_plain, 4), "fused_overhead": round(tf / t_plain - 1.0, 4),
+                        "torch_unfused_ms": round(tu, 4)}
+    return out
+
+
+# --------------------------------------------------------- CPU oracle legs ---
+
+def oracle_sample(host, rows: int, cols: int | None, seed: int = 1234):
+    """Run the fp64 oracle on `rows` seeded output rows (and the first `cols`
+    columns, None = all) of every operator.  Returns (seconds, flops, cores)."""
+    import numpy as np
+
+    from oracle import oracle as orc
+    from tensor_matmul_collective_gb300 import workloads as wl
+
+    def b(ts, c=None):
+        return [wl.bits16(t) if c is None else np.ascontiguousarray(wl.bits16(t)[:, :c]) for t in ts]
+
+    flops = 0.0
+    t0 = time.perf_counter()
+    xs, ws = host["bloom7b"]
+    s = wl.BLOOM7B_AR
+    c = cols or s.n
+    r_ = wl.sample_rows(s.m, rows, seed)
+    orc.matmul_all_reduce(orc.BF16, b(xs), b(ws, c), r_)
+    flops += 2.0 * rows * c * s.K
+
+    xs, ws = host["llama_ag"]
+    s = wl.LLAMA70B_AG
+    c = cols or s.n_shard
+    r_ = wl.sample_rows(s.m, rows, seed)
+    bx, bw = b(xs), b(ws, c)
+    for r in range(s.R):
+        orc.all_gather_matmul(orc.BF16, bx, bw, r, r_)
+        flops += 2.0 * rows * c * s.k
+    orc.all_gather(bx)
+
+    xs, ws = host["llama_rs"]
+    s = wl.LLAMA70B_RS
+    c = cols or s.n
+    bx, bw = b(xs), b(ws, c)
+    r_ = wl.sample_rows(s.m // s.R, max(1, rows // s.R), seed)
+    for r in range(s.R):
+        orc.matmul_reduce_scatter(orc.BF16, bx, bw, r, r_)
+        flops += 2.0 * r_.size * c * s.K
+
+    s = wl.W8A16_AR
+    for code, gran in enumerate(wl.SCALE_GRANS):
+        xs, wqs, scales = host[f"w8_{gran}"]
+        c = cols or s.n
+        wq = [np.ascontiguousarray(w.numpy()[:, :c]) for w in wqs]
+        sc = [wl.bits16(t) for t in scales]
+        if gran != "tensor":
+            sc = [np.ascontiguousarray(x.reshape(-1, s.n)[:, :c]) for x in sc]
+        r_ = wl.sample_rows(s.m, rows, seed)
+        orc.matmul_all_reduce_w8a16(b(xs), wq, sc, code, s.group, r_)
+        flops += 2.0 * rows * c * s.K
+
+    xs, ws = host["bloom176b"]
+    s = wl.BLOOM176B
+    c = cols or s.n
+    bx, bw = b(xs), b(ws, c)
+    r_ = wl.sample_rows(s.m, rows, seed)
+    orc.matmul_all_reduce(orc.BF16, bx, bw, r_)
+    flops += 2.0 * rows * c * s.K
+    r2 = wl.sample_rows(s.m // s.R, max(1, rows // s.R), seed)
+    for r in range(s.R):
+        orc.matmul_reduce_scatter(orc.BF16, bx, bw, r, r2)
+        flops += 2.0 * r2.size * c * s.K
+    return time.perf_counter() - t0, flops, orc.max_threads()
+
+
+def make_host_inputs():
+    from tensor_matmul_collective_gb300 import workloads as wl
+    host = {}
+    host["bloom7b"] = wl.BLOOM7B_AR.make()
+    host["llama_ag"] = wl.LLAMA70B_AG.make()
+    host["llama_rs"] = wl.LLAMA70B_RS.make()
+    for gran in wl.SCALE_GRANS:
+        host[f"w8_{gran}"] = wl.W8A16_AR.make(gran)
+    host["bloom176b"] = wl.BLOOM176B.make()
+    return host
+
+
+def suite_flops() -> float:
+    from tensor_matmul_collective_gb300 import workloads as wl
+    return (wl.BLOOM7B_AR.flops() + wl.LLAMA70B_AG.flops() + wl.LLAMA70B_RS.flops() + 3 * wl.W8A16_AR.flops()
+            + 2 * wl.BLOOM176B.flops())
+
+
+def base_line(n_gpus, steps, warmup):
+    return {"metric": METRIC, "unit": UNIT, "n_gpus": n_gpus, "steps": steps, "warmup": warmup,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded; BLOOM-7B / LLaMA2-70B / BLOOM-176B TP8 layer shapes)"}
+
+
+def config_dict(world):
+    return {"workload": WORKLOAD, "ranks_emulated": 8, "chunks": 4,
+            "compute_types": "bf16 in / fp32 accumulate / bf16 out; w8A16: fp16 x int8 -> fp16",
+            "l2": "no flush: every operator's operands exceed the 129 MB L2 and each step streams > 5 GB",
+            "parallelism": f"replicas x{world} (no cross-GPU exchange on this path)"}
+
+
+# -------------------------------------------------------------------- arms ---
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    host = make_host_inputs()
+    rows, cols = 1, 64
+    for _ in range(args.warmup):
+        oracle_sample(host, rows, cols)
+    secs, flops, cores = [], 0.0, 1
+    for _ in range(args.steps):
+        t, flops, cores = oracle_sample(host, rows, cols)
+        secs.append(t)
+    total = sum(secs)
+    value = flops * args.steps / total / 1e12
+    line = base_line(args.gpus, args.steps, args.warmup)
+    line.update({"impl": "reference", "value": value, "ms_per_step": 1000.0 * total / args.steps,
+                 "dtype": "f64", "config": config_dict(1),
+                 "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                  "sample": f"per step: {rows} seeded output row x first {cols} columns of every "
+                                            f"operator of the suite ({flops / 1e9:.3f} GFLOP)"},
+                 "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}})
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+
+    rank, world, local = dist_env()
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        dist = tdist
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from tensor_matmul_collective_gb300 import build as cbuild
+    from tensor_matmul_collective_gb300 import coc
+    cbuild.build()
+    coc.lib()
+
+    ops, host = build_suite(dev)
+    bus = None
+    try:
+        props = torch.cuda.get_device_properties(dev)
+        bus = "%02x:%02x." % (props.pci_bus_id, props.pci_device_id)
+    except Exception:
+        bus = None
+    sampler = ClockSampler(bus)
+    total_ms, per_op, clocks = time_device(ops, args.steps, args.warmup, dist, sampler)
+
+    elapsed = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    if dist is not None:
+        dist.all_reduce(elapsed, op=dist.ReduceOp.MAX)
+    total_ms = float(elapsed.item())
+    step_flops = sum(op.flops for op in ops)
+    value = world * step_flops * args.steps / (total_ms / 1e3) / 1e12
+
+    peaks = load_peaks()
+    peak = peaks["bf16_tflops_sustained"]
+    dom = max(range(len(ops)), key=lambda i: per_op[i])
+    dom_tf = ops[dom].flops / (per_op[dom] / 1e3) / 1e12
+    traffic = load_traffic(ops[dom].name)
+    per_op_json = {op.name: {"ms": round(t, 4), "tflops": round(op.flops / (t / 1e3) / 1e12, 1),
+                             "frac_of_peak": round(op.flops / (t / 1e3) / 1e12 / peak, 4)}
+                   for op, t in zip(ops, per_op)}
+
+    e2e = None
+    if args.e2e_steps > 0:
+        wall, h2d, d2h = time_e2e(ops, args.e2e_steps, dev)
+        e2e = {"value": world * step_flops * args.e2e_steps / wall / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    context = None if args.no_context else time_context(ops, dev)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rows = 16
+        t, flops, cores = oracle_sample(host, rows, None)
+        cpu = {"value": flops / t / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"{rows} seeded output rows (all columns) of every operator of one suite step "
+                         f"({flops / 1e9:.1f} GFLOP in {t:.1f} s)"}
+
+    if rank == 0:
+        line = base_line(world, args.steps, args.warmup)
+        line.update({
+            "value": value, "ms_per_step": total_ms / args.steps, "config": config_dict(world),
+            "pct_of_peak": round(100.0 * value / world / peak, 2),
+            "peak": {"bf16_tflops_sustained": peak, "bf16_tflops_burst": peaks["bf16_tflops"],
+                     "source": peaks["source"]},
+            "roofline": {"bound": "tensor", "kernel": ops[dom].name, "achieved": round(dom_tf, 1), "peak": peak,
+                         "unit": UNIT, "frac": round(dom_tf / peak, 4), "traffic": traffic,
+                         "peak_source": f"{peaks['source']} sustained bf16 (kernel timed inside a long step)"},
+            "per_op": per_op_json,
+            "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+            "gpu_launches": len(ops) * args.steps,
+            "context": context,
+        })
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
