@@ -206,6 +206,34 @@ coc_status_t coc_matmul(int R, int64_t m, int64_t n, int64_t k_shard,
                         coc_dtype_t dt, coc_stream_t stream);
 
 /*
+ * Allocation-free MATMUL_ALL_REDUCE.  The pages have no counterpart: this
+ * entry point exists for callers that cannot allocate device memory where
+ * they call the operator — runtimes that pre-carve all device memory into
+ * their own pools, latency-critical paths where cudaMalloc's implicit
+ * synchronisation is not acceptable, processes whose allocations must all go
+ * through a custom allocator.
+ *
+ * Same arguments, results and checks as coc_matmul_all_reduce.  The library
+ * makes no cudaMalloc/cudaFree or other allocating call here.  The kernel's
+ * only scratch (its 32-byte status block) lives in a fixed 256-byte
+ * __device__ array that every GPU loading the library holds until the
+ * process exits; this scratch does not grow with m, n or k, and a need
+ * beyond 256 bytes would be rejected with COC_ERR_SHAPE.
+ *   - The first call on a device looks up that array's device address
+ *     (cudaGetSymbolAddress) with the device current; make that first call
+ *     before any stream capture.
+ *   - Every call shares the array.  Each call clears the status block in
+ *     stream order before its kernel; calls whose kernels overlap on the GPU
+ *     (different streams) race on it.
+ *   - The status block is not read by coc_sync_status(): a bounded wait that
+ *     runs out here still stops the kernel cleanly, but is not reported.
+ */
+coc_status_t coc_matmul_all_reduce_noalloc(int R, int64_t m, int64_t n, int64_t k_shard,
+                                           const void* const* x, const void* const* w,
+                                           void* const* out, coc_dtype_t dt,
+                                           int chunks, int deterministic, coc_stream_t stream);
+
+/*
  * Waits for `stream`, then returns and clears the device-side status of
  * this library on the current device: COC_ERR_TIMEOUT if a kernel's bounded
  * wait ran out since the last check, COC_ERR_CUDA if the stream reports an

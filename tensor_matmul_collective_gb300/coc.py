@@ -27,7 +27,7 @@ EXPORTS = (
     "coc_matmul_all_reduce", "coc_matmul_reduce_scatter", "coc_all_gather_matmul",
     "coc_all_gather_matmul_v2", "coc_matmul_all_reduce_w8a16", "coc_matmul",
     "coc_sync_status", "coc_status_string", "coc_last_error", "coc_version",
-    "coc_debug_inject_timeout", "coc_shutdown",
+    "coc_debug_inject_timeout", "coc_shutdown", "coc_matmul_all_reduce_noalloc",
 )
 
 
@@ -55,7 +55,8 @@ def lib() -> ctypes.CDLL:
             i64, i32, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
             pp = ctypes.POINTER(ctypes.c_void_p)
             row = [i32, i64, i64, i64, pp, pp, pp, i32, i32, i32, vp]
-            for name in ("coc_matmul_all_reduce", "coc_matmul_reduce_scatter", "coc_all_gather_matmul"):
+            for name in ("coc_matmul_all_reduce", "coc_matmul_reduce_scatter", "coc_all_gather_matmul",
+                         "coc_matmul_all_reduce_noalloc"):
                 getattr(L, name).argtypes = row
                 getattr(L, name).restype = i32
             L.coc_all_gather_matmul_v2.argtypes = [i32, i64, i64, i64, pp, pp, pp, pp, i32, i32, i32, vp]

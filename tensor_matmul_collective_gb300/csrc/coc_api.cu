@@ -415,3 +415,16 @@ COC_API coc_status_t coc_shutdown(void) {
     g_dev.clear();
     return st;
 }
+
+// ---- helpers shared with the allocation-free entry point (coc_noalloc.cu) ----
+namespace coc {
+
+coc_status_t validate_all_reduce_args(int R, int64_t m, int64_t n, int64_t k_shard, const void* const* x,
+                                      const void* const* w, void* const* out, coc_dtype_t dt, int chunks,
+                                      int deterministic) {
+    return validate_row_parallel(R, m, n, k_shard, x, w, out, R, dt, chunks, deterministic, 2);
+}
+
+coc_status_t report_error(coc_status_t st, const char* msg) { return fail(st, "%s", msg); }
+
+}  // namespace coc

@@ -60,6 +60,13 @@ struct KParams {
     int has_gather;    // AG-V2
 };
 
+// Argument checks of coc_matmul_all_reduce and the per-thread error text
+// (coc_api.cu), reused by the allocation-free entry point (coc_noalloc.cu).
+coc_status_t validate_all_reduce_args(int R, int64_t m, int64_t n, int64_t k_shard, const void* const* x,
+                                      const void* const* w, void* const* out, coc_dtype_t dt, int chunks,
+                                      int deterministic);
+coc_status_t report_error(coc_status_t st, const char* msg);
+
 // Host-side launch helpers implemented in coc_kernel.cu.
 cudaError_t launch(int op, bool bf16, const KParams& p, int grid, cudaStream_t stream);
 size_t smem_bytes(int op);
