@@ -283,35 +283,72 @@ __device__ __forceinline__ void i8x4_to_h2x2(uint32_t w, __half2& h01, __half2& 
     h23 = __hsub2(*reinterpret_cast<__half2*>(&b), bias);
 }
 
+// ALL_GATHER_MATMUL_V2: copy this unit's share of the m-tile's gathered
+// rows to every rank's gather buffer.  The tile's rows are one contiguous run
+// of the gathered matrix; it is cut into R * n_tiles equal pieces, one per
+// work unit of this m-tile, so the copy is spread over the whole kernel.
+// Kept out of line: it runs once per unit, after the tile's epilogue.
+__device__ __noinline__ void gather_slice(const KParams& p, int r, int mt, int nt, int et) {
+    const int rows = min(BM, p.m - mt * BM);
+    const long long vpr = p.k / 8;   // 16-byte vectors per row
+    const long long total = rows * vpr;
+    const long long Q = static_cast<long long>(p.R) * p.n_tiles;
+    const long long qi = static_cast<long long>(r) * p.n_tiles + nt;
+    const long long v0 = total * qi / Q, v1 = total * (qi + 1) / Q;
+    for (long long vv = v0 + et; vv < v1; vv += 32 * NUM_EPI_WARPS) {
+        const int lr = static_cast<int>(vv / vpr);
+        const long long c = vv - lr * vpr;
+        const int g = mt * BM + lr;
+        const int s = g / p.rows_per_rank;
+        const int l = g - s * p.rows_per_rank;
+        const uint4 val = __ldg(reinterpret_cast<const uint4*>(p.gsrc[s] + static_cast<long long>(l) * p.k + c * 8));
+        const long long off = static_cast<long long>(g) * p.k + c * 8;
+        for (int d = 0; d < p.R; ++d)
+            if (p.gdst[d] != nullptr) __stcs(reinterpret_cast<uint4*>(p.gdst[d] + off), val);
+    }
+}
+
 // ------------------------------------------------------------ the kernel ---
 
+// Shared-memory rings.  AR/RS/AG: one ring of SA stages holding an A and a B
+// tile each (TMA fills both, the MMA frees both).  w8A16: three rings — A
+// tiles (TMA -> MMA), raw int8 W tiles (TMA -> dequant warps) and fp16 B
+// tiles (dequant warps -> MMA) — so TMA can run SR k-blocks ahead while the
+// dequantisation and the MMA work on earlier ones.
 template <int OP>
 struct Cfg {
-    static constexpr int STAGES = (OP == OP_W8) ? 3 : 4;
-    static constexpr int WARPS = 2 + NUM_EPI_WARPS + ((OP == OP_W8) ? NUM_XFORM_WARPS : 0);
+    static constexpr bool W8 = (OP == OP_W8);
+    static constexpr int SA = 4;                 // A (+B) stages
+    static constexpr int SB = W8 ? 2 : 4;        // B stages (shared with A except for w8A16)
+    static constexpr int SR = W8 ? 4 : 0;        // raw int8 stages
+    static constexpr int WARPS = 2 + NUM_EPI_WARPS + (W8 ? NUM_XFORM_WARPS : 0);
     static constexpr int THREADS = WARPS * 32;
-    static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES + ((OP == OP_W8) ? RAW_STAGE_BYTES : 0);
     static constexpr int EPI_BYTES = NUM_EPI_WARPS * 2 * EPI_BUF_BYTES;
-    static constexpr int BAR_BYTES = 256;
-    static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
+    static constexpr int BAR_BYTES = 512;
+    static constexpr int SMEM = 1024 + SA * A_STAGE_BYTES + SB * B_STAGE_BYTES + SR * RAW_STAGE_BYTES + EPI_BYTES +
+                                BAR_BYTES;
 };
 
 template <int OP, bool BF16>
 __global__ void __launch_bounds__(Cfg<OP>::THREADS, 1) coc_fused_kernel(const __grid_constant__ KParams p) {
     using C = Cfg<OP>;
-    constexpr int S = C::STAGES;
+    constexpr int S = C::SA;
+    constexpr bool W8 = C::W8;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-    uint8_t* a_st = smem;                                  // S x 16 KiB
-    uint8_t* b_st = a_st + S * A_STAGE_BYTES;              // S x 32 KiB
-    uint8_t* raw_st = b_st + S * B_STAGE_BYTES;            // S x 16 KiB (w8A16)
-    uint8_t* epi = raw_st + ((OP == OP_W8) ? S * RAW_STAGE_BYTES : 0);
+    uint8_t* a_st = smem;                                  // SA x 16 KiB
+    uint8_t* b_st = a_st + C::SA * A_STAGE_BYTES;          // SB x 32 KiB
+    uint8_t* raw_st = b_st + C::SB * B_STAGE_BYTES;        // SR x 16 KiB (w8A16)
+    uint8_t* epi = raw_st + C::SR * RAW_STAGE_BYTES;
     uint64_t* bars = reinterpret_cast<uint64_t*>(epi + C::EPI_BYTES);
-    uint64_t* full = bars;             // [S]  stage ready for the MMA
-    uint64_t* empty = bars + S;        // [S]  stage consumed by the MMA
-    uint64_t* rawfull = bars + 2 * S;  // [S]  w8A16: raw int8 + A tile landed
-    uint64_t* accf = bars + 3 * S;     // [2]  accumulator ready for the epilogue
+    uint64_t* full = bars;             // [SA] A (+B) stage landed
+    uint64_t* empty = full + C::SA;    // [SA] A (+B) stage consumed by the MMA
+    uint64_t* bfull = empty + C::SA;   // [SB] w8A16: fp16 B stage written by the dequant warps
+    uint64_t* bempty = bfull + C::SB;  // [SB] w8A16: fp16 B stage consumed by the MMA
+    uint64_t* rfull = bempty + C::SB;  // [SR] w8A16: raw int8 tile landed
+    uint64_t* rempty = rfull + C::SR;  // [SR] w8A16: raw int8 tile read by the dequant warps
+    uint64_t* accf = rempty + C::SR;   // [2]  accumulator ready for the epilogue
     uint64_t* acce = accf + 2;         // [2]  accumulator drained by the epilogue
     uint64_t* never = acce + 2;        // [1]  nothing arrives here (fault-injection test)
     uint64_t* drain = never + 1;       // [1]  MMA drain before TMEM release
@@ -323,10 +360,17 @@ __global__ void __launch_bounds__(Cfg<OP>::THREADS, 1) coc_fused_kernel(const __
     const Ctl ctl{abort_word, p.status};
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(smem_u32(&full[s]), (OP == OP_W8) ? NUM_XFORM_WARPS : 1);
+        for (int s = 0; s < C::SA; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&empty[s]), 1);
-            mbar_init(smem_u32(&rawfull[s]), 1);
+        }
+        for (int s = 0; s < C::SB; ++s) {
+            mbar_init(smem_u32(&bfull[s]), NUM_XFORM_WARPS);
+            mbar_init(smem_u32(&bempty[s]), 1);
+        }
+        for (int s = 0; s < C::SR; ++s) {
+            mbar_init(smem_u32(&rfull[s]), 1);
+            mbar_init(smem_u32(&rempty[s]), NUM_XFORM_WARPS);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&accf[b]), 1);
@@ -353,29 +397,34 @@ __global__ void __launch_bounds__(Cfg<OP>::THREADS, 1) coc_fused_kernel(const __
         if (lane == 0) {
             for (int i = 0; i < p.num_kshards && i < COC_MAX_RANKS; ++i) prefetch_tmap(&p.tm_a[i]);
         }
-        uint32_t stage = 0, phase = 0;
-        uint32_t filled = 0, fill_parity = 0;   // per-stage bit masks of the last fill
+        uint32_t stage = 0, phase = 0, rstage = 0, rphase = 0;
+        uint32_t filled = 0, fill_parity = 0;     // per-stage bit masks of the last fill (A ring)
+        uint32_t rfilled = 0, rfill_parity = 0;   // same for the raw int8 ring
         bool ok = true;
         for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
             int r, mt, nt;
             decode_unit<OP>(p, u, r, mt, nt);
+            // AllGather with whole-tile boxes: the tile's shard and local row
+            int a_shard = 0, a_row = 0;
+            if constexpr (OP == OP_AG) {
+                a_shard = min(mt * BM / p.rows_per_rank, p.R - 1);
+                a_row = mt * BM - a_shard * p.rows_per_rank;
+            }
             for (int ks = 0; ok && ks < p.num_kshards; ++ks) {
                 for (int kb = 0; kb < p.kblocks; ++kb) {
                     ok = warp_wait(smem_u32(&empty[stage]), phase ^ 1u, ctl, 0x100u + stage);
                     if (!ok) break;
+                    const int kc = kb * BK;
                     if (lane == 0) {
-                        const uint32_t fb = smem_u32((OP == OP_W8) ? &rawfull[stage] : &full[stage]);
+                        const uint32_t fb = smem_u32(&full[stage]);
                         const uint32_t a_dst = smem_u32(a_st + stage * A_STAGE_BYTES);
-                        const int kc = kb * BK;
-                        if constexpr (OP == OP_W8) {
-                            mbar_expect_tx(fb, A_STAGE_BYTES + RAW_STAGE_BYTES);
-                        } else {
-                            mbar_expect_tx(fb, A_STAGE_BYTES + B_STAGE_BYTES);
-                        }
+                        mbar_expect_tx(fb, W8 ? A_STAGE_BYTES : A_STAGE_BYTES + B_STAGE_BYTES);
                         if constexpr (OP == OP_AG) {
                             // gathered rows -> (shard, local row); rows past the
                             // end read beyond the last shard and are zero-filled
-                            for (int rb = 0; rb < BM; rb += p.a_box_rows) {
+                            if (p.a_box_rows == BM) {
+                                tma_load_2d(a_dst, &p.tm_a[a_shard], kc, a_row, fb);
+                            } else for (int rb = 0; rb < BM; rb += p.a_box_rows) {
                                 const int g = mt * BM + rb;
                                 int s = g / p.rows_per_rank;
                                 if (s > p.R - 1) s = p.R - 1;
@@ -384,10 +433,8 @@ __global__ void __launch_bounds__(Cfg<OP>::THREADS, 1) coc_fused_kernel(const __
                         } else {
                             tma_load_2d(a_dst, &p.tm_a[ks], kc, mt * BM, fb);
                         }
-                        const CUtensorMap* bm = &p.tm_b[(OP == OP_AG) ? r : ks];
-                        if constexpr (OP == OP_W8) {
-                            tma_load_2d(smem_u32(raw_st + stage * RAW_STAGE_BYTES), bm, nt * BN, kc, fb);
-                        } else {
+                        if constexpr (!W8) {
+                            const CUtensorMap* bm = &p.tm_b[(OP == OP_AG) ? r : ks];
                             const uint32_t b_dst = smem_u32(b_st + stage * B_STAGE_BYTES);
 #pragma unroll
                             for (int j = 0; j < BN / 64; ++j)
@@ -398,22 +445,34 @@ __global__ void __launch_bounds__(Cfg<OP>::THREADS, 1) coc_fused_kernel(const __
                     }
                     __syncwarp();
                     if (++stage == S) { stage = 0; phase ^= 1u; }
+                    if constexpr (W8) {
+                        // raw int8 W tile into its own ring
+                        ok = warp_wait(smem_u32(&rempty[rstage]), rphase ^ 1u, ctl, 0x140u + rstage);
+                        if (!ok) break;
+                        if (lane == 0) {
+                            const uint32_t rb = smem_u32(&rfull[rstage]);
+                            mbar_expect_tx(rb, RAW_STAGE_BYTES);
+                            tma_load_2d(smem_u32(raw_st + rstage * RAW_STAGE_BYTES), &p.tm_b[ks], nt * BN, kc, rb);
+                            rfilled |= 1u << rstage;
+                            rfill_parity = (rfill_parity & ~(1u << rstage)) | (rphase << rstage);
+                        }
+                        __syncwarp();
+                        if (++rstage == C::SR) { rstage = 0; rphase ^= 1u; }
+                    }
                 }
             }
         }
         if (!ok && lane == 0) {
             // leave no TMA load in flight into shared memory
-            for (int s = 0; s < S; ++s) {
-                if (filled & (1u << s)) {
-                    const uint32_t fb = smem_u32((OP == OP_W8) ? &rawfull[s] : &full[s]);
-                    drain_wait(fb, (fill_parity >> s) & 1u, kDrainNs);
-                }
-            }
+            for (int s = 0; s < C::SA; ++s)
+                if (filled & (1u << s)) drain_wait(smem_u32(&full[s]), (fill_parity >> s) & 1u, kDrainNs);
+            for (int s = 0; s < C::SR; ++s)
+                if (rfilled & (1u << s)) drain_wait(smem_u32(&rfull[s]), (rfill_parity >> s) & 1u, kDrainNs);
         }
     } else if (warp == 1) {
         // ================================================= MMA issuer ===
         constexpr uint32_t idesc = make_idesc(BF16, BM, BN);
-        uint32_t stage = 0, phase = 0;
+        uint32_t stage = 0, phase = 0, bstage = 0, bphase = 0;
         int acc_i = 0;
         bool ok = true;
         for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
@@ -425,11 +484,13 @@ __global__ void __launch_bounds__(Cfg<OP>::THREADS, 1) coc_fused_kernel(const __
             const uint32_t d_tmem = tmem_base + buf * BN;
             for (int i = 0; i < total_kb; ++i) {
                 ok = warp_wait(smem_u32(&full[stage]), phase, ctl, 0x210u + stage);
+                if (W8 && ok) ok = warp_wait(smem_u32(&bfull[bstage]), bphase, ctl, 0x220u + bstage);
                 if (!ok) break;
                 tc_fence_after();
                 if (lane == 0) {
                     const uint64_t ad = make_sdesc(smem_u32(a_st + stage * A_STAGE_BYTES), 16, 1024);
-                    const uint64_t bd = make_sdesc(smem_u32(b_st + stage * B_STAGE_BYTES), 64 * BK * 2, 1024);
+                    const uint64_t bd =
+                        make_sdesc(smem_u32(b_st + (W8 ? bstage : stage) * B_STAGE_BYTES), 64 * BK * 2, 1024);
 #pragma unroll
                     for (int kk = 0; kk < BK / UMMA_K; ++kk) {
                         // A: +32 bytes per 16-element k step inside the 128-byte swizzle row
@@ -438,9 +499,11 @@ __global__ void __launch_bounds__(Cfg<OP>::THREADS, 1) coc_fused_kernel(const __
                                    idesc, (i > 0 || kk > 0) ? 1u : 0u);
                     }
                     tc_commit(smem_u32(&empty[stage]));
+                    if (W8) tc_commit(smem_u32(&bempty[bstage]));
                 }
                 __syncwarp();
                 if (++stage == S) { stage = 0; phase ^= 1u; }
+                if (W8 && ++bstage == C::SB) { bstage = 0; bphase ^= 1u; }
             }
             if (!ok) break;
             if (lane == 0) tc_commit(smem_u32(&accf[buf]));
@@ -525,29 +588,7 @@ __global__ void __launch_bounds__(Cfg<OP>::THREADS, 1) coc_fused_kernel(const __
             }
             ++acc_i;
             if constexpr (OP == OP_AG) {
-                if (p.has_gather) {
-                    // V2: this unit's share of the m-tile's gathered rows.  The
-                    // tile's rows are one contiguous run of the gathered
-                    // matrix; it is cut into R * n_tiles equal pieces, one per
-                    // unit that works on this m-tile.
-                    const int rows = min(BM, p.m - mt * BM);
-                    const long long vpr = p.k / 8;              // 16-byte vectors per row
-                    const long long total = rows * vpr;
-                    const long long Q = static_cast<long long>(p.R) * p.n_tiles;
-                    const long long qi = static_cast<long long>(r) * p.n_tiles + nt;
-                    const long long v0 = total * qi / Q, v1 = total * (qi + 1) / Q;
-                    for (long long vv = v0 + et; vv < v1; vv += 32 * NUM_EPI_WARPS) {
-                        const int lr = static_cast<int>(vv / vpr);
-                        const long long c = vv - lr * vpr;
-                        const int g = mt * BM + lr;
-                        const int s = g / p.rows_per_rank;
-                        const int l = g - s * p.rows_per_rank;
-                        const uint4 val = __ldg(reinterpret_cast<const uint4*>(p.gsrc[s] + (static_cast<long long>(l) * p.k) + c * 8));
-                        const long long off = static_cast<long long>(g) * p.k + c * 8;
-                        for (int d = 0; d < p.R; ++d)
-                            if (p.gdst[d] != nullptr) __stcs(reinterpret_cast<uint4*>(p.gdst[d] + off), val);
-                    }
-                }
+                if (p.has_gather) gather_slice(p, r, mt, nt, et);
             }
         }
         if (lane == 0) bulk_wait_all();
@@ -555,11 +596,14 @@ __global__ void __launch_bounds__(Cfg<OP>::THREADS, 1) coc_fused_kernel(const __
     } else if constexpr (OP == OP_W8) {
         // ================================================= w8A16 dequant ===
         // Thread tt owns 8 consecutive columns (cc) of the 256-wide tile and
-        // rows kr0, kr0 + 4, ..., of the 64-row k-block.
+        // the k-block rows kr0, kr0 + R_STEP, ... (R_STEP = dequant warps).
+        constexpr int R_STEP = NUM_XFORM_WARPS;
+        constexpr int ROWS = BK / R_STEP;
         const int tt = (warp - 2 - NUM_EPI_WARPS) * 32 + lane;
         const int cc = tt & 31;
         const int kr0 = tt >> 5;
-        uint32_t stage = 0, phase = 0;
+        const int blk = cc >> 3, c16 = cc & 7;
+        uint32_t rstage = 0, rphase = 0, bstage = 0, bphase = 0;
         bool ok = true;
         for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
             int r, mt, nt;
@@ -588,17 +632,22 @@ __global__ void __launch_bounds__(Cfg<OP>::THREADS, 1) coc_fused_kernel(const __
                             for (int e = 0; e < 4; ++e) s2[e] = __float2half2_rn(0.f);   // columns past n
                         }
                     }
-                    ok = warp_wait(smem_u32(&rawfull[stage]), phase, ctl, 0x400u + stage);
+                    ok = warp_wait(smem_u32(&rfull[rstage]), rphase, ctl, 0x400u + rstage);
+                    if (ok) ok = warp_wait(smem_u32(&bempty[bstage]), bphase ^ 1u, ctl, 0x410u + bstage);
                     if (!ok) break;
-                    const uint8_t* raw = raw_st + stage * RAW_STAGE_BYTES;
-                    uint8_t* bst = b_st + stage * B_STAGE_BYTES;
-#pragma unroll 4
-                    for (int i = 0; i < BK / 4; ++i) {
-                        const int kk = kr0 + 4 * i;
-                        const uint2 q8 = *reinterpret_cast<const uint2*>(raw + kk * BN + cc * 8);
+                    const uint8_t* raw = raw_st + rstage * RAW_STAGE_BYTES;
+                    uint8_t* bst = b_st + bstage * B_STAGE_BYTES + blk * (64 * BK * 2);
+                    // all loads first, then convert and store (independent work per row)
+                    uint2 q8[ROWS];
+#pragma unroll
+                    for (int i = 0; i < ROWS; ++i)
+                        q8[i] = *reinterpret_cast<const uint2*>(raw + (kr0 + R_STEP * i) * BN + cc * 8);
+#pragma unroll
+                    for (int i = 0; i < ROWS; ++i) {
+                        const int kk = kr0 + R_STEP * i;
                         __half2 h[4];
-                        i8x4_to_h2x2(q8.x, h[0], h[1]);
-                        i8x4_to_h2x2(q8.y, h[2], h[3]);
+                        i8x4_to_h2x2(q8[i].x, h[0], h[1]);
+                        i8x4_to_h2x2(q8[i].y, h[2], h[3]);
                         uint4 o;
                         __half2 m0 = __hmul2_rn(h[0], s2[0]), m1 = __hmul2_rn(h[1], s2[1]);
                         __half2 m2 = __hmul2_rn(h[2], s2[2]), m3 = __hmul2_rn(h[3], s2[3]);
@@ -608,13 +657,16 @@ __global__ void __launch_bounds__(Cfg<OP>::THREADS, 1) coc_fused_kernel(const __
                         o.w = *reinterpret_cast<uint32_t*>(&m3);
                         // MN-major 128-byte-swizzled B layout: 64-column blocks of
                         // 64 rows x 128 bytes, 16-byte chunks XOR-ed with row % 8
-                        const int blk = cc >> 3, c16 = cc & 7;
-                        *reinterpret_cast<uint4*>(bst + blk * (64 * BK * 2) + kk * 128 + ((c16 ^ (kk & 7)) << 4)) = o;
+                        *reinterpret_cast<uint4*>(bst + kk * 128 + ((c16 ^ (kk & 7)) << 4)) = o;
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&full[stage]));
-                    if (++stage == S) { stage = 0; phase ^= 1u; }
+                    if (lane == 0) {
+                        mbar_arrive(smem_u32(&rempty[rstage]));
+                        mbar_arrive(smem_u32(&bfull[bstage]));
+                    }
+                    if (++rstage == C::SR) { rstage = 0; rphase ^= 1u; }
+                    if (++bstage == C::SB) { bstage = 0; bphase ^= 1u; }
                 }
             }
         }
@@ -656,6 +708,7 @@ cudaError_t launch(int op, bool bf16, const KParams& p, int grid, cudaStream_t s
 }
 
 size_t smem_bytes(int op) { return op == OP_W8 ? Cfg<OP_W8>::SMEM : Cfg<OP_AR>::SMEM; }
+static_assert(Cfg<OP_AR>::SMEM <= 232448 && Cfg<OP_W8>::SMEM <= 232448, "shared memory above 227 KiB");
 int block_threads(int op) { return op == OP_W8 ? Cfg<OP_W8>::THREADS : Cfg<OP_AR>::THREADS; }
 
 }  // namespace coc
