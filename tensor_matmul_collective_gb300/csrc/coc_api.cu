@@ -4,6 +4,7 @@
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <unordered_map>
@@ -35,6 +36,7 @@ struct DeviceState {
     int sm_count = 0;
     int cc_major = 0, cc_minor = 0;
     unsigned* status = nullptr;
+    int max_pairs[4][2] = {{-1, -1}, {-1, -1}, {-1, -1}, {-1, -1}};   // per op, per bf16; -1 = not queried
 };
 
 std::mutex g_mu;
@@ -125,9 +127,28 @@ coc_status_t check_ptrs(const void* const* arr, int R, bool needed, const char* 
     return COC_OK;
 }
 
-int chunk_m_tiles(int64_t m, int chunks) {
+int chunk_m_tiles(int64_t m, int chunks, int tile_m) {
     const int64_t rows = m / chunks;
-    return (rows > 0 && rows % BM == 0) ? static_cast<int>(rows / BM) : 0;
+    return (rows > 0 && rows % tile_m == 0) ? static_cast<int>(rows / tile_m) : 0;
+}
+
+// The 2-SM variant (a CTA pair per 256-row tile) is used once the output has
+// more than one 128-row tile, except for w8A16, whose single-CTA variant is
+// faster as measured.  COC_PAIR=0/1 forces a variant (tuning only).
+bool use_pair(int op, int64_t m) {
+    static const int forced = [] {
+        const char* e = std::getenv("COC_PAIR");
+        return e == nullptr ? -1 : (std::atoi(e) != 0 ? 1 : 0);
+    }();
+    if (forced >= 0) return forced == 1;
+    return op != OP_W8 && m > BM;
+}
+
+int pairs_available(DeviceState* ds, int op, bool bf16) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    int& v = ds->max_pairs[op][bf16 ? 1 : 0];
+    if (v < 0) v = max_pairs(op, bf16);
+    return v;
 }
 
 int largest_pow2_divisor_le(int64_t v, int cap) {
@@ -140,11 +161,18 @@ CUtensorMapDataType tma_dtype(coc_dtype_t dt) {
     return dt == COC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
 }
 
-coc_status_t launch_checked(int op, bool bf16, KParams& p, DeviceState* ds, cudaStream_t stream) {
+coc_status_t launch_checked(int op, bool bf16, bool pair, KParams& p, DeviceState* ds, cudaStream_t stream) {
     p.status = ds->status;
     p.inject_timeout = g_inject.load();
-    const int grid = p.units < ds->sm_count ? p.units : ds->sm_count;
-    cudaError_t e = launch(op, bf16, p, grid, stream);
+    int grid;
+    if (pair) {
+        const int pairs = pairs_available(ds, op, bf16);
+        if (pairs <= 0) return fail(COC_ERR_CUDA, "no co-resident CTA pair fits on this device");
+        grid = 2 * (p.units < pairs ? p.units : pairs);
+    } else {
+        grid = p.units < ds->sm_count ? p.units : ds->sm_count;
+    }
+    cudaError_t e = launch(op, bf16, pair, p, grid, stream);
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
     return COC_OK;
 }
@@ -161,11 +189,13 @@ coc_status_t row_parallel(int op, int R, int64_t m, int64_t n, int64_t ks, const
     p.n = static_cast<int>(n);
     p.k = static_cast<int>(ks);
     p.num_kshards = R;
+    const bool pair = use_pair(op, m);
+    const int tile_m = pair ? 2 * BM : BM;
     p.kblocks = static_cast<int>((ks + BK - 1) / BK);
-    p.m_tiles = static_cast<int>((m + BM - 1) / BM);
+    p.m_tiles = static_cast<int>((m + tile_m - 1) / tile_m);
     p.n_tiles = static_cast<int>((n + BN - 1) / BN);
     p.units = p.m_tiles * p.n_tiles;
-    p.chunk_mt = chunk_m_tiles(m, chunks);
+    p.chunk_mt = chunk_m_tiles(m, chunks, tile_m);
     p.rows_per_rank = static_cast<int>(m / R);
     p.store_rows = 32;
     p.a_box_rows = BM;
@@ -183,7 +213,8 @@ coc_status_t row_parallel(int op, int R, int64_t m, int64_t n, int64_t ks, const
         for (int r = 0; r < R; ++r) {
             if ((st = encode(&p.tm_a[r], adt, x[r], ks, m, ks * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B)) != COC_OK) return st;
             if (w8) {
-                st = encode(&p.tm_b[r], CU_TENSOR_MAP_DATA_TYPE_UINT8, w[r], n, ks, n, BN, BK, CU_TENSOR_MAP_SWIZZLE_NONE);
+                st = encode(&p.tm_b[r], CU_TENSOR_MAP_DATA_TYPE_UINT8, w[r], n, ks, n, pair ? BN / 2 : BN, BK,
+                            CU_TENSOR_MAP_SWIZZLE_NONE);
             } else {
                 st = encode(&p.tm_b[r], adt, w[r], n, ks, n * 2, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B);
             }
@@ -197,7 +228,7 @@ coc_status_t row_parallel(int op, int R, int64_t m, int64_t n, int64_t ks, const
     }
     if (w8)
         for (int r = 0; r < R; ++r) p.scale[r] = static_cast<const uint16_t*>(scale[r]);
-    return launch_checked(op, dt == COC_BF16 && !w8, p, ds, stream);
+    return launch_checked(op, dt == COC_BF16 && !w8, pair, p, ds, stream);
 }
 
 coc_status_t validate_row_parallel(int R, int64_t m, int64_t n, int64_t ks, const void* const* x, const void* const* w,
@@ -316,11 +347,13 @@ coc_status_t all_gather(int R, int64_t ms, int64_t ns, int64_t k, const void* co
     p.n = static_cast<int>(ns);
     p.k = static_cast<int>(k);
     p.num_kshards = 1;
+    const bool pair = use_pair(OP_AG, m);
+    const int tile_m = pair ? 2 * BM : BM;
     p.kblocks = static_cast<int>((k + BK - 1) / BK);
-    p.m_tiles = static_cast<int>((m + BM - 1) / BM);
+    p.m_tiles = static_cast<int>((m + tile_m - 1) / tile_m);
     p.n_tiles = static_cast<int>((ns + BN - 1) / BN);
     p.units = R * p.m_tiles * p.n_tiles;
-    p.chunk_mt = chunk_m_tiles(m, chunks);
+    p.chunk_mt = chunk_m_tiles(m, chunks, tile_m);
     p.rows_per_rank = static_cast<int>(ms);
     p.a_box_rows = largest_pow2_divisor_le(ms, BM);
     p.store_rows = 32;
@@ -339,7 +372,7 @@ coc_status_t all_gather(int R, int64_t ms, int64_t ns, int64_t k, const void* co
         p.gsrc[r] = static_cast<const uint16_t*>(x[r]);
         p.gdst[r] = v2 ? static_cast<uint16_t*>(gathered[r]) : nullptr;
     }
-    return launch_checked(OP_AG, dt == COC_BF16, p, ds, stream);
+    return launch_checked(OP_AG, dt == COC_BF16, pair, p, ds, stream);
 }
 
 }  // namespace

@@ -67,9 +67,11 @@ coc_status_t validate_all_reduce_args(int R, int64_t m, int64_t n, int64_t k_sha
                                       int deterministic);
 coc_status_t report_error(coc_status_t st, const char* msg);
 
-// Host-side launch helpers implemented in coc_kernel.cu.
-cudaError_t launch(int op, bool bf16, const KParams& p, int grid, cudaStream_t stream);
-size_t smem_bytes(int op);
-int block_threads(int op);
+// Host-side launch helpers implemented in coc_kernel.cu.  `pair` selects the
+// 2-SM variant (a cluster of two CTAs per 256-row tile; grid = 2 x pairs);
+// otherwise one CTA per 128-row tile.
+cudaError_t launch(int op, bool bf16, bool pair, const KParams& p, int grid, cudaStream_t stream);
+// Co-resident CTA pairs the 2-SM variant can have on the current device.
+int max_pairs(int op, bool bf16);
 
 }  // namespace coc

@@ -169,6 +169,94 @@ __device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&v)[32]
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// ---- CTA pairs (2-SM tcgen05 MMA) ----
+//
+// A cluster of two CTAs on neighbouring SMs computes one 256-row tile: each
+// CTA holds 128 rows of A and 128 of the 256 B columns in its own shared
+// memory and 128 accumulator lanes in its own TMEM; the even CTA ("leader")
+// issues the MMAs for both.  The peer's TMA loads complete on the leader's
+// barriers, the leader's commits arrive on both CTAs' barriers.
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_id() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_count() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// TMA load into this CTA's shared memory, completing on a barrier that may
+// live in the peer CTA (cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                                 uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar_cluster)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_mma_f16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive on the barrier at this offset in both CTAs of the pair once the
+// issuing thread's MMAs are complete.
+__device__ __forceinline__ void tc_commit_pair_both(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            bar),
+        "h"(static_cast<uint16_t>(3))
+        : "memory");
+}
+__device__ __forceinline__ void tc_commit_pair_local(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 // Instruction descriptor, kind::f16: D fp32, A/B both fp16 or both bf16,
 // A K-major, B MN-major ("transposed"), N >> 3 at bit 17, M >> 4 at bit 24.
 __host__ __device__ constexpr uint32_t make_idesc(bool bf16, int M, int N) {
@@ -197,13 +285,21 @@ __device__ __noinline__ void raise_timeout(const Ctl& c, unsigned where) {
     atomicCAS(c.status + 2, 0u, blockIdx.x + 1u);
 }
 
+template <bool CLUSTER>
+__device__ __forceinline__ bool try_wait_scoped(uint32_t bar, uint32_t parity) {
+    if constexpr (CLUSTER) return mbar_try_wait_cluster(bar, parity);
+    else return mbar_try_wait(bar, parity);
+}
+
 // Wait for phase `parity` of `bar`.  False if the CTA is aborting or the wait
-// ran out (which starts the abort).
+// ran out (which starts the abort).  CLUSTER: acquire at cluster scope (the
+// phase may have been completed by the peer CTA).
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const Ctl& c,
                                              unsigned where, unsigned long long limit_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (try_wait_scoped<CLUSTER>(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
-    while (!mbar_try_wait(bar, parity)) {
+    while (!try_wait_scoped<CLUSTER>(bar, parity)) {
         if (*c.abort_flag) return false;
         if (globaltimer() - t0 > limit_ns) {
             raise_timeout(c, where);
@@ -224,8 +320,9 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, unsign
 }
 
 // Whole-warp wait with a warp-uniform outcome.
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const Ctl& c, unsigned where) {
-    const bool ok = wait_bounded(bar, parity, c, where, COC_WAIT_NS);
+    const bool ok = wait_bounded<CLUSTER>(bar, parity, c, where, COC_WAIT_NS);
     return __all_sync(0xffffffffu, ok);
 }
 
@@ -288,17 +385,18 @@ __device__ __forceinline__ void i8x4_to_h2x2(uint32_t w, __half2& h01, __half2& 
 // of the gathered matrix; it is cut into R * n_tiles equal pieces, one per
 // work unit of this m-tile, so the copy is spread over the whole kernel.
 // Kept out of line: it runs once per unit, after the tile's epilogue.
-__device__ __noinline__ void gather_slice(const KParams& p, int r, int mt, int nt, int et) {
-    const int rows = min(BM, p.m - mt * BM);
+__device__ __noinline__ void gather_slice(const KParams& p, int r, int mt, int nt, int tile_m, int tid,
+                                          int nthreads) {
+    const int rows = min(tile_m, p.m - mt * tile_m);
     const long long vpr = p.k / 8;   // 16-byte vectors per row
     const long long total = rows * vpr;
     const long long Q = static_cast<long long>(p.R) * p.n_tiles;
     const long long qi = static_cast<long long>(r) * p.n_tiles + nt;
     const long long v0 = total * qi / Q, v1 = total * (qi + 1) / Q;
-    for (long long vv = v0 + et; vv < v1; vv += 32 * NUM_EPI_WARPS) {
+    for (long long vv = v0 + tid; vv < v1; vv += nthreads) {
         const int lr = static_cast<int>(vv / vpr);
         const long long c = vv - lr * vpr;
-        const int g = mt * BM + lr;
+        const int g = mt * tile_m + lr;
         const int s = g / p.rows_per_rank;
         const int l = g - s * p.rows_per_rank;
         const uint4 val = __ldg(reinterpret_cast<const uint4*>(p.gsrc[s] + static_cast<long long>(l) * p.k + c * 8));
@@ -314,42 +412,48 @@ __device__ __noinline__ void gather_slice(const KParams& p, int r, int mt, int n
 // tile each (TMA fills both, the MMA frees both).  w8A16: three rings — A
 // tiles (TMA -> MMA), raw int8 W tiles (TMA -> dequant warps) and fp16 B
 // tiles (dequant warps -> MMA) — so TMA can run SR k-blocks ahead while the
-// dequantisation and the MMA work on earlier ones.
-template <int OP>
+// dequantisation and the MMA work on earlier ones.  With PAIR each CTA holds
+// half of the B columns, which halves B and raw stage sizes.
+template <int OP, bool PAIR>
 struct Cfg {
     static constexpr bool W8 = (OP == OP_W8);
-    static constexpr int SA = 4;                 // A (+B) stages
-    static constexpr int SB = W8 ? 2 : 4;        // B stages (shared with A except for w8A16)
-    static constexpr int SR = W8 ? 4 : 0;        // raw int8 stages
+    static constexpr int TILE_M = PAIR ? 2 * BM : BM;        // rows per work unit
+    static constexpr int BN_CTA = PAIR ? BN / 2 : BN;        // B columns held by one CTA
+    static constexpr int B_BYTES = BN_CTA * BK * 2;          // fp16/bf16 B stage
+    static constexpr int RAW_BYTES = BN_CTA * BK;            // int8 W stage
+    static constexpr int SA = W8 ? 4 : (PAIR ? 6 : 4);       // A (+B) stages
+    static constexpr int SB = W8 ? (PAIR ? 3 : 2) : SA;      // B stages (shared with A except for w8A16)
+    static constexpr int SR = W8 ? (PAIR ? 6 : 4) : 0;       // raw int8 stages
     static constexpr int WARPS = 2 + NUM_EPI_WARPS + (W8 ? NUM_XFORM_WARPS : 0);
     static constexpr int THREADS = WARPS * 32;
     static constexpr int EPI_BYTES = NUM_EPI_WARPS * 2 * EPI_BUF_BYTES;
     static constexpr int BAR_BYTES = 512;
-    static constexpr int SMEM = 1024 + SA * A_STAGE_BYTES + SB * B_STAGE_BYTES + SR * RAW_STAGE_BYTES + EPI_BYTES +
-                                BAR_BYTES;
+    static constexpr int SMEM = 1024 + SA * A_STAGE_BYTES + (W8 ? SB * B_BYTES : SA * B_BYTES) + SR * RAW_BYTES +
+                                EPI_BYTES + BAR_BYTES;
 };
 
-template <int OP, bool BF16>
-__global__ void __launch_bounds__(Cfg<OP>::THREADS, 1) coc_fused_kernel(const __grid_constant__ KParams p) {
-    using C = Cfg<OP>;
+template <int OP, bool BF16, bool PAIR>
+__global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(const __grid_constant__ KParams p) {
+    using C = Cfg<OP, PAIR>;
     constexpr int S = C::SA;
     constexpr bool W8 = C::W8;
+    constexpr int TILE_M = C::TILE_M;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-    uint8_t* a_st = smem;                                  // SA x 16 KiB
-    uint8_t* b_st = a_st + C::SA * A_STAGE_BYTES;          // SB x 32 KiB
-    uint8_t* raw_st = b_st + C::SB * B_STAGE_BYTES;        // SR x 16 KiB (w8A16)
-    uint8_t* epi = raw_st + C::SR * RAW_STAGE_BYTES;
+    uint8_t* a_st = smem;                                        // SA x 16 KiB
+    uint8_t* b_st = a_st + C::SA * A_STAGE_BYTES;                // (W8 ? SB : SA) x B_BYTES
+    uint8_t* raw_st = b_st + (W8 ? C::SB : C::SA) * C::B_BYTES;  // SR x RAW_BYTES (w8A16)
+    uint8_t* epi = raw_st + C::SR * C::RAW_BYTES;
     uint64_t* bars = reinterpret_cast<uint64_t*>(epi + C::EPI_BYTES);
-    uint64_t* full = bars;             // [SA] A (+B) stage landed
+    uint64_t* full = bars;             // [SA] A (+B) stage landed (the leader's counts both CTAs' bytes)
     uint64_t* empty = full + C::SA;    // [SA] A (+B) stage consumed by the MMA
     uint64_t* bfull = empty + C::SA;   // [SB] w8A16: fp16 B stage written by the dequant warps
     uint64_t* bempty = bfull + C::SB;  // [SB] w8A16: fp16 B stage consumed by the MMA
     uint64_t* rfull = bempty + C::SB;  // [SR] w8A16: raw int8 tile landed
     uint64_t* rempty = rfull + C::SR;  // [SR] w8A16: raw int8 tile read by the dequant warps
     uint64_t* accf = rempty + C::SR;   // [2]  accumulator ready for the epilogue
-    uint64_t* acce = accf + 2;         // [2]  accumulator drained by the epilogue
+    uint64_t* acce = accf + 2;         // [2]  accumulator drained by the epilogue (leader: both CTAs)
     uint64_t* never = acce + 2;        // [1]  nothing arrives here (fault-injection test)
     uint64_t* drain = never + 1;       // [1]  MMA drain before TMEM release
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -358,6 +462,10 @@ __global__ void __launch_bounds__(Cfg<OP>::THREADS, 1) coc_fused_kernel(const __
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const Ctl ctl{abort_word, p.status};
+    const uint32_t rank = PAIR ? cluster_rank() : 0u;       // 0 = leader
+    const int first_unit = PAIR ? static_cast<int>(cluster_id()) : static_cast<int>(blockIdx.x);
+    const int unit_step = PAIR ? static_cast<int>(cluster_count()) : static_cast<int>(gridDim.x);
+    constexpr int NPAIR = PAIR ? 2 : 1;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::SA; ++s) {
@@ -365,7 +473,7 @@ __global__ void __launch_bounds__(Cfg<OP>::THREADS, 1) coc_fused_kernel(const __
             mbar_init(smem_u32(&empty[s]), 1);
         }
         for (int s = 0; s < C::SB; ++s) {
-            mbar_init(smem_u32(&bfull[s]), NUM_XFORM_WARPS);
+            mbar_init(smem_u32(&bfull[s]), NPAIR * NUM_XFORM_WARPS);
             mbar_init(smem_u32(&bempty[s]), 1);
         }
         for (int s = 0; s < C::SR; ++s) {
@@ -374,7 +482,7 @@ __global__ void __launch_bounds__(Cfg<OP>::THREADS, 1) coc_fused_kernel(const __
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&accf[b]), 1);
-            mbar_init(smem_u32(&acce[b]), NUM_EPI_WARPS);
+            mbar_init(smem_u32(&acce[b]), NPAIR * NUM_EPI_WARPS);
         }
         mbar_init(smem_u32(never), 1);
         mbar_init(smem_u32(drain), 1);
@@ -383,11 +491,18 @@ __global__ void __launch_bounds__(Cfg<OP>::THREADS, 1) coc_fused_kernel(const __
         fence_proxy_async_smem();
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), 2 * BN);   // two 128 x 256 fp32 accumulators = all 512 columns
-        tmem_relinquish();
+        // two 128-lane x 256-column fp32 accumulators = all 512 columns
+        if constexpr (PAIR) {
+            tmem_alloc_pair(smem_u32(tmem_slot), 2 * BN);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(tmem_slot), 2 * BN);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
-    __syncthreads();
+    if constexpr (PAIR) cluster_sync();   // both CTAs' barriers exist before any cross-CTA traffic
+    else __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int total_kb = p.num_kshards * p.kblocks;
@@ -400,15 +515,19 @@ __global__ void __launch_bounds__(Cfg<OP>::THREADS, 1) coc_fused_kernel(const __
         uint32_t stage = 0, phase = 0, rstage = 0, rphase = 0;
         uint32_t filled = 0, fill_parity = 0;     // per-stage bit masks of the last fill (A ring)
         uint32_t rfilled = 0, rfill_parity = 0;   // same for the raw int8 ring
+        // bytes the leader's full barrier receives per stage (both CTAs' loads)
+        constexpr uint32_t kFullBytes = NPAIR * (A_STAGE_BYTES + (W8 ? 0 : C::B_BYTES));
         bool ok = true;
-        for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+        for (int u = first_unit; ok && u < p.units; u += unit_step) {
             int r, mt, nt;
             decode_unit<OP>(p, u, r, mt, nt);
+            const int row_base = mt * TILE_M + static_cast<int>(rank) * BM;   // this CTA's first A row
+            const int col_base = nt * BN + static_cast<int>(rank) * C::BN_CTA;  // this CTA's first B column
             // AllGather with whole-tile boxes: the tile's shard and local row
             int a_shard = 0, a_row = 0;
             if constexpr (OP == OP_AG) {
-                a_shard = min(mt * BM / p.rows_per_rank, p.R - 1);
-                a_row = mt * BM - a_shard * p.rows_per_rank;
+                a_shard = min(row_base / p.rows_per_rank, p.R - 1);
+                a_row = row_base - a_shard * p.rows_per_rank;
             }
             for (int ks = 0; ok && ks < p.num_kshards; ++ks) {
                 for (int kb = 0; kb < p.kblocks; ++kb) {
@@ -416,29 +535,36 @@ __global__ void __launch_bounds__(Cfg<OP>::THREADS, 1) coc_fused_kernel(const __
                     if (!ok) break;
                     const int kc = kb * BK;
                     if (lane == 0) {
-                        const uint32_t fb = smem_u32(&full[stage]);
+                        const uint32_t fb_local = smem_u32(&full[stage]);
+                        const uint32_t fb = PAIR ? map_to_rank(fb_local, 0) : fb_local;
                         const uint32_t a_dst = smem_u32(a_st + stage * A_STAGE_BYTES);
-                        mbar_expect_tx(fb, W8 ? A_STAGE_BYTES : A_STAGE_BYTES + B_STAGE_BYTES);
+                        if (rank == 0) mbar_expect_tx(fb_local, kFullBytes);
+                        auto load = [&](uint32_t dst, const CUtensorMap* map, int c0, int c1) {
+                            if constexpr (PAIR) tma_load_2d_pair(dst, map, c0, c1, fb);
+                            else tma_load_2d(dst, map, c0, c1, fb);
+                        };
                         if constexpr (OP == OP_AG) {
                             // gathered rows -> (shard, local row); rows past the
                             // end read beyond the last shard and are zero-filled
                             if (p.a_box_rows == BM) {
-                                tma_load_2d(a_dst, &p.tm_a[a_shard], kc, a_row, fb);
-                            } else for (int rb = 0; rb < BM; rb += p.a_box_rows) {
-                                const int g = mt * BM + rb;
-                                int s = g / p.rows_per_rank;
-                                if (s > p.R - 1) s = p.R - 1;
-                                tma_load_2d(a_dst + rb * 128, &p.tm_a[s], kc, g - s * p.rows_per_rank, fb);
+                                load(a_dst, &p.tm_a[a_shard], kc, a_row);
+                            } else {
+                                for (int rb = 0; rb < BM; rb += p.a_box_rows) {
+                                    const int g = row_base + rb;
+                                    int sh = g / p.rows_per_rank;
+                                    if (sh > p.R - 1) sh = p.R - 1;
+                                    load(a_dst + rb * 128, &p.tm_a[sh], kc, g - sh * p.rows_per_rank);
+                                }
                             }
                         } else {
-                            tma_load_2d(a_dst, &p.tm_a[ks], kc, mt * BM, fb);
+                            load(a_dst, &p.tm_a[ks], kc, row_base);
                         }
                         if constexpr (!W8) {
                             const CUtensorMap* bm = &p.tm_b[(OP == OP_AG) ? r : ks];
-                            const uint32_t b_dst = smem_u32(b_st + stage * B_STAGE_BYTES);
+                            const uint32_t b_dst = smem_u32(b_st + stage * C::B_BYTES);
 #pragma unroll
-                            for (int j = 0; j < BN / 64; ++j)
-                                tma_load_2d(b_dst + j * (64 * BK * 2), bm, nt * BN + j * 64, kc, fb);
+                            for (int j = 0; j < C::BN_CTA / 64; ++j)
+                                load(b_dst + j * (64 * BK * 2), bm, col_base + j * 64, kc);
                         }
                         filled |= 1u << stage;
                         fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
@@ -446,13 +572,13 @@ __global__ void __launch_bounds__(Cfg<OP>::THREADS, 1) coc_fused_kernel(const __
                     __syncwarp();
                     if (++stage == S) { stage = 0; phase ^= 1u; }
                     if constexpr (W8) {
-                        // raw int8 W tile into its own ring
+                        // this CTA's raw int8 W columns into its own ring
                         ok = warp_wait(smem_u32(&rempty[rstage]), rphase ^ 1u, ctl, 0x140u + rstage);
                         if (!ok) break;
                         if (lane == 0) {
                             const uint32_t rb = smem_u32(&rfull[rstage]);
-                            mbar_expect_tx(rb, RAW_STAGE_BYTES);
-                            tma_load_2d(smem_u32(raw_st + rstage * RAW_STAGE_BYTES), &p.tm_b[ks], nt * BN, kc, rb);
+                            mbar_expect_tx(rb, C::RAW_BYTES);
+                            tma_load_2d(smem_u32(raw_st + rstage * C::RAW_BYTES), &p.tm_b[ks], col_base, kc, rb);
                             rfilled |= 1u << rstage;
                             rfill_parity = (rfill_parity & ~(1u << rstage)) | (rphase << rstage);
                         }
@@ -464,75 +590,98 @@ __global__ void __launch_bounds__(Cfg<OP>::THREADS, 1) coc_fused_kernel(const __
         }
         if (!ok && lane == 0) {
             // leave no TMA load in flight into shared memory
-            for (int s = 0; s < C::SA; ++s)
-                if (filled & (1u << s)) drain_wait(smem_u32(&full[s]), (fill_parity >> s) & 1u, kDrainNs);
+            if (rank == 0) {
+                for (int s = 0; s < C::SA; ++s)
+                    if (filled & (1u << s)) drain_wait(smem_u32(&full[s]), (fill_parity >> s) & 1u, kDrainNs);
+            } else {
+                // the peer's loads complete on the leader's barriers: give them time
+                const uint64_t t0 = globaltimer();
+                while (globaltimer() - t0 < 200000ull) {
+                }
+            }
             for (int s = 0; s < C::SR; ++s)
                 if (rfilled & (1u << s)) drain_wait(smem_u32(&rfull[s]), (rfill_parity >> s) & 1u, kDrainNs);
         }
     } else if (warp == 1) {
         // ================================================= MMA issuer ===
-        constexpr uint32_t idesc = make_idesc(BF16, BM, BN);
-        uint32_t stage = 0, phase = 0, bstage = 0, bphase = 0;
-        int acc_i = 0;
-        bool ok = true;
-        for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
-            const int buf = acc_i & 1;
-            const uint32_t aph = (acc_i >> 1) & 1;
-            ok = warp_wait(smem_u32(&acce[buf]), aph ^ 1u, ctl, 0x200u + buf);
-            if (!ok) break;
-            tc_fence_after();
-            const uint32_t d_tmem = tmem_base + buf * BN;
-            for (int i = 0; i < total_kb; ++i) {
-                ok = warp_wait(smem_u32(&full[stage]), phase, ctl, 0x210u + stage);
-                if (W8 && ok) ok = warp_wait(smem_u32(&bfull[bstage]), bphase, ctl, 0x220u + bstage);
+        // (with PAIR only the leader issues; the peer's warp 1 just owns its TMEM)
+        if (rank == 0) {
+            constexpr uint32_t idesc = make_idesc(BF16, TILE_M, BN);
+            uint32_t stage = 0, phase = 0, bstage = 0, bphase = 0;
+            int acc_i = 0;
+            bool ok = true;
+            for (int u = first_unit; ok && u < p.units; u += unit_step) {
+                const int buf = acc_i & 1;
+                const uint32_t aph = (acc_i >> 1) & 1;
+                ok = warp_wait<PAIR>(smem_u32(&acce[buf]), aph ^ 1u, ctl, 0x200u + buf);
                 if (!ok) break;
                 tc_fence_after();
-                if (lane == 0) {
-                    const uint64_t ad = make_sdesc(smem_u32(a_st + stage * A_STAGE_BYTES), 16, 1024);
-                    const uint64_t bd =
-                        make_sdesc(smem_u32(b_st + (W8 ? bstage : stage) * B_STAGE_BYTES), 64 * BK * 2, 1024);
+                const uint32_t d_tmem = tmem_base + buf * BN;
+                for (int i = 0; i < total_kb; ++i) {
+                    ok = warp_wait<PAIR>(smem_u32(&full[stage]), phase, ctl, 0x210u + stage);
+                    if (W8 && ok) ok = warp_wait<PAIR>(smem_u32(&bfull[bstage]), bphase, ctl, 0x220u + bstage);
+                    if (!ok) break;
+                    tc_fence_after();
+                    if (lane == 0) {
+                        const uint64_t ad = make_sdesc(smem_u32(a_st + stage * A_STAGE_BYTES), 16, 1024);
+                        const uint64_t bd =
+                            make_sdesc(smem_u32(b_st + (W8 ? bstage : stage) * C::B_BYTES), 64 * BK * 2, 1024);
 #pragma unroll
-                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                        // A: +32 bytes per 16-element k step inside the 128-byte swizzle row
-                        // B: +2 eight-row groups (2 KiB) per 16-element k step
-                        tc_mma_f16(d_tmem, ad + static_cast<uint64_t>(kk * 2), bd + static_cast<uint64_t>(kk * 128),
-                                   idesc, (i > 0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                            // A: +32 bytes per 16-element k step inside the 128-byte swizzle row
+                            // B: +2 eight-row groups (2 KiB) per 16-element k step
+                            const uint64_t a_k = ad + static_cast<uint64_t>(kk * 2);
+                            const uint64_t b_k = bd + static_cast<uint64_t>(kk * 128);
+                            const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+                            if constexpr (PAIR) tc_mma_f16_pair(d_tmem, a_k, b_k, idesc, acc);
+                            else tc_mma_f16(d_tmem, a_k, b_k, idesc, acc);
+                        }
+                        if constexpr (PAIR) {
+                            tc_commit_pair_both(smem_u32(&empty[stage]));
+                            if (W8) tc_commit_pair_both(smem_u32(&bempty[bstage]));
+                        } else {
+                            tc_commit(smem_u32(&empty[stage]));
+                            if (W8) tc_commit(smem_u32(&bempty[bstage]));
+                        }
                     }
-                    tc_commit(smem_u32(&empty[stage]));
-                    if (W8) tc_commit(smem_u32(&bempty[bstage]));
+                    __syncwarp();
+                    if (++stage == S) { stage = 0; phase ^= 1u; }
+                    if (W8 && ++bstage == C::SB) { bstage = 0; bphase ^= 1u; }
+                }
+                if (!ok) break;
+                if (lane == 0) {
+                    if constexpr (PAIR) tc_commit_pair_both(smem_u32(&accf[buf]));
+                    else tc_commit(smem_u32(&accf[buf]));
                 }
                 __syncwarp();
-                if (++stage == S) { stage = 0; phase ^= 1u; }
-                if (W8 && ++bstage == C::SB) { bstage = 0; bphase ^= 1u; }
+                ++acc_i;
             }
-            if (!ok) break;
-            if (lane == 0) tc_commit(smem_u32(&accf[buf]));
+            // every issued MMA must finish before TMEM is released
+            if (lane == 0) {
+                if constexpr (PAIR) tc_commit_pair_local(smem_u32(drain));
+                else tc_commit(smem_u32(drain));
+                drain_wait(smem_u32(drain), 0, kDrainNs);
+            }
             __syncwarp();
-            ++acc_i;
         }
-        // every issued MMA must finish before TMEM is released
-        if (lane == 0) {
-            tc_commit(smem_u32(drain));
-            drain_wait(smem_u32(drain), 0, kDrainNs);
-        }
-        __syncwarp();
     } else if (warp < 2 + NUM_EPI_WARPS) {
         // ================================================= epilogue ===
         const int q = warp & 3;                 // TMEM lane quadrant this warp may read
-        const int et = (warp - 2) * 32 + lane;  // 0..127 among epilogue threads
+        const int et = (warp - 2) * 32 + lane;  // 0..127 among this CTA's epilogue threads
         uint8_t* my_epi = epi + (warp - 2) * 2 * EPI_BUF_BYTES;
+        const uint32_t acce_base = PAIR ? map_to_rank(smem_u32(acce), 0) : smem_u32(acce);
         int acc_i = 0, sb_i = 0;
         bool ok = true;
         if (p.inject_timeout) ok = warp_wait(smem_u32(never), 0, ctl, 0x300u);
-        for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+        for (int u = first_unit; ok && u < p.units; u += unit_step) {
             int r, mt, nt;
             decode_unit<OP>(p, u, r, mt, nt);
             const int buf = acc_i & 1;
             const uint32_t aph = (acc_i >> 1) & 1;
-            ok = warp_wait(smem_u32(&accf[buf]), aph, ctl, 0x310u + buf);
+            ok = warp_wait<PAIR>(smem_u32(&accf[buf]), aph, ctl, 0x310u + buf);
             if (!ok) break;
             tc_fence_after();
-            const int row0 = mt * BM + 32 * q;
+            const int row0 = mt * TILE_M + static_cast<int>(rank) * BM + 32 * q;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + buf * BN;
             for (int sub = 0; sub < BN / EPI_COLS; ++sub) {
                 uint32_t va[32], vb[32];
@@ -547,7 +696,11 @@ __global__ void __launch_bounds__(Cfg<OP>::THREADS, 1) coc_fused_kernel(const __
                 if (sub == BN / EPI_COLS - 1) {
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&acce[buf]));
+                    if (lane == 0) {
+                        const uint32_t ab = acce_base + buf * static_cast<uint32_t>(sizeof(uint64_t));
+                        if constexpr (PAIR) mbar_arrive_cluster(ab);
+                        else mbar_arrive(ab);
+                    }
                 }
                 const int col = nt * BN + sub * EPI_COLS;
                 if (col >= p.n || row0 >= p.m) continue;   // sub-tile entirely outside the output
@@ -588,35 +741,39 @@ __global__ void __launch_bounds__(Cfg<OP>::THREADS, 1) coc_fused_kernel(const __
             }
             ++acc_i;
             if constexpr (OP == OP_AG) {
-                if (p.has_gather) gather_slice(p, r, mt, nt, et);
+                if (p.has_gather)
+                    gather_slice(p, r, mt, nt, TILE_M, static_cast<int>(rank) * 32 * NUM_EPI_WARPS + et,
+                                 NPAIR * 32 * NUM_EPI_WARPS);
             }
         }
         if (lane == 0) bulk_wait_all();
         __syncwarp();
-    } else if constexpr (OP == OP_W8) {
+    } else if constexpr (W8) {
         // ================================================= w8A16 dequant ===
-        // Thread tt owns 8 consecutive columns (cc) of the 256-wide tile and
-        // the k-block rows kr0, kr0 + R_STEP, ... (R_STEP = dequant warps).
-        constexpr int R_STEP = NUM_XFORM_WARPS;
+        // Thread tt owns 8 consecutive columns (cc) of this CTA's B columns and
+        // the k-block rows kr0, kr0 + R_STEP, ...
+        constexpr int CHUNKS = C::BN_CTA / 8;                       // 8-column chunks per row
+        constexpr int R_STEP = (NUM_XFORM_WARPS * 32) / CHUNKS;     // rows covered per pass
         constexpr int ROWS = BK / R_STEP;
         const int tt = (warp - 2 - NUM_EPI_WARPS) * 32 + lane;
-        const int cc = tt & 31;
-        const int kr0 = tt >> 5;
+        const int cc = tt % CHUNKS;
+        const int kr0 = tt / CHUNKS;
         const int blk = cc >> 3, c16 = cc & 7;
+        const uint32_t bfull_base = PAIR ? map_to_rank(smem_u32(bfull), 0) : smem_u32(bfull);
         uint32_t rstage = 0, rphase = 0, bstage = 0, bphase = 0;
         bool ok = true;
-        for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+        for (int u = first_unit; ok && u < p.units; u += unit_step) {
             int r, mt, nt;
             decode_unit<OP>(p, u, r, mt, nt);
-            const int j0 = nt * BN + cc * 8;   // first global column of this thread
+            const int j0 = nt * BN + static_cast<int>(rank) * C::BN_CTA + cc * 8;   // first global column
             for (int ks = 0; ok && ks < p.num_kshards; ++ks) {
                 const __half* sc = reinterpret_cast<const __half*>(p.scale[ks]);
                 for (int kb = 0; kb < p.kblocks; ++kb) {
                     __half2 s2[4];
                     if (p.gran == COC_SCALE_TENSOR) {
-                        const __half s = sc[0];
+                        const __half sv = sc[0];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) s2[e] = __halves2half2(s, s);
+                        for (int e = 0; e < 4; ++e) s2[e] = __halves2half2(sv, sv);
                     } else {
                         const __half* row = sc + ((p.gran == COC_SCALE_GROUP)
                                                       ? static_cast<long long>((kb * BK) / p.group) * p.n
@@ -633,15 +790,15 @@ __global__ void __launch_bounds__(Cfg<OP>::THREADS, 1) coc_fused_kernel(const __
                         }
                     }
                     ok = warp_wait(smem_u32(&rfull[rstage]), rphase, ctl, 0x400u + rstage);
-                    if (ok) ok = warp_wait(smem_u32(&bempty[bstage]), bphase ^ 1u, ctl, 0x410u + bstage);
+                    if (ok) ok = warp_wait<PAIR>(smem_u32(&bempty[bstage]), bphase ^ 1u, ctl, 0x410u + bstage);
                     if (!ok) break;
-                    const uint8_t* raw = raw_st + rstage * RAW_STAGE_BYTES;
-                    uint8_t* bst = b_st + bstage * B_STAGE_BYTES + blk * (64 * BK * 2);
+                    const uint8_t* raw = raw_st + rstage * C::RAW_BYTES;
+                    uint8_t* bst = b_st + bstage * C::B_BYTES + blk * (64 * BK * 2);
                     // all loads first, then convert and store (independent work per row)
                     uint2 q8[ROWS];
 #pragma unroll
                     for (int i = 0; i < ROWS; ++i)
-                        q8[i] = *reinterpret_cast<const uint2*>(raw + (kr0 + R_STEP * i) * BN + cc * 8);
+                        q8[i] = *reinterpret_cast<const uint2*>(raw + (kr0 + R_STEP * i) * C::BN_CTA + cc * 8);
 #pragma unroll
                     for (int i = 0; i < ROWS; ++i) {
                         const int kk = kr0 + R_STEP * i;
@@ -663,7 +820,9 @@ __global__ void __launch_bounds__(Cfg<OP>::THREADS, 1) coc_fused_kernel(const __
                     __syncwarp();
                     if (lane == 0) {
                         mbar_arrive(smem_u32(&rempty[rstage]));
-                        mbar_arrive(smem_u32(&bfull[bstage]));
+                        const uint32_t bf = bfull_base + bstage * static_cast<uint32_t>(sizeof(uint64_t));
+                        if constexpr (PAIR) mbar_arrive_cluster(bf);
+                        else mbar_arrive(bf);
                     }
                     if (++rstage == C::SR) { rstage = 0; rphase ^= 1u; }
                     if (++bstage == C::SB) { bstage = 0; bphase ^= 1u; }
@@ -673,42 +832,94 @@ __global__ void __launch_bounds__(Cfg<OP>::THREADS, 1) coc_fused_kernel(const __
     }
 
     tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
-        tc_fence_after();
-        tmem_dealloc(tmem_base, 2 * BN);
+    if constexpr (PAIR) {
+        cluster_sync();   // the leader's MMAs (which write both TMEMs) and all cross-CTA traffic are done
+        if (warp == 1) {
+            tc_fence_after();
+            tmem_dealloc_pair(tmem_base, 2 * BN);
+        }
+    } else {
+        __syncthreads();
+        if (warp == 1) {
+            tc_fence_after();
+            tmem_dealloc(tmem_base, 2 * BN);
+        }
     }
 }
 
-template <int OP, bool BF16>
+template <int OP, bool BF16, bool PAIR>
 cudaError_t launch_t(const KParams& p, int grid, cudaStream_t stream) {
-    auto kern = coc_fused_kernel<OP, BF16>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<OP>::SMEM);
+    using C = Cfg<OP, PAIR>;
+    auto kern = coc_fused_kernel<OP, BF16, PAIR>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
+    cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
-    cfg.blockDim = dim3(Cfg<OP>::THREADS, 1, 1);
-    cfg.dynamicSmemBytes = Cfg<OP>::SMEM;
+    cfg.blockDim = dim3(C::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = stream;
     cfg.attrs = nullptr;
     cfg.numAttrs = 0;
+    if constexpr (PAIR) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
     return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+template <int OP, bool BF16>
+int max_pairs_t() {
+    using C = Cfg<OP, true>;
+    auto kern = coc_fused_kernel<OP, BF16, true>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess) return 0;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(C::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) return 0;
+    return n;
 }
 
 }  // namespace
 
-cudaError_t launch(int op, bool bf16, const KParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch(int op, bool bf16, bool pair, const KParams& p, int grid, cudaStream_t stream) {
+#define COC_LAUNCH(OPV, B16)                                                                       \
+    return pair ? launch_t<OPV, B16, true>(p, grid, stream) : launch_t<OPV, B16, false>(p, grid, stream)
     switch (op) {
-        case OP_AR: return bf16 ? launch_t<OP_AR, true>(p, grid, stream) : launch_t<OP_AR, false>(p, grid, stream);
-        case OP_RS: return bf16 ? launch_t<OP_RS, true>(p, grid, stream) : launch_t<OP_RS, false>(p, grid, stream);
-        case OP_AG: return bf16 ? launch_t<OP_AG, true>(p, grid, stream) : launch_t<OP_AG, false>(p, grid, stream);
-        case OP_W8: return launch_t<OP_W8, false>(p, grid, stream);
+        case OP_AR: if (bf16) { COC_LAUNCH(OP_AR, true); } else { COC_LAUNCH(OP_AR, false); }
+        case OP_RS: if (bf16) { COC_LAUNCH(OP_RS, true); } else { COC_LAUNCH(OP_RS, false); }
+        case OP_AG: if (bf16) { COC_LAUNCH(OP_AG, true); } else { COC_LAUNCH(OP_AG, false); }
+        case OP_W8: COC_LAUNCH(OP_W8, false);
         default: return cudaErrorInvalidValue;
+    }
+#undef COC_LAUNCH
+}
+
+int max_pairs(int op, bool bf16) {
+    switch (op) {
+        case OP_AR: return bf16 ? max_pairs_t<OP_AR, true>() : max_pairs_t<OP_AR, false>();
+        case OP_RS: return bf16 ? max_pairs_t<OP_RS, true>() : max_pairs_t<OP_RS, false>();
+        case OP_AG: return bf16 ? max_pairs_t<OP_AG, true>() : max_pairs_t<OP_AG, false>();
+        case OP_W8: return max_pairs_t<OP_W8, false>();
+        default: return 0;
     }
 }
 
-size_t smem_bytes(int op) { return op == OP_W8 ? Cfg<OP_W8>::SMEM : Cfg<OP_AR>::SMEM; }
-static_assert(Cfg<OP_AR>::SMEM <= 232448 && Cfg<OP_W8>::SMEM <= 232448, "shared memory above 227 KiB");
-int block_threads(int op) { return op == OP_W8 ? Cfg<OP_W8>::THREADS : Cfg<OP_AR>::THREADS; }
+static_assert(Cfg<OP_AR, false>::SMEM <= 232448 && Cfg<OP_W8, false>::SMEM <= 232448 &&
+                  Cfg<OP_AR, true>::SMEM <= 232448 && Cfg<OP_W8, true>::SMEM <= 232448,
+              "shared memory above 227 KiB");
 
 }  // namespace coc

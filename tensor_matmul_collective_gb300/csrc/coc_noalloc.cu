@@ -149,6 +149,6 @@ extern "C" __attribute__((visibility("default"))) coc_status_t coc_matmul_all_re
     if (e != cudaSuccess) return cuda_error(e, "cudaMemsetAsync(scratch)");
     p.status = d->scratch;
     const int grid = p.units < d->sm_count ? p.units : d->sm_count;
-    if ((e = launch(OP_AR, dt == COC_BF16, p, grid, s)) != cudaSuccess) return cuda_error(e, "kernel launch");
+    if ((e = launch(OP_AR, dt == COC_BF16, false, p, grid, s)) != cudaSuccess) return cuda_error(e, "kernel launch");
     return COC_OK;
 }
