@@ -133,15 +133,15 @@ int chunk_m_tiles(int64_t m, int chunks, int tile_m) {
 }
 
 // The 2-SM variant (a CTA pair per 256-row tile) is used once the output has
-// more than one 128-row tile, except for w8A16, whose single-CTA variant is
-// faster as measured.  COC_PAIR=0/1 forces a variant (tuning only).
+// more than one 128-row tile.  COC_PAIR=0/1 forces a variant (tuning only).
 bool use_pair(int op, int64_t m) {
+    (void)op;
     static const int forced = [] {
         const char* e = std::getenv("COC_PAIR");
         return e == nullptr ? -1 : (std::atoi(e) != 0 ? 1 : 0);
     }();
     if (forced >= 0) return forced == 1;
-    return op != OP_W8 && m > BM;
+    return m > BM;
 }
 
 int pairs_available(DeviceState* ds, int op, bool bf16) {

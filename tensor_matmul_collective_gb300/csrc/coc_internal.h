@@ -19,6 +19,8 @@ constexpr int UMMA_K = 16;      // k per tcgen05.mma kind::f16
 constexpr int EPI_COLS = 64;    // epilogue sub-tile width (one 128-byte swizzle row)
 constexpr int NUM_EPI_WARPS = 4;
 constexpr int NUM_XFORM_WARPS = 8;   // w8A16 dequant warps (2 per SM sub-partition)
+constexpr int XFORM_GROUPS = 2;      // dequant warp groups taking alternate k-blocks
+constexpr int XFORM_GROUP_WARPS = NUM_XFORM_WARPS / XFORM_GROUPS;
 
 constexpr int A_STAGE_BYTES = BM * BK * 2;        // 16 KiB
 constexpr int B_STAGE_BYTES = BN * BK * 2;        // 32 KiB

@@ -225,6 +225,17 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar_cluster)
         : "memory");
 }
+// Bulk copy from this CTA's shared memory to a (peer) CTA's shared memory,
+// completing `bytes` of transaction count on a barrier in the destination CTA.
+// Used as an async-proxy "ready" signal that follows a fence.proxy.async.
+__device__ __forceinline__ void bulk_copy_s2s_signal(uint32_t dst_cluster, uint32_t src, uint32_t bytes,
+                                                     uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst_cluster),
+        "r"(src), "r"(bytes), "r"(bar_cluster)
+        : "memory");
+}
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
                  : "memory");
@@ -421,9 +432,13 @@ struct Cfg {
     static constexpr int BN_CTA = PAIR ? BN / 2 : BN;        // B columns held by one CTA
     static constexpr int B_BYTES = BN_CTA * BK * 2;          // fp16/bf16 B stage
     static constexpr int RAW_BYTES = BN_CTA * BK;            // int8 W stage
+    // w8A16 raw and B rings have an even depth: with XFORM_GROUPS = 2 groups
+    // taking alternate k-blocks, each stage then belongs to one group, so a
+    // stage's barrier phases are always consumed in order by one waiter.
     static constexpr int SA = W8 ? 4 : (PAIR ? 6 : 4);       // A (+B) stages
-    static constexpr int SB = W8 ? (PAIR ? 3 : 2) : SA;      // B stages (shared with A except for w8A16)
-    static constexpr int SR = W8 ? (PAIR ? 6 : 4) : 0;       // raw int8 stages
+    static constexpr int SB = W8 ? (PAIR ? 4 : 2) : SA;      // B stages (shared with A except for w8A16)
+    static constexpr int SR = W8 ? (PAIR ? 8 : 4) : 0;       // raw int8 stages
+    static_assert(!W8 || (SB % XFORM_GROUPS == 0 && SR % XFORM_GROUPS == 0), "rings must split between groups");
     static constexpr int WARPS = 2 + NUM_EPI_WARPS + (W8 ? NUM_XFORM_WARPS : 0);
     static constexpr int THREADS = WARPS * 32;
     static constexpr int EPI_BYTES = NUM_EPI_WARPS * 2 * EPI_BUF_BYTES;
@@ -458,6 +473,8 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
     uint64_t* drain = never + 1;       // [1]  MMA drain before TMEM release
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     uint32_t* abort_word = tmem_slot + 1;
+    // w8A16 pair: 16-byte landing slots for the peer's per-stage "B half ready" copies
+    uint8_t* sig_slots = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(abort_word + 1) + 15) & ~uintptr_t(15));
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -473,12 +490,12 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
             mbar_init(smem_u32(&empty[s]), 1);
         }
         for (int s = 0; s < C::SB; ++s) {
-            mbar_init(smem_u32(&bfull[s]), NPAIR * NUM_XFORM_WARPS);
+            mbar_init(smem_u32(&bfull[s]), 1);   // the (leader's) dequant group; the peer's copy adds tx bytes
             mbar_init(smem_u32(&bempty[s]), 1);
         }
         for (int s = 0; s < C::SR; ++s) {
             mbar_init(smem_u32(&rfull[s]), 1);
-            mbar_init(smem_u32(&rempty[s]), NUM_XFORM_WARPS);
+            mbar_init(smem_u32(&rempty[s]), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&accf[b]), 1);
@@ -750,17 +767,22 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
         __syncwarp();
     } else if constexpr (W8) {
         // ================================================= w8A16 dequant ===
-        // Thread tt owns 8 consecutive columns (cc) of this CTA's B columns and
-        // the k-block rows kr0, kr0 + R_STEP, ...
+        // Two groups of dequant warps take alternate k-blocks, so two
+        // k-blocks are in conversion at once.  In a group, thread tt owns 8
+        // consecutive columns (cc) of this CTA's B columns and the k-block
+        // rows kr0, kr0 + R_STEP, ...
+        constexpr int GT = XFORM_GROUP_WARPS * 32;                  // threads per group
         constexpr int CHUNKS = C::BN_CTA / 8;                       // 8-column chunks per row
-        constexpr int R_STEP = (NUM_XFORM_WARPS * 32) / CHUNKS;     // rows covered per pass
+        constexpr int R_STEP = GT / CHUNKS;                         // rows covered per pass
         constexpr int ROWS = BK / R_STEP;
-        const int tt = (warp - 2 - NUM_EPI_WARPS) * 32 + lane;
+        const int xw = warp - 2 - NUM_EPI_WARPS;                     // 0 .. NUM_XFORM_WARPS-1
+        const int group = xw / XFORM_GROUP_WARPS;
+        const int tt = (xw % XFORM_GROUP_WARPS) * 32 + lane;
         const int cc = tt % CHUNKS;
         const int kr0 = tt / CHUNKS;
         const int blk = cc >> 3, c16 = cc & 7;
         const uint32_t bfull_base = PAIR ? map_to_rank(smem_u32(bfull), 0) : smem_u32(bfull);
-        uint32_t rstage = 0, rphase = 0, bstage = 0, bphase = 0;
+        uint32_t cnt = 0;   // global k-block counter (all units, ranks, k-blocks in order)
         bool ok = true;
         for (int u = first_unit; ok && u < p.units; u += unit_step) {
             int r, mt, nt;
@@ -768,7 +790,10 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
             const int j0 = nt * BN + static_cast<int>(rank) * C::BN_CTA + cc * 8;   // first global column
             for (int ks = 0; ok && ks < p.num_kshards; ++ks) {
                 const __half* sc = reinterpret_cast<const __half*>(p.scale[ks]);
-                for (int kb = 0; kb < p.kblocks; ++kb) {
+                for (int kb = 0; kb < p.kblocks; ++kb, ++cnt) {
+                    if (static_cast<int>(cnt % XFORM_GROUPS) != group) continue;
+                    const uint32_t rstage = cnt % C::SR, rphase = (cnt / C::SR) & 1u;
+                    const uint32_t bstage = cnt % C::SB, bphase = (cnt / C::SB) & 1u;
                     __half2 s2[4];
                     if (p.gran == COC_SCALE_TENSOR) {
                         const __half sv = sc[0];
@@ -789,43 +814,64 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
                             for (int e = 0; e < 4; ++e) s2[e] = __float2half2_rn(0.f);   // columns past n
                         }
                     }
-                    ok = warp_wait(smem_u32(&rfull[rstage]), rphase, ctl, 0x400u + rstage);
-                    if (ok) ok = warp_wait<PAIR>(smem_u32(&bempty[bstage]), bphase ^ 1u, ctl, 0x410u + bstage);
-                    if (!ok) break;
-                    const uint8_t* raw = raw_st + rstage * C::RAW_BYTES;
-                    uint8_t* bst = b_st + bstage * C::B_BYTES + blk * (64 * BK * 2);
-                    // all loads first, then convert and store (independent work per row)
-                    uint2 q8[ROWS];
+                    bool ok_k = warp_wait(smem_u32(&rfull[rstage]), rphase, ctl, 0x400u + rstage);
+                    if (ok_k) ok_k = warp_wait<PAIR>(smem_u32(&bempty[bstage]), bphase ^ 1u, ctl, 0x410u + bstage);
+                    if (ok_k) {
+                        const uint8_t* raw = raw_st + rstage * C::RAW_BYTES;
+                        uint8_t* bst = b_st + bstage * C::B_BYTES + blk * (64 * BK * 2);
+                        // all loads first, then convert and store (independent work per row)
+                        uint2 q8[ROWS];
 #pragma unroll
-                    for (int i = 0; i < ROWS; ++i)
-                        q8[i] = *reinterpret_cast<const uint2*>(raw + (kr0 + R_STEP * i) * C::BN_CTA + cc * 8);
+                        for (int i = 0; i < ROWS; ++i)
+                            q8[i] = *reinterpret_cast<const uint2*>(raw + (kr0 + R_STEP * i) * C::BN_CTA + cc * 8);
 #pragma unroll
-                    for (int i = 0; i < ROWS; ++i) {
-                        const int kk = kr0 + R_STEP * i;
-                        __half2 h[4];
-                        i8x4_to_h2x2(q8[i].x, h[0], h[1]);
-                        i8x4_to_h2x2(q8[i].y, h[2], h[3]);
-                        uint4 o;
-                        __half2 m0 = __hmul2_rn(h[0], s2[0]), m1 = __hmul2_rn(h[1], s2[1]);
-                        __half2 m2 = __hmul2_rn(h[2], s2[2]), m3 = __hmul2_rn(h[3], s2[3]);
-                        o.x = *reinterpret_cast<uint32_t*>(&m0);
-                        o.y = *reinterpret_cast<uint32_t*>(&m1);
-                        o.z = *reinterpret_cast<uint32_t*>(&m2);
-                        o.w = *reinterpret_cast<uint32_t*>(&m3);
-                        // MN-major 128-byte-swizzled B layout: 64-column blocks of
-                        // 64 rows x 128 bytes, 16-byte chunks XOR-ed with row % 8
-                        *reinterpret_cast<uint4*>(bst + kk * 128 + ((c16 ^ (kk & 7)) << 4)) = o;
+                        for (int i = 0; i < ROWS; ++i) {
+                            const int kk = kr0 + R_STEP * i;
+                            __half2 h[4];
+                            i8x4_to_h2x2(q8[i].x, h[0], h[1]);
+                            i8x4_to_h2x2(q8[i].y, h[2], h[3]);
+                            uint4 o;
+                            __half2 m0 = __hmul2_rn(h[0], s2[0]), m1 = __hmul2_rn(h[1], s2[1]);
+                            __half2 m2 = __hmul2_rn(h[2], s2[2]), m3 = __hmul2_rn(h[3], s2[3]);
+                            o.x = *reinterpret_cast<uint32_t*>(&m0);
+                            o.y = *reinterpret_cast<uint32_t*>(&m1);
+                            o.z = *reinterpret_cast<uint32_t*>(&m2);
+                            o.w = *reinterpret_cast<uint32_t*>(&m3);
+                            // MN-major 128-byte-swizzled B layout: 64-column blocks of
+                            // 64 rows x 128 bytes, 16-byte chunks XOR-ed with row % 8
+                            *reinterpret_cast<uint4*>(bst + kk * 128 + ((c16 ^ (kk & 7)) << 4)) = o;
+                        }
+                        fence_proxy_async_smem();
                     }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
+                    // The group's warps agree (barrier with OR-reduction) on whether every
+                    // warp converted this stage; on any failure they all leave together,
+                    // so no warp is left waiting at a named barrier.
+                    const uint32_t fail = (!ok_k || *reinterpret_cast<volatile uint32_t*>(abort_word) != 0u) ? 1u : 0u;
+                    uint32_t any_fail;
+                    asm volatile(
+                        "{\n\t.reg .pred pf, pa;\n\t"
+                        "setp.ne.u32 pf, %1, 0;\n\t"
+                        "bar.red.or.pred pa, %2, %3, pf;\n\t"
+                        "selp.u32 %0, 1, 0, pa;\n\t}"
+                        : "=r"(any_fail)
+                        : "r"(fail), "r"(1 + group), "n"(GT)
+                        : "memory");
+                    if (any_fail) { ok = false; break; }
+                    if (tt == 0) {
                         mbar_arrive(smem_u32(&rempty[rstage]));
                         const uint32_t bf = bfull_base + bstage * static_cast<uint32_t>(sizeof(uint64_t));
-                        if constexpr (PAIR) mbar_arrive_cluster(bf);
-                        else mbar_arrive(bf);
+                        if constexpr (PAIR) {
+                            if (rank == 0) {
+                                mbar_expect_tx(smem_u32(&bfull[bstage]), 16);   // arrive + the peer's 16 bytes
+                            } else {
+                                // async-proxy signal: ordered after this group's fenced B writes
+                                const uint32_t slot = map_to_rank(smem_u32(sig_slots + 16 * bstage), 0);
+                                bulk_copy_s2s_signal(slot, smem_u32(b_st + bstage * C::B_BYTES), 16, bf);
+                            }
+                        } else {
+                            mbar_arrive(bf);
+                        }
                     }
-                    if (++rstage == C::SR) { rstage = 0; rphase ^= 1u; }
-                    if (++bstage == C::SB) { bstage = 0; bphase ^= 1u; }
                 }
             }
         }
@@ -833,6 +879,14 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
 
     tc_fence_before();
     if constexpr (PAIR) {
+        // After an abort the peer may still have loads or signal copies in
+        // flight toward the leader's shared memory: give them time to land
+        // before either CTA can exit.
+        if (*reinterpret_cast<volatile uint32_t*>(abort_word) != 0u) {
+            const uint64_t t0 = globaltimer();
+            while (globaltimer() - t0 < 200000ull) {
+            }
+        }
         cluster_sync();   // the leader's MMAs (which write both TMEMs) and all cross-CTA traffic are done
         if (warp == 1) {
             tc_fence_after();
