@@ -76,16 +76,16 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:12]
 
 
-def load_traffic(op: str):
-    """DRAM bytes per launch of `op` from the committed ncu summary, if it was
-    taken on the current kernel source; else None."""
+def load_traffic(op: str, chunks: int):
+    """DRAM bytes per launch of `op` at `chunks` from the committed ncu
+    summary, if it was taken on the current kernel source; else None."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
-    want = kernel_source_hash()
+    want, key = kernel_source_hash(), f"{op}@c{chunks}"
     for line in open(path):
         parts = line.split()
-        if len(parts) >= 3 and not line.startswith("#") and parts[0] == op and parts[2] == want:
+        if len(parts) >= 3 and not line.startswith("#") and parts[0] == key and parts[2] == want:
             return float(parts[1])
     return None
 
@@ -151,6 +151,7 @@ def build_suite(dev):
     from tensor_matmul_collective_gb300 import workloads as wl
 
     ops, host = [], {}
+    C = {w.name: w.chunks for w in wl.TP8_SUITE}
 
     def up(ts):
         return [t.to(dev) for t in ts]
@@ -160,7 +161,7 @@ def build_suite(dev):
     host["bloom7b"] = (xs, ws)
     dx, dw = up(xs), up(ws)
     out7 = [torch.empty(s.m, s.n, dtype=s.dtype, device=dev) for _ in range(s.R)]
-    ops.append(Op("bloom7b_ar", "ar", s.flops(), lambda dx=dx, dw=dw, o=out7: coc.matmul_all_reduce(dx, dw, o, chunks=4),
+    ops.append(Op("bloom7b_ar", "ar", s.flops(), lambda dx=dx, dw=dw, o=out7: coc.matmul_all_reduce(dx, dw, o, chunks=C["bloom7b_ar"]),
                   dx + dw, out7, s))
 
     s = wl.LLAMA70B_AG
@@ -170,7 +171,7 @@ def build_suite(dev):
     outg = [torch.empty(s.m, s.n_shard, dtype=s.dtype, device=dev) for _ in range(s.R)]
     gat = [torch.empty(s.m, s.k, dtype=s.dtype, device=dev) for _ in range(s.R)]
     ops.append(Op("llama70b_ag_v2", "ag_v2", s.flops(),
-                  lambda dx=dx, dw=dw, o=outg, g=gat: coc.all_gather_matmul_v2(dx, dw, o, g, chunks=4),
+                  lambda dx=dx, dw=dw, o=outg, g=gat: coc.all_gather_matmul_v2(dx, dw, o, g, chunks=C["llama70b_ag_v2"]),
                   dx + dw, outg + gat, s))
 
     s = wl.LLAMA70B_RS
@@ -179,7 +180,8 @@ def build_suite(dev):
     dx, dw = up(xs), up(ws)
     outr = [torch.empty(s.m // s.R, s.n, dtype=s.dtype, device=dev) for _ in range(s.R)]
     ops.append(Op("llama70b_rs", "rs", s.flops(),
-                  lambda dx=dx, dw=dw, o=outr: coc.matmul_reduce_scatter(dx, dw, o, chunks=4), dx + dw, outr, s))
+                  lambda dx=dx, dw=dw, o=outr: coc.matmul_reduce_scatter(dx, dw, o, chunks=C["llama70b_rs"]),
+                  dx + dw, outr, s))
 
     s = wl.W8A16_AR
     xs8 = wqs = None
@@ -198,7 +200,7 @@ def build_suite(dev):
         out8 = [torch.empty(s.m, s.n, dtype=torch.float16, device=dev) for _ in range(s.R)]
         op = Op(f"w8a16_ar_{gran}", "w8a16_ar", s.flops(),
                 lambda dx=dx8, dw=dwq, sc=dsc, o=out8, g=gran, grp=s.group: coc.matmul_all_reduce_w8a16(
-                    dx, dw, sc, g, grp, o, chunks=4),
+                    dx, dw, sc, g, grp, o, chunks=C["w8a16_ar"]),
                 (dx8 + dwq if gran == "tensor" else []) + uniq, out8, s, gran)
         op.shares_prev_inputs = gran != "tensor"
         ops.append(op)
@@ -210,10 +212,12 @@ def build_suite(dev):
     outa = [torch.empty(s.m, s.n, dtype=s.dtype, device=dev) for _ in range(s.R)]
     outs = [torch.empty(s.m // s.R, s.n, dtype=s.dtype, device=dev) for _ in range(s.R)]
     ops.append(Op("bloom176b_det_ar", "ar", s.flops(),
-                  lambda dx=dx, dw=dw, o=outa: coc.matmul_all_reduce(dx, dw, o, chunks=4, deterministic=True),
+                  lambda dx=dx, dw=dw, o=outa: coc.matmul_all_reduce(dx, dw, o, chunks=C["bloom176b_det_ar"],
+                                                                    deterministic=True),
                   dx + dw, outa, s))
     op = Op("bloom176b_det_rs", "rs", s.flops(),
-            lambda dx=dx, dw=dw, o=outs: coc.matmul_reduce_scatter(dx, dw, o, chunks=4, deterministic=True),
+            lambda dx=dx, dw=dw, o=outs: coc.matmul_reduce_scatter(dx, dw, o, chunks=C["bloom176b_det_rs"],
+                                                                deterministic=True),
             [], outs, s)
     op.shares_prev_inputs = True
     ops.append(op)
@@ -362,7 +366,7 @@ def time_context(ops, dev):
         outs = op.outputs[:s.R]
         xg = op.outputs[s.R]
         tf = t(op.run)
-        t_ag = t(lambda: coc.all_gather_matmul(dx, dw, outs, chunks=4))
+        t_ag = t(lambda: coc.all_gather_matmul(dx, dw, outs, chunks=1))
         t_plain = t(lambda: [coc.matmul([xg], [dw[r]], outs[r]) for r in range(s.R)])
         tu = t(lambda: [torch.matmul(torch.cat(dx, 0), dw[r]) for r in range(s.R)], 3)
         out[op.name] = {"fused_ms": round(tf, 4), "all_gather_matmul_ms": round(t_ag, 4),
@@ -463,7 +467,8 @@ def base_line(n_gpus, steps, warmup):
 
 
 def config_dict(world):
-    return {"workload": WORKLOAD, "ranks_emulated": 8, "chunks": 4,
+    from tensor_matmul_collective_gb300 import workloads as wl
+    return {"workload": WORKLOAD, "ranks_emulated": 8, "chunks": {w.name: w.chunks for w in wl.TP8_SUITE},
             "compute_types": "bf16 in / fp32 accumulate / bf16 out; w8A16: fp16 x int8 -> fp16",
             "l2": "no flush: every operator's operands exceed the 129 MB L2 and each step streams > 5 GB",
             "parallelism": f"replicas x{world} (no cross-GPU exchange on this path)"}
@@ -534,7 +539,9 @@ def run_ours(args):
     peak = peaks["bf16_tflops_sustained"]
     dom = max(range(len(ops)), key=lambda i: per_op[i])
     dom_tf = ops[dom].flops / (per_op[dom] / 1e3) / 1e12
-    traffic = load_traffic(ops[dom].name)
+    from tensor_matmul_collective_gb300 import workloads as wl
+    chunks_of = {w.name: w.chunks for w in wl.TP8_SUITE}
+    traffic = load_traffic(ops[dom].name, chunks_of.get(ops[dom].name, chunks_of.get("w8a16_ar", 1)))
     per_op_json = {op.name: {"ms": round(t, 4), "tflops": round(op.flops / (t / 1e3) / 1e12, 1),
                              "frac_of_peak": round(op.flops / (t / 1e3) / 1e12 / peak, 4)}
                    for op, t in zip(ops, per_op)}

@@ -144,6 +144,16 @@ bool use_pair(int op, int64_t m) {
     return m > BM;
 }
 
+// Largest divisor of chunk_mt whose A rows (row_tile_bytes each) fit in
+// 32 MiB of L2; 0 (no grouping) when the whole chunk fits or nothing does.
+int l2_group(int chunk_mt, int64_t row_tile_bytes) {
+    constexpr int64_t kBudget = int64_t(32) << 20;
+    if (chunk_mt <= 0 || row_tile_bytes <= 0 || chunk_mt * row_tile_bytes <= kBudget) return 0;
+    for (int g = chunk_mt - 1; g >= 2; --g)
+        if (chunk_mt % g == 0 && g * row_tile_bytes <= kBudget) return g;
+    return 0;
+}
+
 int pairs_available(DeviceState* ds, int op, bool bf16) {
     std::lock_guard<std::mutex> lk(g_mu);
     int& v = ds->max_pairs[op][bf16 ? 1 : 0];
@@ -358,6 +368,13 @@ coc_status_t all_gather(int R, int64_t ms, int64_t ns, int64_t k, const void* co
     p.a_box_rows = largest_pow2_divisor_le(ms, BM);
     p.store_rows = 32;
     p.has_gather = (v2 && k > 0) ? 1 : 0;
+    // The gathered X is re-read by every (rank, n-tile) column.  Take the
+    // row tiles in groups whose X rows fit comfortably in L2 (32 MiB) and
+    // mark those loads evict-last, so W streams past a resident X slice:
+    // W is then read once per group instead of X once per wave of columns.
+    p.a_hint = 2;
+    p.b_hint = 0;
+    p.group_mt = l2_group(p.chunk_mt, static_cast<int64_t>(tile_m) * k * 2);
 
     DeviceState* ds = nullptr;
     if ((st = device_state(&ds)) != COC_OK) return st;

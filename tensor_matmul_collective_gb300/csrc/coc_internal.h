@@ -53,6 +53,7 @@ struct KParams {
     int m_tiles, n_tiles;
     int units;         // work units (tiles; AG: R * tiles)
     int chunk_mt;      // m-tiles per chunk for chunk-major order; 0 = row order
+    int group_mt;      // m-tiles per L2 group inside a chunk (divides chunk_mt); 0 = whole chunk
     int rows_per_rank; // RS: m/R; AG: m_shard
     int a_box_rows;    // AG: rows per A TMA box (divides m_shard and BM)
     int store_rows;    // rows per output TMA store box (divides 32)
@@ -60,6 +61,7 @@ struct KParams {
     int group;         // w8A16 group size (rows of K)
     int inject_timeout;
     int has_gather;    // AG-V2
+    int a_hint, b_hint;  // L2 policy of A / B loads: 0 evict_normal, 1 evict_first, 2 evict_last
 };
 
 // Argument checks of coc_matmul_all_reduce and the per-thread error text

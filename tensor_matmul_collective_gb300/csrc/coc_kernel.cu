@@ -93,6 +93,25 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// Same, with an L2 eviction-priority policy for the loaded lines.
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                                 uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+// L2 policies: 0 evict_normal, 1 evict_first (streamed once), 2 evict_last (reused).
+__device__ __forceinline__ uint64_t make_l2_policy(int kind) {
+    uint64_t pol;
+    if (kind == 1) asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    else if (kind == 2) asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    else asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int c0, int c1) {
     asm volatile(
         "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
@@ -218,11 +237,11 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 // TMA load into this CTA's shared memory, completing on a barrier that may
 // live in the peer CTA (cluster address).
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int c0, int c1,
-                                                 uint32_t bar_cluster) {
+                                                 uint32_t bar_cluster, uint64_t policy) {
     asm volatile(
         "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar_cluster)
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar_cluster), "l"(policy)
         : "memory");
 }
 // Bulk copy from this CTA's shared memory to a (peer) CTA's shared memory,
@@ -340,8 +359,10 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const C
 // ------------------------------------------------------------ scheduling ---
 
 // Work unit -> (rank r for AllGather, m-tile, n-tile).  Units go chunk by
-// chunk; inside a chunk the m-tiles of one (rank, n-tile) column are adjacent
-// so concurrently running CTAs share their B tiles in L2.
+// chunk; inside a chunk, m-tiles are taken in groups of group_mt (an L2-sized
+// slice of the A rows), and inside a group the m-tiles of one (rank, n-tile)
+// column are adjacent, so concurrently running CTAs share their B tiles and
+// the group's A rows stay in L2 while the columns stream past.
 template <int OP>
 __device__ __forceinline__ void decode_unit(const KParams& p, int u, int& r, int& mt, int& nt) {
     const int rg = (OP == OP_AG) ? p.R : 1;
@@ -349,11 +370,15 @@ __device__ __forceinline__ void decode_unit(const KParams& p, int u, int& r, int
         const int per_chunk = p.chunk_mt * p.n_tiles * rg;
         const int c = u / per_chunk;
         int v = u - c * per_chunk;
-        const int mi = v % p.chunk_mt;
-        v /= p.chunk_mt;
+        const int G = p.group_mt > 0 ? p.group_mt : p.chunk_mt;
+        const int per_group = G * p.n_tiles * rg;
+        const int g = v / per_group;
+        v -= g * per_group;
+        const int mi = v % G;
+        v /= G;
         nt = v % p.n_tiles;
         r = v / p.n_tiles;
-        mt = c * p.chunk_mt + mi;
+        mt = c * p.chunk_mt + g * G + mi;
     } else {
         const int per_row = p.n_tiles * rg;
         mt = u / per_row;
@@ -534,6 +559,7 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
         uint32_t rfilled = 0, rfill_parity = 0;   // same for the raw int8 ring
         // bytes the leader's full barrier receives per stage (both CTAs' loads)
         constexpr uint32_t kFullBytes = NPAIR * (A_STAGE_BYTES + (W8 ? 0 : C::B_BYTES));
+        const uint64_t pol_a = make_l2_policy(p.a_hint), pol_b = make_l2_policy(p.b_hint);
         bool ok = true;
         for (int u = first_unit; ok && u < p.units; u += unit_step) {
             int r, mt, nt;
@@ -556,32 +582,32 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
                         const uint32_t fb = PAIR ? map_to_rank(fb_local, 0) : fb_local;
                         const uint32_t a_dst = smem_u32(a_st + stage * A_STAGE_BYTES);
                         if (rank == 0) mbar_expect_tx(fb_local, kFullBytes);
-                        auto load = [&](uint32_t dst, const CUtensorMap* map, int c0, int c1) {
-                            if constexpr (PAIR) tma_load_2d_pair(dst, map, c0, c1, fb);
-                            else tma_load_2d(dst, map, c0, c1, fb);
+                        auto load = [&](uint32_t dst, const CUtensorMap* map, int c0, int c1, uint64_t pol) {
+                            if constexpr (PAIR) tma_load_2d_pair(dst, map, c0, c1, fb, pol);
+                            else tma_load_2d_hint(dst, map, c0, c1, fb, pol);
                         };
                         if constexpr (OP == OP_AG) {
                             // gathered rows -> (shard, local row); rows past the
                             // end read beyond the last shard and are zero-filled
                             if (p.a_box_rows == BM) {
-                                load(a_dst, &p.tm_a[a_shard], kc, a_row);
+                                load(a_dst, &p.tm_a[a_shard], kc, a_row, pol_a);
                             } else {
                                 for (int rb = 0; rb < BM; rb += p.a_box_rows) {
                                     const int g = row_base + rb;
                                     int sh = g / p.rows_per_rank;
                                     if (sh > p.R - 1) sh = p.R - 1;
-                                    load(a_dst + rb * 128, &p.tm_a[sh], kc, g - sh * p.rows_per_rank);
+                                    load(a_dst + rb * 128, &p.tm_a[sh], kc, g - sh * p.rows_per_rank, pol_a);
                                 }
                             }
                         } else {
-                            load(a_dst, &p.tm_a[ks], kc, row_base);
+                            load(a_dst, &p.tm_a[ks], kc, row_base, pol_a);
                         }
                         if constexpr (!W8) {
                             const CUtensorMap* bm = &p.tm_b[(OP == OP_AG) ? r : ks];
                             const uint32_t b_dst = smem_u32(b_st + stage * C::B_BYTES);
 #pragma unroll
                             for (int j = 0; j < C::BN_CTA / 64; ++j)
-                                load(b_dst + j * (64 * BK * 2), bm, col_base + j * 64, kc);
+                                load(b_dst + j * (64 * BK * 2), bm, col_base + j * 64, kc, pol_b);
                         }
                         filled |= 1u << stage;
                         fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
@@ -595,7 +621,8 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
                         if (lane == 0) {
                             const uint32_t rb = smem_u32(&rfull[rstage]);
                             mbar_expect_tx(rb, C::RAW_BYTES);
-                            tma_load_2d(smem_u32(raw_st + rstage * C::RAW_BYTES), &p.tm_b[ks], col_base, kc, rb);
+                            tma_load_2d_hint(smem_u32(raw_st + rstage * C::RAW_BYTES), &p.tm_b[ks], col_base, kc, rb,
+                                             pol_b);
                             rfilled |= 1u << rstage;
                             rfill_parity = (rfill_parity & ~(1u << rstage)) | (rphase << rstage);
                         }
