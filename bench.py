@@ -60,6 +60,22 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest value of x over all ranks (x itself without a process group)."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(step_flops: float, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job TFLOP/s: every rank ran `steps` steps of `step_flops`; the job
+    took as long as its slowest rank."""
+    return world * step_flops * steps / (max_ms / 1e3) / 1e12
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -528,12 +544,9 @@ def run_ours(args):
     sampler = ClockSampler(bus)
     total_ms, per_op, clocks = time_device(ops, args.steps, args.warmup, dist, sampler)
 
-    elapsed = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if dist is not None:
-        dist.all_reduce(elapsed, op=dist.ReduceOp.MAX)
-    total_ms = float(elapsed.item())
+    total_ms = max_over_ranks(total_ms, dist, dev)
     step_flops = sum(op.flops for op in ops)
-    value = world * step_flops * args.steps / (total_ms / 1e3) / 1e12
+    value = job_value(step_flops, args.steps, world, total_ms)
 
     peaks = load_peaks()
     peak = peaks["bf16_tflops_sustained"]
@@ -549,7 +562,8 @@ def run_ours(args):
     e2e = None
     if args.e2e_steps > 0:
         wall, h2d, d2h = time_e2e(ops, args.e2e_steps, dev)
-        e2e = {"value": world * step_flops * args.e2e_steps / wall / 1e12, "unit": UNIT,
+        wall_ms = max_over_ranks(wall * 1e3, dist, dev)
+        e2e = {"value": job_value(step_flops, args.e2e_steps, world, wall_ms), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     context = None if args.no_context else time_context(ops, dev)
