@@ -416,6 +416,29 @@ __device__ __forceinline__ void i8x4_to_h2x2(uint32_t w, __half2& h01, __half2& 
     h23 = __hsub2(*reinterpret_cast<__half2*>(&b), bias);
 }
 
+// fp16 scales for the 8 columns j0..j0+7 of k-block kb of one rank's w8A16
+// weight (`sc` = that rank's scale view), as four half2 pairs.
+__device__ __forceinline__ void load_w8_scales(const KParams& p, const __half* sc, int kb, int j0, __half2 (&s2)[4]) {
+    if (p.gran == COC_SCALE_TENSOR) {
+        const __half sv = sc[0];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s2[e] = __halves2half2(sv, sv);
+        return;
+    }
+    const __half* row =
+        sc + ((p.gran == COC_SCALE_GROUP) ? static_cast<long long>((kb * BK) / p.group) * p.n : 0LL);
+    if (j0 + 8 <= p.n) {
+        const uint4 s8 = __ldg(reinterpret_cast<const uint4*>(row + j0));
+        s2[0] = *reinterpret_cast<const __half2*>(&s8.x);
+        s2[1] = *reinterpret_cast<const __half2*>(&s8.y);
+        s2[2] = *reinterpret_cast<const __half2*>(&s8.z);
+        s2[3] = *reinterpret_cast<const __half2*>(&s8.w);
+    } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s2[e] = __float2half2_rn(0.f);   // columns past n
+    }
+}
+
 // ALL_GATHER_MATMUL_V2: copy this unit's share of the m-tile's gathered
 // rows to every rank's gather buffer.  The tile's rows are one contiguous run
 // of the gathered matrix; it is cut into R * n_tiles equal pieces, one per
@@ -460,9 +483,9 @@ struct Cfg {
     // w8A16 raw and B rings have an even depth: with XFORM_GROUPS = 2 groups
     // taking alternate k-blocks, each stage then belongs to one group, so a
     // stage's barrier phases are always consumed in order by one waiter.
-    static constexpr int SA = W8 ? 4 : (PAIR ? 6 : 4);       // A (+B) stages
+    static constexpr int SA = W8 ? (PAIR ? 6 : 4) : (PAIR ? 6 : 4);   // A (+B) stages
     static constexpr int SB = W8 ? (PAIR ? 4 : 2) : SA;      // B stages (shared with A except for w8A16)
-    static constexpr int SR = W8 ? (PAIR ? 8 : 4) : 0;       // raw int8 stages
+    static constexpr int SR = W8 ? 4 : 0;                    // raw int8 stages
     static_assert(!W8 || (SB % XFORM_GROUPS == 0 && SR % XFORM_GROUPS == 0), "rings must split between groups");
     static constexpr int WARPS = 2 + NUM_EPI_WARPS + (W8 ? NUM_XFORM_WARPS : 0);
     static constexpr int THREADS = WARPS * 32;
@@ -817,30 +840,15 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
             const int j0 = nt * BN + static_cast<int>(rank) * C::BN_CTA + cc * 8;   // first global column
             for (int ks = 0; ok && ks < p.num_kshards; ++ks) {
                 const __half* sc = reinterpret_cast<const __half*>(p.scale[ks]);
+                // per-tensor / per-channel scales do not depend on the k-block:
+                // load them once per rank; per-group scales per k-block below
+                __half2 s2[4];
+                if (p.gran != COC_SCALE_GROUP) load_w8_scales(p, sc, 0, j0, s2);
                 for (int kb = 0; kb < p.kblocks; ++kb, ++cnt) {
                     if (static_cast<int>(cnt % XFORM_GROUPS) != group) continue;
                     const uint32_t rstage = cnt % C::SR, rphase = (cnt / C::SR) & 1u;
                     const uint32_t bstage = cnt % C::SB, bphase = (cnt / C::SB) & 1u;
-                    __half2 s2[4];
-                    if (p.gran == COC_SCALE_TENSOR) {
-                        const __half sv = sc[0];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) s2[e] = __halves2half2(sv, sv);
-                    } else {
-                        const __half* row = sc + ((p.gran == COC_SCALE_GROUP)
-                                                      ? static_cast<long long>((kb * BK) / p.group) * p.n
-                                                      : 0LL);
-                        if (j0 + 8 <= p.n) {
-                            const uint4 s8 = __ldg(reinterpret_cast<const uint4*>(row + j0));
-                            s2[0] = *reinterpret_cast<const __half2*>(&s8.x);
-                            s2[1] = *reinterpret_cast<const __half2*>(&s8.y);
-                            s2[2] = *reinterpret_cast<const __half2*>(&s8.z);
-                            s2[3] = *reinterpret_cast<const __half2*>(&s8.w);
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) s2[e] = __float2half2_rn(0.f);   // columns past n
-                        }
-                    }
+                    if (p.gran == COC_SCALE_GROUP) load_w8_scales(p, sc, kb, j0, s2);
                     bool ok_k = warp_wait(smem_u32(&rfull[rstage]), rphase, ctl, 0x400u + rstage);
                     if (ok_k) ok_k = warp_wait<PAIR>(smem_u32(&bempty[bstage]), bphase ^ 1u, ctl, 0x410u + bstage);
                     if (ok_k) {
