@@ -90,6 +90,20 @@ typedef enum {
     COC_SCALE_GROUP = 2        /* one scale per (group of group_size rows of K, column j) */
 } coc_scale_t;
 
+/* Fused operator selector for coc_fused_matmul. */
+typedef enum {
+    COC_OP_ALL_REDUCE = 0,      /* MATMUL_ALL_REDUCE */
+    COC_OP_REDUCE_SCATTER = 1,  /* MATMUL_REDUCE_SCATTER */
+    COC_OP_ALL_GATHER = 2,      /* ALL_GATHER_MATMUL */
+    COC_OP_ALL_GATHER_V2 = 3    /* ALL_GATHER_MATMUL_V2 */
+} coc_op_t;
+
+/* Storage of each weight shard. */
+typedef enum {
+    COC_W_KN = 0,   /* k x n row-major (inner x cols): the layout of the named entry points */
+    COC_W_NK = 1    /* n x k row-major (cols x inner): Megatron's [out_features, in_features] */
+} coc_wlayout_t;
+
 /* Opaque CUDA stream handle; identical to cudaStream_t / CUstream. */
 typedef struct CUstream_st* coc_stream_t;
 
@@ -193,6 +207,36 @@ coc_status_t coc_matmul_all_reduce_w8a16(int R, int64_t m, int64_t n, int64_t k_
                                          const void* const* scale, coc_scale_t gran,
                                          int64_t group_size, void* const* out,
                                          int chunks, int deterministic, coc_stream_t stream);
+
+/*
+ * Any of the four bf16/fp16 fused operators with a choice of weight layout.
+ * The operators are those above (CoC page, 融合算子实现); the layouts are
+ * those of the Megatron layers the page's 问题分析 section names: a linear
+ * layer keeps its weight as [out_features, in_features] (COC_W_NK), so its
+ * forward pass is X @ W^T, while its backward (data-gradient) pass multiplies
+ * by W itself — which, read as a k x n matrix, is the COC_W_KN layout.  Both
+ * layouts therefore cover the forward and the backward pairings:
+ *
+ *   RowParallelLinear forward:  AR / RS of X_r @ W_r^T        (COC_W_NK)
+ *   ColumnParallelLinear fwd:   AllGather(X) @ W_r^T           (COC_W_NK)
+ *   RowParallel backward, SP:   AllGather(dY) @ W_r            (COC_W_KN)
+ *   ColumnParallel backward SP: ReduceScatter(dY_r @ W_r)      (COC_W_KN)
+ *
+ * op       COC_OP_ALL_REDUCE / _REDUCE_SCATTER: (rows, cols, inner) =
+ *          (m, n, k_shard), x[r] m x k_shard, out[r] m x n (AR) or
+ *          (m/R) x n (RS).  COC_OP_ALL_GATHER / _V2: (rows, cols, inner) =
+ *          (m_shard, n_shard, k), x[r] m_shard x k, out[r] (R*m_shard) x n_shard.
+ * w[r]     COC_W_KN: inner x cols row-major; COC_W_NK: cols x inner row-major.
+ * gathered used by COC_OP_ALL_GATHER_V2 only (as in coc_all_gather_matmul_v2).
+ * Results, constraints, alignment and errors are those of the named entry
+ * point of the same operator; with COC_W_KN the call is identical to it.
+ * With COC_W_NK the products and their accumulation order are the same, so
+ * the result is bit-identical to the COC_W_KN call on the transposed weights.
+ */
+coc_status_t coc_fused_matmul(coc_op_t op, int R, int64_t rows, int64_t cols, int64_t inner,
+                              const void* const* x, const void* const* w, coc_wlayout_t layout,
+                              void* const* out, void* const* gathered, coc_dtype_t dt,
+                              int chunks, int deterministic, coc_stream_t stream);
 
 /*
  * Plain sharded contraction with a single output: out = round_rne(sum_r X_r @ W_r).

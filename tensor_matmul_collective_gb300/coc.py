@@ -28,7 +28,13 @@ EXPORTS = (
     "coc_all_gather_matmul_v2", "coc_matmul_all_reduce_w8a16", "coc_matmul",
     "coc_sync_status", "coc_status_string", "coc_last_error", "coc_version",
     "coc_debug_inject_timeout", "coc_shutdown", "coc_matmul_all_reduce_noalloc",
+    "coc_fused_matmul",
 )
+
+OP_ALL_REDUCE, OP_REDUCE_SCATTER, OP_ALL_GATHER, OP_ALL_GATHER_V2 = range(4)
+_OPS = {"all_reduce": OP_ALL_REDUCE, "reduce_scatter": OP_REDUCE_SCATTER,
+        "all_gather": OP_ALL_GATHER, "all_gather_v2": OP_ALL_GATHER_V2}
+W_KN, W_NK = 0, 1
 
 
 class CocError(RuntimeError):
@@ -63,6 +69,8 @@ def lib() -> ctypes.CDLL:
             L.coc_all_gather_matmul_v2.restype = i32
             L.coc_matmul_all_reduce_w8a16.argtypes = [i32, i64, i64, i64, pp, pp, pp, i32, i64, pp, i32, i32, vp]
             L.coc_matmul_all_reduce_w8a16.restype = i32
+            L.coc_fused_matmul.argtypes = [i32, i32, i64, i64, i64, pp, pp, i32, pp, pp, i32, i32, i32, vp]
+            L.coc_fused_matmul.restype = i32
             L.coc_matmul.argtypes = [i32, i64, i64, i64, pp, pp, vp, i32, vp]
             L.coc_matmul.restype = i32
             L.coc_sync_status.argtypes = [vp]
@@ -239,6 +247,49 @@ def matmul_all_reduce_w8a16(xs, wqs, scales, gran, group_size: int = 0, outs=Non
                                              int(group_size), _ptrs(outs), int(chunks), int(bool(deterministic)),
                                              _stream(stream)))
     return outs
+
+
+def fused_matmul(op, xs, ws, w_layout: str = "kn", outs=None, gathered=None, chunks: int = 1,
+                 deterministic: bool = False, stream=None):
+    """Any of the four fused operators with a choice of weight layout.
+
+    op: "all_reduce" | "reduce_scatter" | "all_gather" | "all_gather_v2".
+    w_layout: "kn" (W_r is inner x cols, as the named functions) or "nk"
+    (W_r is cols x inner: Megatron's [out_features, in_features]).
+    Returns outs, or (outs, gathered) for "all_gather_v2"."""
+    code = _OPS[op] if isinstance(op, str) else int(op)
+    nk = {"kn": False, "nk": True}[w_layout]
+    R, x0, w0 = _prep(xs, ws)
+    rows, inner = x0.shape
+    cols = w0.shape[0] if nk else w0.shape[1]
+    wshape = (cols, inner) if nk else (inner, cols)
+    _check_list(xs, "xs", (rows, inner), x0.dtype, x0.device)
+    _check_list(ws, "ws", wshape, x0.dtype, x0.device)
+    if code == OP_REDUCE_SCATTER:
+        if rows % R:
+            raise CocError(ERR_SHAPE, "COC_ERR_SHAPE", f"m = {rows} is not a multiple of R = {R}")
+        oshape = (rows // R, cols)
+    elif code in (OP_ALL_GATHER, OP_ALL_GATHER_V2):
+        oshape = (R * rows, cols)
+    else:
+        oshape = (rows, cols)
+    outs = _outs(outs, R, oshape, x0.dtype, x0.device)
+    if code == OP_ALL_GATHER_V2:
+        if gathered is None:
+            gathered = [torch.empty((R * rows, inner), dtype=x0.dtype, device=x0.device) for _ in range(R)]
+        elif len(gathered) != R:
+            raise ValueError("need one gathered entry per rank (None to skip)")
+        else:
+            present = [g for g in gathered if g is not None]
+            if present:
+                _check_list(present, "gathered", (R * rows, inner), x0.dtype, x0.device)
+        gptr = _ptrs(gathered)
+    else:
+        gptr = None
+    _check(lib().coc_fused_matmul(code, R, rows, cols, inner, _ptrs(xs), _ptrs(ws), W_NK if nk else W_KN,
+                                  _ptrs(outs), gptr, _dtype_code(x0.dtype), int(chunks), int(bool(deterministic)),
+                                  _stream(stream)))
+    return (outs, gathered) if code == OP_ALL_GATHER_V2 else outs
 
 
 def matmul(xs, ws, out=None, stream=None):

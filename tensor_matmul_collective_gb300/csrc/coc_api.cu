@@ -188,11 +188,15 @@ coc_status_t launch_checked(int op, bool bf16, bool pair, KParams& p, DeviceStat
 }
 
 // ---- row-parallel family: AR, RS, W8, plain ----------------------------------
+// w_nk: each W shard is stored n x k_shard (Megatron's [out, in]) instead of
+// k_shard x n; the kernel then reads B K-major.
 coc_status_t row_parallel(int op, int R, int64_t m, int64_t n, int64_t ks, const void* const* x,
                           const void* const* w, void* const* out, int n_out, coc_dtype_t dt, int chunks,
-                          const void* const* scale, coc_scale_t gran, int64_t group, cudaStream_t stream) {
+                          const void* const* scale, coc_scale_t gran, int64_t group, cudaStream_t stream,
+                          bool w_nk = false) {
     KParams p;
     std::memset(&p, 0, sizeof p);
+    p.b_kmajor = w_nk ? 1 : 0;
     p.R = R;
     p.n_out = n_out;
     p.m = static_cast<int>(m);
@@ -225,6 +229,8 @@ coc_status_t row_parallel(int op, int R, int64_t m, int64_t n, int64_t ks, const
             if (w8) {
                 st = encode(&p.tm_b[r], CU_TENSOR_MAP_DATA_TYPE_UINT8, w[r], n, ks, n, pair ? BN / 2 : BN, BK,
                             CU_TENSOR_MAP_SWIZZLE_NONE);
+            } else if (w_nk) {
+                st = encode(&p.tm_b[r], adt, w[r], ks, n, ks * 2, BK, pair ? BN / 2 : BN, CU_TENSOR_MAP_SWIZZLE_128B);
             } else {
                 st = encode(&p.tm_b[r], adt, w[r], n, ks, n * 2, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B);
             }
@@ -329,7 +335,7 @@ namespace {
 
 coc_status_t all_gather(int R, int64_t ms, int64_t ns, int64_t k, const void* const* x, const void* const* w,
                         void* const* out, void* const* gathered, bool v2, coc_dtype_t dt, int chunks, int det,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, bool w_nk = false) {
     coc_status_t st;
     if ((st = check_common(R, chunks, dt, det)) != COC_OK) return st;
     if ((st = check_dims(ms, ns, k)) != COC_OK) return st;
@@ -368,6 +374,7 @@ coc_status_t all_gather(int R, int64_t ms, int64_t ns, int64_t k, const void* co
     p.a_box_rows = largest_pow2_divisor_le(ms, BM);
     p.store_rows = 32;
     p.has_gather = (v2 && k > 0) ? 1 : 0;
+    p.b_kmajor = w_nk ? 1 : 0;
     // The gathered X is re-read by every (rank, n-tile) column.  Take the
     // row tiles in groups whose X rows fit comfortably in L2 (32 MiB) and
     // mark those loads evict-last, so W streams past a resident X slice:
@@ -382,7 +389,9 @@ coc_status_t all_gather(int R, int64_t ms, int64_t ns, int64_t k, const void* co
     for (int r = 0; r < R; ++r) {
         if (k > 0) {
             if ((st = encode(&p.tm_a[r], tdt, x[r], k, ms, k * 2, BK, p.a_box_rows, CU_TENSOR_MAP_SWIZZLE_128B)) != COC_OK) return st;
-            if ((st = encode(&p.tm_b[r], tdt, w[r], ns, k, ns * 2, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B)) != COC_OK) return st;
+            st = w_nk ? encode(&p.tm_b[r], tdt, w[r], k, ns, k * 2, BK, pair ? BN / 2 : BN, CU_TENSOR_MAP_SWIZZLE_128B)
+                      : encode(&p.tm_b[r], tdt, w[r], ns, k, ns * 2, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B);
+            if (st != COC_OK) return st;
         }
         if ((st = encode(&p.tm_out[r], tdt, out[r], ns, m, ns * 2, EPI_COLS, p.store_rows, CU_TENSOR_MAP_SWIZZLE_128B)) != COC_OK)
             return st;
@@ -407,6 +416,39 @@ COC_API coc_status_t coc_all_gather_matmul_v2(int R, int64_t m_shard, int64_t n_
                                               coc_dtype_t dt, int chunks, int deterministic, coc_stream_t stream) {
     return all_gather(R, m_shard, n_shard, k, x, w, out, gathered, true, dt, chunks, deterministic,
                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+COC_API coc_status_t coc_fused_matmul(coc_op_t op, int R, int64_t rows, int64_t cols, int64_t inner,
+                                      const void* const* x, const void* const* w, coc_wlayout_t layout,
+                                      void* const* out, void* const* gathered, coc_dtype_t dt, int chunks,
+                                      int deterministic, coc_stream_t stream) {
+    if (layout != COC_W_KN && layout != COC_W_NK)
+        return fail(COC_ERR_INVALID_ARG, "unknown weight layout %d", static_cast<int>(layout));
+    const bool nk = (layout == COC_W_NK);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    coc_status_t st;
+    switch (op) {
+        case COC_OP_ALL_REDUCE:
+            st = validate_row_parallel(R, rows, cols, inner, x, w, out, R, dt, chunks, deterministic, 2);
+            if (st != COC_OK || rows == 0 || cols == 0) return st;
+            return row_parallel(OP_AR, R, rows, cols, inner, x, w, out, R, dt, chunks, nullptr, COC_SCALE_TENSOR, 0,
+                                s, nk);
+        case COC_OP_REDUCE_SCATTER:
+            st = validate_row_parallel(R, rows, cols, inner, x, w, out, R, dt, chunks, deterministic, 2);
+            if (st != COC_OK) return st;
+            if (rows % R != 0) return fail(COC_ERR_SHAPE, "ReduceScatter: m = %lld is not a multiple of R = %d", (long long)rows, R);
+            if ((rows / R) % 8 != 0)
+                return fail(COC_ERR_SHAPE, "ReduceScatter: m / R = %lld is not a multiple of 8", (long long)(rows / R));
+            if (rows == 0 || cols == 0) return COC_OK;
+            return row_parallel(OP_RS, R, rows, cols, inner, x, w, out, R, dt, chunks, nullptr, COC_SCALE_TENSOR, 0,
+                                s, nk);
+        case COC_OP_ALL_GATHER:
+            return all_gather(R, rows, cols, inner, x, w, out, nullptr, false, dt, chunks, deterministic, s, nk);
+        case COC_OP_ALL_GATHER_V2:
+            return all_gather(R, rows, cols, inner, x, w, out, gathered, true, dt, chunks, deterministic, s, nk);
+        default:
+            return fail(COC_ERR_INVALID_ARG, "unknown operator %d", static_cast<int>(op));
+    }
 }
 
 COC_API coc_status_t coc_sync_status(coc_stream_t stream) {

@@ -628,9 +628,15 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
                         if constexpr (!W8) {
                             const CUtensorMap* bm = &p.tm_b[(OP == OP_AG) ? r : ks];
                             const uint32_t b_dst = smem_u32(b_st + stage * C::B_BYTES);
+                            if (p.b_kmajor) {
+                                // W stored n x k: one box of this CTA's B rows (n) x 64 k, laid
+                                // out like the A tile (K-major, 128-byte swizzle)
+                                load(b_dst, bm, kc, col_base, pol_b);
+                            } else {
 #pragma unroll
-                            for (int j = 0; j < C::BN_CTA / 64; ++j)
-                                load(b_dst + j * (64 * BK * 2), bm, col_base + j * 64, kc, pol_b);
+                                for (int j = 0; j < C::BN_CTA / 64; ++j)
+                                    load(b_dst + j * (64 * BK * 2), bm, col_base + j * 64, kc, pol_b);
+                            }
                         }
                         filled |= 1u << stage;
                         fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
@@ -673,7 +679,10 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
         // ================================================= MMA issuer ===
         // (with PAIR only the leader issues; the peer's warp 1 just owns its TMEM)
         if (rank == 0) {
-            constexpr uint32_t idesc = make_idesc(BF16, TILE_M, BN);
+            // B K-major (W stored n x k) clears the "B transposed" bit of the descriptor
+            const uint32_t idesc = make_idesc(BF16, TILE_M, BN) & (p.b_kmajor ? ~(1u << 16) : ~0u);
+            const uint32_t b_lbo = p.b_kmajor ? 16u : 64u * BK * 2u;
+            const uint64_t b_step = p.b_kmajor ? 2u : 128u;   // 16-element k step, in 16-byte units
             uint32_t stage = 0, phase = 0, bstage = 0, bphase = 0;
             int acc_i = 0;
             bool ok = true;
@@ -691,14 +700,13 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
                     tc_fence_after();
                     if (lane == 0) {
                         const uint64_t ad = make_sdesc(smem_u32(a_st + stage * A_STAGE_BYTES), 16, 1024);
-                        const uint64_t bd =
-                            make_sdesc(smem_u32(b_st + (W8 ? bstage : stage) * C::B_BYTES), 64 * BK * 2, 1024);
+                        const uint64_t bd = make_sdesc(smem_u32(b_st + (W8 ? bstage : stage) * C::B_BYTES), b_lbo, 1024);
 #pragma unroll
                         for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                            // A: +32 bytes per 16-element k step inside the 128-byte swizzle row
-                            // B: +2 eight-row groups (2 KiB) per 16-element k step
+                            // A (and K-major B): +32 bytes per 16-element k step inside the
+                            // 128-byte swizzle row; MN-major B: +2 eight-row groups (2 KiB)
                             const uint64_t a_k = ad + static_cast<uint64_t>(kk * 2);
-                            const uint64_t b_k = bd + static_cast<uint64_t>(kk * 128);
+                            const uint64_t b_k = bd + static_cast<uint64_t>(kk) * b_step;
                             const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
                             if constexpr (PAIR) tc_mma_f16_pair(d_tmem, a_k, b_k, idesc, acc);
                             else tc_mma_f16(d_tmem, a_k, b_k, idesc, acc);

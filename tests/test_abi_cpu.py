@@ -151,3 +151,16 @@ def test_binding_rejects_cpu_tensors():
     xs = [torch.zeros(8, 8, dtype=torch.bfloat16)] * 2
     with pytest.raises(ValueError):
         coc.matmul_all_reduce(xs, xs)
+
+
+def test_fused_matmul_rejects_bad_enums(L):
+    x = _arr([A] * 2)
+    # unknown weight layout / operator: rejected before any CUDA call
+    assert L.coc_fused_matmul(0, 2, 64, 128, 128, x, x, 2, x, None, 1, 1, 0, None) == coc.ERR_INVALID_ARG
+    assert L.coc_fused_matmul(7, 2, 64, 128, 128, x, x, 0, x, None, 1, 1, 0, None) == coc.ERR_INVALID_ARG
+    # the named operators' checks apply: m % chunks, RS rows, V2 needs `gathered`
+    assert L.coc_fused_matmul(0, 2, 66, 128, 128, x, x, 1, x, None, 1, 4, 0, None) == coc.ERR_SHAPE
+    assert L.coc_fused_matmul(1, 4, 48, 128, 128, _arr([A] * 4), _arr([A] * 4), 1, _arr([A] * 4), None, 1, 1, 0,
+                              None) == coc.ERR_SHAPE
+    assert L.coc_fused_matmul(3, 2, 16, 64, 64, x, x, 1, x, None, 1, 1, 0, None) == coc.ERR_INVALID_ARG
+    assert L.coc_fused_matmul(0, 2, 0, 128, 128, x, x, 1, x, None, 1, 1, 0, None) == coc.OK   # empty: no-op
