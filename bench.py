@@ -388,6 +388,46 @@ def time_context(ops, dev):
         out[op.name] = {"fused_ms": round(tf, 4), "all_gather_matmul_ms": round(t_ag, 4),
                         "plain_epilogue_ms": round(t_plain, 4), "fused_overhead": round(tf / t_plain - 1.0, 4),
                         "torch_unfused_ms": round(tu, 4)}
+    # The pages' Python-script CoC (CoC page, Python脚本层面实现): the left
+    # operand is cut along m into C chunks; each chunk's per-rank matmuls and
+    # reduction run on a compute stream while the previous chunk's
+    # "collective" (the reduced rows copied into every rank's buffer) runs on
+    # a second stream.  2 + R launches per chunk from the host.
+    ar7 = [o for o in ops if o.name == "bloom7b_ar"]
+    if ar7:
+        op = ar7[0]
+        s = op.shape
+        dx, dw = op.inputs[:s.R], op.inputs[s.R:2 * s.R]
+        outs = op.outputs
+        comp, comm = torch.cuda.Stream(), torch.cuda.Stream()
+
+        def python_coc(C):
+            rows = s.m // C
+            cur = torch.cuda.current_stream()
+            comp.wait_stream(cur)
+            comm.wait_stream(cur)
+            for c in range(C):
+                sl = slice(c * rows, (c + 1) * rows)
+                with torch.cuda.stream(comp):
+                    acc = torch.matmul(dx[0][sl], dw[0]).float()
+                    for r in range(1, s.R):
+                        acc += torch.matmul(dx[r][sl], dw[r]).float()
+                    red = acc.to(s.dtype)
+                    ev = torch.cuda.Event()
+                    ev.record(comp)
+                with torch.cuda.stream(comm):
+                    comm.wait_event(ev)
+                    for r in range(s.R):
+                        outs[r][sl].copy_(red)
+                    red.record_stream(comm)
+            cur.wait_stream(comp)
+            cur.wait_stream(comm)
+        fused = {}
+        for C in (1, 2, 4, 8):
+            fused[C] = t(lambda C=C: coc.matmul_all_reduce(dx, dw, outs, chunks=C))
+        out["bloom7b_ar_python_chunking"] = {
+            "python_chunked_ms": {str(C): round(t(lambda C=C: python_coc(C), 5), 4) for C in (1, 2, 4, 8)},
+            "fused_ms": {str(C): round(v, 4) for C, v in fused.items()}}
     return out
 
 
