@@ -84,16 +84,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
-                                            uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
-        : "memory");
-}
-
-// Same, with an L2 eviction-priority policy for the loaded lines.
+// TMA tile load into shared memory with an L2 eviction-priority policy for the loaded lines.
 __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map, int c0, int c1,
                                                  uint32_t bar, uint64_t policy) {
     asm volatile(
@@ -439,30 +430,66 @@ __device__ __forceinline__ void load_w8_scales(const KParams& p, const __half* s
     }
 }
 
-// ALL_GATHER_MATMUL_V2: copy this unit's share of the m-tile's gathered
-// rows to every rank's gather buffer.  The tile's rows are one contiguous run
-// of the gathered matrix; it is cut into R * n_tiles equal pieces, one per
-// work unit of this m-tile, so the copy is spread over the whole kernel.
-// Kept out of line: it runs once per unit, after the tile's epilogue.
-__device__ __noinline__ void gather_slice(const KParams& p, int r, int mt, int nt, int tile_m, int tid,
-                                          int nthreads) {
+// Bulk copies (no tensor map): global -> this CTA's shared memory completing
+// on a barrier, and shared memory -> global in the bulk-group of the thread.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(dst)),
+                 "r"(src), "r"(bytes)
+                 : "memory");
+}
+
+// ALL_GATHER_MATMUL_V2: copy this unit's share of the m-tile's gathered rows
+// to every rank's gather buffer.  The tile's rows are one contiguous run of
+// the gathered matrix; it is cut into R * n_tiles equal pieces, one per work
+// unit of this m-tile (so the copy is spread over the whole kernel), and this
+// unit's piece is cut again between the epilogue warps (`wi` of `nw`).  One
+// thread per warp streams its part through the warp's two 4 KiB staging
+// buffers with the bulk-copy engine: a global -> shared copy completing on
+// the warp's barrier `gbar`, then one shared -> global copy per rank.  Pieces
+// never cross a shard boundary (the source is contiguous within a shard).
+// Returns false if a bounded wait ran out (the CTA is aborting).
+__device__ __noinline__ bool gather_slice_bulk(const KParams& p, int r, int mt, int nt, int tile_m, int wi, int nw,
+                                               uint8_t* my_epi, int& sb_i, uint32_t gbar, uint32_t& gphase,
+                                               const Ctl& ctl) {
     const int rows = min(tile_m, p.m - mt * tile_m);
     const long long vpr = p.k / 8;   // 16-byte vectors per row
     const long long total = rows * vpr;
     const long long Q = static_cast<long long>(p.R) * p.n_tiles;
     const long long qi = static_cast<long long>(r) * p.n_tiles + nt;
-    const long long v0 = total * qi / Q, v1 = total * (qi + 1) / Q;
-    for (long long vv = v0 + tid; vv < v1; vv += nthreads) {
-        const int lr = static_cast<int>(vv / vpr);
+    const long long u0 = total * qi / Q, u1 = total * (qi + 1) / Q;
+    const long long a = u0 + (u1 - u0) * wi / nw, b = u0 + (u1 - u0) * (wi + 1) / nw;
+    const long long tile_base = static_cast<long long>(mt) * tile_m * p.k;   // elements
+    constexpr long long kPiece = EPI_BUF_BYTES / 16;                          // vectors per staging buffer
+    for (long long vv = a; vv < b;) {
+        const long long lr = vv / vpr;
+        const int g = mt * tile_m + static_cast<int>(lr);
+        const int sh = g / p.rows_per_rank;
+        const long long shard_end = (static_cast<long long>(sh + 1) * p.rows_per_rank - mt * tile_m) * vpr;
+        long long lim = vv + kPiece;
+        if (lim > b) lim = b;
+        if (lim > shard_end) lim = shard_end;
+        const uint32_t bytes = static_cast<uint32_t>((lim - vv) * 16);
         const long long c = vv - lr * vpr;
-        const int g = mt * tile_m + lr;
-        const int s = g / p.rows_per_rank;
-        const int l = g - s * p.rows_per_rank;
-        const uint4 val = __ldg(reinterpret_cast<const uint4*>(p.gsrc[s] + static_cast<long long>(l) * p.k + c * 8));
-        const long long off = static_cast<long long>(g) * p.k + c * 8;
+        const uint16_t* src = p.gsrc[sh] + (static_cast<long long>(g - sh * p.rows_per_rank) * p.k + c * 8);
+        const uint32_t buf = smem_u32(my_epi + (sb_i & 1) * EPI_BUF_BYTES);
+        ++sb_i;
+        bulk_wait_read<1>();   // the stores that last read this buffer are done
+        mbar_expect_tx(gbar, bytes);
+        bulk_g2s(buf, src, bytes, gbar);
+        if (!wait_bounded(gbar, gphase, ctl, 0x320u, COC_WAIT_NS)) return false;
+        gphase ^= 1u;
+        const long long off = tile_base + vv * 8;
         for (int d = 0; d < p.R; ++d)
-            if (p.gdst[d] != nullptr) __stcs(reinterpret_cast<uint4*>(p.gdst[d] + off), val);
+            if (p.gdst[d] != nullptr) bulk_s2g(p.gdst[d] + off, buf, bytes);
+        bulk_commit();
+        vv = lim;
     }
+    return true;
 }
 
 // ------------------------------------------------------------ the kernel ---
@@ -519,7 +546,8 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
     uint64_t* acce = accf + 2;         // [2]  accumulator drained by the epilogue (leader: both CTAs)
     uint64_t* never = acce + 2;        // [1]  nothing arrives here (fault-injection test)
     uint64_t* drain = never + 1;       // [1]  MMA drain before TMEM release
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* gbar = drain + 1;        // [NUM_EPI_WARPS] AG-V2 gather copies (global -> shared)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbar + NUM_EPI_WARPS);
     uint32_t* abort_word = tmem_slot + 1;
     // w8A16 pair: 16-byte landing slots for the peer's per-stage "B half ready" copies
     uint8_t* sig_slots = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(abort_word + 1) + 15) & ~uintptr_t(15));
@@ -551,6 +579,7 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
         }
         mbar_init(smem_u32(never), 1);
         mbar_init(smem_u32(drain), 1);
+        for (int w = 0; w < NUM_EPI_WARPS; ++w) mbar_init(smem_u32(&gbar[w]), 1);
         *abort_word = 0u;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         fence_proxy_async_smem();
@@ -742,10 +771,10 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
     } else if (warp < 2 + NUM_EPI_WARPS) {
         // ================================================= epilogue ===
         const int q = warp & 3;                 // TMEM lane quadrant this warp may read
-        const int et = (warp - 2) * 32 + lane;  // 0..127 among this CTA's epilogue threads
         uint8_t* my_epi = epi + (warp - 2) * 2 * EPI_BUF_BYTES;
         const uint32_t acce_base = PAIR ? map_to_rank(smem_u32(acce), 0) : smem_u32(acce);
         int acc_i = 0, sb_i = 0;
+        uint32_t gphase = 0;   // AG-V2: phase of this warp's gather barrier
         bool ok = true;
         if (p.inject_timeout) ok = warp_wait(smem_u32(never), 0, ctl, 0x300u);
         for (int u = first_unit; ok && u < p.units; u += unit_step) {
@@ -816,9 +845,16 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
             }
             ++acc_i;
             if constexpr (OP == OP_AG) {
-                if (p.has_gather)
-                    gather_slice(p, r, mt, nt, TILE_M, static_cast<int>(rank) * 32 * NUM_EPI_WARPS + et,
-                                 NPAIR * 32 * NUM_EPI_WARPS);
+                if (p.has_gather) {
+                    bool ok_g = true;
+                    if (lane == 0)
+                        ok_g = gather_slice_bulk(p, r, mt, nt, TILE_M,
+                                                 static_cast<int>(rank) * NUM_EPI_WARPS + (warp - 2),
+                                                 NPAIR * NUM_EPI_WARPS, my_epi, sb_i, smem_u32(&gbar[warp - 2]),
+                                                 gphase, ctl);
+                    sb_i = __shfl_sync(0xffffffffu, sb_i, 0);
+                    ok = __shfl_sync(0xffffffffu, ok_g ? 1 : 0, 0) != 0;
+                }
             }
         }
         if (lane == 0) bulk_wait_all();
