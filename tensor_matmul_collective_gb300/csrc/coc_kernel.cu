@@ -516,7 +516,10 @@ struct Cfg {
     static_assert(!W8 || (SB % XFORM_GROUPS == 0 && SR % XFORM_GROUPS == 0), "rings must split between groups");
     static constexpr int WARPS = 2 + NUM_EPI_WARPS + (W8 ? NUM_XFORM_WARPS : 0);
     static constexpr int THREADS = WARPS * 32;
-    static constexpr int EPI_BYTES = NUM_EPI_WARPS * 2 * EPI_BUF_BYTES;
+    // Epilogue staging buffers per warp: two (a sub-tile's stores drain while the
+    // next is written) except for w8A16, which trades the second for ring depth.
+    static constexpr int EPI_NBUF = W8 ? 1 : 2;
+    static constexpr int EPI_BYTES = NUM_EPI_WARPS * EPI_NBUF * EPI_BUF_BYTES;
     static constexpr int BAR_BYTES = 512;
     static constexpr int SMEM = 1024 + SA * A_STAGE_BYTES + (W8 ? SB * B_BYTES : SA * B_BYTES) + SR * RAW_BYTES +
                                 EPI_BYTES + BAR_BYTES;
@@ -771,7 +774,7 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
     } else if (warp < 2 + NUM_EPI_WARPS) {
         // ================================================= epilogue ===
         const int q = warp & 3;                 // TMEM lane quadrant this warp may read
-        uint8_t* my_epi = epi + (warp - 2) * 2 * EPI_BUF_BYTES;
+        uint8_t* my_epi = epi + (warp - 2) * C::EPI_NBUF * EPI_BUF_BYTES;
         const uint32_t acce_base = PAIR ? map_to_rank(smem_u32(acce), 0) : smem_u32(acce);
         int acc_i = 0, sb_i = 0;
         uint32_t gphase = 0;   // AG-V2: phase of this warp's gather barrier
@@ -808,9 +811,13 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
                 }
                 const int col = nt * BN + sub * EPI_COLS;
                 if (col >= p.n || row0 >= p.m) continue;   // sub-tile entirely outside the output
-                uint8_t* sbuf = my_epi + (sb_i & 1) * EPI_BUF_BYTES;
+                uint8_t* sbuf = my_epi + (sb_i % C::EPI_NBUF) * EPI_BUF_BYTES;
                 ++sb_i;
-                if (lane == 0) bulk_wait_read<1>();   // the store that last read this buffer is done
+                // the stores that last read this buffer are done
+                if (lane == 0) {
+                    if constexpr (C::EPI_NBUF == 2) bulk_wait_read<1>();
+                    else bulk_wait_read<0>();
+                }
                 __syncwarp();
                 uint8_t* rowp = sbuf + lane * 128;
 #pragma unroll
