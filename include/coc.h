@@ -95,7 +95,8 @@ typedef enum {
     COC_OP_ALL_REDUCE = 0,      /* MATMUL_ALL_REDUCE */
     COC_OP_REDUCE_SCATTER = 1,  /* MATMUL_REDUCE_SCATTER */
     COC_OP_ALL_GATHER = 2,      /* ALL_GATHER_MATMUL */
-    COC_OP_ALL_GATHER_V2 = 3    /* ALL_GATHER_MATMUL_V2 */
+    COC_OP_ALL_GATHER_V2 = 3,   /* ALL_GATHER_MATMUL_V2 */
+    COC_OP_WEIGHT_GRAD = 4      /* per-rank weight gradient dW_r = dY_r^T X_r (no collective) */
 } coc_op_t;
 
 /* Storage of each weight shard. */
@@ -222,11 +223,20 @@ coc_status_t coc_matmul_all_reduce_w8a16(int R, int64_t m, int64_t n, int64_t k_
  *   RowParallel backward, SP:   AllGather(dY) @ W_r            (COC_W_KN)
  *   ColumnParallel backward SP: ReduceScatter(dY_r @ W_r)      (COC_W_KN)
  *
+ * The weight-gradient pass completes the pairings: dW_r = dY_r^T X_r, with
+ * X_r the layer input as rank r holds it after the forward pass — for a
+ * ColumnParallel layer with SP, the gathered input ALL_GATHER_MATMUL_V2
+ * returned (the reason V2 returns it), for a RowParallel layer its own X_r.
+ *
  * op       COC_OP_ALL_REDUCE / _REDUCE_SCATTER: (rows, cols, inner) =
  *          (m, n, k_shard), x[r] m x k_shard, out[r] m x n (AR) or
  *          (m/R) x n (RS).  COC_OP_ALL_GATHER / _V2: (rows, cols, inner) =
  *          (m_shard, n_shard, k), x[r] m_shard x k, out[r] (R*m_shard) x n_shard.
  * w[r]     COC_W_KN: inner x cols row-major; COC_W_NK: cols x inner row-major.
+ *          COC_OP_WEIGHT_GRAD: (rows, cols, inner) = (out_features, in_features,
+ *          tokens); x[r] = dY_r, inner x rows; w[r] = X_r, inner x cols
+ *          (COC_W_KN only); out[r] = dW_r, rows x cols ([out, in], Megatron's
+ *          weight layout).  rows % 8 == 0, cols % 8 == 0, rows % chunks == 0.
  * gathered used by COC_OP_ALL_GATHER_V2 only (as in coc_all_gather_matmul_v2).
  * Results, constraints, alignment and errors are those of the named entry
  * point of the same operator; with COC_W_KN the call is identical to it.

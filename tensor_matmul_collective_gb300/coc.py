@@ -31,7 +31,7 @@ EXPORTS = (
     "coc_fused_matmul",
 )
 
-OP_ALL_REDUCE, OP_REDUCE_SCATTER, OP_ALL_GATHER, OP_ALL_GATHER_V2 = range(4)
+OP_ALL_REDUCE, OP_REDUCE_SCATTER, OP_ALL_GATHER, OP_ALL_GATHER_V2, OP_WEIGHT_GRAD = range(5)
 _OPS = {"all_reduce": OP_ALL_REDUCE, "reduce_scatter": OP_REDUCE_SCATTER,
         "all_gather": OP_ALL_GATHER, "all_gather_v2": OP_ALL_GATHER_V2}
 W_KN, W_NK = 0, 1
@@ -290,6 +290,23 @@ def fused_matmul(op, xs, ws, w_layout: str = "kn", outs=None, gathered=None, chu
                                   _ptrs(outs), gptr, _dtype_code(x0.dtype), int(chunks), int(bool(deterministic)),
                                   _stream(stream)))
     return (outs, gathered) if code == OP_ALL_GATHER_V2 else outs
+
+
+def weight_grad(dys, xs, outs=None, chunks: int = 1, stream=None):
+    """Weight gradient of a TP linear layer on every rank: outs[r] = dys[r]^T @ xs[r].
+
+    dys[r]: tokens x out_features, xs[r]: tokens x in_features (for a
+    ColumnParallel layer with sequence parallelism, the gathered input that
+    all_gather_matmul_v2 returned), outs[r]: out_features x in_features."""
+    R, d0, x0 = _prep(dys, xs)
+    inner, rows = d0.shape
+    cols = x0.shape[1]
+    _check_list(dys, "dys", (inner, rows), d0.dtype, d0.device)
+    _check_list(xs, "xs", (inner, cols), d0.dtype, d0.device)
+    outs = _outs(outs, R, (rows, cols), d0.dtype, d0.device)
+    _check(lib().coc_fused_matmul(OP_WEIGHT_GRAD, R, rows, cols, inner, _ptrs(dys), _ptrs(xs), W_KN, _ptrs(outs),
+                                  None, _dtype_code(d0.dtype), int(chunks), 1, _stream(stream)))
+    return outs
 
 
 def matmul(xs, ws, out=None, stream=None):

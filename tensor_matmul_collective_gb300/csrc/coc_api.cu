@@ -418,6 +418,68 @@ COC_API coc_status_t coc_all_gather_matmul_v2(int R, int64_t m_shard, int64_t n_
                       reinterpret_cast<cudaStream_t>(stream));
 }
 
+namespace coc {
+namespace {
+
+// Weight gradient of a TP linear layer: dW_r = dY_r^T X_r for every rank r
+// (no collective).  dY_r is inner x rows (tokens x out_features), X_r inner x
+// cols (tokens x in_features), dW_r rows x cols.  Runs on the AllGather path
+// of the kernel with A read per rank and MN-major.
+coc_status_t weight_grad(int R, int64_t rows, int64_t cols, int64_t inner, const void* const* dy,
+                         const void* const* x, void* const* out, coc_dtype_t dt, int chunks, int det,
+                         cudaStream_t stream) {
+    coc_status_t st;
+    if ((st = check_common(R, chunks, dt, det)) != COC_OK) return st;
+    if ((st = check_dims(rows, cols, inner)) != COC_OK) return st;
+    const bool empty = (rows == 0 || cols == 0);
+    if ((st = check_ptrs(dy, R, !empty && inner > 0, "x (dY)")) != COC_OK) return st;
+    if ((st = check_ptrs(x, R, !empty && inner > 0, "w (X)")) != COC_OK) return st;
+    if ((st = check_ptrs(out, R, !empty, "out")) != COC_OK) return st;
+    if (rows % chunks != 0) return fail(COC_ERR_SHAPE, "rows = %lld is not a multiple of chunks = %d", (long long)rows, chunks);
+    if ((rows * 2) % 16 != 0) return fail(COC_ERR_ALIGN, "rows = %lld: dY rows must span a multiple of 16 bytes", (long long)rows);
+    if ((cols * 2) % 16 != 0) return fail(COC_ERR_ALIGN, "cols = %lld: X rows must span a multiple of 16 bytes", (long long)cols);
+    if (empty) return COC_OK;
+
+    KParams p;
+    std::memset(&p, 0, sizeof p);
+    const bool pair = use_pair(OP_AG, rows);
+    const int tile_m = pair ? 2 * BM : BM;
+    p.R = R;
+    p.n_out = R;
+    p.m = static_cast<int>(rows);
+    p.n = static_cast<int>(cols);
+    p.k = static_cast<int>(inner);
+    p.num_kshards = 1;
+    p.kblocks = static_cast<int>((inner + BK - 1) / BK);
+    p.m_tiles = static_cast<int>((rows + tile_m - 1) / tile_m);
+    p.n_tiles = static_cast<int>((cols + BN - 1) / BN);
+    p.units = R * p.m_tiles * p.n_tiles;
+    p.chunk_mt = chunk_m_tiles(rows, chunks, tile_m);
+    p.rows_per_rank = static_cast<int>(rows);
+    p.a_box_rows = BM;
+    p.store_rows = 32;
+    p.a_mnmajor = 1;
+
+    DeviceState* ds = nullptr;
+    if ((st = device_state(&ds)) != COC_OK) return st;
+    const CUtensorMapDataType tdt = tma_dtype(dt);
+    for (int r = 0; r < R; ++r) {
+        if (inner > 0) {
+            if ((st = encode(&p.tm_a[r], tdt, dy[r], rows, inner, rows * 2, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B)) != COC_OK)
+                return st;
+            if ((st = encode(&p.tm_b[r], tdt, x[r], cols, inner, cols * 2, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B)) != COC_OK)
+                return st;
+        }
+        if ((st = encode(&p.tm_out[r], tdt, out[r], cols, rows, cols * 2, EPI_COLS, p.store_rows,
+                         CU_TENSOR_MAP_SWIZZLE_128B)) != COC_OK)
+            return st;
+    }
+    return launch_checked(OP_AG, dt == COC_BF16, pair, p, ds, stream);
+}
+
+}  // namespace
+}  // namespace coc
+
 COC_API coc_status_t coc_fused_matmul(coc_op_t op, int R, int64_t rows, int64_t cols, int64_t inner,
                                       const void* const* x, const void* const* w, coc_wlayout_t layout,
                                       void* const* out, void* const* gathered, coc_dtype_t dt, int chunks,
@@ -446,6 +508,9 @@ COC_API coc_status_t coc_fused_matmul(coc_op_t op, int R, int64_t rows, int64_t 
             return all_gather(R, rows, cols, inner, x, w, out, nullptr, false, dt, chunks, deterministic, s, nk);
         case COC_OP_ALL_GATHER_V2:
             return all_gather(R, rows, cols, inner, x, w, out, gathered, true, dt, chunks, deterministic, s, nk);
+        case COC_OP_WEIGHT_GRAD:
+            if (nk) return fail(COC_ERR_INVALID_ARG, "the weight-gradient pass takes X as tokens x in_features (COC_W_KN)");
+            return weight_grad(R, rows, cols, inner, x, w, out, dt, chunks, deterministic, s);
         default:
             return fail(COC_ERR_INVALID_ARG, "unknown operator %d", static_cast<int>(op));
     }

@@ -63,6 +63,7 @@ struct KParams {
     int has_gather;    // AG-V2
     int a_hint, b_hint;  // L2 policy of A / B loads: 0 evict_normal, 1 evict_first, 2 evict_last
     int b_kmajor;      // W stored n x k (K-major B operand) instead of k x n
+    int a_mnmajor;     // weight gradient: A = dY_r^T read MN-major from rank r's dY (AG path only)
 };
 
 // Argument checks of coc_matmul_all_reduce and the per-thread error text

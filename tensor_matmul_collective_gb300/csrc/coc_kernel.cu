@@ -644,7 +644,13 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
                         if constexpr (OP == OP_AG) {
                             // gathered rows -> (shard, local row); rows past the
                             // end read beyond the last shard and are zero-filled
-                            if (p.a_box_rows == BM) {
+                            if (p.a_mnmajor) {
+                                // weight gradient: A = dY_r^T, read from rank r's dY (tokens x
+                                // rows) as two 64-row blocks of 64 tokens (MN-major, like B)
+#pragma unroll
+                                for (int j = 0; j < BM / 64; ++j)
+                                    load(a_dst + j * (64 * BK * 2), &p.tm_a[r], row_base + j * 64, kc, pol_a);
+                            } else if (p.a_box_rows == BM) {
                                 load(a_dst, &p.tm_a[a_shard], kc, a_row, pol_a);
                             } else {
                                 for (int rb = 0; rb < BM; rb += p.a_box_rows) {
@@ -711,8 +717,12 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
         // ================================================= MMA issuer ===
         // (with PAIR only the leader issues; the peer's warp 1 just owns its TMEM)
         if (rank == 0) {
-            // B K-major (W stored n x k) clears the "B transposed" bit of the descriptor
-            const uint32_t idesc = make_idesc(BF16, TILE_M, BN) & (p.b_kmajor ? ~(1u << 16) : ~0u);
+            // B K-major (W stored n x k) clears the "B transposed" bit; an MN-major A
+            // (the weight-gradient pass) sets the "A transposed" bit
+            const uint32_t idesc =
+                (make_idesc(BF16, TILE_M, BN) & (p.b_kmajor ? ~(1u << 16) : ~0u)) | (p.a_mnmajor ? (1u << 15) : 0u);
+            const uint32_t a_lbo = p.a_mnmajor ? 64u * BK * 2u : 16u;
+            const uint64_t a_step = p.a_mnmajor ? 128u : 2u;
             const uint32_t b_lbo = p.b_kmajor ? 16u : 64u * BK * 2u;
             const uint64_t b_step = p.b_kmajor ? 2u : 128u;   // 16-element k step, in 16-byte units
             uint32_t stage = 0, phase = 0, bstage = 0, bphase = 0;
@@ -731,13 +741,13 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
                     if (!ok) break;
                     tc_fence_after();
                     if (lane == 0) {
-                        const uint64_t ad = make_sdesc(smem_u32(a_st + stage * A_STAGE_BYTES), 16, 1024);
+                        const uint64_t ad = make_sdesc(smem_u32(a_st + stage * A_STAGE_BYTES), a_lbo, 1024);
                         const uint64_t bd = make_sdesc(smem_u32(b_st + (W8 ? bstage : stage) * C::B_BYTES), b_lbo, 1024);
 #pragma unroll
                         for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                            // A (and K-major B): +32 bytes per 16-element k step inside the
-                            // 128-byte swizzle row; MN-major B: +2 eight-row groups (2 KiB)
-                            const uint64_t a_k = ad + static_cast<uint64_t>(kk * 2);
+                            // K-major operand: +32 bytes per 16-element k step inside the
+                            // 128-byte swizzle row; MN-major operand: +2 eight-row groups (2 KiB)
+                            const uint64_t a_k = ad + static_cast<uint64_t>(kk) * a_step;
                             const uint64_t b_k = bd + static_cast<uint64_t>(kk) * b_step;
                             const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
                             if constexpr (PAIR) tc_mma_f16_pair(d_tmem, a_k, b_k, idesc, acc);

@@ -164,3 +164,13 @@ def test_fused_matmul_rejects_bad_enums(L):
                               None) == coc.ERR_SHAPE
     assert L.coc_fused_matmul(3, 2, 16, 64, 64, x, x, 1, x, None, 1, 1, 0, None) == coc.ERR_INVALID_ARG
     assert L.coc_fused_matmul(0, 2, 0, 128, 128, x, x, 1, x, None, 1, 1, 0, None) == coc.OK   # empty: no-op
+
+
+def test_weight_grad_argument_checks(L):
+    x = _arr([A] * 2)
+    # (rows, cols, inner) = (out_features, in_features, tokens)
+    assert L.coc_fused_matmul(4, 2, 64, 128, 256, x, x, 1, x, None, 1, 1, 0, None) == coc.ERR_INVALID_ARG  # n x k
+    assert L.coc_fused_matmul(4, 2, 60, 128, 256, x, x, 0, x, None, 1, 1, 0, None) == coc.ERR_ALIGN        # dY rows
+    assert L.coc_fused_matmul(4, 2, 64, 132, 256, x, x, 0, x, None, 1, 1, 0, None) == coc.ERR_ALIGN        # X rows
+    assert L.coc_fused_matmul(4, 2, 64, 128, 256, x, x, 0, x, None, 1, 3, 0, None) == coc.ERR_INVALID_ARG  # chunks
+    assert L.coc_fused_matmul(4, 2, 0, 128, 256, x, x, 0, x, None, 1, 1, 0, None) == coc.OK                # empty

@@ -120,3 +120,42 @@ def test_megatron_column_parallel_sp_forward_backward():
         assert_close(y[r], orc.all_gather_matmul(orc.BF16, bits(xs), bits(ws), r), k, f"fwd rank {r}")
         ref = orc.matmul_reduce_scatter(orc.BF16, bits(dys), bits(w_nk), r)   # rows of sum_r dY_r @ W_r
         assert_close(dx[r], ref, R * ns, f"dgrad rank {r}")
+
+
+# ------------------------------------------------------- weight gradient ---
+
+WG_CASES = [
+    # R, tokens (inner), out_features (rows), in_features (cols), dtype
+    (2, 200, 96, 136, BF16),      # <= 128 rows: single-CTA kernel, ragged tokens
+    (4, 256, 264, 72, F16),       # CTA pairs, ragged rows and cols
+]
+
+
+@pytest.mark.parametrize("R,t,rows,cols,dt", WG_CASES)
+def test_weight_grad_parity(R, t, rows, cols, dt):
+    dys = [wl.to16(wl.uniform((t, rows), -1, 1, 95, r), dt) for r in range(R)]
+    xs = [wl.to16(wl.uniform((t, cols), -1, 1, 96, r), dt) for r in range(R)]
+    outs = coc.weight_grad(to_dev(dys), to_dev(xs))
+    coc.sync_status()
+    for r in range(R):
+        dyt = np.ascontiguousarray(wl.bits16(dys[r]).T)                      # rows x tokens
+        ref = orc.partial_sum(CODE[dt], [dyt], [wl.bits16(xs[r])], np.arange(rows))   # dY_r^T @ X_r
+        assert_close(outs[r], ref, t, f"wgrad rank {r}")
+
+
+def test_megatron_column_parallel_sp_weight_grad_uses_v2_gather():
+    """ColumnParallelLinear with SP: the forward pass's V2 gather output is the
+    X the weight gradient needs: dW_r = dY_r^T @ AllGather(X)."""
+    R, ms, ns, k = 4, 64, 136, 128
+    s = wl.ColumnParallelSP(R=R, m_shard=ms, n_shard=ns, k=k, dtype=BF16, x_dist="normal(0,1)",
+                            w_dist="normal(0,0.02)", seed=97)
+    xs, ws = s.make()
+    _, gathered = coc.fused_matmul("all_gather_v2", to_dev(xs), to_dev(_nk(ws)), w_layout="nk")
+    dys = [wl.to16(wl.normal((R * ms, ns), 1.0, 98, r), BF16) for r in range(R)]
+    dw = coc.weight_grad(to_dev(dys), gathered)
+    coc.sync_status()
+    xg = orc.all_gather(bits(xs))
+    for r in range(R):
+        ref = orc.partial_sum(orc.BF16, [np.ascontiguousarray(wl.bits16(dys[r]).T)], [xg], np.arange(ns))
+        assert_close(dw[r], ref, R * ms, f"wgrad rank {r}")
+        assert dw[r].shape == ws[r].t().shape          # Megatron's [out, in] layout
