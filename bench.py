@@ -86,8 +86,10 @@ def load_peaks():
 
 
 def kernel_source_hash() -> str:
+    """Hash of the kernel and of the host code that sets its launch (tile
+    order, L2 grouping): DRAM traffic taken on other sources is stale."""
     h = hashlib.sha256()
-    for f in ("coc_kernel.cu", "coc_internal.h"):
+    for f in ("coc_kernel.cu", "coc_internal.h", "coc_api.cu"):
         h.update(open(os.path.join(ROOT, "tensor_matmul_collective_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:12]
 

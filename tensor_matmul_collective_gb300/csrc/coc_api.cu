@@ -154,6 +154,30 @@ int l2_group(int chunk_mt, int64_t row_tile_bytes) {
     return 0;
 }
 
+// Row-parallel operators (AR/RS/w8A16): every (m-tile, n-tile) unit reads an
+// X row tile of x_tile bytes (all ranks' shards) and a W column tile of
+// w_tile bytes.  In m-tile-inner order the concurrently running units share
+// W columns and need all of the chunk's X rows, which are re-read once per
+// wave of units when they do not fit in L2.  Grouping G m-tiles (their X
+// rows held in L2) reads X once but W once per group.  Returns the group
+// size with the smaller modelled DRAM read volume, 0 for no grouping.
+int row_group(int chunk_mt, int n_tiles, int64_t x_tile, int64_t w_tile, int concurrent) {
+    constexpr int64_t kBudget = int64_t(32) << 20;
+    if (chunk_mt <= 0 || x_tile <= 0 || chunk_mt * x_tile <= kBudget || concurrent <= 0) return 0;
+    const int64_t waves = (static_cast<int64_t>(chunk_mt) * n_tiles + concurrent - 1) / concurrent;
+    int64_t best = waves * chunk_mt * x_tile + n_tiles * w_tile;
+    int best_g = 0;
+    for (int g = chunk_mt - 1; g >= 2; --g) {
+        if (chunk_mt % g != 0 || g * x_tile > kBudget) continue;
+        const int64_t t = chunk_mt * x_tile + static_cast<int64_t>(chunk_mt / g) * n_tiles * w_tile;
+        if (t < best) {
+            best = t;
+            best_g = g;
+        }
+    }
+    return best_g;
+}
+
 int pairs_available(DeviceState* ds, int op, bool bf16) {
     std::lock_guard<std::mutex> lk(g_mu);
     int& v = ds->max_pairs[op][bf16 ? 1 : 0];
@@ -223,6 +247,13 @@ coc_status_t row_parallel(int op, int R, int64_t m, int64_t n, int64_t ks, const
 
     const bool w8 = (op == OP_W8);
     const CUtensorMapDataType adt = w8 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : tma_dtype(dt);
+    {
+        const int64_t k_total = static_cast<int64_t>(R) * ks;
+        const int concurrent = pair ? pairs_available(ds, op, dt == COC_BF16 && !w8) : ds->sm_count;
+        p.group_mt = row_group(p.chunk_mt, p.n_tiles, int64_t(tile_m) * k_total * 2, int64_t(BN) * k_total * (w8 ? 1 : 2),
+                               concurrent);
+        if (p.group_mt > 0) p.a_hint = 2;   // the group's X rows stay in L2 while W streams past
+    }
     if (ks > 0) {
         for (int r = 0; r < R; ++r) {
             if ((st = encode(&p.tm_a[r], adt, x[r], ks, m, ks * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B)) != COC_OK) return st;
@@ -244,6 +275,10 @@ coc_status_t row_parallel(int op, int R, int64_t m, int64_t n, int64_t ks, const
     }
     if (w8)
         for (int r = 0; r < R; ++r) p.scale[r] = static_cast<const uint16_t*>(scale[r]);
+    if ((op == OP_AR || op == OP_W8) && n_out > 1) {
+        for (int o = 0; o < n_out; ++o) p.outp[o] = static_cast<uint16_t*>(out[o]);
+        p.replica_stores = 1;
+    }
     return launch_checked(op, dt == COC_BF16 && !w8, pair, p, ds, stream);
 }
 

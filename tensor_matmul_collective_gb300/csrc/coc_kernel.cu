@@ -854,9 +854,38 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
                     } else if constexpr (OP == OP_AG) {
                         tma_store_2d(&p.tm_out[r], src, col, row0);
                     } else {
-                        for (int o = 0; o < p.n_out; ++o) tma_store_2d(&p.tm_out[o], src, col, row0);
+                        if (!p.replica_stores)
+                            for (int o = 0; o < p.n_out; ++o) tma_store_2d(&p.tm_out[o], src, col, row0);
                     }
                     bulk_commit();
+                }
+                if constexpr (OP == OP_AR || OP == OP_W8) {
+                    if (p.replica_stores) {
+                        // The R copies of this AllReduce sub-tile: read it back once in
+                        // coalesced order (lane l: 16-byte chunk l % 8 of rows l / 8 + 4i)
+                        // and write it to every rank's output with plain global stores,
+                        // each warp store covering four whole 128-byte row segments.  This
+                        // keeps the R-fold output off the TMA unit that feeds the mainloop
+                        // (measured: R TMA stores of each staged sub-tile cost more).
+                        const int ch = lane & 7;
+                        uint4 v[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int rr = (lane >> 3) + 4 * i;
+                            v[i] = *reinterpret_cast<const uint4*>(sbuf + rr * 128 + ((ch ^ (rr & 7)) << 4));
+                        }
+                        const int c = col + ch * 8;   // n % 8 == 0: a chunk is wholly inside or outside
+                        if (c < p.n) {
+                            for (int o = 0; o < p.n_out; ++o) {
+                                uint16_t* base = p.outp[o] + c;
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) {
+                                    const int g = row0 + (lane >> 3) + 4 * i;
+                                    if (g < p.m) *reinterpret_cast<uint4*>(base + static_cast<long long>(g) * p.n) = v[i];
+                                }
+                            }
+                        }
+                    }
                 }
                 __syncwarp();
             }
