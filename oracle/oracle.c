@@ -101,6 +101,38 @@ uint16_t oracle_f64_to_f16_rne(double x)
     return (uint16_t)(sign | ((uint32_t)(e + 15) << 10) | (n - 1024));
 }
 
+/* Round an exact double to the nearest bfloat16, ties to even, overflowing to
+ * +-inf.  bfloat16 is binary32's sign, 8 exponent bits (bias 127) and the top
+ * 7 fraction bits: in the binade [2^e, 2^(e+1)) the quantum is 2^(e-7), and
+ * below 2^-126 the subnormal quantum 2^-133.  Same method as the binary16
+ * encoder above: count quanta exactly, round ties to even, re-encode. */
+uint16_t oracle_f64_to_bf16_rne(double x)
+{
+    const uint16_t sign = signbit(x) ? 0x8000 : 0;
+    if (isnan(x)) return (uint16_t)(sign | 0x7fc0);
+    double a = fabs(x);
+    if (isinf(a)) return (uint16_t)(sign | 0x7f80);
+    if (a == 0.0) return sign;
+
+    int E;
+    (void)frexp(a, &E);
+    int e = E - 1;            /* a in [2^e, 2^(e+1)) */
+    if (e < -126) e = -126;   /* subnormal range shares the quantum 2^-133 */
+    const double q = ldexp(1.0, e - 7);
+    const double nq = a / q;
+    double fl = floor(nq);
+    const double frac = nq - fl;
+    if (frac > 0.5 || (frac == 0.5 && fmod(fl, 2.0) != 0.0)) fl += 1.0;
+    /* fl is now an integer in [0, 256] */
+    uint32_t n = (uint32_t)fl;
+    if (e == -126 && n < 128) {
+        return (uint16_t)(sign | n);    /* subnormal (or zero) */
+    }
+    if (n == 256) { n = 128; e += 1; }
+    if (e + 127 >= 255) return (uint16_t)(sign | 0x7f80);
+    return (uint16_t)(sign | ((uint32_t)(e + 127) << 7) | (n - 128));
+}
+
 static inline double decode16(int dtype, uint16_t v)
 {
     return dtype == 1 ? oracle_bf16_to_f64(v) : oracle_f16_to_f64(v);
@@ -115,6 +147,11 @@ void oracle_decode16(int dtype, const uint16_t* in, double* out, int64_t count)
 void oracle_encode_f16(const double* in, uint16_t* out, int64_t count)
 {
     for (int64_t i = 0; i < count; ++i) out[i] = oracle_f64_to_f16_rne(in[i]);
+}
+
+void oracle_encode_bf16(const double* in, uint16_t* out, int64_t count)
+{
+    for (int64_t i = 0; i < count; ++i) out[i] = oracle_f64_to_bf16_rne(in[i]);
 }
 
 /* ---- one rank's partial product -------------------------------------------
@@ -189,6 +226,34 @@ void oracle_dequant_w8(const int8_t* q, int64_t k, int64_t n,
             else if (gran == 2) si = ((k_offset + t) / group) * n + j;
             const double s = oracle_f16_to_f64(scale[si]);
             out[t * n + j] = oracle_f64_to_f16_rne((double)q[t * n + j] * s);
+        }
+    }
+}
+
+/* ---- w8A16 extensions: zero point and bfloat16 activations -------------------
+ * The page names the fp16 form only; these are the asymmetric and bfloat16
+ * readings.  With an int8 zero point z(t, j) laid out like the scale (NULL:
+ * symmetric, z = 0) and the activation type `dtype` (0 binary16, 1 bfloat16,
+ * which is also the type of the scale and of the result):
+ *
+ *     Wd[t, j] = RNE_dtype( (q[t, j] - z(t, j)) * s(t, j) )
+ *
+ * (q - z) is an integer in [-255, 255] and the product is exact in fp64, so
+ * the result is rounded once.  z(t, j) is indexed exactly like s(t, j).
+ */
+void oracle_dequant_w8_ex(const int8_t* q, int64_t k, int64_t n,
+                          const uint16_t* scale, const int8_t* zero, int gran, int64_t group,
+                          int64_t k_offset, int dtype, uint16_t* out)
+{
+    for (int64_t t = 0; t < k; ++t) {
+        for (int64_t j = 0; j < n; ++j) {
+            int64_t si = 0;
+            if (gran == 1) si = j;
+            else if (gran == 2) si = ((k_offset + t) / group) * n + j;
+            const double s = decode16(dtype, scale[si]);
+            const double z = zero ? (double)zero[si] : 0.0;
+            const double v = ((double)q[t * n + j] - z) * s;
+            out[t * n + j] = dtype == 1 ? oracle_f64_to_bf16_rne(v) : oracle_f64_to_f16_rne(v);
         }
     }
 }

@@ -76,6 +76,8 @@ def _load():
             lib.oracle_accumulate_partial.argtypes = [
                 ctypes.c_int, p, i64, p, i64, i64, i64, p, i64, p, ctypes.c_int]
             lib.oracle_dequant_w8.argtypes = [p, i64, i64, p, ctypes.c_int, i64, i64, p]
+            lib.oracle_dequant_w8_ex.argtypes = [p, i64, i64, p, p, ctypes.c_int, i64, i64, ctypes.c_int, p]
+            lib.oracle_encode_bf16.argtypes = [p, p, i64]
             lib.oracle_max_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -111,6 +113,14 @@ def encode_f16(values) -> np.ndarray:
     v = np.ascontiguousarray(values, dtype=np.float64)
     out = np.empty(v.shape, dtype=np.uint16)
     _load().oracle_encode_f16(_ptr(v), _ptr(out), v.size)
+    return out
+
+
+def encode_bf16(values) -> np.ndarray:
+    """Round fp64 values to bfloat16 (ties to even, overflow to inf); returns bits."""
+    v = np.ascontiguousarray(values, dtype=np.float64)
+    out = np.empty(v.shape, dtype=np.uint16)
+    _load().oracle_encode_bf16(_ptr(v), _ptr(out), v.size)
     return out
 
 
@@ -223,13 +233,55 @@ def dequant_w8a16(wq, scale_bits, gran: int, group: int = 0, k_offset: int = 0) 
     return out
 
 
-def matmul_all_reduce_w8a16(xs, wqs, scales, gran: int, group: int = 0, rows=None, nthreads=None):
-    """w8A16 MATMUL_ALL_REDUCE (same section, last bullet), fp16 only.
+def dequant_w8a16_ex(wq, scale_bits, gran: int, group: int = 0, k_offset: int = 0, zero=None,
+                     dtype: int = F16) -> np.ndarray:
+    """Extended w8A16 weight of one rank: bits (in `dtype`) of RNE((q - z) * s).
 
-    xs[r]: fp16 bits (m x k_r); wqs[r]: int8 (k_r x n); scales[r]: this rank's
-    scale view (the shared scalar, the shared per-column vector, or this
-    rank's rows of the per-group table, so k_offset is 0 within the view).
-    Y = sum_r X_r @ Wd_r with Wd_r the dequantised binary16 weight.
+    The zero point `zero` (int8, laid out like the scale; None = symmetric)
+    and the bfloat16 activation type are this build's reading of the
+    "antiquant offset" and "bf16 activation" extensions; the scale is in
+    `dtype` too.  With zero=None and dtype=F16 this is dequant_w8a16.
     """
-    wds = [dequant_w8a16(wq, s, gran, group, 0) for wq, s in zip(wqs, scales)]
-    return matmul_all_reduce(F16, xs, wds, rows, nthreads)
+    q = np.ascontiguousarray(wq, dtype=np.int8)
+    s = _c16(scale_bits)
+    k, n = q.shape
+    if gran == SCALE_TENSOR:
+        need = 1
+    elif gran == SCALE_CHANNEL:
+        need = n
+    elif gran == SCALE_GROUP:
+        if group <= 0:
+            raise ValueError("group size must be positive")
+        need = ((k_offset + k - 1) // group + 1) * n if k else 0
+    else:
+        raise ValueError("unknown scale granularity")
+    if s.size < need:
+        raise ValueError("scale tensor too small for this granularity")
+    z = None
+    if zero is not None:
+        z = np.ascontiguousarray(zero, dtype=np.int8)
+        if z.size < need:
+            raise ValueError("zero-point tensor too small for this granularity")
+    out = np.empty((k, n), dtype=np.uint16)
+    _load().oracle_dequant_w8_ex(_ptr(q), k, n, _ptr(s), _ptr(z) if z is not None else None, int(gran), int(group),
+                                 int(k_offset), int(dtype), _ptr(out))
+    return out
+
+
+def matmul_all_reduce_w8a16(xs, wqs, scales, gran: int, group: int = 0, rows=None, nthreads=None, zeros=None,
+                            dtype: int = F16):
+    """w8A16 MATMUL_ALL_REDUCE (same section, last bullet).
+
+    xs[r]: activation bits (m x k_r) in `dtype` (the page's fp16, or the
+    bfloat16 extension); wqs[r]: int8 (k_r x n); scales[r]: this rank's scale
+    view in `dtype` (the shared scalar, the shared per-column vector, or this
+    rank's rows of the per-group table, so k_offset is 0 within the view);
+    zeros[r]: optional int8 zero points laid out like scales[r].
+    Y = sum_r X_r @ Wd_r with Wd_r the dequantised weight.
+    """
+    if zeros is None and dtype == F16:
+        wds = [dequant_w8a16(wq, s, gran, group, 0) for wq, s in zip(wqs, scales)]
+    else:
+        zs = zeros if zeros is not None else [None] * len(wqs)
+        wds = [dequant_w8a16_ex(wq, s, gran, group, 0, z, dtype) for wq, s, z in zip(wqs, scales, zs)]
+    return matmul_all_reduce(dtype, xs, wds, rows, nthreads)

@@ -151,7 +151,8 @@ SCALE_GRANS = ("tensor", "channel", "group")
 
 @dataclass
 class W8A16:
-    """w8A16 AllReduce shapes: fp16 X_r m x k_shard, int8 W_r k_shard x n, fp16 scales."""
+    """w8A16 AllReduce shapes: X_r m x k_shard and scales in `dtype` (the pages'
+    fp16, or bf16), int8 W_r k_shard x n, optional int8 zero points."""
     R: int
     m: int
     n: int
@@ -159,6 +160,7 @@ class W8A16:
     group: int
     seed: int
     x_dist: str = "normal(0,1)"
+    dtype: torch.dtype = torch.float16
 
     @property
     def K(self) -> int:
@@ -171,24 +173,36 @@ class W8A16:
         """Returns (xs, wqs, scales): scales[r] is rank r's view of the scale
         tensor — the shared scalar (1,), the shared per-column vector (n,), or
         rank r's rows of the (K/group) x n per-group table."""
-        X = to16(_draw(self.x_dist, (self.m, self.K), self.seed, 0), torch.float16)
+        dt = self.dtype
+        X = to16(_draw(self.x_dist, (self.m, self.K), self.seed, 0), dt)
         Wq = torch.from_numpy(int8_uniform((self.K, self.n), -127, 127, self.seed, 1))
         if gran == "tensor":
-            S = to16(uniform((1,), 0.001, 0.01, self.seed, 2), torch.float16)
-            scales = [S] * self.R
+            S = to16(uniform((1,), 0.001, 0.01, self.seed, 2), dt)
         elif gran == "channel":
-            S = to16(uniform((self.n,), 0.001, 0.01, self.seed, 3), torch.float16)
-            scales = [S] * self.R
+            S = to16(uniform((self.n,), 0.001, 0.01, self.seed, 3), dt)
         elif gran == "group":
-            S = to16(uniform((self.K // self.group, self.n), 0.001, 0.01, self.seed, 4), torch.float16)
-            gpr = self.k_shard // self.group
-            scales = [S[r * gpr:(r + 1) * gpr].contiguous() for r in range(self.R)]
+            S = to16(uniform((self.K // self.group, self.n), 0.001, 0.01, self.seed, 4), dt)
         else:
             raise ValueError(gran)
         ks = self.k_shard
         xs = [X[:, r * ks:(r + 1) * ks].contiguous() for r in range(self.R)]
         wqs = [Wq[r * ks:(r + 1) * ks, :].contiguous() for r in range(self.R)]
-        return xs, wqs, scales
+        return xs, wqs, self._views(S, gran)
+
+    def _views(self, T: torch.Tensor, gran: str):
+        """Rank views of a scale-shaped tensor: the shared scalar or per-column
+        vector, or rank r's rows of the per-group table."""
+        if gran != "group":
+            return [T] * self.R
+        gpr = self.k_shard // self.group
+        return [T[r * gpr:(r + 1) * gpr].contiguous() for r in range(self.R)]
+
+    def zeros(self, gran: str, lo: int = -128, hi: int = 127):
+        """Rank views of int8 zero points laid out like the scales of `gran`
+        (asymmetric quantisation; seeded independently of the scales)."""
+        shape = {"tensor": (1,), "channel": (self.n,), "group": (self.K // self.group, self.n)}[gran]
+        Z = torch.from_numpy(int8_uniform(shape, lo, hi, self.seed, 5))
+        return self._views(Z, gran)
 
 
 @dataclass

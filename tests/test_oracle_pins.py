@@ -270,6 +270,102 @@ def test_w8a16_unit_scale_is_plain_fp16_ar(oracle_mod):
     assert np.array_equal(got, oracle_mod.matmul_all_reduce(oracle_mod.F16, xs, wf))
 
 
+# ------------------------------------------- w8A16 extensions (zero point, bf16) ---
+
+def _bf16_bits_of_f32(x):
+    """torch's fp32 -> bfloat16 cast (round to nearest, ties to even)."""
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def test_bf16_encode_ties_and_random_vs_torch(oracle_mod):
+    # Values exact in fp32 (so torch's fp32 -> bf16 cast sees the exact value):
+    # every tie between neighbouring bf16 values of a few binades, the floats
+    # on either side of each tie, random fp32 values and the edges.
+    rng = np.random.default_rng(8)
+    bits = np.arange(0x3700, 0x4400, dtype=np.uint32)             # [2^-17, 2^9)
+    v = (bits << 16).view(np.float32).astype(np.float64)
+    mids = (v[:-1] + v[1:]) / 2
+    near = np.concatenate([np.nextafter(mids.astype(np.float32), np.float32(0)),
+                           np.nextafter(mids.astype(np.float32), np.float32(np.inf))]).astype(np.float64)
+    rand = rng.standard_normal(200000).astype(np.float32).astype(np.float64) * 10.0 ** rng.integers(-30, 30, 200000)
+    rand = rand.astype(np.float32).astype(np.float64)
+    edge = np.array([3.3895313892515355e38, 3.4e38, 1e-40, 9.18355e-41, 1.1754943508222875e-38, 0.0, 1.0, 255.0, 257.0])
+    x = np.concatenate([mids, near, rand, edge])
+    x = x[np.isfinite(x.astype(np.float32))]
+    x = np.concatenate([x, -x])
+    assert np.array_equal(oracle_mod.encode_bf16(x), _bf16_bits_of_f32(x))
+    assert oracle_mod.encode_bf16(np.array([1e39]))[0] == 0x7f80          # overflow -> inf
+
+
+def _scale_full(S, gran, group, shape, dt):
+    s = _dec(S, dt)
+    if gran == "tensor":
+        return np.broadcast_to(s.reshape(1, 1), shape)
+    if gran == "channel":
+        return np.broadcast_to(s.reshape(1, -1), shape)
+    return np.repeat(s, group, axis=0)[: shape[0]]
+
+
+def _zero_full(Z, gran, group, shape):
+    z = np.asarray(Z, dtype=np.float64)
+    if gran == "tensor":
+        return np.broadcast_to(z.reshape(1, 1), shape)
+    if gran == "channel":
+        return np.broadcast_to(z.reshape(1, -1), shape)
+    return np.repeat(z, group, axis=0)[: shape[0]]
+
+
+@pytest.mark.parametrize("gran", ["tensor", "channel", "group"])
+@pytest.mark.parametrize("dt", [torch.float16, torch.bfloat16])
+def test_w8a16_zero_point_dequant_vs_brute_force(oracle_mod, gran, dt):
+    shape = wl.W8A16(R=4, m=12, n=48, k_shard=64, group=32, seed=13, dtype=dt)
+    xs, wqs, scales = shape.make(gran)
+    zeros = shape.zeros(gran)
+    code = oracle_mod.BF16 if dt == torch.bfloat16 else oracle_mod.F16
+    wds = []
+    for wq, S, Z in zip(wqs, scales, zeros):
+        q, Sb, Zn = wq.numpy(), wl.bits16(S), Z.numpy()
+        got = oracle_mod.dequant_w8a16_ex(q, Sb, GRAN_CODE[gran], shape.group, 0, Zn, code)
+        exact = (q.astype(np.float64) - _zero_full(Zn, gran, shape.group, q.shape)) * \
+            _scale_full(Sb, gran, shape.group, q.shape, dt)
+        # the product is exact in fp32 (<= 9 x 11 significant bits), so a single
+        # rounding by numpy (binary16) or torch (bfloat16) is the reference
+        with np.errstate(over="ignore"):
+            ref = exact.astype(np.float16).view(np.uint16) if dt == torch.float16 else _bf16_bits_of_f32(exact)
+        assert np.array_equal(got, ref)
+        wds.append(got)
+    xb = [wl.bits16(x) for x in xs]
+    sb = [wl.bits16(S) for S in scales]
+    y = oracle_mod.matmul_all_reduce_w8a16(xb, [w.numpy() for w in wqs], sb, GRAN_CODE[gran], shape.group,
+                                           zeros=[Z.numpy() for Z in zeros], dtype=code)
+    assert _rel(y, _unsharded(xb, wds, dt)) < 1e-13
+    # a mutant that ignores the zero point is rejected
+    wrong = oracle_mod.dequant_w8a16_ex(wqs[0].numpy(), sb[0], GRAN_CODE[gran], shape.group, 0, None, code)
+    assert not np.array_equal(wrong, wds[0])
+
+
+def test_w8a16_zero_point_special_cases(oracle_mod):
+    rng = np.random.default_rng(21)
+    k, n = 64, 32
+    q = rng.integers(-127, 128, (k, n)).astype(np.int8)
+    S = wl.bits16(wl.to16(wl.uniform((n,), 0.001, 0.01, 3, 1), torch.float16))
+    # z = 0 is the symmetric form, bit for bit
+    sym = oracle_mod.dequant_w8a16(q, S, 1, 0)
+    assert np.array_equal(oracle_mod.dequant_w8a16_ex(q, S, 1, 0, 0, np.zeros(n, np.int8), oracle_mod.F16), sym)
+    assert np.array_equal(oracle_mod.dequant_w8a16_ex(q, S, 1, 0, 0, None, oracle_mod.F16), sym)
+    # q == z everywhere: the weight is exactly zero, so is the AllReduce
+    zq = q[0].copy()
+    qz = np.broadcast_to(zq, (k, n)).copy()
+    assert not np.any(oracle_mod.dequant_w8a16_ex(qz, S, 1, 0, 0, zq, oracle_mod.F16) & 0x7FFF)
+    # extreme zero points: q - z = +-255 is exact in both formats
+    one16, one_bf = np.array([0x3C00], np.uint16), np.array([0x3F80], np.uint16)
+    qe = np.array([[127, -128]], dtype=np.int8).reshape(1, 2)
+    ze = np.array([-128], dtype=np.int8)
+    d16 = oracle_mod.dequant_w8a16_ex(qe, one16, 0, 0, 0, ze, oracle_mod.F16).view(np.float16).astype(np.float64)
+    dbf = _dec(oracle_mod.dequant_w8a16_ex(qe, one_bf, 0, 0, 0, ze, oracle_mod.BF16), torch.bfloat16)
+    assert d16.tolist() == [[255.0, 0.0]] and dbf.tolist() == [[255.0, 0.0]]
+
+
 def test_thread_count_does_not_change_results(oracle_mod):
     xs = [_rand16((20, 64), torch.bfloat16, 100 + r) for r in range(2)]
     ws = [_rand16((64, 37), torch.bfloat16, 110 + r) for r in range(2)]
