@@ -11,6 +11,7 @@
  *   ALL_GATHER_MATMUL_V2 (also returns the gather)      coc_all_gather_matmul_v2
  *   w8A16 pseudo-quantised MATMUL_ALL_REDUCE, fp16,
  *     per tensor / per channel / per group scales       coc_matmul_all_reduce_w8a16
+ *     + zero point, bf16 activations (extension)         coc_matmul_all_reduce_w8a16_ex
  *
  * The same page's section 问题分析 ("problem analysis") places them in the
  * Megatron ColumnParallelLinear / RowParallelLinear layers: the matmul is
@@ -208,6 +209,32 @@ coc_status_t coc_matmul_all_reduce_w8a16(int R, int64_t m, int64_t n, int64_t k_
                                          const void* const* scale, coc_scale_t gran,
                                          int64_t group_size, void* const* out,
                                          int chunks, int deterministic, coc_stream_t stream);
+
+/*
+ * w8A16 MATMUL_ALL_REDUCE with the two extensions the page does not spell
+ * out (its 融合算子实现 section names only the symmetric fp16 form): an int8
+ * zero point (asymmetric quantisation) and bf16 activations.
+ *
+ *   Wd_r[t, j] = rne_dt( (Wq_r[t, j] - z_r(t, j)) * s_r(t, j) )   (exact, one rounding)
+ *   Y = sum_r X_r @ Wd_r;  out[r] = rne_dt(Y) for every r
+ *
+ * dt        COC_FP16 or COC_BF16: the type of x, scale and out.
+ * zero      NULL (symmetric, z = 0) or one int8 zero-point view per rank,
+ *           laid out and indexed exactly like scale[r] (1 value, n values,
+ *           or (k_shard/group_size) x n).  q - z lies in [-255, 255].
+ * Other arguments as coc_matmul_all_reduce_w8a16, whose call equals this one
+ * with zero = NULL and dt = COC_FP16.
+ * Alignment: per-channel / per-group scale[r] and zero[r] 16-byte aligned;
+ * per-tensor: scale 2-byte aligned, zero unconstrained.
+ * Errors: COC_ERR_INVALID_ARG (NULL entries, unknown dt or granularity),
+ * COC_ERR_SHAPE, COC_ERR_ALIGN as coc_matmul_all_reduce_w8a16.
+ */
+coc_status_t coc_matmul_all_reduce_w8a16_ex(int R, int64_t m, int64_t n, int64_t k_shard,
+                                            const void* const* x, const void* const* w,
+                                            const void* const* scale, const void* const* zero,
+                                            coc_scale_t gran, int64_t group_size, void* const* out,
+                                            coc_dtype_t dt, int chunks, int deterministic,
+                                            coc_stream_t stream);
 
 /*
  * Any of the four bf16/fp16 fused operators with a choice of weight layout.

@@ -28,7 +28,7 @@ EXPORTS = (
     "coc_all_gather_matmul_v2", "coc_matmul_all_reduce_w8a16", "coc_matmul",
     "coc_sync_status", "coc_status_string", "coc_last_error", "coc_version",
     "coc_debug_inject_timeout", "coc_shutdown", "coc_matmul_all_reduce_noalloc",
-    "coc_fused_matmul",
+    "coc_fused_matmul", "coc_matmul_all_reduce_w8a16_ex",
 )
 
 OP_ALL_REDUCE, OP_REDUCE_SCATTER, OP_ALL_GATHER, OP_ALL_GATHER_V2, OP_WEIGHT_GRAD = range(5)
@@ -69,6 +69,9 @@ def lib() -> ctypes.CDLL:
             L.coc_all_gather_matmul_v2.restype = i32
             L.coc_matmul_all_reduce_w8a16.argtypes = [i32, i64, i64, i64, pp, pp, pp, i32, i64, pp, i32, i32, vp]
             L.coc_matmul_all_reduce_w8a16.restype = i32
+            L.coc_matmul_all_reduce_w8a16_ex.argtypes = [i32, i64, i64, i64, pp, pp, pp, pp, i32, i64, pp, i32, i32,
+                                                         i32, vp]
+            L.coc_matmul_all_reduce_w8a16_ex.restype = i32
             L.coc_fused_matmul.argtypes = [i32, i32, i64, i64, i64, pp, pp, i32, pp, pp, i32, i32, i32, vp]
             L.coc_fused_matmul.restype = i32
             L.coc_matmul.argtypes = [i32, i64, i64, i64, pp, pp, vp, i32, vp]
@@ -222,30 +225,39 @@ def all_gather_matmul_v2(xs, ws, outs=None, gathered=None, chunks: int = 1, dete
 
 
 def matmul_all_reduce_w8a16(xs, wqs, scales, gran, group_size: int = 0, outs=None, chunks: int = 1,
-                            deterministic: bool = False, stream=None):
-    """w8A16 MATMUL_ALL_REDUCE: outs[r] = sum_q xs[q] @ fp16(wqs[q] * s_q) for every r.
+                            deterministic: bool = False, stream=None, zeros=None):
+    """w8A16 MATMUL_ALL_REDUCE: outs[r] = sum_q xs[q] @ rne((wqs[q] - z_q) * s_q) for every r.
 
-    gran: "tensor" | "channel" | "group" (or the SCALE_* codes); scales[q] is
-    rank q's view of the fp16 scale tensor."""
+    The activations xs set the type (fp16 as on the page, or bf16); scales
+    are in that type.  gran: "tensor" | "channel" | "group" (or the SCALE_*
+    codes); scales[q] is rank q's view of the scale tensor.  zeros: None
+    (symmetric) or one int8 zero-point view per rank, laid out like scales."""
     R, x0, w0 = _prep(xs, wqs)
     gcode = _GRAN[gran] if isinstance(gran, str) else int(gran)
     m, ks = x0.shape
     n = w0.shape[1]
-    _check_list(xs, "xs", (m, ks), torch.float16, x0.device)
+    if x0.dtype not in (torch.float16, torch.bfloat16):
+        raise ValueError("w8A16 activations must be fp16 or bf16")
+    dt = x0.dtype
+    _check_list(xs, "xs", (m, ks), dt, x0.device)
     _check_list(wqs, "wqs", (ks, n), torch.int8, x0.device)
-    if len(scales) != R:
-        raise ValueError("need one scale view per rank")
-    for i, s in enumerate(scales):
-        if s.dtype != torch.float16 or s.device != x0.device or not s.is_contiguous():
-            raise ValueError(f"scales[{i}] must be a contiguous fp16 tensor on {x0.device}")
-        need = 1 if gcode == SCALE_TENSOR else n if gcode == SCALE_CHANNEL else \
-            (ks // group_size) * n if group_size > 0 else 0
-        if s.numel() < need:
-            raise ValueError(f"scales[{i}] has {s.numel()} values, needs {need}")
-    outs = _outs(outs, R, (m, n), torch.float16, x0.device)
-    _check(lib().coc_matmul_all_reduce_w8a16(R, m, n, ks, _ptrs(xs), _ptrs(wqs), _ptrs(scales), gcode,
-                                             int(group_size), _ptrs(outs), int(chunks), int(bool(deterministic)),
-                                             _stream(stream)))
+    need = 1 if gcode == SCALE_TENSOR else n if gcode == SCALE_CHANNEL else \
+        (ks // group_size) * n if group_size > 0 else 0
+    for name, views, want in (("scales", scales, dt), ("zeros", zeros, torch.int8)):
+        if views is None:
+            continue
+        if len(views) != R:
+            raise ValueError(f"need one {name} view per rank")
+        for i, s in enumerate(views):
+            if s.dtype != want or s.device != x0.device or not s.is_contiguous():
+                raise ValueError(f"{name}[{i}] must be a contiguous {want} tensor on {x0.device}")
+            if s.numel() < need:
+                raise ValueError(f"{name}[{i}] has {s.numel()} values, needs {need}")
+    outs = _outs(outs, R, (m, n), dt, x0.device)
+    _check(lib().coc_matmul_all_reduce_w8a16_ex(R, m, n, ks, _ptrs(xs), _ptrs(wqs), _ptrs(scales),
+                                                _ptrs(zeros) if zeros is not None else None, gcode,
+                                                int(group_size), _ptrs(outs), BF16 if dt == torch.bfloat16 else FP16,
+                                                int(chunks), int(bool(deterministic)), _stream(stream)))
     return outs
 
 

@@ -217,7 +217,7 @@ coc_status_t launch_checked(int op, bool bf16, bool pair, KParams& p, DeviceStat
 coc_status_t row_parallel(int op, int R, int64_t m, int64_t n, int64_t ks, const void* const* x,
                           const void* const* w, void* const* out, int n_out, coc_dtype_t dt, int chunks,
                           const void* const* scale, coc_scale_t gran, int64_t group, cudaStream_t stream,
-                          bool w_nk = false) {
+                          bool w_nk = false, const void* const* zero = nullptr) {
     KParams p;
     std::memset(&p, 0, sizeof p);
     p.b_kmajor = w_nk ? 1 : 0;
@@ -246,10 +246,10 @@ coc_status_t row_parallel(int op, int R, int64_t m, int64_t n, int64_t ks, const
     if (st != COC_OK) return st;
 
     const bool w8 = (op == OP_W8);
-    const CUtensorMapDataType adt = w8 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : tma_dtype(dt);
+    const CUtensorMapDataType adt = tma_dtype(dt);
     {
         const int64_t k_total = static_cast<int64_t>(R) * ks;
-        const int concurrent = pair ? pairs_available(ds, op, dt == COC_BF16 && !w8) : ds->sm_count;
+        const int concurrent = pair ? pairs_available(ds, op, dt == COC_BF16) : ds->sm_count;
         p.group_mt = row_group(p.chunk_mt, p.n_tiles, int64_t(tile_m) * k_total * 2, int64_t(BN) * k_total * (w8 ? 1 : 2),
                                concurrent);
         if (p.group_mt > 0) p.a_hint = 2;   // the group's X rows stay in L2 while W streams past
@@ -273,13 +273,18 @@ coc_status_t row_parallel(int op, int R, int64_t m, int64_t n, int64_t ks, const
         if ((st = encode(&p.tm_out[o], adt, out[o], n, out_rows, n * 2, EPI_COLS, p.store_rows, CU_TENSOR_MAP_SWIZZLE_128B)) != COC_OK)
             return st;
     }
-    if (w8)
+    if (w8) {
         for (int r = 0; r < R; ++r) p.scale[r] = static_cast<const uint16_t*>(scale[r]);
+        if (zero != nullptr) {
+            p.has_zero = 1;
+            for (int r = 0; r < R; ++r) p.zero[r] = static_cast<const int8_t*>(zero[r]);
+        }
+    }
     if ((op == OP_AR || op == OP_W8) && n_out > 1) {
         for (int o = 0; o < n_out; ++o) p.outp[o] = static_cast<uint16_t*>(out[o]);
         p.replica_stores = 1;
     }
-    return launch_checked(op, dt == COC_BF16 && !w8, pair, p, ds, stream);
+    return launch_checked(op, dt == COC_BF16, pair, p, ds, stream);
 }
 
 coc_status_t validate_row_parallel(int R, int64_t m, int64_t n, int64_t ks, const void* const* x, const void* const* w,
@@ -336,11 +341,13 @@ COC_API coc_status_t coc_matmul_reduce_scatter(int R, int64_t m, int64_t n, int6
                         reinterpret_cast<cudaStream_t>(stream));
 }
 
-COC_API coc_status_t coc_matmul_all_reduce_w8a16(int R, int64_t m, int64_t n, int64_t k_shard, const void* const* x,
-                                                 const void* const* w, const void* const* scale, coc_scale_t gran,
-                                                 int64_t group_size, void* const* out, int chunks, int deterministic,
-                                                 coc_stream_t stream) {
-    coc_status_t st = validate_row_parallel(R, m, n, k_shard, x, w, out, R, COC_FP16, chunks, deterministic, 1);
+COC_API coc_status_t coc_matmul_all_reduce_w8a16_ex(int R, int64_t m, int64_t n, int64_t k_shard, const void* const* x,
+                                                    const void* const* w, const void* const* scale,
+                                                    const void* const* zero, coc_scale_t gran, int64_t group_size,
+                                                    void* const* out, coc_dtype_t dt, int chunks, int deterministic,
+                                                    coc_stream_t stream) {
+    if (dt != COC_FP16 && dt != COC_BF16) return fail(COC_ERR_INVALID_ARG, "unknown dtype %d", static_cast<int>(dt));
+    coc_status_t st = validate_row_parallel(R, m, n, k_shard, x, w, out, R, dt, chunks, deterministic, 1);
     if (st != COC_OK) return st;
     if (gran != COC_SCALE_TENSOR && gran != COC_SCALE_CHANNEL && gran != COC_SCALE_GROUP)
         return fail(COC_ERR_INVALID_ARG, "unknown scale granularity %d", static_cast<int>(gran));
@@ -352,6 +359,11 @@ COC_API coc_status_t coc_matmul_all_reduce_w8a16(int R, int64_t m, int64_t n, in
             return fail(COC_ERR_ALIGN, "scale[%d] is not 16-byte aligned", r);
         if (gran == COC_SCALE_TENSOR && (reinterpret_cast<uintptr_t>(scale[r]) & 1u))
             return fail(COC_ERR_ALIGN, "scale[%d] is not 2-byte aligned", r);
+        if (zero != nullptr) {
+            if (zero[r] == nullptr) return fail(COC_ERR_INVALID_ARG, "zero[%d] is NULL", r);
+            if (gran != COC_SCALE_TENSOR && !aligned16(zero[r]))
+                return fail(COC_ERR_ALIGN, "zero[%d] is not 16-byte aligned", r);
+        }
     }
     if (gran == COC_SCALE_GROUP) {
         if (group_size <= 0 || group_size % BK != 0)
@@ -361,8 +373,16 @@ COC_API coc_status_t coc_matmul_all_reduce_w8a16(int R, int64_t m, int64_t n, in
                         (long long)group_size);
     }
     if (empty) return COC_OK;
-    return row_parallel(OP_W8, R, m, n, k_shard, x, w, out, R, COC_FP16, chunks, scale, gran, group_size,
-                        reinterpret_cast<cudaStream_t>(stream));
+    return row_parallel(OP_W8, R, m, n, k_shard, x, w, out, R, dt, chunks, scale, gran, group_size,
+                        reinterpret_cast<cudaStream_t>(stream), false, zero);
+}
+
+COC_API coc_status_t coc_matmul_all_reduce_w8a16(int R, int64_t m, int64_t n, int64_t k_shard, const void* const* x,
+                                                 const void* const* w, const void* const* scale, coc_scale_t gran,
+                                                 int64_t group_size, void* const* out, int chunks, int deterministic,
+                                                 coc_stream_t stream) {
+    return coc_matmul_all_reduce_w8a16_ex(R, m, n, k_shard, x, w, scale, nullptr, gran, group_size, out, COC_FP16,
+                                          chunks, deterministic, stream);
 }
 
 namespace coc {

@@ -40,7 +40,8 @@ struct KParams {
 
     const uint16_t* gsrc[COC_MAX_RANKS];  // AG-V2: X shards (gather source)
     uint16_t* gdst[COC_MAX_RANKS];        // AG-V2: gathered outputs (NULL = skip)
-    const uint16_t* scale[COC_MAX_RANKS]; // w8A16 scales (rank views)
+    const uint16_t* scale[COC_MAX_RANKS]; // w8A16 scales (rank views, activation type)
+    const int8_t* zero[COC_MAX_RANKS];    // w8A16 zero points (rank views; has_zero)
     uint16_t* outp[COC_MAX_RANKS];        // AllReduce outputs (m x n) written by plain stores (replica_stores)
     unsigned* status;                     // STATUS_WORDS device words
 
@@ -65,6 +66,7 @@ struct KParams {
     int a_hint, b_hint;  // L2 policy of A / B loads: 0 evict_normal, 1 evict_first, 2 evict_last
     int b_kmajor;      // W stored n x k (K-major B operand) instead of k x n
     int a_mnmajor;     // weight gradient: A = dY_r^T read MN-major from rank r's dY (AG path only)
+    int has_zero;      // w8A16: zero points given
     int replica_stores; // AllReduce: write the n_out outputs with plain stores (outp) instead of TMA
 };
 

@@ -33,6 +33,7 @@ def main():
     ap.add_argument("--gran", choices=list(wl.SCALE_GRANS), default="group")
     ap.add_argument("--group", type=int, default=128)
     ap.add_argument("--iters", type=int, default=3)
+    ap.add_argument("--zero", action="store_true", help="w8a16: int8 zero points (asymmetric weights)")
     a = ap.parse_args()
 
     dev = torch.device("cuda:0")
@@ -50,11 +51,13 @@ def main():
             run = lambda: coc.all_gather_matmul(dx, dw, outs, chunks=a.chunks)  # noqa: E731
         flops = s.flops()
     elif a.op == "w8a16":
-        s = wl.W8A16(R=a.R, m=a.m, n=a.n, k_shard=a.k, group=a.group, seed=3)
+        s = wl.W8A16(R=a.R, m=a.m, n=a.n, k_shard=a.k, group=a.group, seed=3, dtype=dt)
         xs, wqs, scales = s.make(a.gran)
         dx, dw, dsc = [x.to(dev) for x in xs], [w.to(dev) for w in wqs], [t.to(dev) for t in scales]
-        outs = [torch.empty(s.m, s.n, dtype=torch.float16, device=dev) for _ in range(a.R)]
-        run = lambda: coc.matmul_all_reduce_w8a16(dx, dw, dsc, a.gran, a.group, outs, chunks=a.chunks)  # noqa: E731
+        dz = [z.to(dev) for z in s.zeros(a.gran)] if a.zero else None
+        outs = [torch.empty(s.m, s.n, dtype=dt, device=dev) for _ in range(a.R)]
+        run = lambda: coc.matmul_all_reduce_w8a16(dx, dw, dsc, a.gran, a.group, outs, chunks=a.chunks,  # noqa: E731
+                                                  zeros=dz)
         flops = s.flops()
     else:
         s = wl.RowParallel(R=a.R, m=a.m, n=a.n, k_shard=a.k, dtype=dt, x_dist="normal(0,1)",

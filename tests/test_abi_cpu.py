@@ -131,6 +131,21 @@ def test_w8a16_constraints(L):
     assert f(2, 64, 128, 128, x, x, _arr([A, MIS]), 1, 0, x, 1, 0, None) == coc.ERR_ALIGN
 
 
+def test_w8a16_ex_constraints(L):
+    # extended entry point: argument order (R, m, n, k_shard, x, w, scale, zero, gran,
+    # group, out, dt, chunks, det, stream); every call below fails host validation
+    x = _arr([A] * 2)
+    f = L.coc_matmul_all_reduce_w8a16_ex
+    assert f(2, 64, 128, 128, x, x, x, None, 0, 0, x, 7, 1, 0, None) == coc.ERR_INVALID_ARG    # dtype
+    assert f(2, 64, 128, 128, x, x, x, _arr([A, None]), 1, 0, x, 1, 1, 0, None) == coc.ERR_INVALID_ARG
+    assert f(2, 64, 128, 128, x, x, x, _arr([A, MIS]), 1, 0, x, 0, 1, 0, None) == coc.ERR_ALIGN  # zero, channel
+    assert f(2, 64, 128, 128, x, x, x, _arr([A, MIS]), 2, 64, x, 1, 1, 0, None) == coc.ERR_ALIGN  # zero, group
+    assert f(2, 64, 136, 128, x, x, x, x, 0, 0, x, 1, 1, 0, None) == coc.ERR_ALIGN        # n % 16
+    assert f(2, 64, 128, 128, x, x, x, x, 3, 0, x, 1, 1, 0, None) == coc.ERR_INVALID_ARG  # granularity
+    assert f(2, 64, 128, 192, x, x, x, x, 2, 128, x, 0, 1, 0, None) == coc.ERR_SHAPE      # k_shard % group
+    assert f(2, 0, 128, 128, x, x, x, x, 1, 0, x, 1, 1, 0, None) == coc.OK                # empty: no-op
+
+
 def test_empty_problems_are_noops(L):
     # m == 0 or n == 0: documented no-op, returns before any CUDA call
     assert ar(L, m=0) == coc.OK

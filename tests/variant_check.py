@@ -58,15 +58,18 @@ def check_ag(R, ms, ns, k, dt, chunks):
         assert np.array_equal(wl.bits16(gathered[r].cpu()), xg)
 
 
-def check_w8(R, m, n, ks, group, gran):
-    s = wl.W8A16(R=R, m=m, n=n, k_shard=ks, group=group, seed=m)
+def check_w8(R, m, n, ks, group, gran, dt=F16, zero=False):
+    s = wl.W8A16(R=R, m=m, n=n, k_shard=ks, group=group, seed=m, dtype=dt)
     xs, wqs, scales = s.make(gran)
-    outs = coc.matmul_all_reduce_w8a16(to_dev(xs), to_dev(wqs), to_dev(scales), gran, group)
+    zs = s.zeros(gran) if zero else None
+    outs = coc.matmul_all_reduce_w8a16(to_dev(xs), to_dev(wqs), to_dev(scales), gran, group,
+                                       zeros=to_dev(zs) if zs is not None else None)
     coc.sync_status()
     code = {"tensor": 0, "channel": 1, "group": 2}[gran]
-    ref = orc.matmul_all_reduce_w8a16(bits(xs), [w.numpy() for w in wqs], bits(scales), code, group)
+    ref = orc.matmul_all_reduce_w8a16(bits(xs), [w.numpy() for w in wqs], bits(scales), code, group,
+                                      zeros=[z.numpy() for z in zs] if zs is not None else None, dtype=CODE[dt])
     for r, o in enumerate(outs):
-        assert_close(o, ref, s.K, f"w8A16 {gran} m={m} rank {r}")
+        assert_close(o, ref, s.K, f"w8A16 {dt} zero={zero} {gran} m={m} rank {r}")
 
 
 def main():
@@ -80,6 +83,7 @@ def main():
     check_ag(8, 512, 264, 64, BF16, 1)      # whole-tile A boxes from 512-row shards
     for gran in ("tensor", "channel", "group"):
         check_w8(2, 200, 272, 256, 128, gran)
+        check_w8(2, 200, 272, 256, 128, gran, dt=BF16, zero=True)
     print("variant ok:", os.environ.get("COC_PAIR", "auto"))
 
 
