@@ -430,7 +430,58 @@ def time_context(ops, dev):
         out["bloom7b_ar_python_chunking"] = {
             "python_chunked_ms": {str(C): round(t(lambda C=C: python_coc(C), 5), 4) for C in (1, 2, 4, 8)},
             "fused_ms": {str(C): round(v, 4) for C, v in fused.items()}}
+    out["next_rows"] = time_next_rows(ops, dev, t)
     return out
+
+
+def time_next_rows(ops, dev, t):
+    """The rows built beyond the headline suite, on the suite's layer shapes:
+    Megatron's n x k weight and the weight-gradient pass (LLaMA2-70B layers),
+    and the w8A16 extensions (bf16 activations, int8 zero points)."""
+    import torch
+
+    from tensor_matmul_collective_gb300 import coc
+    from tensor_matmul_collective_gb300 import workloads as wl
+
+    res = {}
+    rs = [o for o in ops if o.name == "llama70b_rs"]
+    if rs:
+        op = rs[0]
+        s = op.shape
+        dx, dw = op.inputs[:s.R], op.inputs[s.R:2 * s.R]
+        wnk = [w.t().contiguous() for w in dw]
+        outs = [torch.empty(s.m // s.R, s.n, dtype=s.dtype, device=dev) for _ in range(s.R)]
+        tk = t(op.run)
+        tn = t(lambda: coc.fused_matmul("reduce_scatter", dx, wnk, w_layout="nk", outs=outs))
+        res["llama70b_rs_weight_nk"] = {"kn_ms": round(tk, 4), "nk_ms": round(tn, 4),
+                                        "nk_tflops": round(s.flops() / tn / 1e9, 1)}
+        del wnk, outs
+    ag = [o for o in ops if o.kind == "ag_v2"]
+    if ag:
+        op = ag[0]
+        s = op.shape
+        dys = op.outputs[:s.R]                 # tokens x n_shard per rank (stands in for dY)
+        xgs = op.outputs[s.R:2 * s.R]          # the gathered X V2 returned, per rank (tokens x k)
+        dws = [torch.empty(s.n_shard, s.k, dtype=s.dtype, device=dev) for _ in range(s.R)]
+        tw = t(lambda: coc.weight_grad(dys, xgs, dws), 5)
+        flops = 2.0 * s.m * s.n_shard * s.k * s.R
+        res["llama70b_weight_grad"] = {"ms": round(tw, 4), "tflops": round(flops / tw / 1e9, 1)}
+        del dws
+    w8 = [o for o in ops if o.kind == "w8a16_ar"]
+    if w8:
+        base = w8[0].shape
+        for dt, zero in ((torch.float16, True), (torch.bfloat16, False), (torch.bfloat16, True)):
+            s = wl.W8A16(R=base.R, m=base.m, n=base.n, k_shard=base.k_shard, group=base.group, seed=base.seed,
+                         dtype=dt)
+            xs, wqs, scales = s.make("channel")
+            dx, dq, ds = [x.to(dev) for x in xs], [w.to(dev) for w in wqs], [c.to(dev) for c in scales]
+            dz = [z.to(dev) for z in s.zeros("channel")] if zero else None
+            outs = [torch.empty(s.m, s.n, dtype=dt, device=dev) for _ in range(s.R)]
+            tm = t(lambda: coc.matmul_all_reduce_w8a16(dx, dq, ds, "channel", s.group, outs, zeros=dz))
+            name = f"w8a16_ar_channel_{'bf16' if dt == torch.bfloat16 else 'fp16'}_{'zp' if zero else 'sym'}"
+            res[name] = {"ms": round(tm, 4), "tflops": round(s.flops() / tm / 1e9, 1)}
+            del dx, dq, ds, dz, outs
+    return res
 
 
 # --------------------------------------------------------- CPU oracle legs ---

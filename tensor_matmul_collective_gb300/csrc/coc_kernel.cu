@@ -350,25 +350,31 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const C
 // ------------------------------------------------------------ scheduling ---
 
 // Work unit -> (rank r for AllGather, m-tile, n-tile).  Units go chunk by
-// chunk; inside a chunk, m-tiles are taken in groups of group_mt (an L2-sized
-// slice of the A rows), and inside a group the m-tiles of one (rank, n-tile)
-// column are adjacent, so concurrently running CTAs share their B tiles and
-// the group's A rows stay in L2 while the columns stream past.
+// chunk; inside a chunk, AllGather takes the ranks one after another (rank r's
+// units read only W_r, so W_r's reuse across row groups stays within L2 reach
+// instead of being separated by every other rank's weights).  Inside a rank,
+// m-tiles are taken in groups of group_mt (an L2-sized slice of the A rows);
+// inside a group the m-tiles of one n-tile column are adjacent, so
+// concurrently running CTAs share their B tiles and the group's A rows stay in
+// L2 while the columns stream past.  Odd groups walk the columns backwards,
+// starting on the W columns the previous group read last.
 template <int OP>
 __device__ __forceinline__ void decode_unit(const KParams& p, int u, int& r, int& mt, int& nt) {
     const int rg = (OP == OP_AG) ? p.R : 1;
     if (p.chunk_mt > 0) {
-        const int per_chunk = p.chunk_mt * p.n_tiles * rg;
+        const int per_rank = p.chunk_mt * p.n_tiles;
+        const int per_chunk = per_rank * rg;
         const int c = u / per_chunk;
         int v = u - c * per_chunk;
+        r = v / per_rank;
+        v -= r * per_rank;
         const int G = p.group_mt > 0 ? p.group_mt : p.chunk_mt;
-        const int per_group = G * p.n_tiles * rg;
+        const int per_group = G * p.n_tiles;
         const int g = v / per_group;
         v -= g * per_group;
         const int mi = v % G;
-        v /= G;
-        nt = v % p.n_tiles;
-        r = v / p.n_tiles;
+        nt = v / G;
+        if (g & 1) nt = p.n_tiles - 1 - nt;
         mt = c * p.chunk_mt + g * G + mi;
     } else {
         const int per_row = p.n_tiles * rg;
@@ -524,32 +530,17 @@ struct Dq<true> {
     }
 };
 
-// Bulk copies (no tensor map): global -> this CTA's shared memory completing
-// on a barrier, and shared memory -> global in the bulk-group of the thread.
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
-                 : "memory");
-}
-__device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(dst)),
-                 "r"(src), "r"(bytes)
-                 : "memory");
-}
-
 // ALL_GATHER_MATMUL_V2: copy this unit's share of the m-tile's gathered rows
 // to every rank's gather buffer.  The tile's rows are one contiguous run of
 // the gathered matrix; it is cut into R * n_tiles equal pieces, one per work
 // unit of this m-tile (so the copy is spread over the whole kernel), and this
-// unit's piece is cut again between the epilogue warps (`wi` of `nw`).  One
-// thread per warp streams its part through the warp's two 4 KiB staging
-// buffers with the bulk-copy engine: a global -> shared copy completing on
-// the warp's barrier `gbar`, then one shared -> global copy per rank.  Pieces
-// never cross a shard boundary (the source is contiguous within a shard).
-// Returns false if a bounded wait ran out (the CTA is aborting).
-__device__ __noinline__ bool gather_slice_bulk(const KParams& p, int r, int mt, int nt, int tile_m, int wi, int nw,
-                                               uint8_t* my_epi, int& sb_i, uint32_t gbar, uint32_t& gphase,
-                                               const Ctl& ctl) {
+// unit's piece is cut again between the epilogue warps (`wi` of `nw`).  The
+// warp copies its part with plain 16-byte loads (lane l takes vectors l,
+// l + 32, ...; four per lane in flight) and writes each vector to every
+// rank's buffer, each warp access covering 512 contiguous bytes.  Shared
+// memory and the bulk-copy engine, which feed the mainloop, are not used.
+__device__ __forceinline__ void gather_slice_warp(const KParams& p, int r, int mt, int nt, int tile_m, int wi, int nw,
+                                                  int lane) {
     const int rows = min(tile_m, p.m - mt * tile_m);
     const long long vpr = p.k / 8;   // 16-byte vectors per row
     const long long total = rows * vpr;
@@ -557,33 +548,30 @@ __device__ __noinline__ bool gather_slice_bulk(const KParams& p, int r, int mt, 
     const long long qi = static_cast<long long>(r) * p.n_tiles + nt;
     const long long u0 = total * qi / Q, u1 = total * (qi + 1) / Q;
     const long long a = u0 + (u1 - u0) * wi / nw, b = u0 + (u1 - u0) * (wi + 1) / nw;
-    const long long tile_base = static_cast<long long>(mt) * tile_m * p.k;   // elements
-    constexpr long long kPiece = EPI_BUF_BYTES / 16;                          // vectors per staging buffer
-    for (long long vv = a; vv < b;) {
-        const long long lr = vv / vpr;
-        const int g = mt * tile_m + static_cast<int>(lr);
-        const int sh = g / p.rows_per_rank;
-        const long long shard_end = (static_cast<long long>(sh + 1) * p.rows_per_rank - mt * tile_m) * vpr;
-        long long lim = vv + kPiece;
-        if (lim > b) lim = b;
-        if (lim > shard_end) lim = shard_end;
-        const uint32_t bytes = static_cast<uint32_t>((lim - vv) * 16);
-        const long long c = vv - lr * vpr;
-        const uint16_t* src = p.gsrc[sh] + (static_cast<long long>(g - sh * p.rows_per_rank) * p.k + c * 8);
-        const uint32_t buf = smem_u32(my_epi + (sb_i & 1) * EPI_BUF_BYTES);
-        ++sb_i;
-        bulk_wait_read<1>();   // the stores that last read this buffer are done
-        mbar_expect_tx(gbar, bytes);
-        bulk_g2s(buf, src, bytes, gbar);
-        if (!wait_bounded(gbar, gphase, ctl, 0x320u, COC_WAIT_NS)) return false;
-        gphase ^= 1u;
-        const long long off = tile_base + vv * 8;
-        for (int d = 0; d < p.R; ++d)
-            if (p.gdst[d] != nullptr) bulk_s2g(p.gdst[d] + off, buf, bytes);
-        bulk_commit();
-        vv = lim;
+    const long long gbase = static_cast<long long>(mt) * tile_m * vpr;       // tile's first vector
+    const long long shard_vecs = static_cast<long long>(p.rows_per_rank) * vpr;
+    for (long long v0 = a; v0 < b; v0 += 32 * 4) {
+        uint4 d[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const long long v = v0 + u * 32 + lane;
+            d[u] = make_uint4(0u, 0u, 0u, 0u);
+            if (v < b) {
+                const long long gv = gbase + v;
+                const long long sh = gv / shard_vecs;   // the shard holding this row
+                d[u] = __ldg(reinterpret_cast<const uint4*>(p.gsrc[sh] + (gv - sh * shard_vecs) * 8));
+            }
+        }
+        for (int dd = 0; dd < p.R; ++dd) {
+            uint16_t* dst = p.gdst[dd];
+            if (dst == nullptr) continue;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const long long v = v0 + u * 32 + lane;
+                if (v < b) *reinterpret_cast<uint4*>(dst + (gbase + v) * 8) = d[u];
+            }
+        }
     }
-    return true;
 }
 
 // ------------------------------------------------------------ the kernel ---
@@ -643,8 +631,7 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
     uint64_t* acce = accf + 2;         // [2]  accumulator drained by the epilogue (leader: both CTAs)
     uint64_t* never = acce + 2;        // [1]  nothing arrives here (fault-injection test)
     uint64_t* drain = never + 1;       // [1]  MMA drain before TMEM release
-    uint64_t* gbar = drain + 1;        // [NUM_EPI_WARPS] AG-V2 gather copies (global -> shared)
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbar + NUM_EPI_WARPS);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     uint32_t* abort_word = tmem_slot + 1;
     // w8A16 pair: 16-byte landing slots for the peer's per-stage "B half ready" copies
     uint8_t* sig_slots = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(abort_word + 1) + 15) & ~uintptr_t(15));
@@ -676,7 +663,6 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
         }
         mbar_init(smem_u32(never), 1);
         mbar_init(smem_u32(drain), 1);
-        for (int w = 0; w < NUM_EPI_WARPS; ++w) mbar_init(smem_u32(&gbar[w]), 1);
         *abort_word = 0u;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         fence_proxy_async_smem();
@@ -710,17 +696,12 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
         constexpr uint32_t kFullBytes = NPAIR * (A_STAGE_BYTES + (W8 ? 0 : C::B_BYTES));
         const uint64_t pol_a = make_l2_policy(p.a_hint), pol_b = make_l2_policy(p.b_hint);
         bool ok = true;
-        for (int u = first_unit; ok && u < p.units; u += unit_step) {
-            int r, mt, nt;
-            decode_unit<OP>(p, u, r, mt, nt);
-            const int row_base = mt * TILE_M + static_cast<int>(rank) * BM;   // this CTA's first A row
-            const int col_base = nt * BN + static_cast<int>(rank) * C::BN_CTA;  // this CTA's first B column
-            // AllGather with whole-tile boxes: the tile's shard and local row
-            int a_shard = 0, a_row = 0;
-            if constexpr (OP == OP_AG) {
-                a_shard = min(row_base / p.rows_per_rank, p.R - 1);
-                a_row = row_base - a_shard * p.rows_per_rank;
-            }
+        // One unit's k-loop.  issue_a / issue_b put the unit's A and B boxes of
+        // one k-block into a stage; they are chosen once per unit (below), so
+        // the loop that runs per k-block has no layout branches: measured,
+        // deciding the AllGather A-box layout inside this loop cost ~13% on the
+        // LLaMA2-70B AG layer.
+        auto unit_loop = [&](int col_base, auto&& issue_a, auto&& issue_b) {
             for (int ks = 0; ok && ks < p.num_kshards; ++ks) {
                 for (int kb = 0; kb < p.kblocks; ++kb) {
                     ok = warp_wait(smem_u32(&empty[stage]), phase ^ 1u, ctl, 0x100u + stage);
@@ -729,47 +710,13 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
                     if (lane == 0) {
                         const uint32_t fb_local = smem_u32(&full[stage]);
                         const uint32_t fb = PAIR ? map_to_rank(fb_local, 0) : fb_local;
-                        const uint32_t a_dst = smem_u32(a_st + stage * A_STAGE_BYTES);
                         if (rank == 0) mbar_expect_tx(fb_local, kFullBytes);
                         auto load = [&](uint32_t dst, const CUtensorMap* map, int c0, int c1, uint64_t pol) {
                             if constexpr (PAIR) tma_load_2d_pair(dst, map, c0, c1, fb, pol);
                             else tma_load_2d_hint(dst, map, c0, c1, fb, pol);
                         };
-                        if constexpr (OP == OP_AG) {
-                            // gathered rows -> (shard, local row); rows past the
-                            // end read beyond the last shard and are zero-filled
-                            if (p.a_mnmajor) {
-                                // weight gradient: A = dY_r^T, read from rank r's dY (tokens x
-                                // rows) as two 64-row blocks of 64 tokens (MN-major, like B)
-#pragma unroll
-                                for (int j = 0; j < BM / 64; ++j)
-                                    load(a_dst + j * (64 * BK * 2), &p.tm_a[r], row_base + j * 64, kc, pol_a);
-                            } else if (p.a_box_rows == BM) {
-                                load(a_dst, &p.tm_a[a_shard], kc, a_row, pol_a);
-                            } else {
-                                for (int rb = 0; rb < BM; rb += p.a_box_rows) {
-                                    const int g = row_base + rb;
-                                    int sh = g / p.rows_per_rank;
-                                    if (sh > p.R - 1) sh = p.R - 1;
-                                    load(a_dst + rb * 128, &p.tm_a[sh], kc, g - sh * p.rows_per_rank, pol_a);
-                                }
-                            }
-                        } else {
-                            load(a_dst, &p.tm_a[ks], kc, row_base, pol_a);
-                        }
-                        if constexpr (!W8) {
-                            const CUtensorMap* bm = &p.tm_b[(OP == OP_AG) ? r : ks];
-                            const uint32_t b_dst = smem_u32(b_st + stage * C::B_BYTES);
-                            if (p.b_kmajor) {
-                                // W stored n x k: one box of this CTA's B rows (n) x 64 k, laid
-                                // out like the A tile (K-major, 128-byte swizzle)
-                                load(b_dst, bm, kc, col_base, pol_b);
-                            } else {
-#pragma unroll
-                                for (int j = 0; j < C::BN_CTA / 64; ++j)
-                                    load(b_dst + j * (64 * BK * 2), bm, col_base + j * 64, kc, pol_b);
-                            }
-                        }
+                        issue_a(load, smem_u32(a_st + stage * A_STAGE_BYTES), ks, kc);
+                        if constexpr (!W8) issue_b(load, smem_u32(b_st + stage * C::B_BYTES), ks, kc);
                         filled |= 1u << stage;
                         fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
                     }
@@ -791,6 +738,61 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
                         if (++rstage == C::SR) { rstage = 0; rphase ^= 1u; }
                     }
                 }
+            }
+        };
+        for (int u = first_unit; ok && u < p.units; u += unit_step) {
+            int r, mt, nt;
+            decode_unit<OP>(p, u, r, mt, nt);
+            const int row_base = mt * TILE_M + static_cast<int>(rank) * BM;   // this CTA's first A row
+            const int col_base = nt * BN + static_cast<int>(rank) * C::BN_CTA;  // this CTA's first B column
+            // A: one 128-row box (AllGather: from the shard holding the rows,
+            // which then hold the whole tile; rows past the end read beyond the
+            // last shard and are zero-filled), ...
+            int a_shard = 0, a_row = row_base;
+            if constexpr (OP == OP_AG) {
+                a_shard = min(row_base / p.rows_per_rank, p.R - 1);
+                a_row = row_base - a_shard * p.rows_per_rank;
+            }
+            auto a_single = [&](auto& load, uint32_t dst, int ks, int kc) {
+                load(dst, &p.tm_a[(OP == OP_AG) ? a_shard : ks], kc, a_row, pol_a);
+            };
+            // ... several boxes when a shard holds fewer rows than a tile, ...
+            auto a_multi = [&](auto& load, uint32_t dst, int, int kc) {
+                for (int rb = 0; rb < BM; rb += p.a_box_rows) {
+                    const int g = row_base + rb;
+                    int sh = g / p.rows_per_rank;
+                    if (sh > p.R - 1) sh = p.R - 1;
+                    load(dst + rb * 128, &p.tm_a[sh], kc, g - sh * p.rows_per_rank, pol_a);
+                }
+            };
+            // ... or, for the weight gradient, A = dY_r^T read from rank r's dY
+            // (tokens x rows) as two 64-row blocks of 64 tokens (MN-major, like B).
+            auto a_mn = [&](auto& load, uint32_t dst, int, int kc) {
+#pragma unroll
+                for (int j = 0; j < BM / 64; ++j) load(dst + j * (64 * BK * 2), &p.tm_a[r], row_base + j * 64, kc, pol_a);
+            };
+            // B: W stored k x n, read as 64-column MN-major boxes, or W stored
+            // n x k, one box of this CTA's B rows (n) x 64 k laid out like A.
+            const CUtensorMap* bmaps = &p.tm_b[(OP == OP_AG) ? r : 0];
+            auto b_mn = [&](auto& load, uint32_t dst, int ks, int kc) {
+                const CUtensorMap* bm = (OP == OP_AG) ? bmaps : &p.tm_b[ks];
+#pragma unroll
+                for (int j = 0; j < C::BN_CTA / 64; ++j) load(dst + j * (64 * BK * 2), bm, col_base + j * 64, kc, pol_b);
+            };
+            auto b_kmaj = [&](auto& load, uint32_t dst, int ks, int kc) {
+                load(dst, (OP == OP_AG) ? bmaps : &p.tm_b[ks], kc, col_base, pol_b);
+            };
+            auto with_b = [&](auto&& issue_a) {
+                if constexpr (W8) unit_loop(col_base, issue_a, b_mn);   // B comes from the dequant warps
+                else if (p.b_kmajor) unit_loop(col_base, issue_a, b_kmaj);
+                else unit_loop(col_base, issue_a, b_mn);
+            };
+            if constexpr (OP == OP_AG) {
+                if (p.a_mnmajor) with_b(a_mn);
+                else if (p.a_box_rows == BM) with_b(a_single);
+                else with_b(a_multi);
+            } else {
+                with_b(a_single);
             }
         }
         if (!ok && lane == 0) {
@@ -881,7 +883,6 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
         uint8_t* my_epi = epi + (warp - 2) * C::EPI_NBUF * EPI_BUF_BYTES;
         const uint32_t acce_base = PAIR ? map_to_rank(smem_u32(acce), 0) : smem_u32(acce);
         int acc_i = 0, sb_i = 0;
-        uint32_t gphase = 0;   // AG-V2: phase of this warp's gather barrier
         bool ok = true;
         if (p.inject_timeout) ok = warp_wait(smem_u32(never), 0, ctl, 0x300u);
         for (int u = first_unit; ok && u < p.units; u += unit_step) {
@@ -985,16 +986,9 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
             }
             ++acc_i;
             if constexpr (OP == OP_AG) {
-                if (p.has_gather) {
-                    bool ok_g = true;
-                    if (lane == 0)
-                        ok_g = gather_slice_bulk(p, r, mt, nt, TILE_M,
-                                                 static_cast<int>(rank) * NUM_EPI_WARPS + (warp - 2),
-                                                 NPAIR * NUM_EPI_WARPS, my_epi, sb_i, smem_u32(&gbar[warp - 2]),
-                                                 gphase, ctl);
-                    sb_i = __shfl_sync(0xffffffffu, sb_i, 0);
-                    ok = __shfl_sync(0xffffffffu, ok_g ? 1 : 0, 0) != 0;
-                }
+                if (p.has_gather)
+                    gather_slice_warp(p, r, mt, nt, TILE_M, static_cast<int>(rank) * NUM_EPI_WARPS + (warp - 2),
+                                      NPAIR * NUM_EPI_WARPS, lane);
             }
         }
         if (lane == 0) bulk_wait_all();
