@@ -350,36 +350,33 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const C
 // ------------------------------------------------------------ scheduling ---
 
 // Work unit -> (rank r for AllGather, m-tile, n-tile).  Units go chunk by
-// chunk; inside a chunk, AllGather takes the ranks one after another (rank r's
-// units read only W_r, so W_r's reuse across row groups stays within L2 reach
-// instead of being separated by every other rank's weights).  Inside a rank,
-// m-tiles are taken in groups of group_mt (an L2-sized slice of the A rows);
-// inside a group the m-tiles of one n-tile column are adjacent, so
-// concurrently running CTAs share their B tiles and the group's A rows stay in
-// L2 while the columns stream past.  Odd groups walk the columns backwards,
-// starting on the W columns the previous group read last.
+// chunk; inside a chunk, m-tiles are taken in groups of group_mt (an L2-sized
+// slice of the A rows), and inside a group the m-tiles of one (rank, n-tile)
+// column are adjacent, so concurrently running CTAs share their B tiles and
+// the group's A rows stay in L2 while the columns stream past.  Odd groups
+// walk the columns backwards, starting on the W columns the previous group
+// read last.
 template <int OP>
 __device__ __forceinline__ void decode_unit(const KParams& p, int u, int& r, int& mt, int& nt) {
     const int rg = (OP == OP_AG) ? p.R : 1;
+    const int ncols = p.n_tiles * rg;   // (rank, n-tile) columns
     if (p.chunk_mt > 0) {
-        const int per_rank = p.chunk_mt * p.n_tiles;
-        const int per_chunk = per_rank * rg;
+        const int per_chunk = p.chunk_mt * ncols;
         const int c = u / per_chunk;
         int v = u - c * per_chunk;
-        r = v / per_rank;
-        v -= r * per_rank;
         const int G = p.group_mt > 0 ? p.group_mt : p.chunk_mt;
-        const int per_group = G * p.n_tiles;
+        const int per_group = G * ncols;
         const int g = v / per_group;
         v -= g * per_group;
         const int mi = v % G;
-        nt = v / G;
-        if (g & 1) nt = p.n_tiles - 1 - nt;
+        int col = v / G;
+        if (g & 1) col = ncols - 1 - col;
+        nt = col % p.n_tiles;
+        r = col / p.n_tiles;
         mt = c * p.chunk_mt + g * G + mi;
     } else {
-        const int per_row = p.n_tiles * rg;
-        mt = u / per_row;
-        const int v = u - mt * per_row;
+        mt = u / ncols;
+        const int v = u - mt * ncols;
         nt = v % p.n_tiles;
         r = v / p.n_tiles;
     }
