@@ -37,6 +37,7 @@ struct DeviceState {
     int cc_major = 0, cc_minor = 0;
     unsigned* status = nullptr;
     int max_pairs[4][2] = {{-1, -1}, {-1, -1}, {-1, -1}, {-1, -1}};   // per op, per bf16; -1 = not queried
+    cudaMemPool_t pool = nullptr;   // stream-ordered workspace (w8A16 pre-pass), kept between calls
 };
 
 std::mutex g_mu;
@@ -304,6 +305,82 @@ coc_status_t validate_row_parallel(int R, int64_t m, int64_t n, int64_t ks, cons
     return COC_OK;
 }
 
+// w8A16 path choice.  The fused kernel dequantises each weight tile in shared
+// memory once per 256-row tile; the pre-pass dequantises every weight element
+// once through HBM (1 byte read, 2 written) and then runs the AllReduce
+// kernel.  The pre-pass costs about 3 K n / HBM bandwidth against the fused
+// path's ~20% of the GEMM time (measured: 14.5% conversion traffic in shared
+// memory plus the extra barrier handshake), so it wins from roughly m = 1700
+// rows.  COC_W8_PATH=fused|prepass forces a path (tests, tuning).
+constexpr int64_t kW8PrepassMinRows = 2048;
+
+bool w8_use_prepass(int64_t m) {
+    const char* e = std::getenv("COC_W8_PATH");
+    if (e != nullptr && std::strcmp(e, "fused") == 0) return false;
+    if (e != nullptr && std::strcmp(e, "prepass") == 0) return true;
+    return m >= kW8PrepassMinRows;
+}
+
+coc_status_t device_pool(DeviceState* ds, cudaMemPool_t* out) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (ds->pool == nullptr) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t pool = nullptr;
+        if ((e = cudaMemPoolCreate(&pool, &props)) != cudaSuccess) return cuda_fail(e, "cudaMemPoolCreate");
+        uint64_t keep = UINT64_MAX;   // keep freed workspace for the next call
+        if ((e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep)) != cudaSuccess) {
+            cudaMemPoolDestroy(pool);
+            return cuda_fail(e, "cudaMemPoolSetAttribute");
+        }
+        ds->pool = pool;
+    }
+    *out = ds->pool;
+    return COC_OK;
+}
+
+// Pre-pass path: dequantise all ranks' weights into a stream-ordered
+// workspace, run the AllReduce on it, release the workspace on the stream.
+coc_status_t w8_prepass_all_reduce(int R, int64_t m, int64_t n, int64_t ks, const void* const* x, const void* const* w,
+                                   const void* const* scale, const void* const* zero, coc_scale_t gran, int64_t group,
+                                   void* const* out, coc_dtype_t dt, int chunks, cudaStream_t stream) {
+    DeviceState* ds = nullptr;
+    coc_status_t st = device_state(&ds);
+    if (st != COC_OK) return st;
+    cudaMemPool_t pool = nullptr;
+    if ((st = device_pool(ds, &pool)) != COC_OK) return st;
+    const size_t per_rank = static_cast<size_t>(ks) * static_cast<size_t>(n);   // elements
+    void* ws = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, per_rank * 2 * R, pool, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMallocFromPoolAsync (w8A16 workspace)");
+    W8PrepassArgs a;
+    std::memset(&a, 0, sizeof a);
+    const void* wd[COC_MAX_RANKS] = {};
+    for (int r = 0; r < R; ++r) {
+        a.q[r] = static_cast<const int8_t*>(w[r]);
+        a.scale[r] = static_cast<const uint16_t*>(scale[r]);
+        a.zero[r] = zero ? static_cast<const int8_t*>(zero[r]) : nullptr;
+        a.out[r] = static_cast<uint16_t*>(ws) + per_rank * r;
+        wd[r] = a.out[r];
+    }
+    a.R = R;
+    a.k = static_cast<int>(ks);
+    a.n = static_cast<int>(n);
+    a.gran = static_cast<int>(gran);
+    a.group = static_cast<int>(group);
+    e = launch_w8_prepass(a, dt == COC_BF16, ds->sm_count, stream);
+    if (e != cudaSuccess) st = cuda_fail(e, "w8A16 pre-pass launch");
+    else st = row_parallel(OP_AR, R, m, n, ks, x, wd, out, R, dt, chunks, nullptr, COC_SCALE_TENSOR, 0, stream);
+    const cudaError_t ef = cudaFreeAsync(ws, stream);
+    if (st == COC_OK && ef != cudaSuccess) st = cuda_fail(ef, "cudaFreeAsync (w8A16 workspace)");
+    return st;
+}
+
 }  // namespace
 }  // namespace coc
 
@@ -373,6 +450,9 @@ COC_API coc_status_t coc_matmul_all_reduce_w8a16_ex(int R, int64_t m, int64_t n,
                         (long long)group_size);
     }
     if (empty) return COC_OK;
+    if (k_shard > 0 && w8_use_prepass(m))
+        return w8_prepass_all_reduce(R, m, n, k_shard, x, w, scale, zero, gran, group_size, out, dt, chunks,
+                                     reinterpret_cast<cudaStream_t>(stream));
     return row_parallel(OP_W8, R, m, n, k_shard, x, w, out, R, dt, chunks, scale, gran, group_size,
                         reinterpret_cast<cudaStream_t>(stream), false, zero);
 }
@@ -616,6 +696,12 @@ COC_API coc_status_t coc_shutdown(void) {
     const bool have_cur = cudaGetDevice(&cur) == cudaSuccess;
     coc_status_t st = COC_OK;
     for (auto& kv : g_dev) {
+        if (kv.second.pool != nullptr) {
+            if (cudaSetDevice(kv.first) == cudaSuccess && cudaMemPoolDestroy(kv.second.pool) == cudaSuccess)
+                kv.second.pool = nullptr;
+            else
+                st = fail(COC_ERR_CUDA, "could not destroy the workspace pool of device %d", kv.first);
+        }
         if (kv.second.status != nullptr) {
             if (cudaSetDevice(kv.first) == cudaSuccess && cudaFree(kv.second.status) == cudaSuccess)
                 kv.second.status = nullptr;

@@ -77,6 +77,18 @@ coc_status_t validate_all_reduce_args(int R, int64_t m, int64_t n, int64_t k_sha
                                       int deterministic);
 coc_status_t report_error(coc_status_t st, const char* msg);
 
+// w8A16 streaming pre-pass (coc_w8_prepass.cu): dequantise every rank's int8
+// weight once, Wd = rne((q - z) * s) in the activation type, into a 16-bit
+// k x n buffer per rank (same conversion code as the fused kernel).
+struct W8PrepassArgs {
+    const int8_t* q[COC_MAX_RANKS];        // k x n int8 per rank
+    const uint16_t* scale[COC_MAX_RANKS];  // scale views (activation type)
+    const int8_t* zero[COC_MAX_RANKS];     // zero-point views, NULL = symmetric
+    uint16_t* out[COC_MAX_RANKS];          // k x n fp16/bf16 per rank
+    int R, k, n, gran, group;
+};
+cudaError_t launch_w8_prepass(const W8PrepassArgs& a, bool bf16, int sm_count, cudaStream_t stream);
+
 // Host-side launch helpers implemented in coc_kernel.cu.  `pair` selects the
 // 2-SM variant (a cluster of two CTAs per 256-row tile; grid = 2 x pairs);
 // otherwise one CTA per 128-row tile.

@@ -89,3 +89,45 @@ def test_zero_point_equal_to_weight_gives_zero():
                                        zeros=to_dev([z, z]))
     coc.sync_status()
     assert not torch.any(outs[0])
+
+
+def _force_path(monkeypatch, path):
+    monkeypatch.setenv("COC_W8_PATH", path)
+
+
+@pytest.mark.parametrize("dt", [torch.float16, torch.bfloat16], ids=["fp16", "bf16"])
+@pytest.mark.parametrize("zero", [False, True], ids=["sym", "zp"])
+@pytest.mark.parametrize("gran", ["tensor", "channel", "group"])
+def test_prepass_and_fused_paths_give_the_same_bits(monkeypatch, dt, zero, gran):
+    """Large m dequantises the weight once in a pre-pass and runs the AllReduce
+    kernel; small m dequantises per tile inside the fused kernel.  Both use the
+    same conversion and the same accumulation order: identical outputs."""
+    shape = wl.W8A16(R=4, m=512, n=272, k_shard=192, group=64, seed=31, dtype=dt)
+    xs, wqs, scales = shape.make(gran)
+    zs = shape.zeros(gran) if zero else None
+    args = (to_dev(xs), to_dev(wqs), to_dev(scales), gran, 64)
+    kw = dict(zeros=to_dev(zs) if zs is not None else None, chunks=2)
+    _force_path(monkeypatch, "fused")
+    a = coc.matmul_all_reduce_w8a16(*args, **kw)
+    _force_path(monkeypatch, "prepass")
+    b = coc.matmul_all_reduce_w8a16(*args, **kw)
+    coc.sync_status()
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    ref = orc.matmul_all_reduce_w8a16(bits(xs), [w.numpy() for w in wqs], bits(scales), GRAN[gran], 64,
+                                      zeros=[z.numpy() for z in zs] if zs is not None else None, dtype=CODE[dt])
+    assert_close(b[0], ref, shape.K, f"pre-pass {dt} zero={zero} {gran}")
+
+
+def test_prepass_dequant_bitwise(monkeypatch):
+    """The pre-pass's dequantised weight, read back through one-hot rows."""
+    R, n, ks, group = 2, 256, 128, 64
+    shape = wl.W8A16(R=R, m=ks, n=n, k_shard=ks, group=group, seed=6, dtype=torch.bfloat16)
+    _, wqs, scales = shape.make("group")
+    zs = shape.zeros("group")
+    xs = [torch.eye(ks, dtype=torch.bfloat16)] + [torch.zeros(ks, ks, dtype=torch.bfloat16)]
+    _force_path(monkeypatch, "prepass")
+    outs = coc.matmul_all_reduce_w8a16(to_dev(xs), to_dev(wqs), to_dev(scales), "group", group, zeros=to_dev(zs))
+    coc.sync_status()
+    wd = orc.dequant_w8a16_ex(wqs[0].numpy(), wl.bits16(scales[0]), 2, group, 0, zs[0].numpy(), orc.BF16)
+    assert np.array_equal(wl.bits16(outs[0].cpu()), wd)
