@@ -285,3 +285,51 @@ def matmul_all_reduce_w8a16(xs, wqs, scales, gran: int, group: int = 0, rows=Non
         zs = zeros if zeros is not None else [None] * len(wqs)
         wds = [dequant_w8a16_ex(wq, s, gran, group, 0, z, dtype) for wq, s, z in zip(wqs, scales, zs)]
     return matmul_all_reduce(dtype, xs, wds, rows, nthreads)
+
+
+# ------------------------------------------- MoE dispatch + GroupedMatMul ---
+#
+# The MindSpeed-LLM overlap blog (section 第二层MC2) names an expert-parallel
+# form of the fused operators: the MoE token all-to-all fused with the
+# experts' GroupedMatMul.  It gives no formula; the reading used here is the
+# plain one of expert parallelism with top-1 routing:
+#
+# * R expert-parallel ranks, E = R * E_loc experts, expert e held by rank
+#   e // E_loc; rank r holds tokens X_r (T x h) and their expert ids idx_r.
+# * Dispatch (the all-to-all): destination rank q receives every token routed
+#   to one of its experts, grouped by expert (ascending), inside an expert by
+#   source rank (ascending), inside a source rank by token index (ascending).
+# * GroupedMatMul: each expert's group of rows times that expert's weight
+#   W_e (h x f).
+
+def moe_dispatch_order(idxs, E: int):
+    """For every expert e (0..E-1): the list of (source rank, token) pairs in
+    dispatch order, as an (n_e x 2) int64 array."""
+    R = len(idxs)
+    out = []
+    for e in range(E):
+        pairs = []
+        for r in range(R):
+            t = np.nonzero(np.asarray(idxs[r]) == e)[0]
+            pairs.append(np.stack([np.full(t.size, r, dtype=np.int64), t.astype(np.int64)], axis=1))
+        out.append(np.concatenate(pairs, axis=0) if pairs else np.zeros((0, 2), np.int64))
+    return out
+
+
+def moe_dispatch_grouped_matmul(dtype: int, xs, idxs, ws, nthreads=None):
+    """Dispatch + GroupedMatMul.  xs[r]: token bits (T x h) in `dtype`;
+    idxs[r]: int expert ids (T); ws[e]: expert weight bits (h x f), E = len(ws).
+    Returns, per expert e, (pairs_e, Xd_e, Y_e): the dispatch order, the
+    dispatched token bits (n_e x h, a bit-exact copy) and Y_e = Xd_e @ W_e in
+    fp64 (n_e x f)."""
+    E = len(ws)
+    res = []
+    for e, pairs in enumerate(moe_dispatch_order(idxs, E)):
+        h = xs[0].shape[1]
+        Xd = np.empty((pairs.shape[0], h), dtype=np.uint16)
+        for i, (r, t) in enumerate(pairs):
+            Xd[i] = xs[r][t]
+        f = ws[e].shape[1]
+        Y = matmul_all_reduce(dtype, [Xd], [ws[e]], None, nthreads) if pairs.shape[0] else np.zeros((0, f))
+        res.append((pairs, Xd, Y))
+    return res

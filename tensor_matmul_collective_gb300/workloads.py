@@ -206,6 +206,42 @@ class W8A16:
 
 
 @dataclass
+class MoEDispatch:
+    """Expert-parallel MoE layer input: R ranks with T tokens each (T x h),
+    top-1 expert ids in [0, E) with E = R * e_loc (expert e on rank
+    e // e_loc), and one h x f weight per expert.  Expert popularity is
+    skewed (weights (e + 1)^-skew, shuffled) so groups have unequal sizes."""
+    R: int
+    T: int
+    h: int
+    f: int
+    e_loc: int
+    seed: int
+    dtype: torch.dtype = torch.bfloat16
+    skew: float = 0.5
+
+    @property
+    def E(self) -> int:
+        return self.R * self.e_loc
+
+    def flops(self) -> float:
+        return 2.0 * self.R * self.T * self.h * self.f
+
+    def routing(self):
+        g = np.random.Generator(np.random.PCG64(self.seed * 7919 + 11))
+        w = (np.arange(self.E) + 1.0) ** (-self.skew)
+        w = w[g.permutation(self.E)]
+        p = w / w.sum()
+        return [torch.from_numpy(g.choice(self.E, size=self.T, p=p).astype(np.int32)) for _ in range(self.R)]
+
+    def make(self):
+        """Returns (xs, idxs, ws)."""
+        xs = [to16(normal((self.T, self.h), 1.0, self.seed, 20 + r), self.dtype) for r in range(self.R)]
+        ws = [to16(normal((self.h, self.f), 0.02, self.seed, 40 + e), self.dtype) for e in range(self.E)]
+        return xs, self.routing(), ws
+
+
+@dataclass
 class Workload:
     name: str
     op: str            # "ar", "rs", "ag_v2", "w8a16_ar"

@@ -366,6 +366,71 @@ def test_w8a16_zero_point_special_cases(oracle_mod):
     assert d16.tolist() == [[255.0, 0.0]] and dbf.tolist() == [[255.0, 0.0]]
 
 
+# ------------------------------------------- MoE dispatch + GroupedMatMul ---
+
+def _dispatch_properties(groups, idxs, T):
+    """Checks that do not re-run the construction: every token is dispatched
+    exactly once, to the expert it was routed to, and each expert's group is
+    ordered by (source rank, token index)."""
+    seen = np.zeros((len(idxs), T), dtype=np.int64)
+    for e, pairs in enumerate(groups):
+        for r, t in pairs:
+            seen[r, t] += 1
+            if int(idxs[r][t]) != e:
+                return False
+        keys = pairs[:, 0] * T + pairs[:, 1]
+        if np.any(np.diff(keys) <= 0):
+            return False
+    return bool(np.all(seen == 1))
+
+
+@pytest.mark.parametrize("R,e_loc", [(1, 1), (2, 2), (4, 3)])
+def test_moe_dispatch_properties_and_grouped_gemm(oracle_mod, R, e_loc):
+    s = wl.MoEDispatch(R=R, T=37, h=24, f=20, e_loc=e_loc, seed=3 + R, dtype=torch.bfloat16)
+    xs, idxs, ws = s.make()
+    xb, ib, wb = [wl.bits16(x) for x in xs], [i.numpy() for i in idxs], [wl.bits16(w) for w in ws]
+    res = oracle_mod.moe_dispatch_grouped_matmul(oracle_mod.BF16, xb, ib, wb)
+    assert len(res) == s.E
+    assert _dispatch_properties([g[0] for g in res], ib, s.T)
+    assert sum(g[0].shape[0] for g in res) == R * s.T
+    for e, (pairs, Xd, Y) in enumerate(res):
+        # the dispatched rows are the source rows, bit for bit
+        for i, (r, t) in enumerate(pairs):
+            assert np.array_equal(Xd[i], xb[r][t])
+        if pairs.shape[0]:
+            ref = _dec(Xd, torch.bfloat16) @ _dec(wb[e], torch.bfloat16)   # numpy float64
+            assert _rel(Y, ref) < 1e-13
+
+
+def test_moe_single_expert_is_plain_gemm(oracle_mod):
+    s = wl.MoEDispatch(R=1, T=16, h=32, f=8, e_loc=1, seed=5, dtype=torch.float16)
+    xs, idxs, ws = s.make()
+    (pairs, Xd, Y), = oracle_mod.moe_dispatch_grouped_matmul(oracle_mod.F16, [wl.bits16(xs[0])], [idxs[0].numpy()],
+                                                             [wl.bits16(ws[0])])
+    assert np.array_equal(pairs[:, 1], np.arange(16)) and np.array_equal(Xd, wl.bits16(xs[0]))
+    ref = _dec(wl.bits16(xs[0]), torch.float16) @ _dec(wl.bits16(ws[0]), torch.float16)
+    assert _rel(Y, ref) < 1e-13
+
+
+def test_moe_dispatch_mutants_rejected(oracle_mod):
+    s = wl.MoEDispatch(R=3, T=20, h=8, f=8, e_loc=2, seed=9)
+    _, idxs, _ = s.make()
+    ib = [i.numpy() for i in idxs]
+    groups = oracle_mod.moe_dispatch_order(ib, s.E)
+    assert _dispatch_properties(groups, ib, s.T)
+    big = max(range(s.E), key=lambda e: groups[e].shape[0])
+    swapped = [g.copy() for g in groups]
+    swapped[big] = swapped[big][::-1].copy()               # rank/token order reversed
+    assert not _dispatch_properties(swapped, ib, s.T)
+    dropped = [g.copy() for g in groups]
+    dropped[big] = dropped[big][1:]                         # one token lost
+    assert not _dispatch_properties(dropped, ib, s.T)
+    moved = [g.copy() for g in groups]
+    moved[(big + 1) % s.E] = np.concatenate([moved[(big + 1) % s.E], moved[big][:1]])
+    moved[big] = moved[big][1:]                             # a token sent to the wrong expert
+    assert not _dispatch_properties(moved, ib, s.T)
+
+
 def test_thread_count_does_not_change_results(oracle_mod):
     xs = [_rand16((20, 64), torch.bfloat16, 100 + r) for r in range(2)]
     ws = [_rand16((64, 37), torch.bfloat16, 110 + r) for r in range(2)]
