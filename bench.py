@@ -90,7 +90,7 @@ def kernel_source_hash() -> str:
     """Hash of the kernel and of the host code that sets its launch (tile
     order, L2 grouping): DRAM traffic taken on other sources is stale."""
     h = hashlib.sha256()
-    for f in ("coc_kernel.cu", "coc_internal.h", "coc_api.cu", "coc_dequant.cuh", "coc_w8_prepass.cu"):
+    for f in ("coc_kernel.cu", "coc_internal.h", "coc_api.cu", "coc_dequant.cuh", "coc_w8_prepass.cu", "coc_moe.cu"):
         h.update(open(os.path.join(ROOT, "tensor_matmul_collective_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:12]
 

@@ -13,6 +13,9 @@
  *     per tensor / per channel / per group scales       coc_matmul_all_reduce_w8a16
  *     + zero point, bf16 activations (extension)         coc_matmul_all_reduce_w8a16_ex
  *
+ * and the expert-parallel form of the blog's MC2 section (extension):
+ *   MoE token dispatch + expert GroupedMatMul           coc_moe_dispatch_grouped_matmul
+ *
  * The same page's section 问题分析 ("problem analysis") places them in the
  * Megatron ColumnParallelLinear / RowParallelLinear layers: the matmul is
  * followed by AllReduce without sequence parallelism, by AllGather or
@@ -235,6 +238,49 @@ coc_status_t coc_matmul_all_reduce_w8a16_ex(int R, int64_t m, int64_t n, int64_t
                                             coc_scale_t gran, int64_t group_size, void* const* out,
                                             coc_dtype_t dt, int chunks, int deterministic,
                                             coc_stream_t stream);
+
+/*
+ * MoE expert-parallel dispatch fused with the experts' GroupedMatMul (the
+ * "EP MC2" form named in the MindSpeed-LLM overlap blog, section 第二层MC2:
+ * the token all-to-all fused with the expert GroupedMatMul).  Reading of the
+ * blog (it gives no formula): R expert-parallel ranks, E = R * experts_per_rank
+ * experts with expert e held by rank q = e / experts_per_rank, top-1 routing.
+ *
+ *   Dispatch (the all-to-all): rank q receives every token routed to one of
+ *   its experts, grouped by expert (ascending), inside an expert by source
+ *   rank (ascending), inside a source rank by token index (ascending).
+ *   Expert e's group occupies rows offsets[e] .. offsets[e] + counts[e] - 1
+ *   of xd[q] and y[q]; offsets are multiples of 256 (the rows between groups
+ *   are unspecified).
+ *   GroupedMatMul: y[q][row] = xd[q][row] @ W_e  (fp32 accumulate, RNE to dt).
+ *
+ * x[r]        tokens x h, rank r's tokens (dt)
+ * idx[r]      tokens int32 expert ids in [0, E); others are not dispatched
+ *             and coc_sync_status then reports COC_ERR_INVALID_ARG
+ * w           E x h x f, the experts' weights stacked (expert e's h x f block
+ *             at e * h * f elements), dt
+ * xd[q], y[q] capacity x h and capacity x f, written (the dispatched tokens,
+ *             a bit-exact copy, and the expert outputs)
+ * counts, offsets  E int32 each, written by the device
+ * capacity    rows of xd[q] / y[q]; at least coc_moe_capacity(R, tokens,
+ *             experts_per_rank)
+ * Shape: h a positive multiple of 64; f * 2 % 16 == 0; E <= 256.
+ * Alignment: x, xd, y, w 16-byte aligned; idx, counts, offsets 4-byte.
+ * Ownership: all buffers are the caller's device memory; a routing table of
+ * R x tokens int32 is taken from the library's stream-ordered pool for the
+ * duration of the call.  Runs on `stream` (three kernels: routing, token
+ * copy, grouped GEMM); no host synchronisation.
+ */
+coc_status_t coc_moe_dispatch_grouped_matmul(int R, int64_t tokens, int64_t h, int64_t f, int experts_per_rank,
+                                             const void* const* x, const int32_t* const* idx, const void* w,
+                                             void* const* xd, void* const* y, int64_t capacity,
+                                             int32_t* counts, int32_t* offsets, coc_dtype_t dt,
+                                             coc_stream_t stream);
+
+/* Rows xd[q] / y[q] need for coc_moe_dispatch_grouped_matmul: R * tokens plus
+ * 255 rows of padding per expert of a rank, rounded up to 256; -1 on bad
+ * arguments.  Host only. */
+int64_t coc_moe_capacity(int R, int64_t tokens, int experts_per_rank);
 
 /*
  * Any of the four bf16/fp16 fused operators with a choice of weight layout.

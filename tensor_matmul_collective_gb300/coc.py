@@ -28,7 +28,7 @@ EXPORTS = (
     "coc_all_gather_matmul_v2", "coc_matmul_all_reduce_w8a16", "coc_matmul",
     "coc_sync_status", "coc_status_string", "coc_last_error", "coc_version",
     "coc_debug_inject_timeout", "coc_shutdown", "coc_matmul_all_reduce_noalloc",
-    "coc_fused_matmul", "coc_matmul_all_reduce_w8a16_ex",
+    "coc_fused_matmul", "coc_matmul_all_reduce_w8a16_ex", "coc_moe_dispatch_grouped_matmul", "coc_moe_capacity",
 )
 
 OP_ALL_REDUCE, OP_REDUCE_SCATTER, OP_ALL_GATHER, OP_ALL_GATHER_V2, OP_WEIGHT_GRAD = range(5)
@@ -72,6 +72,11 @@ def lib() -> ctypes.CDLL:
             L.coc_matmul_all_reduce_w8a16_ex.argtypes = [i32, i64, i64, i64, pp, pp, pp, pp, i32, i64, pp, i32, i32,
                                                          i32, vp]
             L.coc_matmul_all_reduce_w8a16_ex.restype = i32
+            L.coc_moe_dispatch_grouped_matmul.argtypes = [i32, i64, i64, i64, i32, pp, pp, vp, pp, pp, i64, vp, vp,
+                                                          i32, vp]
+            L.coc_moe_dispatch_grouped_matmul.restype = i32
+            L.coc_moe_capacity.argtypes = [i32, i64, i32]
+            L.coc_moe_capacity.restype = i64
             L.coc_fused_matmul.argtypes = [i32, i32, i64, i64, i64, pp, pp, i32, pp, pp, i32, i32, i32, vp]
             L.coc_fused_matmul.restype = i32
             L.coc_matmul.argtypes = [i32, i64, i64, i64, pp, pp, vp, i32, vp]
@@ -319,6 +324,51 @@ def weight_grad(dys, xs, outs=None, chunks: int = 1, stream=None):
     _check(lib().coc_fused_matmul(OP_WEIGHT_GRAD, R, rows, cols, inner, _ptrs(dys), _ptrs(xs), W_KN, _ptrs(outs),
                                   None, _dtype_code(d0.dtype), int(chunks), 1, _stream(stream)))
     return outs
+
+
+def moe_capacity(R: int, tokens: int, experts_per_rank: int) -> int:
+    """Rows each destination buffer of moe_dispatch_grouped_matmul needs."""
+    v = int(lib().coc_moe_capacity(int(R), int(tokens), int(experts_per_rank)))
+    if v < 0:
+        raise ValueError("bad MoE capacity arguments")
+    return v
+
+
+def moe_dispatch_grouped_matmul(xs, idxs, w, experts_per_rank: int, xd=None, y=None, counts=None, offsets=None,
+                                stream=None):
+    """MoE token dispatch (all-to-all) + expert GroupedMatMul on every rank.
+
+    xs[r]: tokens x h (fp16/bf16); idxs[r]: int32 expert ids; w: experts x h x
+    f stacked weights (expert e = rank e // experts_per_rank).  Returns
+    (y, xd, counts, offsets): expert e's rows are offsets[e] ..
+    offsets[e] + counts[e] - 1 of y[q] / xd[q] with q = e // experts_per_rank."""
+    R = len(xs)
+    if R < 1 or R > MAX_RANKS or len(idxs) != R:
+        raise ValueError("need 1..8 ranks and one idx per rank")
+    x0 = xs[0]
+    T, h = x0.shape
+    if x0.dtype not in (torch.float16, torch.bfloat16):
+        raise ValueError("tokens must be fp16 or bf16")
+    dt = x0.dtype
+    _check_list(xs, "xs", (T, h), dt, x0.device)
+    _check_list(idxs, "idxs", (T,), torch.int32, x0.device)
+    E = R * int(experts_per_rank)
+    if w.dim() != 3 or w.shape[0] != E or w.shape[1] != h or w.dtype != dt or w.device != x0.device \
+            or not w.is_contiguous():
+        raise ValueError(f"w must be a contiguous {dt} tensor of shape ({E}, {h}, f) on {x0.device}")
+    f = w.shape[2]
+    cap = moe_capacity(R, T, experts_per_rank)
+    xd = _outs(xd, R, (cap, h), dt, x0.device)
+    y = _outs(y, R, (cap, f), dt, x0.device)
+    if counts is None:
+        counts = torch.empty(E, dtype=torch.int32, device=x0.device)
+    if offsets is None:
+        offsets = torch.empty(E, dtype=torch.int32, device=x0.device)
+    _check_list([counts, offsets], "counts/offsets", (E,), torch.int32, x0.device)
+    _check(lib().coc_moe_dispatch_grouped_matmul(R, T, h, f, int(experts_per_rank), _ptrs(xs), _ptrs(idxs),
+                                                 w.data_ptr(), _ptrs(xd), _ptrs(y), cap, counts.data_ptr(),
+                                                 offsets.data_ptr(), _dtype_code(dt), _stream(stream)))
+    return y, xd, counts, offsets
 
 
 def matmul(xs, ws, out=None, stream=None):

@@ -36,7 +36,7 @@ struct DeviceState {
     int sm_count = 0;
     int cc_major = 0, cc_minor = 0;
     unsigned* status = nullptr;
-    int max_pairs[4][2] = {{-1, -1}, {-1, -1}, {-1, -1}, {-1, -1}};   // per op, per bf16; -1 = not queried
+    int max_pairs[NUM_OPS][2] = {{-1, -1}, {-1, -1}, {-1, -1}, {-1, -1}, {-1, -1}};   // per op, per bf16; -1 = not queried
     cudaMemPool_t pool = nullptr;   // stream-ordered workspace (w8A16 pre-pass), kept between calls
 };
 
@@ -381,6 +381,14 @@ coc_status_t w8_prepass_all_reduce(int R, int64_t m, int64_t n, int64_t ks, cons
     return st;
 }
 
+// Rows each destination buffer of the MoE dispatch needs in the worst case:
+// all tokens of all ranks, each of the rank's eloc expert groups padded to a
+// 256-row boundary.
+int64_t moe_capacity(int R, int64_t T, int eloc) {
+    const int64_t rows = static_cast<int64_t>(R) * T + static_cast<int64_t>(eloc) * (MOE_GROUP_ALIGN - 1);
+    return (rows + MOE_GROUP_ALIGN - 1) / MOE_GROUP_ALIGN * MOE_GROUP_ALIGN;
+}
+
 }  // namespace
 }  // namespace coc
 
@@ -651,6 +659,124 @@ COC_API coc_status_t coc_fused_matmul(coc_op_t op, int R, int64_t rows, int64_t 
     }
 }
 
+COC_API int64_t coc_moe_capacity(int R, int64_t tokens, int experts_per_rank) {
+    if (R < 1 || R > COC_MAX_RANKS || tokens < 0 || experts_per_rank < 1) return -1;
+    return moe_capacity(R, tokens, experts_per_rank);
+}
+
+COC_API coc_status_t coc_moe_dispatch_grouped_matmul(int R, int64_t tokens, int64_t h, int64_t f, int experts_per_rank,
+                                                     const void* const* x, const int32_t* const* idx, const void* w,
+                                                     void* const* xd, void* const* y, int64_t capacity,
+                                                     int32_t* counts, int32_t* offsets, coc_dtype_t dt,
+                                                     coc_stream_t stream) {
+    if (R < 1 || R > COC_MAX_RANKS) return fail(COC_ERR_INVALID_ARG, "R = %d outside [1, %d]", R, COC_MAX_RANKS);
+    if (dt != COC_FP16 && dt != COC_BF16) return fail(COC_ERR_INVALID_ARG, "unknown dtype %d", static_cast<int>(dt));
+    const int eloc = experts_per_rank;
+    if (eloc < 1 || static_cast<int64_t>(R) * eloc > MOE_MAX_EXPERTS)
+        return fail(COC_ERR_INVALID_ARG, "experts = R x %d must lie in [1, %d]", eloc, MOE_MAX_EXPERTS);
+    if (tokens < 0 || tokens > (int64_t(1) << 24)) return fail(COC_ERR_SHAPE, "tokens = %lld per rank", (long long)tokens);
+    if (h <= 0 || h % BK != 0) return fail(COC_ERR_SHAPE, "h = %lld must be a positive multiple of %d", (long long)h, BK);
+    if (f <= 0 || (f * 2) % 16 != 0) return fail(COC_ERR_ALIGN, "f = %lld: rows of W and Y must span a multiple of 16 bytes", (long long)f);
+    if (h > (int64_t(1) << 20) || f > (int64_t(1) << 20)) return fail(COC_ERR_SHAPE, "h or f too large");
+    const int64_t need = moe_capacity(R, tokens, eloc);
+    if (capacity < need)
+        return fail(COC_ERR_SHAPE, "capacity = %lld rows, needs %lld (coc_moe_capacity)", (long long)capacity, (long long)need);
+    if (capacity > (int64_t(1) << 30)) return fail(COC_ERR_SHAPE, "capacity too large");
+    if (counts == nullptr || offsets == nullptr) return fail(COC_ERR_INVALID_ARG, "counts / offsets is NULL");
+    if ((reinterpret_cast<uintptr_t>(counts) | reinterpret_cast<uintptr_t>(offsets)) & 3u)
+        return fail(COC_ERR_ALIGN, "counts / offsets not 4-byte aligned");
+    coc_status_t st;
+    if ((st = check_ptrs(xd, R, true, "xd")) != COC_OK) return st;
+    if ((st = check_ptrs(y, R, true, "y")) != COC_OK) return st;
+    if (w == nullptr || !aligned16(w)) return fail(w == nullptr ? COC_ERR_INVALID_ARG : COC_ERR_ALIGN, "w is NULL or not 16-byte aligned");
+    if (tokens > 0) {
+        if ((st = check_ptrs(x, R, true, "x")) != COC_OK) return st;
+        if (idx == nullptr) return fail(COC_ERR_INVALID_ARG, "idx is NULL");
+        for (int r = 0; r < R; ++r)
+            if (idx[r] == nullptr || (reinterpret_cast<uintptr_t>(idx[r]) & 3u))
+                return fail(idx[r] == nullptr ? COC_ERR_INVALID_ARG : COC_ERR_ALIGN, "idx[%d] is NULL or misaligned", r);
+    }
+    DeviceState* ds = nullptr;
+    if ((st = device_state(&ds)) != COC_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int E = R * eloc;
+
+    MoeRouteArgs ra;
+    std::memset(&ra, 0, sizeof ra);
+    void* ws = nullptr;
+    cudaMemPool_t pool = nullptr;
+    if (tokens > 0) {
+        if ((st = device_pool(ds, &pool)) != COC_OK) return st;
+        cudaError_t e = cudaMallocFromPoolAsync(&ws, static_cast<size_t>(R) * tokens * sizeof(int32_t), pool, s);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMallocFromPoolAsync (MoE routing table)");
+    }
+    for (int r = 0; r < R; ++r) ra.idx[r] = tokens > 0 ? idx[r] : nullptr;
+    ra.dest = static_cast<int32_t*>(ws);
+    ra.counts = counts;
+    ra.offsets = offsets;
+    ra.status = ds->status;
+    ra.R = R;
+    ra.T = static_cast<int>(tokens);
+    ra.E = E;
+    ra.eloc = eloc;
+    cudaError_t e = launch_moe_route(ra, s);
+    if (e != cudaSuccess) st = cuda_fail(e, "MoE routing launch");
+    if (st == COC_OK && tokens > 0) {
+        MoePermuteArgs pa;
+        std::memset(&pa, 0, sizeof pa);
+        for (int r = 0; r < R; ++r) {
+            pa.x[r] = static_cast<const uint16_t*>(x[r]);
+            pa.xd[r] = static_cast<uint16_t*>(xd[r]);
+            pa.idx[r] = idx[r];
+        }
+        pa.dest = ra.dest;
+        pa.R = R;
+        pa.T = static_cast<int>(tokens);
+        pa.h = static_cast<int>(h);
+        pa.E = E;
+        pa.eloc = eloc;
+        if ((e = launch_moe_permute(pa, ds->sm_count, s)) != cudaSuccess) st = cuda_fail(e, "MoE permute launch");
+    }
+    if (st == COC_OK && tokens > 0) {
+        // grouped GEMM on the dispatched rows: units come from the device counts
+        KParams p;
+        std::memset(&p, 0, sizeof p);
+        const bool pair = use_pair(OP_GMM, static_cast<int64_t>(R) * tokens);
+        const int tile_m = pair ? 2 * BM : BM;
+        (void)tile_m;
+        p.R = R;
+        p.n_out = 1;
+        p.m = static_cast<int>(capacity);
+        p.n = static_cast<int>(f);
+        p.k = static_cast<int>(h);
+        p.num_kshards = 1;
+        p.kblocks = static_cast<int>(h / BK);
+        p.n_tiles = static_cast<int>((f + BN - 1) / BN);
+        p.units = 1 << 30;   // upper bound for the grid size; the kernel counts its units
+        p.rows_per_rank = static_cast<int>(capacity);
+        p.a_box_rows = BM;
+        p.store_rows = 32;
+        p.gmm_counts = counts;
+        p.gmm_offsets = offsets;
+        p.gmm_E = E;
+        p.gmm_eloc = eloc;
+        const CUtensorMapDataType tdt = tma_dtype(dt);
+        for (int q = 0; q < R && st == COC_OK; ++q) {
+            st = encode(&p.tm_a[q], tdt, xd[q], h, capacity, h * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B);
+            if (st == COC_OK)
+                st = encode(&p.tm_out[q], tdt, y[q], f, capacity, f * 2, EPI_COLS, p.store_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+        }
+        if (st == COC_OK)
+            st = encode(&p.tm_b[0], tdt, w, f, static_cast<int64_t>(E) * h, f * 2, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B);
+        if (st == COC_OK) st = launch_checked(OP_GMM, dt == COC_BF16, pair, p, ds, s);
+    }
+    if (ws != nullptr) {
+        const cudaError_t ef = cudaFreeAsync(ws, s);
+        if (st == COC_OK && ef != cudaSuccess) st = cuda_fail(ef, "cudaFreeAsync (MoE routing table)");
+    }
+    return st;
+}
+
 COC_API coc_status_t coc_sync_status(coc_stream_t stream) {
     cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
@@ -662,6 +788,8 @@ COC_API coc_status_t coc_sync_status(coc_stream_t stream) {
         return cuda_fail(e, "cudaMemcpy(status)");
     if (words[0] != 0) {
         if ((e = cudaMemset(ds->status, 0, sizeof words)) != cudaSuccess) return cuda_fail(e, "cudaMemset(status)");
+        if (words[0] == DEV_ERR_BAD_INDEX)
+            return fail(COC_ERR_INVALID_ARG, "MoE dispatch: an expert id was outside [0, E); those tokens were not dispatched");
         return fail(COC_ERR_TIMEOUT, "device wait timed out (flags 0x%x, first wait site 0x%x, block %u)", words[0],
                     words[1], words[2] ? words[2] - 1 : 0);
     }

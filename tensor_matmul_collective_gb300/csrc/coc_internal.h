@@ -27,10 +27,11 @@ constexpr int B_STAGE_BYTES = BN * BK * 2;        // 32 KiB
 constexpr int RAW_STAGE_BYTES = BN * BK;          // 16 KiB int8 (w8A16)
 constexpr int EPI_BUF_BYTES = 32 * EPI_COLS * 2;  // 4 KiB per warp per buffer
 
-enum OpKind : int { OP_AR = 0, OP_RS = 1, OP_AG = 2, OP_W8 = 3 };
+enum OpKind : int { OP_AR = 0, OP_RS = 1, OP_AG = 2, OP_W8 = 3, OP_GMM = 4 };
+constexpr int NUM_OPS = 5;
 
 // Device status words (per device, zero when healthy).
-enum : unsigned { DEV_ERR_TIMEOUT = 1u };
+enum : unsigned { DEV_ERR_TIMEOUT = 1u, DEV_ERR_BAD_INDEX = 2u };
 constexpr int STATUS_WORDS = 8;   // [0] error bits, [1] first "where" code, [2] block
 
 struct KParams {
@@ -67,6 +68,9 @@ struct KParams {
     int b_kmajor;      // W stored n x k (K-major B operand) instead of k x n
     int a_mnmajor;     // weight gradient: A = dY_r^T read MN-major from rank r's dY (AG path only)
     int has_zero;      // w8A16: zero points given
+    const int32_t* gmm_counts;   // grouped GEMM: rows per expert (device, written by the routing kernel)
+    const int32_t* gmm_offsets;  // grouped GEMM: first row of each expert's group (multiple of 256)
+    int gmm_E, gmm_eloc;         // grouped GEMM: experts, experts per rank
     int replica_stores; // AllReduce: write the n_out outputs with plain stores (outp) instead of TMA
 };
 
@@ -88,6 +92,31 @@ struct W8PrepassArgs {
     int R, k, n, gran, group;
 };
 cudaError_t launch_w8_prepass(const W8PrepassArgs& a, bool bf16, int sm_count, cudaStream_t stream);
+
+// MoE dispatch (coc_moe.cu): the routing kernel counts each rank's tokens per
+// expert and gives every token its row in its expert's (256-row aligned)
+// group on the destination rank; the permute kernel copies the token rows
+// there (the all-to-all).  Tokens with an expert id outside [0, E) are not
+// dispatched and set DEV_ERR_BAD_INDEX.
+constexpr int MOE_GROUP_ALIGN = 256;
+constexpr int MOE_MAX_EXPERTS = 256;
+struct MoeRouteArgs {
+    const int32_t* idx[COC_MAX_RANKS];   // T expert ids per rank
+    int32_t* dest;                        // R x T: destination row (-1: not dispatched)
+    int32_t* counts;                      // E
+    int32_t* offsets;                     // E
+    unsigned* status;
+    int R, T, E, eloc;
+};
+struct MoePermuteArgs {
+    const uint16_t* x[COC_MAX_RANKS];     // T x h per rank
+    uint16_t* xd[COC_MAX_RANKS];          // cap x h per destination rank
+    const int32_t* idx[COC_MAX_RANKS];
+    const int32_t* dest;
+    int R, T, h, E, eloc;
+};
+cudaError_t launch_moe_route(const MoeRouteArgs& a, cudaStream_t stream);
+cudaError_t launch_moe_permute(const MoePermuteArgs& a, int sm_count, cudaStream_t stream);
 
 // Host-side launch helpers implemented in coc_kernel.cu.  `pair` selects the
 // 2-SM variant (a cluster of two CTAs per 256-row tile; grid = 2 x pairs);

@@ -383,6 +383,35 @@ __device__ __forceinline__ void decode_unit(const KParams& p, int u, int& r, int
     }
 }
 
+// Grouped GEMM (MoE dispatch): unit -> (expert e, global row tile mt, n-tile
+// nt).  Experts in order; inside an expert the row tiles of one n-tile column
+// are adjacent (running CTAs share the expert's W tile).  Each expert's group
+// starts on a 256-row boundary of its rank's buffer, so a row tile never
+// straddles two experts.  Counts and offsets come from the routing kernel.
+__device__ __forceinline__ void gmm_decode(const KParams& p, int u, int tile_m, int& e, int& mt, int& nt) {
+    int acc = 0;
+    e = 0;
+    mt = 0;
+    nt = 0;
+    for (int x = 0; x < p.gmm_E; ++x) {
+        const int mte = (__ldg(p.gmm_counts + x) + tile_m - 1) / tile_m;
+        const int ue = mte * p.n_tiles;
+        if (u < acc + ue) {
+            const int v = u - acc;
+            e = x;
+            nt = v / mte;
+            mt = __ldg(p.gmm_offsets + x) / tile_m + (v - nt * mte);
+            return;
+        }
+        acc += ue;
+    }
+}
+__device__ __forceinline__ int gmm_units(const KParams& p, int tile_m) {
+    int acc = 0;
+    for (int x = 0; x < p.gmm_E; ++x) acc += (__ldg(p.gmm_counts + x) + tile_m - 1) / tile_m * p.n_tiles;
+    return acc;
+}
+
 // ------------------------------------------------------------ conversions ---
 
 template <bool BF16>
@@ -550,6 +579,14 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int total_kb = p.num_kshards * p.kblocks;
+    // work units: fixed by the host, except for the grouped GEMM whose expert
+    // group sizes the routing kernel wrote to device memory
+    int n_units = p.units;
+    if constexpr (OP == OP_GMM) n_units = gmm_units(p, TILE_M);
+    auto decode = [&](int u, int& r, int& mt, int& nt) {
+        if constexpr (OP == OP_GMM) gmm_decode(p, u, TILE_M, r, mt, nt);
+        else decode_unit<OP>(p, u, r, mt, nt);
+    };
 
     if (warp == 0) {
         // ================================================= TMA producer ===
@@ -607,9 +644,9 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
                 }
             }
         };
-        for (int u = first_unit; ok && u < p.units; u += unit_step) {
+        for (int u = first_unit; ok && u < n_units; u += unit_step) {
             int r, mt, nt;
-            decode_unit<OP>(p, u, r, mt, nt);
+            decode(u, r, mt, nt);
             const int row_base = mt * TILE_M + static_cast<int>(rank) * BM;   // this CTA's first A row
             const int col_base = nt * BN + static_cast<int>(rank) * C::BN_CTA;  // this CTA's first B column
             // A: one 128-row box (AllGather: from the shard holding the rows,
@@ -621,7 +658,7 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
                 a_row = row_base - a_shard * p.rows_per_rank;
             }
             auto a_single = [&](auto& load, uint32_t dst, int ks, int kc) {
-                load(dst, &p.tm_a[(OP == OP_AG) ? a_shard : ks], kc, a_row, pol_a);
+                load(dst, &p.tm_a[(OP == OP_AG) ? a_shard : (OP == OP_GMM) ? r / p.gmm_eloc : ks], kc, a_row, pol_a);
             };
             // ... several boxes when a shard holds fewer rows than a tile, ...
             auto a_multi = [&](auto& load, uint32_t dst, int, int kc) {
@@ -640,18 +677,22 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
             };
             // B: W stored k x n, read as 64-column MN-major boxes, or W stored
             // n x k, one box of this CTA's B rows (n) x 64 k laid out like A.
+            // (grouped GEMM: one map over the stacked expert weights, expert r's
+            // rows starting at r * k)
             const CUtensorMap* bmaps = &p.tm_b[(OP == OP_AG) ? r : 0];
+            const int b_k0 = (OP == OP_GMM) ? r * p.k : 0;
             auto b_mn = [&](auto& load, uint32_t dst, int ks, int kc) {
-                const CUtensorMap* bm = (OP == OP_AG) ? bmaps : &p.tm_b[ks];
+                const CUtensorMap* bm = (OP == OP_AG || OP == OP_GMM) ? bmaps : &p.tm_b[ks];
 #pragma unroll
-                for (int j = 0; j < C::BN_CTA / 64; ++j) load(dst + j * (64 * BK * 2), bm, col_base + j * 64, kc, pol_b);
+                for (int j = 0; j < C::BN_CTA / 64; ++j)
+                    load(dst + j * (64 * BK * 2), bm, col_base + j * 64, b_k0 + kc, pol_b);
             };
             auto b_kmaj = [&](auto& load, uint32_t dst, int ks, int kc) {
                 load(dst, (OP == OP_AG) ? bmaps : &p.tm_b[ks], kc, col_base, pol_b);
             };
             auto with_b = [&](auto&& issue_a) {
                 if constexpr (W8) unit_loop(col_base, issue_a, b_mn);   // B comes from the dequant warps
-                else if (p.b_kmajor) unit_loop(col_base, issue_a, b_kmaj);
+                else if (OP != OP_GMM && p.b_kmajor) unit_loop(col_base, issue_a, b_kmaj);
                 else unit_loop(col_base, issue_a, b_mn);
             };
             if constexpr (OP == OP_AG) {
@@ -691,7 +732,7 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
             uint32_t stage = 0, phase = 0, bstage = 0, bphase = 0;
             int acc_i = 0;
             bool ok = true;
-            for (int u = first_unit; ok && u < p.units; u += unit_step) {
+            for (int u = first_unit; ok && u < n_units; u += unit_step) {
                 const int buf = acc_i & 1;
                 const uint32_t aph = (acc_i >> 1) & 1;
                 ok = warp_wait<PAIR>(smem_u32(&acce[buf]), aph ^ 1u, ctl, 0x200u + buf);
@@ -752,9 +793,9 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
         int acc_i = 0, sb_i = 0;
         bool ok = true;
         if (p.inject_timeout) ok = warp_wait(smem_u32(never), 0, ctl, 0x300u);
-        for (int u = first_unit; ok && u < p.units; u += unit_step) {
+        for (int u = first_unit; ok && u < n_units; u += unit_step) {
             int r, mt, nt;
-            decode_unit<OP>(p, u, r, mt, nt);
+            decode(u, r, mt, nt);
             const int buf = acc_i & 1;
             const uint32_t aph = (acc_i >> 1) & 1;
             ok = warp_wait<PAIR>(smem_u32(&accf[buf]), aph, ctl, 0x310u + buf);
@@ -815,6 +856,8 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
                         }
                     } else if constexpr (OP == OP_AG) {
                         tma_store_2d(&p.tm_out[r], src, col, row0);
+                    } else if constexpr (OP == OP_GMM) {
+                        tma_store_2d(&p.tm_out[r / p.gmm_eloc], src, col, row0);
                     } else {
                         if (!p.replica_stores)
                             for (int o = 0; o < p.n_out; ++o) tma_store_2d(&p.tm_out[o], src, col, row0);
@@ -880,9 +923,9 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
         const W8Layout w8l{p.gran, p.group, p.n};
         uint32_t cnt = 0;   // global k-block counter (all units, ranks, k-blocks in order)
         bool ok = true;
-        for (int u = first_unit; ok && u < p.units; u += unit_step) {
+        for (int u = first_unit; ok && u < n_units; u += unit_step) {
             int r, mt, nt;
-            decode_unit<OP>(p, u, r, mt, nt);
+            decode(u, r, mt, nt);
             const int j0 = nt * BN + static_cast<int>(rank) * C::BN_CTA + cc * 8;   // first global column
             for (int ks = 0; ok && ks < p.num_kshards; ++ks) {
                 const uint16_t* sc = p.scale[ks];
@@ -1030,6 +1073,7 @@ cudaError_t launch(int op, bool bf16, bool pair, const KParams& p, int grid, cud
         case OP_RS: if (bf16) { COC_LAUNCH(OP_RS, true); } else { COC_LAUNCH(OP_RS, false); }
         case OP_AG: if (bf16) { COC_LAUNCH(OP_AG, true); } else { COC_LAUNCH(OP_AG, false); }
         case OP_W8: if (bf16) { COC_LAUNCH(OP_W8, true); } else { COC_LAUNCH(OP_W8, false); }
+        case OP_GMM: if (bf16) { COC_LAUNCH(OP_GMM, true); } else { COC_LAUNCH(OP_GMM, false); }
         default: return cudaErrorInvalidValue;
     }
 #undef COC_LAUNCH
@@ -1041,6 +1085,7 @@ int max_pairs(int op, bool bf16) {
         case OP_RS: return bf16 ? max_pairs_t<OP_RS, true>() : max_pairs_t<OP_RS, false>();
         case OP_AG: return bf16 ? max_pairs_t<OP_AG, true>() : max_pairs_t<OP_AG, false>();
         case OP_W8: return bf16 ? max_pairs_t<OP_W8, true>() : max_pairs_t<OP_W8, false>();
+        case OP_GMM: return bf16 ? max_pairs_t<OP_GMM, true>() : max_pairs_t<OP_GMM, false>();
         default: return 0;
     }
 }

@@ -1,0 +1,152 @@
+// MoE expert-parallel dispatch (the token all-to-all in front of the experts'
+// GroupedMatMul; MindSpeed-LLM overlap blog, section 第二层MC2, "EP MC2").
+// R ranks, E = R * eloc experts, expert e on rank e / eloc, top-1 routing.
+// Destination rank q receives every token routed to one of its experts,
+// grouped by expert (ascending), inside an expert by source rank, inside a
+// source rank by token index; each expert's group starts on a 256-row
+// boundary of q's buffer so that the grouped GEMM's row tiles never straddle
+// two experts.
+//
+// moe_route_kernel    one CTA, one warp per source rank: counts, offsets and
+//                     every token's destination row (deterministic, stable)
+// moe_permute_kernel  one warp per token row: the copy itself
+#include "coc_internal.h"
+
+namespace coc {
+namespace {
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+constexpr int kRouteAhead = 8;   // 32-token chunks of expert ids loaded ahead
+
+// Expert id of token t of this warp's rank, -1 if t is past the end or the id
+// is out of range (which is reported and the token not dispatched).
+__device__ __forceinline__ int route_id(const MoeRouteArgs& a, const int32_t* idx, int t) {
+    if (t >= a.T) return -1;
+    const int e = __ldg(idx + t);
+    if (e < 0 || e >= a.E) {
+        atomicOr(a.status, DEV_ERR_BAD_INDEX);
+        return -1;
+    }
+    return e;
+}
+
+__global__ void __launch_bounds__(32 * COC_MAX_RANKS) moe_route_kernel(const __grid_constant__ MoeRouteArgs a) {
+    __shared__ int cnt[COC_MAX_RANKS][MOE_MAX_EXPERTS];   // tokens of rank r for expert e, later its base
+    __shared__ int off[MOE_MAX_EXPERTS];                   // group offset of expert e in its rank's buffer
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i < COC_MAX_RANKS * MOE_MAX_EXPERTS; i += blockDim.x) (&cnt[0][0])[i] = 0;
+    __syncthreads();
+
+    // 1. counts: warp r alone writes row r
+    const int r = warp;
+    if (r < a.R) {
+        const int32_t* idx = a.idx[r];
+        for (int t0 = 0; t0 < a.T; t0 += 32 * kRouteAhead) {
+            int e[kRouteAhead];
+#pragma unroll
+            for (int i = 0; i < kRouteAhead; ++i) e[i] = route_id(a, idx, t0 + 32 * i + lane);
+#pragma unroll
+            for (int i = 0; i < kRouteAhead; ++i) {
+                const uint32_t same = __match_any_sync(0xffffffffu, e[i]);
+                if (e[i] >= 0 && lane == __ffs(same) - 1) cnt[r][e[i]] += __popc(same);
+                __syncwarp();
+            }
+        }
+    }
+    __syncthreads();
+
+    // 2. per expert: group size and offset (groups of a rank padded to 256 rows)
+    for (int e = threadIdx.x; e < a.E; e += blockDim.x) {
+        int n = 0;
+        for (int s = 0; s < a.R; ++s) n += cnt[s][e];
+        int o = 0;
+        for (int x = (e / a.eloc) * a.eloc; x < e; ++x) {
+            int nx = 0;
+            for (int s = 0; s < a.R; ++s) nx += cnt[s][x];
+            o += (nx + MOE_GROUP_ALIGN - 1) / MOE_GROUP_ALIGN * MOE_GROUP_ALIGN;
+        }
+        off[e] = o;
+        a.counts[e] = n;
+        a.offsets[e] = o;
+    }
+    __syncthreads();
+    // 3. within expert e, rank s's tokens start after those of ranks < s
+    for (int e = threadIdx.x; e < a.E; e += blockDim.x) {
+        int run = 0;
+        for (int s = 0; s < a.R; ++s) {
+            const int c = cnt[s][e];
+            cnt[s][e] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+
+    // 4. placement: token t of rank r goes after the earlier tokens of rank r
+    //    routed to the same expert (match_any ranks equal ids inside a chunk)
+    if (r < a.R) {
+        const int32_t* idx = a.idx[r];
+        const uint32_t lt = lanemask_lt();
+        for (int t0 = 0; t0 < a.T; t0 += 32 * kRouteAhead) {
+            int e[kRouteAhead];
+#pragma unroll
+            for (int i = 0; i < kRouteAhead; ++i) {
+                const int t = t0 + 32 * i + lane;
+                e[i] = (t < a.T) ? __ldg(idx + t) : -1;
+                if (e[i] < 0 || e[i] >= a.E) e[i] = -1;
+            }
+#pragma unroll
+            for (int i = 0; i < kRouteAhead; ++i) {
+                const int t = t0 + 32 * i + lane;
+                const uint32_t same = __match_any_sync(0xffffffffu, e[i]);
+                const int pos = (e[i] >= 0) ? off[e[i]] + cnt[r][e[i]] + __popc(same & lt) : -1;
+                __syncwarp();
+                if (e[i] >= 0 && lane == __ffs(same) - 1) cnt[r][e[i]] += __popc(same);
+                __syncwarp();
+                if (t < a.T) a.dest[static_cast<long long>(r) * a.T + t] = pos;
+            }
+        }
+    }
+}
+
+// One warp per token row: 16-byte vectors of X_r[t] to xd[q][dest].
+__global__ void __launch_bounds__(256) moe_permute_kernel(const __grid_constant__ MoePermuteArgs a) {
+    const long long nrows = static_cast<long long>(a.R) * a.T;
+    const int lane = threadIdx.x & 31;
+    const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+    const int vecs = a.h / 8;
+    for (long long w = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); w < nrows;
+         w += warps) {
+        const int r = static_cast<int>(w / a.T);
+        const int t = static_cast<int>(w - static_cast<long long>(r) * a.T);
+        const int dst_row = __ldg(a.dest + w);
+        if (dst_row < 0) continue;
+        const int q = __ldg(a.idx[r] + t) / a.eloc;
+        const uint4* src = reinterpret_cast<const uint4*>(a.x[r] + static_cast<long long>(t) * a.h);
+        uint4* dst = reinterpret_cast<uint4*>(a.xd[q] + static_cast<long long>(dst_row) * a.h);
+        for (int v = lane; v < vecs; v += 32) dst[v] = __ldg(src + v);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_moe_route(const MoeRouteArgs& a, cudaStream_t stream) {
+    moe_route_kernel<<<1, 32 * COC_MAX_RANKS, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_moe_permute(const MoePermuteArgs& a, int sm_count, cudaStream_t stream) {
+    const long long rows = static_cast<long long>(a.R) * a.T;
+    if (rows <= 0) return cudaSuccess;
+    long long blocks = (rows + 7) / 8;
+    const long long cap = static_cast<long long>(sm_count > 0 ? sm_count : 1) * 8;
+    if (blocks > cap) blocks = cap;
+    moe_permute_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace coc

@@ -146,6 +146,36 @@ def test_w8a16_ex_constraints(L):
     assert f(2, 0, 128, 128, x, x, x, x, 1, 0, x, 1, 1, 0, None) == coc.OK                # empty: no-op
 
 
+def test_moe_constraints(L):
+    # (R, tokens, h, f, experts_per_rank, x, idx, w, xd, y, capacity, counts, offsets, dt, stream);
+    # every call below fails host validation before any CUDA call
+    f = L.coc_moe_dispatch_grouped_matmul
+    x = _arr([A] * 2)
+    cap = L.coc_moe_capacity(2, 100, 2)
+    assert cap == 768                                   # 2 x 100 + 2 x 255 = 710, rounded up to 256
+    assert L.coc_moe_capacity(0, 100, 1) == -1 and L.coc_moe_capacity(2, -1, 1) == -1
+
+    def call(R=2, T=100, h=128, fo=136, el=2, xp=x, ip=x, w=A, xd=x, y=x, cap=cap, cnt=A, off=A, dt=1):
+        return f(R, T, h, fo, el, xp, ip, w, xd, y, cap, cnt, off, dt, None)
+    assert call(R=0) == coc.ERR_INVALID_ARG
+    assert call(R=9) == coc.ERR_INVALID_ARG
+    assert call(dt=5) == coc.ERR_INVALID_ARG
+    assert call(el=0) == coc.ERR_INVALID_ARG
+    assert call(el=129) == coc.ERR_INVALID_ARG          # 2 x 129 > 256 experts
+    assert call(h=100) == coc.ERR_SHAPE                 # h % 64
+    assert call(fo=100) == coc.ERR_ALIGN                # f * 2 % 16
+    assert call(cap=cap - 1) == coc.ERR_SHAPE           # capacity too small
+    assert call(cnt=None) == coc.ERR_INVALID_ARG
+    assert call(off=A + 2) == coc.ERR_ALIGN
+    assert call(w=A + 8) == coc.ERR_ALIGN
+    assert call(xd=_arr([A, MIS])) == coc.ERR_ALIGN
+    assert call(y=_arr([MIS, A])) == coc.ERR_ALIGN
+    assert call(xp=_arr([A, MIS])) == coc.ERR_ALIGN
+    assert call(y=_arr([A, None])) == coc.ERR_INVALID_ARG
+    assert call(ip=_arr([A, None])) == coc.ERR_INVALID_ARG
+    assert call(ip=_arr([A, A + 2])) == coc.ERR_ALIGN
+
+
 def test_empty_problems_are_noops(L):
     # m == 0 or n == 0: documented no-op, returns before any CUDA call
     assert ar(L, m=0) == coc.OK
