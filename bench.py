@@ -487,6 +487,21 @@ def time_next_rows(ops, dev, t):
             name = f"w8a16_ar_channel_{'bf16' if dt == torch.bfloat16 else 'fp16'}_{'zp' if zero else 'sym'}"
             res[name] = {"ms": round(tm, 4), "tflops": round(s.flops() / tm / 1e9, 1)}
             del dx, dq, ds, dz, outs
+    # MoE dispatch + GroupedMatMul (EP form of the fused operators): a
+    # Mixtral-style layer on 8 EP ranks, one expert each, 4096 tokens per rank,
+    # against one plain GEMM over the same number of rows
+    s = wl.MoEDispatch(R=8, T=4096, h=4096, f=14336, e_loc=1, seed=21)
+    xs, idxs, ws = s.make()
+    dx, di, w = [x.to(dev) for x in xs], [i.to(dev) for i in idxs], torch.stack(ws).to(dev)
+    y, xd, cnt, off = coc.moe_dispatch_grouped_matmul(dx, di, w, s.e_loc)
+    tm = t(lambda: coc.moe_dispatch_grouped_matmul(dx, di, w, s.e_loc, xd=xd, y=y, counts=cnt, offsets=off), 5)
+    xg = torch.cat(dx, 0)
+    og = torch.empty(xg.shape[0], s.f, dtype=s.dtype, device=dev)
+    tp = t(lambda: coc.matmul([xg], [w[0]], og), 5)
+    res["moe_dispatch_grouped_matmul_mixtral_ep8"] = {
+        "ms": round(tm, 4), "tflops": round(s.flops() / tm / 1e9, 1), "plain_gemm_same_rows_ms": round(tp, 4),
+        "tokens_per_expert": [int(v) for v in cnt.cpu().tolist()]}
+    del dx, di, w, y, xd, xg, og
     return res
 
 

@@ -1,6 +1,7 @@
 // Host side of the C ABI declared in include/coc.h: argument validation
 // (before any CUDA call), TMA descriptor encoding, launch of the persistent
 // fused kernel, and the device status buffer used by the bounded waits.
+#include <algorithm>
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
@@ -743,7 +744,11 @@ COC_API coc_status_t coc_moe_dispatch_grouped_matmul(int R, int64_t tokens, int6
         std::memset(&p, 0, sizeof p);
         const bool pair = use_pair(OP_GMM, static_cast<int64_t>(R) * tokens);
         const int tile_m = pair ? 2 * BM : BM;
-        (void)tile_m;
+        // inside an expert, row tiles in groups whose token rows fit in 32 MiB
+        // of L2 (held there, evict-last) while the expert's W streams past
+        const int64_t row_tile_bytes = static_cast<int64_t>(tile_m) * h * 2;
+        p.group_mt = static_cast<int>(std::max<int64_t>(1, (int64_t(32) << 20) / row_tile_bytes));
+        p.a_hint = 2;
         p.R = R;
         p.n_out = 1;
         p.m = static_cast<int>(capacity);

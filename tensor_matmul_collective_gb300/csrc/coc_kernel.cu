@@ -384,10 +384,13 @@ __device__ __forceinline__ void decode_unit(const KParams& p, int u, int& r, int
 }
 
 // Grouped GEMM (MoE dispatch): unit -> (expert e, global row tile mt, n-tile
-// nt).  Experts in order; inside an expert the row tiles of one n-tile column
-// are adjacent (running CTAs share the expert's W tile).  Each expert's group
-// starts on a 256-row boundary of its rank's buffer, so a row tile never
-// straddles two experts.  Counts and offsets come from the routing kernel.
+// nt).  Experts in order; inside an expert, its row tiles are taken in L2
+// groups of group_mt (the last group may be smaller) and inside a group the
+// row tiles of one n-tile column are adjacent, so running CTAs share the
+// expert's W tile while the group's token rows stay in L2; odd groups walk
+// the columns backwards.  Each expert's group starts on a 256-row boundary of
+// its rank's buffer, so a row tile never straddles two experts.  Counts and
+// offsets come from the routing kernel.
 __device__ __forceinline__ void gmm_decode(const KParams& p, int u, int tile_m, int& e, int& mt, int& nt) {
     int acc = 0;
     e = 0;
@@ -398,9 +401,15 @@ __device__ __forceinline__ void gmm_decode(const KParams& p, int u, int tile_m, 
         const int ue = mte * p.n_tiles;
         if (u < acc + ue) {
             const int v = u - acc;
+            const int G = (p.group_mt > 0 && p.group_mt < mte) ? p.group_mt : mte;
+            const int g = v / (G * p.n_tiles);
+            const int w = v - g * G * p.n_tiles;
+            const int Gg = min(G, mte - g * G);   // rows tiles in this group
+            int col = w / Gg;
+            if (g & 1) col = p.n_tiles - 1 - col;
             e = x;
-            nt = v / mte;
-            mt = __ldg(p.gmm_offsets + x) / tile_m + (v - nt * mte);
+            nt = col;
+            mt = __ldg(p.gmm_offsets + x) / tile_m + g * G + (w - (w / Gg) * Gg);
             return;
         }
         acc += ue;
@@ -657,8 +666,13 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
                 a_shard = min(row_base / p.rows_per_rank, p.R - 1);
                 a_row = row_base - a_shard * p.rows_per_rank;
             }
+            // (the unit's map is resolved here: kernel parameters are re-read after
+            // every asm with a memory clobber, so nothing is hoisted out of the loop)
+            const CUtensorMap* amap_unit = (OP == OP_AG)    ? &p.tm_a[a_shard]
+                                           : (OP == OP_GMM) ? &p.tm_a[r / p.gmm_eloc]
+                                                            : &p.tm_a[0];
             auto a_single = [&](auto& load, uint32_t dst, int ks, int kc) {
-                load(dst, &p.tm_a[(OP == OP_AG) ? a_shard : (OP == OP_GMM) ? r / p.gmm_eloc : ks], kc, a_row, pol_a);
+                load(dst, (OP == OP_AG || OP == OP_GMM) ? amap_unit : &p.tm_a[ks], kc, a_row, pol_a);
             };
             // ... several boxes when a shard holds fewer rows than a tile, ...
             auto a_multi = [&](auto& load, uint32_t dst, int, int kc) {

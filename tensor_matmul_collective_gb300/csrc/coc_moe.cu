@@ -7,8 +7,9 @@
 // boundary of q's buffer so that the grouped GEMM's row tiles never straddle
 // two experts.
 //
-// moe_route_kernel    one CTA, one warp per source rank: counts, offsets and
-//                     every token's destination row (deterministic, stable)
+// moe_route_kernel    one CTA, 32 warps over contiguous segments of the source
+//                     ranks' tokens: counts, offsets and every token's
+//                     destination row (deterministic, stable)
 // moe_permute_kernel  one warp per token row: the copy itself
 #include "coc_internal.h"
 
@@ -35,25 +36,38 @@ __device__ __forceinline__ int route_id(const MoeRouteArgs& a, const int32_t* id
     return e;
 }
 
-__global__ void __launch_bounds__(32 * COC_MAX_RANKS) moe_route_kernel(const __grid_constant__ MoeRouteArgs a) {
-    __shared__ int cnt[COC_MAX_RANKS][MOE_MAX_EXPERTS];   // tokens of rank r for expert e, later its base
-    __shared__ int off[MOE_MAX_EXPERTS];                   // group offset of expert e in its rank's buffer
+// Each source rank's tokens are cut into S contiguous segments (S = 32 / R
+// warps per rank, at least one); warp (r, s) counts and later places segment
+// s of rank r.  Segment order within a rank is token order, so the placement
+// is the same as one pass over the rank's tokens.
+constexpr int kRouteWarps = 32;
+
+__global__ void __launch_bounds__(32 * kRouteWarps) moe_route_kernel(const __grid_constant__ MoeRouteArgs a) {
+    __shared__ int cnt[kRouteWarps][MOE_MAX_EXPERTS];   // per warp: tokens per expert, later its base
+    __shared__ int off[MOE_MAX_EXPERTS];                 // group offset of expert e in its rank's buffer
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int i = threadIdx.x; i < COC_MAX_RANKS * MOE_MAX_EXPERTS; i += blockDim.x) (&cnt[0][0])[i] = 0;
+    const int S = kRouteWarps / a.R;                     // segments per rank (R <= 8)
+    const int seg_len = ((a.T + S - 1) / S + 31) / 32 * 32;
+    for (int i = threadIdx.x; i < kRouteWarps * MOE_MAX_EXPERTS; i += blockDim.x) (&cnt[0][0])[i] = 0;
     __syncthreads();
 
-    // 1. counts: warp r alone writes row r
-    const int r = warp;
-    if (r < a.R) {
+    const int r = warp / S, sgm = warp - r * S;
+    const bool active = r < a.R;
+    const int t_begin = sgm * seg_len, t_end = min(a.T, t_begin + seg_len);
+    // 1. counts: warp w alone writes row w
+    if (active) {
         const int32_t* idx = a.idx[r];
-        for (int t0 = 0; t0 < a.T; t0 += 32 * kRouteAhead) {
+        for (int t0 = t_begin; t0 < t_end; t0 += 32 * kRouteAhead) {
             int e[kRouteAhead];
 #pragma unroll
-            for (int i = 0; i < kRouteAhead; ++i) e[i] = route_id(a, idx, t0 + 32 * i + lane);
+            for (int i = 0; i < kRouteAhead; ++i) {
+                const int t = t0 + 32 * i + lane;
+                e[i] = (t < t_end) ? route_id(a, idx, t) : -1;
+            }
 #pragma unroll
             for (int i = 0; i < kRouteAhead; ++i) {
                 const uint32_t same = __match_any_sync(0xffffffffu, e[i]);
-                if (e[i] >= 0 && lane == __ffs(same) - 1) cnt[r][e[i]] += __popc(same);
+                if (e[i] >= 0 && lane == __ffs(same) - 1) cnt[warp][e[i]] += __popc(same);
                 __syncwarp();
             }
         }
@@ -61,13 +75,14 @@ __global__ void __launch_bounds__(32 * COC_MAX_RANKS) moe_route_kernel(const __g
     __syncthreads();
 
     // 2. per expert: group size and offset (groups of a rank padded to 256 rows)
+    const int W = a.R * S;
     for (int e = threadIdx.x; e < a.E; e += blockDim.x) {
         int n = 0;
-        for (int s = 0; s < a.R; ++s) n += cnt[s][e];
+        for (int w = 0; w < W; ++w) n += cnt[w][e];
         int o = 0;
         for (int x = (e / a.eloc) * a.eloc; x < e; ++x) {
             int nx = 0;
-            for (int s = 0; s < a.R; ++s) nx += cnt[s][x];
+            for (int w = 0; w < W; ++w) nx += cnt[w][x];
             o += (nx + MOE_GROUP_ALIGN - 1) / MOE_GROUP_ALIGN * MOE_GROUP_ALIGN;
         }
         off[e] = o;
@@ -75,39 +90,40 @@ __global__ void __launch_bounds__(32 * COC_MAX_RANKS) moe_route_kernel(const __g
         a.offsets[e] = o;
     }
     __syncthreads();
-    // 3. within expert e, rank s's tokens start after those of ranks < s
+    // 3. within expert e, warp (r, s)'s tokens start after those of earlier
+    //    ranks and of earlier segments of rank r
     for (int e = threadIdx.x; e < a.E; e += blockDim.x) {
         int run = 0;
-        for (int s = 0; s < a.R; ++s) {
-            const int c = cnt[s][e];
-            cnt[s][e] = run;
+        for (int w = 0; w < W; ++w) {
+            const int c = cnt[w][e];
+            cnt[w][e] = run;
             run += c;
         }
     }
     __syncthreads();
 
-    // 4. placement: token t of rank r goes after the earlier tokens of rank r
-    //    routed to the same expert (match_any ranks equal ids inside a chunk)
-    if (r < a.R) {
+    // 4. placement: after the earlier tokens of this segment routed to the
+    //    same expert (match_any ranks equal ids inside a 32-token chunk)
+    if (active) {
         const int32_t* idx = a.idx[r];
         const uint32_t lt = lanemask_lt();
-        for (int t0 = 0; t0 < a.T; t0 += 32 * kRouteAhead) {
+        for (int t0 = t_begin; t0 < t_end; t0 += 32 * kRouteAhead) {
             int e[kRouteAhead];
 #pragma unroll
             for (int i = 0; i < kRouteAhead; ++i) {
                 const int t = t0 + 32 * i + lane;
-                e[i] = (t < a.T) ? __ldg(idx + t) : -1;
+                e[i] = (t < t_end) ? __ldg(idx + t) : -1;
                 if (e[i] < 0 || e[i] >= a.E) e[i] = -1;
             }
 #pragma unroll
             for (int i = 0; i < kRouteAhead; ++i) {
                 const int t = t0 + 32 * i + lane;
                 const uint32_t same = __match_any_sync(0xffffffffu, e[i]);
-                const int pos = (e[i] >= 0) ? off[e[i]] + cnt[r][e[i]] + __popc(same & lt) : -1;
+                const int pos = (e[i] >= 0) ? off[e[i]] + cnt[warp][e[i]] + __popc(same & lt) : -1;
                 __syncwarp();
-                if (e[i] >= 0 && lane == __ffs(same) - 1) cnt[r][e[i]] += __popc(same);
+                if (e[i] >= 0 && lane == __ffs(same) - 1) cnt[warp][e[i]] += __popc(same);
                 __syncwarp();
-                if (t < a.T) a.dest[static_cast<long long>(r) * a.T + t] = pos;
+                if (t < t_end) a.dest[static_cast<long long>(r) * a.T + t] = pos;
             }
         }
     }
@@ -135,7 +151,7 @@ __global__ void __launch_bounds__(256) moe_permute_kernel(const __grid_constant_
 }  // namespace
 
 cudaError_t launch_moe_route(const MoeRouteArgs& a, cudaStream_t stream) {
-    moe_route_kernel<<<1, 32 * COC_MAX_RANKS, 0, stream>>>(a);
+    moe_route_kernel<<<1, 32 * kRouteWarps, 0, stream>>>(a);
     return cudaGetLastError();
 }
 
