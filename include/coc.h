@@ -15,6 +15,7 @@
  *
  * and the expert-parallel form of the blog's MC2 section (extension):
  *   MoE token dispatch + expert GroupedMatMul           coc_moe_dispatch_grouped_matmul
+ *     + the combine (all-to-all back)                   coc_moe_dispatch_grouped_matmul_combine
  *
  * The same page's section 问题分析 ("problem analysis") places them in the
  * Megatron ColumnParallelLinear / RowParallelLinear layers: the matmul is
@@ -276,6 +277,25 @@ coc_status_t coc_moe_dispatch_grouped_matmul(int R, int64_t tokens, int64_t h, i
                                              void* const* xd, void* const* y, int64_t capacity,
                                              int32_t* counts, int32_t* offsets, coc_dtype_t dt,
                                              coc_stream_t stream);
+
+/*
+ * The same dispatch and GroupedMatMul followed by the combine, the all-to-all
+ * back: each expert output row is written to its token's row on the source
+ * rank instead of to the dispatched layout,
+ *
+ *   y_tok[r][t] = x[r][t] @ W_{idx[r][t]}      (top-1 routing: one expert per token)
+ *
+ * y_tok[r]  tokens x f (dt), rank r's tokens in their own order; rows of
+ *           tokens with an out-of-range expert id are not written.
+ * Other arguments as coc_moe_dispatch_grouped_matmul (xd still receives the
+ * dispatched tokens).  The routing table grows by R x capacity int32 (the
+ * source token of each dispatched row), from the same pool.
+ */
+coc_status_t coc_moe_dispatch_grouped_matmul_combine(int R, int64_t tokens, int64_t h, int64_t f, int experts_per_rank,
+                                                     const void* const* x, const int32_t* const* idx, const void* w,
+                                                     void* const* xd, void* const* y_tok, int64_t capacity,
+                                                     int32_t* counts, int32_t* offsets, coc_dtype_t dt,
+                                                     coc_stream_t stream);
 
 /* Rows xd[q] / y[q] need for coc_moe_dispatch_grouped_matmul: R * tokens plus
  * 255 rows of padding per expert of a rank, rounded up to 256; -1 on bad

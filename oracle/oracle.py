@@ -333,3 +333,21 @@ def moe_dispatch_grouped_matmul(dtype: int, xs, idxs, ws, nthreads=None):
         Y = matmul_all_reduce(dtype, [Xd], [ws[e]], None, nthreads) if pairs.shape[0] else np.zeros((0, f))
         res.append((pairs, Xd, Y))
     return res
+
+
+def moe_token_outputs(dtype: int, xs, idxs, ws, nthreads=None):
+    """The combine (all-to-all back) written per token, without any dispatch
+    order: Y_r[t] = X_r[t] @ W_{idx_r[t]} (fp64), rows of ids outside [0, E)
+    left NaN.  Returns one (T x f) array per rank."""
+    E = len(ws)
+    f = ws[0].shape[1]
+    out = []
+    for x, idx in zip(xs, idxs):
+        idx = np.asarray(idx)
+        Y = np.full((x.shape[0], f), np.nan)
+        for e in range(E):
+            rows = np.nonzero(idx == e)[0]
+            if rows.size:
+                Y[rows] = matmul_all_reduce(dtype, [x], [ws[e]], rows, nthreads)
+        out.append(Y)
+    return out

@@ -29,6 +29,7 @@ EXPORTS = (
     "coc_sync_status", "coc_status_string", "coc_last_error", "coc_version",
     "coc_debug_inject_timeout", "coc_shutdown", "coc_matmul_all_reduce_noalloc",
     "coc_fused_matmul", "coc_matmul_all_reduce_w8a16_ex", "coc_moe_dispatch_grouped_matmul", "coc_moe_capacity",
+    "coc_moe_dispatch_grouped_matmul_combine",
 )
 
 OP_ALL_REDUCE, OP_REDUCE_SCATTER, OP_ALL_GATHER, OP_ALL_GATHER_V2, OP_WEIGHT_GRAD = range(5)
@@ -75,6 +76,8 @@ def lib() -> ctypes.CDLL:
             L.coc_moe_dispatch_grouped_matmul.argtypes = [i32, i64, i64, i64, i32, pp, pp, vp, pp, pp, i64, vp, vp,
                                                           i32, vp]
             L.coc_moe_dispatch_grouped_matmul.restype = i32
+            L.coc_moe_dispatch_grouped_matmul_combine.argtypes = L.coc_moe_dispatch_grouped_matmul.argtypes
+            L.coc_moe_dispatch_grouped_matmul_combine.restype = i32
             L.coc_moe_capacity.argtypes = [i32, i64, i32]
             L.coc_moe_capacity.restype = i64
             L.coc_fused_matmul.argtypes = [i32, i32, i64, i64, i64, pp, pp, i32, pp, pp, i32, i32, i32, vp]
@@ -335,13 +338,15 @@ def moe_capacity(R: int, tokens: int, experts_per_rank: int) -> int:
 
 
 def moe_dispatch_grouped_matmul(xs, idxs, w, experts_per_rank: int, xd=None, y=None, counts=None, offsets=None,
-                                stream=None):
+                                stream=None, combine: bool = False):
     """MoE token dispatch (all-to-all) + expert GroupedMatMul on every rank.
 
     xs[r]: tokens x h (fp16/bf16); idxs[r]: int32 expert ids; w: experts x h x
     f stacked weights (expert e = rank e // experts_per_rank).  Returns
     (y, xd, counts, offsets): expert e's rows are offsets[e] ..
-    offsets[e] + counts[e] - 1 of y[q] / xd[q] with q = e // experts_per_rank."""
+    offsets[e] + counts[e] - 1 of y[q] / xd[q] with q = e // experts_per_rank.
+    combine=True adds the all-to-all back: y[r] is then tokens x f, row t the
+    output of rank r's token t."""
     R = len(xs)
     if R < 1 or R > MAX_RANKS or len(idxs) != R:
         raise ValueError("need 1..8 ranks and one idx per rank")
@@ -359,15 +364,15 @@ def moe_dispatch_grouped_matmul(xs, idxs, w, experts_per_rank: int, xd=None, y=N
     f = w.shape[2]
     cap = moe_capacity(R, T, experts_per_rank)
     xd = _outs(xd, R, (cap, h), dt, x0.device)
-    y = _outs(y, R, (cap, f), dt, x0.device)
+    y = _outs(y, R, (T, f) if combine else (cap, f), dt, x0.device)
     if counts is None:
         counts = torch.empty(E, dtype=torch.int32, device=x0.device)
     if offsets is None:
         offsets = torch.empty(E, dtype=torch.int32, device=x0.device)
     _check_list([counts, offsets], "counts/offsets", (E,), torch.int32, x0.device)
-    _check(lib().coc_moe_dispatch_grouped_matmul(R, T, h, f, int(experts_per_rank), _ptrs(xs), _ptrs(idxs),
-                                                 w.data_ptr(), _ptrs(xd), _ptrs(y), cap, counts.data_ptr(),
-                                                 offsets.data_ptr(), _dtype_code(dt), _stream(stream)))
+    fn = lib().coc_moe_dispatch_grouped_matmul_combine if combine else lib().coc_moe_dispatch_grouped_matmul
+    _check(fn(R, T, h, f, int(experts_per_rank), _ptrs(xs), _ptrs(idxs), w.data_ptr(), _ptrs(xd), _ptrs(y), cap,
+              counts.data_ptr(), offsets.data_ptr(), _dtype_code(dt), _stream(stream)))
     return y, xd, counts, offsets
 
 

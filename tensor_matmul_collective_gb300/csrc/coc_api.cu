@@ -665,11 +665,12 @@ COC_API int64_t coc_moe_capacity(int R, int64_t tokens, int experts_per_rank) {
     return moe_capacity(R, tokens, experts_per_rank);
 }
 
-COC_API coc_status_t coc_moe_dispatch_grouped_matmul(int R, int64_t tokens, int64_t h, int64_t f, int experts_per_rank,
-                                                     const void* const* x, const int32_t* const* idx, const void* w,
-                                                     void* const* xd, void* const* y, int64_t capacity,
-                                                     int32_t* counts, int32_t* offsets, coc_dtype_t dt,
-                                                     coc_stream_t stream) {
+// Shared by the dispatch-only and the dispatch + combine entry points: y
+// (dispatched layout) or y_tok (token order on the source ranks) is NULL.
+static coc_status_t moe_impl(int R, int64_t tokens, int64_t h, int64_t f, int experts_per_rank, const void* const* x,
+                             const int32_t* const* idx, const void* w, void* const* xd, void* const* y,
+                             void* const* y_tok, int64_t capacity, int32_t* counts, int32_t* offsets, coc_dtype_t dt,
+                             coc_stream_t stream) {
     if (R < 1 || R > COC_MAX_RANKS) return fail(COC_ERR_INVALID_ARG, "R = %d outside [1, %d]", R, COC_MAX_RANKS);
     if (dt != COC_FP16 && dt != COC_BF16) return fail(COC_ERR_INVALID_ARG, "unknown dtype %d", static_cast<int>(dt));
     const int eloc = experts_per_rank;
@@ -688,7 +689,8 @@ COC_API coc_status_t coc_moe_dispatch_grouped_matmul(int R, int64_t tokens, int6
         return fail(COC_ERR_ALIGN, "counts / offsets not 4-byte aligned");
     coc_status_t st;
     if ((st = check_ptrs(xd, R, true, "xd")) != COC_OK) return st;
-    if ((st = check_ptrs(y, R, true, "y")) != COC_OK) return st;
+    if (y != nullptr && (st = check_ptrs(y, R, true, "y")) != COC_OK) return st;
+    if (y_tok != nullptr && (st = check_ptrs(y_tok, R, true, "y_tok")) != COC_OK) return st;
     if (w == nullptr || !aligned16(w)) return fail(w == nullptr ? COC_ERR_INVALID_ARG : COC_ERR_ALIGN, "w is NULL or not 16-byte aligned");
     if (tokens > 0) {
         if ((st = check_ptrs(x, R, true, "x")) != COC_OK) return st;
@@ -706,13 +708,23 @@ COC_API coc_status_t coc_moe_dispatch_grouped_matmul(int R, int64_t tokens, int6
     std::memset(&ra, 0, sizeof ra);
     void* ws = nullptr;
     cudaMemPool_t pool = nullptr;
+    // routing table: R x tokens destination rows, then (combine) R x capacity source tokens
+    const size_t dest_ints = static_cast<size_t>(R) * tokens;
+    const size_t src_ints = y_tok != nullptr ? static_cast<size_t>(R) * capacity : 0;
     if (tokens > 0) {
         if ((st = device_pool(ds, &pool)) != COC_OK) return st;
-        cudaError_t e = cudaMallocFromPoolAsync(&ws, static_cast<size_t>(R) * tokens * sizeof(int32_t), pool, s);
+        cudaError_t e = cudaMallocFromPoolAsync(&ws, (dest_ints + src_ints) * sizeof(int32_t), pool, s);
         if (e != cudaSuccess) return cuda_fail(e, "cudaMallocFromPoolAsync (MoE routing table)");
+        if (src_ints > 0 &&
+            (e = cudaMemsetAsync(static_cast<int32_t*>(ws) + dest_ints, 0xFF, src_ints * sizeof(int32_t), s)) != cudaSuccess) {
+            cudaFreeAsync(ws, s);
+            return cuda_fail(e, "cudaMemsetAsync (MoE source map)");
+        }
     }
     for (int r = 0; r < R; ++r) ra.idx[r] = tokens > 0 ? idx[r] : nullptr;
     ra.dest = static_cast<int32_t*>(ws);
+    ra.srcmap = (tokens > 0 && src_ints > 0) ? static_cast<int32_t*>(ws) + dest_ints : nullptr;
+    ra.cap = static_cast<int>(capacity);
     ra.counts = counts;
     ra.offsets = offsets;
     ra.status = ds->status;
@@ -765,10 +777,16 @@ COC_API coc_status_t coc_moe_dispatch_grouped_matmul(int R, int64_t tokens, int6
         p.gmm_offsets = offsets;
         p.gmm_E = E;
         p.gmm_eloc = eloc;
+        if (y_tok != nullptr) {
+            // combine: the epilogue writes each row to its token's row of y_tok[source rank]
+            p.gmm_srcmap = ra.srcmap;
+            p.gmm_T = static_cast<int>(tokens);
+            for (int r = 0; r < R; ++r) p.outp[r] = static_cast<uint16_t*>(y_tok[r]);
+        }
         const CUtensorMapDataType tdt = tma_dtype(dt);
         for (int q = 0; q < R && st == COC_OK; ++q) {
             st = encode(&p.tm_a[q], tdt, xd[q], h, capacity, h * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B);
-            if (st == COC_OK)
+            if (st == COC_OK && y != nullptr)
                 st = encode(&p.tm_out[q], tdt, y[q], f, capacity, f * 2, EPI_COLS, p.store_rows, CU_TENSOR_MAP_SWIZZLE_128B);
         }
         if (st == COC_OK)
@@ -780,6 +798,25 @@ COC_API coc_status_t coc_moe_dispatch_grouped_matmul(int R, int64_t tokens, int6
         if (st == COC_OK && ef != cudaSuccess) st = cuda_fail(ef, "cudaFreeAsync (MoE routing table)");
     }
     return st;
+}
+
+COC_API coc_status_t coc_moe_dispatch_grouped_matmul(int R, int64_t tokens, int64_t h, int64_t f, int experts_per_rank,
+                                                     const void* const* x, const int32_t* const* idx, const void* w,
+                                                     void* const* xd, void* const* y, int64_t capacity,
+                                                     int32_t* counts, int32_t* offsets, coc_dtype_t dt,
+                                                     coc_stream_t stream) {
+    if (y == nullptr) return fail(COC_ERR_INVALID_ARG, "y is NULL");
+    return moe_impl(R, tokens, h, f, experts_per_rank, x, idx, w, xd, y, nullptr, capacity, counts, offsets, dt, stream);
+}
+
+COC_API coc_status_t coc_moe_dispatch_grouped_matmul_combine(int R, int64_t tokens, int64_t h, int64_t f,
+                                                             int experts_per_rank, const void* const* x,
+                                                             const int32_t* const* idx, const void* w, void* const* xd,
+                                                             void* const* y_tok, int64_t capacity, int32_t* counts,
+                                                             int32_t* offsets, coc_dtype_t dt, coc_stream_t stream) {
+    if (y_tok == nullptr) return fail(COC_ERR_INVALID_ARG, "y_tok is NULL");
+    return moe_impl(R, tokens, h, f, experts_per_rank, x, idx, w, xd, nullptr, y_tok, capacity, counts, offsets, dt,
+                    stream);
 }
 
 COC_API coc_status_t coc_sync_status(coc_stream_t stream) {

@@ -71,6 +71,9 @@ struct KParams {
     const int32_t* gmm_counts;   // grouped GEMM: rows per expert (device, written by the routing kernel)
     const int32_t* gmm_offsets;  // grouped GEMM: first row of each expert's group (multiple of 256)
     int gmm_E, gmm_eloc;         // grouped GEMM: experts, experts per rank
+    const int32_t* gmm_srcmap;   // combine: per destination rank (stride rows_per_rank) the source
+                                 // token r * gmm_T + t of each dispatched row, -1 for padding; NULL: no combine
+    int gmm_T;                   // combine: tokens per rank
     int replica_stores; // AllReduce: write the n_out outputs with plain stores (outp) instead of TMA
 };
 
@@ -103,6 +106,8 @@ constexpr int MOE_MAX_EXPERTS = 256;
 struct MoeRouteArgs {
     const int32_t* idx[COC_MAX_RANKS];   // T expert ids per rank
     int32_t* dest;                        // R x T: destination row (-1: not dispatched)
+    int32_t* srcmap;                      // R x cap: source token of each dispatched row (NULL: not kept)
+    int cap;
     int32_t* counts;                      // E
     int32_t* offsets;                     // E
     unsigned* status;

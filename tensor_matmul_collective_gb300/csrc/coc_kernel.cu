@@ -871,12 +871,33 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
                     } else if constexpr (OP == OP_AG) {
                         tma_store_2d(&p.tm_out[r], src, col, row0);
                     } else if constexpr (OP == OP_GMM) {
-                        tma_store_2d(&p.tm_out[r / p.gmm_eloc], src, col, row0);
+                        if (p.gmm_srcmap == nullptr) tma_store_2d(&p.tm_out[r / p.gmm_eloc], src, col, row0);
                     } else {
                         if (!p.replica_stores)
                             for (int o = 0; o < p.n_out; ++o) tma_store_2d(&p.tm_out[o], src, col, row0);
                     }
                     bulk_commit();
+                }
+                if constexpr (OP == OP_GMM) {
+                    if (p.gmm_srcmap != nullptr) {
+                        // MoE combine (the all-to-all back): each row of the sub-tile goes
+                        // to its token's row on the source rank.  Coalesced read-back as
+                        // for the AllReduce copies (lane l: chunk l % 8 of rows l / 8 + 4i).
+                        const int ch = lane & 7;
+                        const int c = col + ch * 8;
+                        const int32_t* smap = p.gmm_srcmap + static_cast<long long>(r / p.gmm_eloc) * p.rows_per_rank;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int rr = (lane >> 3) + 4 * i;
+                            const uint4 v = *reinterpret_cast<const uint4*>(sbuf + rr * 128 + ((ch ^ (rr & 7)) << 4));
+                            const int g = row0 + rr;
+                            const int tok = (g < p.m) ? __ldg(smap + g) : -1;
+                            if (tok >= 0 && c < p.n) {
+                                const int sr = tok / p.gmm_T;
+                                *reinterpret_cast<uint4*>(p.outp[sr] + static_cast<long long>(tok - sr * p.gmm_T) * p.n + c) = v;
+                            }
+                        }
+                    }
                 }
                 if constexpr (OP == OP_AR || OP == OP_W8) {
                     if (p.replica_stores) {

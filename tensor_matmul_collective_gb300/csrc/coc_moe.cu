@@ -123,7 +123,11 @@ __global__ void __launch_bounds__(32 * kRouteWarps) moe_route_kernel(const __gri
                 __syncwarp();
                 if (e[i] >= 0 && lane == __ffs(same) - 1) cnt[warp][e[i]] += __popc(same);
                 __syncwarp();
-                if (t < t_end) a.dest[static_cast<long long>(r) * a.T + t] = pos;
+                if (t < t_end) {
+                    a.dest[static_cast<long long>(r) * a.T + t] = pos;
+                    if (a.srcmap != nullptr && pos >= 0)
+                        a.srcmap[static_cast<long long>(e[i] / a.eloc) * a.cap + pos] = r * a.T + t;
+                }
             }
         }
     }

@@ -130,3 +130,47 @@ def test_moe_layer_shape_sampled():
         assert np.array_equal(wl.bits16(xd[e][pick].cpu()), Xd)
         ref = orc.matmul_all_reduce(orc.BF16, [Xd], [wl.bits16(ws[e])])
         assert_close(y[e][pick], ref, s.h, f"expert {e}")
+
+
+@pytest.mark.parametrize("R,T,h,f,e_loc,dt", CASES)
+def test_moe_combine_parity(R, T, h, f, e_loc, dt):
+    """The all-to-all back: y_tok[r][t] = x[r][t] @ W_{idx[r][t]} for every token."""
+    s = wl.MoEDispatch(R=R, T=T, h=h, f=f, e_loc=e_loc, seed=R + 3 * T, dtype=dt)
+    xs, idxs, ws = s.make()
+    y, xd, counts, offsets = coc.moe_dispatch_grouped_matmul([x.to(DEV) for x in xs], [i.to(DEV) for i in idxs],
+                                                             torch.stack(ws).to(DEV), s.e_loc, combine=True)
+    coc.sync_status()
+    ref = orc.moe_token_outputs(CODE[s.dtype], bits(xs), [i.numpy() for i in idxs], bits(ws))
+    for r in range(R):
+        assert y[r].shape == (T, f)
+        assert_close(y[r], ref[r], s.h, f"combine rank {r}")
+
+
+def test_moe_combine_matches_dispatched_layout_bits():
+    """Combine and the dispatched layout hold the same bits, row for row."""
+    s = wl.MoEDispatch(R=4, T=200, h=128, f=136, e_loc=2, seed=17)
+    xs, idxs, ws = s.make()
+    args = ([x.to(DEV) for x in xs], [i.to(DEV) for i in idxs], torch.stack(ws).to(DEV), s.e_loc)
+    y, _, counts, offsets = coc.moe_dispatch_grouped_matmul(*args)
+    yt, _, _, _ = coc.moe_dispatch_grouped_matmul(*args, combine=True)
+    coc.sync_status()
+    groups = orc.moe_dispatch_order([i.numpy() for i in idxs], s.E)
+    off = offsets.cpu().tolist()
+    for e, pairs in enumerate(groups):
+        q = e // s.e_loc
+        for i, (r, t) in enumerate(pairs):
+            assert torch.equal(y[q][off[e] + i], yt[r][t])
+
+
+def test_moe_combine_layer_shape_sampled():
+    s = wl.MoEDispatch(R=8, T=4096, h=4096, f=14336, e_loc=1, seed=22)
+    xs, idxs, ws = s.make()
+    y, _, _, _ = coc.moe_dispatch_grouped_matmul([x.to(DEV) for x in xs], [i.to(DEV) for i in idxs],
+                                                 torch.stack(ws).to(DEV), s.e_loc, combine=True)
+    coc.sync_status()
+    xb, wb = bits(xs), bits(ws)
+    for r in range(s.R):
+        pick = np.linspace(0, s.T - 1, 16).astype(int)
+        ib = idxs[r].numpy()
+        ref = np.concatenate([orc.matmul_all_reduce(orc.BF16, [xb[r][t:t + 1]], [wb[ib[t]]]) for t in pick])
+        assert_close(y[r][pick], ref, s.h, f"combine rank {r}")

@@ -412,6 +412,25 @@ def test_moe_single_expert_is_plain_gemm(oracle_mod):
     assert _rel(Y, ref) < 1e-13
 
 
+@pytest.mark.parametrize("R,e_loc", [(2, 1), (3, 2)])
+def test_moe_combine_per_token_matches_dispatch_and_numpy(oracle_mod, R, e_loc):
+    """Two formulations of the combined output: per token (no dispatch order)
+    and the dispatched groups mapped back; plus numpy per token."""
+    s = wl.MoEDispatch(R=R, T=29, h=16, f=12, e_loc=e_loc, seed=40 + R)
+    xs, idxs, ws = s.make()
+    xb, ib, wb = [wl.bits16(x) for x in xs], [i.numpy() for i in idxs], [wl.bits16(w) for w in ws]
+    per_tok = oracle_mod.moe_token_outputs(oracle_mod.BF16, xb, ib, wb)
+    back = [np.full((s.T, s.f), np.nan) for _ in range(R)]
+    for pairs, _, Y in oracle_mod.moe_dispatch_grouped_matmul(oracle_mod.BF16, xb, ib, wb):
+        for i, (r, t) in enumerate(pairs):
+            back[r][t] = Y[i]
+    for r in range(R):
+        assert np.array_equal(per_tok[r], back[r])
+        ref = np.stack([_dec(xb[r][t:t + 1], torch.bfloat16)[0] @ _dec(wb[ib[r][t]], torch.bfloat16)
+                        for t in range(s.T)])
+        assert _rel(per_tok[r], ref) < 1e-13
+
+
 def test_moe_dispatch_mutants_rejected(oracle_mod):
     s = wl.MoEDispatch(R=3, T=20, h=8, f=8, e_loc=2, seed=9)
     _, idxs, _ = s.make()
