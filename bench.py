@@ -525,7 +525,17 @@ def time_next_rows(ops, dev, t):
     res["moe_dispatch_grouped_matmul_mixtral_ep8"] = {
         "ms": round(tm, 4), "tflops": round(s.flops() / tm / 1e9, 1), "plain_gemm_same_rows_ms": round(tp, 4),
         "tokens_per_expert": [int(v) for v in cnt.cpu().tolist()]}
-    del dx, di, w, y, xd, xg, og
+    del y, xd, xg, og
+    # the same layer with Mixtral's top-2 routing and the gated combine
+    ti, tg = s.routing_topk(2)
+    ti, tg = [i.to(dev) for i in ti], [g.to(dev) for g in tg]
+    yt, y2, xd2, cnt2, off2 = coc.moe_topk_grouped_matmul_combine(dx, ti, tg, w, s.e_loc)
+    tk = t(lambda: coc.moe_topk_grouped_matmul_combine(dx, ti, tg, w, s.e_loc, xd=xd2, y=y2, y_tok=yt, counts=cnt2,
+                                                       offsets=off2), 5)
+    res["moe_top2_grouped_matmul_combine_mixtral_ep8"] = {
+        "ms": round(tk, 4), "tflops": round(2 * s.flops() / tk / 1e9, 1),
+        "entries_per_expert": [int(v) for v in cnt2.cpu().tolist()]}
+    del dx, di, w, ti, tg, yt, y2, xd2
     return res
 
 

@@ -16,6 +16,7 @@
  * and the expert-parallel form of the blog's MC2 section (extension):
  *   MoE token dispatch + expert GroupedMatMul           coc_moe_dispatch_grouped_matmul
  *     + the combine (all-to-all back)                   coc_moe_dispatch_grouped_matmul_combine
+ *     top-k routing with the gated combine              coc_moe_topk_grouped_matmul_combine
  *
  * The same page's section 问题分析 ("problem analysis") places them in the
  * Megatron ColumnParallelLinear / RowParallelLinear layers: the matmul is
@@ -296,6 +297,27 @@ coc_status_t coc_moe_dispatch_grouped_matmul_combine(int R, int64_t tokens, int6
                                                      void* const* xd, void* const* y_tok, int64_t capacity,
                                                      int32_t* counts, int32_t* offsets, coc_dtype_t dt,
                                                      coc_stream_t stream);
+
+/*
+ * Top-k routing: every token has k expert ids idx[r][t*k + j] (j < k) and k
+ * fp32 gates gates[r][t*k + j].  Each (token, slot) entry is dispatched as
+ * its own row (inside an expert ordered by source rank, token, slot), the
+ * GroupedMatMul writes the dispatched layout y[q] (as
+ * coc_moe_dispatch_grouped_matmul), and the combine then forms
+ *
+ *   y_tok[r][t] = rne( sum_{j < k} gates[r][t*k+j] * y[e_j's rank][row of (t, j)] )
+ *
+ * in fp32, slots in order (deterministic).  capacity must be at least
+ * coc_moe_capacity(R, tokens * k, experts_per_rank); k in [1, 8]; gates 4-byte
+ * aligned.  Entries with an out-of-range id contribute nothing (and
+ * coc_sync_status reports COC_ERR_INVALID_ARG).  Four kernels on `stream`.
+ */
+coc_status_t coc_moe_topk_grouped_matmul_combine(int R, int64_t tokens, int k, int64_t h, int64_t f,
+                                                 int experts_per_rank, const void* const* x,
+                                                 const int32_t* const* idx, const float* const* gates, const void* w,
+                                                 void* const* xd, void* const* y, void* const* y_tok,
+                                                 int64_t capacity, int32_t* counts, int32_t* offsets,
+                                                 coc_dtype_t dt, coc_stream_t stream);
 
 /* Rows xd[q] / y[q] need for coc_moe_dispatch_grouped_matmul: R * tokens plus
  * 255 rows of padding per expert of a rank, rounded up to 256; -1 on bad

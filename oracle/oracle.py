@@ -351,3 +351,26 @@ def moe_token_outputs(dtype: int, xs, idxs, ws, nthreads=None):
                 Y[rows] = matmul_all_reduce(dtype, [x], [ws[e]], rows, nthreads)
         out.append(Y)
     return out
+
+
+def moe_topk_combine(dtype: int, xs, idxs, gates, ws, nthreads=None):
+    """Top-k combine: out_r[t] = sum_j g[t, j] * rne_dtype(X_r[t] @ W_{idx[t, j]})
+    (the expert outputs in the activation type, as the GroupedMatMul
+    produces them, weighted and summed in fp64).  idxs[r] / gates[r]: T x k.
+    Entries with an id outside [0, E) contribute nothing."""
+    E = len(ws)
+    f = ws[0].shape[1]
+    enc = encode_bf16 if dtype == BF16 else encode_f16
+    out = []
+    for x, idx, g in zip(xs, idxs, gates):
+        idx = np.asarray(idx).reshape(x.shape[0], -1)
+        g = np.asarray(g, dtype=np.float64).reshape(idx.shape)
+        acc = np.zeros((x.shape[0], f))
+        for j in range(idx.shape[1]):
+            for e in range(E):
+                rows = np.nonzero(idx[:, j] == e)[0]
+                if rows.size:
+                    Y = decode16(enc(matmul_all_reduce(dtype, [x], [ws[e]], rows, nthreads)), dtype)
+                    acc[rows] += g[rows, j:j + 1] * Y
+        out.append(acc)
+    return out

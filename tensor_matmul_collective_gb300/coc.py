@@ -29,7 +29,7 @@ EXPORTS = (
     "coc_sync_status", "coc_status_string", "coc_last_error", "coc_version",
     "coc_debug_inject_timeout", "coc_shutdown", "coc_matmul_all_reduce_noalloc",
     "coc_fused_matmul", "coc_matmul_all_reduce_w8a16_ex", "coc_moe_dispatch_grouped_matmul", "coc_moe_capacity",
-    "coc_moe_dispatch_grouped_matmul_combine",
+    "coc_moe_dispatch_grouped_matmul_combine", "coc_moe_topk_grouped_matmul_combine",
 )
 
 OP_ALL_REDUCE, OP_REDUCE_SCATTER, OP_ALL_GATHER, OP_ALL_GATHER_V2, OP_WEIGHT_GRAD = range(5)
@@ -78,6 +78,9 @@ def lib() -> ctypes.CDLL:
             L.coc_moe_dispatch_grouped_matmul.restype = i32
             L.coc_moe_dispatch_grouped_matmul_combine.argtypes = L.coc_moe_dispatch_grouped_matmul.argtypes
             L.coc_moe_dispatch_grouped_matmul_combine.restype = i32
+            L.coc_moe_topk_grouped_matmul_combine.argtypes = [i32, i64, i32, i64, i64, i32, pp, pp, pp, vp, pp, pp, pp,
+                                                              i64, vp, vp, i32, vp]
+            L.coc_moe_topk_grouped_matmul_combine.restype = i32
             L.coc_moe_capacity.argtypes = [i32, i64, i32]
             L.coc_moe_capacity.restype = i64
             L.coc_fused_matmul.argtypes = [i32, i32, i64, i64, i64, pp, pp, i32, pp, pp, i32, i32, i32, vp]
@@ -374,6 +377,44 @@ def moe_dispatch_grouped_matmul(xs, idxs, w, experts_per_rank: int, xd=None, y=N
     _check(fn(R, T, h, f, int(experts_per_rank), _ptrs(xs), _ptrs(idxs), w.data_ptr(), _ptrs(xd), _ptrs(y), cap,
               counts.data_ptr(), offsets.data_ptr(), _dtype_code(dt), _stream(stream)))
     return y, xd, counts, offsets
+
+
+def moe_topk_grouped_matmul_combine(xs, idxs, gates, w, experts_per_rank: int, xd=None, y=None, y_tok=None,
+                                    counts=None, offsets=None, stream=None):
+    """Top-k MoE: dispatch every (token, slot) entry, GroupedMatMul, gated
+    combine.  idxs[r] / gates[r]: tokens x k int32 / float32.  Returns
+    (y_tok, y, xd, counts, offsets); y_tok[r] is tokens x f."""
+    R = len(xs)
+    if R < 1 or R > MAX_RANKS or len(idxs) != R or len(gates) != R:
+        raise ValueError("need 1..8 ranks and one idx / gates tensor per rank")
+    x0 = xs[0]
+    T, h = x0.shape
+    if x0.dtype not in (torch.float16, torch.bfloat16):
+        raise ValueError("tokens must be fp16 or bf16")
+    dt = x0.dtype
+    k = idxs[0].shape[1] if idxs[0].dim() == 2 else 1
+    _check_list(xs, "xs", (T, h), dt, x0.device)
+    _check_list(idxs, "idxs", (T, k), torch.int32, x0.device)
+    _check_list(gates, "gates", (T, k), torch.float32, x0.device)
+    E = R * int(experts_per_rank)
+    if w.dim() != 3 or w.shape[0] != E or w.shape[1] != h or w.dtype != dt or w.device != x0.device \
+            or not w.is_contiguous():
+        raise ValueError(f"w must be a contiguous {dt} tensor of shape ({E}, {h}, f) on {x0.device}")
+    f = w.shape[2]
+    cap = moe_capacity(R, T * k, experts_per_rank)
+    xd = _outs(xd, R, (cap, h), dt, x0.device)
+    y = _outs(y, R, (cap, f), dt, x0.device)
+    y_tok = _outs(y_tok, R, (T, f), dt, x0.device)
+    if counts is None:
+        counts = torch.empty(E, dtype=torch.int32, device=x0.device)
+    if offsets is None:
+        offsets = torch.empty(E, dtype=torch.int32, device=x0.device)
+    _check_list([counts, offsets], "counts/offsets", (E,), torch.int32, x0.device)
+    _check(lib().coc_moe_topk_grouped_matmul_combine(R, T, k, h, f, int(experts_per_rank), _ptrs(xs), _ptrs(idxs),
+                                                     _ptrs(gates), w.data_ptr(), _ptrs(xd), _ptrs(y), _ptrs(y_tok),
+                                                     cap, counts.data_ptr(), offsets.data_ptr(), _dtype_code(dt),
+                                                     _stream(stream)))
+    return y_tok, y, xd, counts, offsets
 
 
 def matmul(xs, ws, out=None, stream=None):

@@ -667,20 +667,26 @@ COC_API int64_t coc_moe_capacity(int R, int64_t tokens, int experts_per_rank) {
 
 // Shared by the dispatch-only and the dispatch + combine entry points: y
 // (dispatched layout) or y_tok (token order on the source ranks) is NULL.
-static coc_status_t moe_impl(int R, int64_t tokens, int64_t h, int64_t f, int experts_per_rank, const void* const* x,
-                             const int32_t* const* idx, const void* w, void* const* xd, void* const* y,
-                             void* const* y_tok, int64_t capacity, int32_t* counts, int32_t* offsets, coc_dtype_t dt,
-                             coc_stream_t stream) {
+// k routing entries per token (entry i of rank r: token i / k, slot i % k).
+// gates != NULL: weighted top-k combine after the grouped GEMM (y holds the
+// dispatched expert outputs, y_tok receives the combined tokens); gates ==
+// NULL with y_tok: the k = 1 combine fused into the grouped GEMM's epilogue.
+static coc_status_t moe_impl(int R, int64_t tokens, int k, int64_t h, int64_t f, int experts_per_rank,
+                             const void* const* x, const int32_t* const* idx, const float* const* gates, const void* w,
+                             void* const* xd, void* const* y, void* const* y_tok, int64_t capacity, int32_t* counts,
+                             int32_t* offsets, coc_dtype_t dt, coc_stream_t stream) {
     if (R < 1 || R > COC_MAX_RANKS) return fail(COC_ERR_INVALID_ARG, "R = %d outside [1, %d]", R, COC_MAX_RANKS);
     if (dt != COC_FP16 && dt != COC_BF16) return fail(COC_ERR_INVALID_ARG, "unknown dtype %d", static_cast<int>(dt));
     const int eloc = experts_per_rank;
     if (eloc < 1 || static_cast<int64_t>(R) * eloc > MOE_MAX_EXPERTS)
         return fail(COC_ERR_INVALID_ARG, "experts = R x %d must lie in [1, %d]", eloc, MOE_MAX_EXPERTS);
-    if (tokens < 0 || tokens > (int64_t(1) << 24)) return fail(COC_ERR_SHAPE, "tokens = %lld per rank", (long long)tokens);
+    if (k < 1 || k > 8) return fail(COC_ERR_INVALID_ARG, "top-k = %d outside [1, 8]", k);
+    if (tokens < 0 || tokens * k > (int64_t(1) << 24)) return fail(COC_ERR_SHAPE, "tokens = %lld per rank", (long long)tokens);
+    const int64_t entries = tokens * k;   // routing entries per rank
     if (h <= 0 || h % BK != 0) return fail(COC_ERR_SHAPE, "h = %lld must be a positive multiple of %d", (long long)h, BK);
     if (f <= 0 || (f * 2) % 16 != 0) return fail(COC_ERR_ALIGN, "f = %lld: rows of W and Y must span a multiple of 16 bytes", (long long)f);
     if (h > (int64_t(1) << 20) || f > (int64_t(1) << 20)) return fail(COC_ERR_SHAPE, "h or f too large");
-    const int64_t need = moe_capacity(R, tokens, eloc);
+    const int64_t need = moe_capacity(R, entries, eloc);
     if (capacity < need)
         return fail(COC_ERR_SHAPE, "capacity = %lld rows, needs %lld (coc_moe_capacity)", (long long)capacity, (long long)need);
     if (capacity > (int64_t(1) << 30)) return fail(COC_ERR_SHAPE, "capacity too large");
@@ -698,6 +704,10 @@ static coc_status_t moe_impl(int R, int64_t tokens, int64_t h, int64_t f, int ex
         for (int r = 0; r < R; ++r)
             if (idx[r] == nullptr || (reinterpret_cast<uintptr_t>(idx[r]) & 3u))
                 return fail(idx[r] == nullptr ? COC_ERR_INVALID_ARG : COC_ERR_ALIGN, "idx[%d] is NULL or misaligned", r);
+        if (gates != nullptr)
+            for (int r = 0; r < R; ++r)
+                if (gates[r] == nullptr || (reinterpret_cast<uintptr_t>(gates[r]) & 3u))
+                    return fail(gates[r] == nullptr ? COC_ERR_INVALID_ARG : COC_ERR_ALIGN, "gates[%d] is NULL or misaligned", r);
     }
     DeviceState* ds = nullptr;
     if ((st = device_state(&ds)) != COC_OK) return st;
@@ -709,8 +719,9 @@ static coc_status_t moe_impl(int R, int64_t tokens, int64_t h, int64_t f, int ex
     void* ws = nullptr;
     cudaMemPool_t pool = nullptr;
     // routing table: R x tokens destination rows, then (combine) R x capacity source tokens
-    const size_t dest_ints = static_cast<size_t>(R) * tokens;
-    const size_t src_ints = y_tok != nullptr ? static_cast<size_t>(R) * capacity : 0;
+    const bool fused_combine = y_tok != nullptr && gates == nullptr;
+    const size_t dest_ints = static_cast<size_t>(R) * entries;
+    const size_t src_ints = fused_combine ? static_cast<size_t>(R) * capacity : 0;
     if (tokens > 0) {
         if ((st = device_pool(ds, &pool)) != COC_OK) return st;
         cudaError_t e = cudaMallocFromPoolAsync(&ws, (dest_ints + src_ints) * sizeof(int32_t), pool, s);
@@ -729,7 +740,7 @@ static coc_status_t moe_impl(int R, int64_t tokens, int64_t h, int64_t f, int ex
     ra.offsets = offsets;
     ra.status = ds->status;
     ra.R = R;
-    ra.T = static_cast<int>(tokens);
+    ra.T = static_cast<int>(entries);
     ra.E = E;
     ra.eloc = eloc;
     cudaError_t e = launch_moe_route(ra, s);
@@ -744,10 +755,11 @@ static coc_status_t moe_impl(int R, int64_t tokens, int64_t h, int64_t f, int ex
         }
         pa.dest = ra.dest;
         pa.R = R;
-        pa.T = static_cast<int>(tokens);
+        pa.T = static_cast<int>(entries);
         pa.h = static_cast<int>(h);
         pa.E = E;
         pa.eloc = eloc;
+        pa.k = k;
         if ((e = launch_moe_permute(pa, ds->sm_count, s)) != cudaSuccess) st = cuda_fail(e, "MoE permute launch");
     }
     if (st == COC_OK && tokens > 0) {
@@ -777,7 +789,7 @@ static coc_status_t moe_impl(int R, int64_t tokens, int64_t h, int64_t f, int ex
         p.gmm_offsets = offsets;
         p.gmm_E = E;
         p.gmm_eloc = eloc;
-        if (y_tok != nullptr) {
+        if (fused_combine) {
             // combine: the epilogue writes each row to its token's row of y_tok[source rank]
             p.gmm_srcmap = ra.srcmap;
             p.gmm_T = static_cast<int>(tokens);
@@ -793,6 +805,25 @@ static coc_status_t moe_impl(int R, int64_t tokens, int64_t h, int64_t f, int ex
             st = encode(&p.tm_b[0], tdt, w, f, static_cast<int64_t>(E) * h, f * 2, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B);
         if (st == COC_OK) st = launch_checked(OP_GMM, dt == COC_BF16, pair, p, ds, s);
     }
+    if (st == COC_OK && tokens > 0 && gates != nullptr) {
+        MoeCombineArgs ca;
+        std::memset(&ca, 0, sizeof ca);
+        for (int r = 0; r < R; ++r) {
+            ca.y[r] = static_cast<const uint16_t*>(y[r]);
+            ca.idx[r] = idx[r];
+            ca.gates[r] = gates[r];
+            ca.out[r] = static_cast<uint16_t*>(y_tok[r]);
+        }
+        ca.dest = ra.dest;
+        ca.R = R;
+        ca.tokens = static_cast<int>(tokens);
+        ca.k = k;
+        ca.f = static_cast<int>(f);
+        ca.E = E;
+        ca.eloc = eloc;
+        e = launch_moe_combine(ca, dt == COC_BF16, ds->sm_count, s);
+        if (e != cudaSuccess) st = cuda_fail(e, "MoE top-k combine launch");
+    }
     if (ws != nullptr) {
         const cudaError_t ef = cudaFreeAsync(ws, s);
         if (st == COC_OK && ef != cudaSuccess) st = cuda_fail(ef, "cudaFreeAsync (MoE routing table)");
@@ -806,7 +837,8 @@ COC_API coc_status_t coc_moe_dispatch_grouped_matmul(int R, int64_t tokens, int6
                                                      int32_t* counts, int32_t* offsets, coc_dtype_t dt,
                                                      coc_stream_t stream) {
     if (y == nullptr) return fail(COC_ERR_INVALID_ARG, "y is NULL");
-    return moe_impl(R, tokens, h, f, experts_per_rank, x, idx, w, xd, y, nullptr, capacity, counts, offsets, dt, stream);
+    return moe_impl(R, tokens, 1, h, f, experts_per_rank, x, idx, nullptr, w, xd, y, nullptr, capacity, counts, offsets, dt,
+                    stream);
 }
 
 COC_API coc_status_t coc_moe_dispatch_grouped_matmul_combine(int R, int64_t tokens, int64_t h, int64_t f,
@@ -815,8 +847,20 @@ COC_API coc_status_t coc_moe_dispatch_grouped_matmul_combine(int R, int64_t toke
                                                              void* const* y_tok, int64_t capacity, int32_t* counts,
                                                              int32_t* offsets, coc_dtype_t dt, coc_stream_t stream) {
     if (y_tok == nullptr) return fail(COC_ERR_INVALID_ARG, "y_tok is NULL");
-    return moe_impl(R, tokens, h, f, experts_per_rank, x, idx, w, xd, nullptr, y_tok, capacity, counts, offsets, dt,
-                    stream);
+    return moe_impl(R, tokens, 1, h, f, experts_per_rank, x, idx, nullptr, w, xd, nullptr, y_tok, capacity, counts,
+                    offsets, dt, stream);
+}
+
+COC_API coc_status_t coc_moe_topk_grouped_matmul_combine(int R, int64_t tokens, int k, int64_t h, int64_t f,
+                                                         int experts_per_rank, const void* const* x,
+                                                         const int32_t* const* idx, const float* const* gates,
+                                                         const void* w, void* const* xd, void* const* y,
+                                                         void* const* y_tok, int64_t capacity, int32_t* counts,
+                                                         int32_t* offsets, coc_dtype_t dt, coc_stream_t stream) {
+    if (y == nullptr || y_tok == nullptr || gates == nullptr)
+        return fail(COC_ERR_INVALID_ARG, "y, y_tok and gates are required");
+    return moe_impl(R, tokens, k, h, f, experts_per_rank, x, idx, gates, w, xd, y, y_tok, capacity, counts, offsets,
+                    dt, stream);
 }
 
 COC_API coc_status_t coc_sync_status(coc_stream_t stream) {

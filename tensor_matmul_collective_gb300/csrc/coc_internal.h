@@ -23,8 +23,6 @@ constexpr int XFORM_GROUPS = 2;      // dequant warp groups taking alternate k-b
 constexpr int XFORM_GROUP_WARPS = NUM_XFORM_WARPS / XFORM_GROUPS;
 
 constexpr int A_STAGE_BYTES = BM * BK * 2;        // 16 KiB
-constexpr int B_STAGE_BYTES = BN * BK * 2;        // 32 KiB
-constexpr int RAW_STAGE_BYTES = BN * BK;          // 16 KiB int8 (w8A16)
 constexpr int EPI_BUF_BYTES = 32 * EPI_COLS * 2;  // 4 KiB per warp per buffer
 
 enum OpKind : int { OP_AR = 0, OP_RS = 1, OP_AG = 2, OP_W8 = 3, OP_GMM = 4 };
@@ -114,14 +112,24 @@ struct MoeRouteArgs {
     int R, T, E, eloc;
 };
 struct MoePermuteArgs {
-    const uint16_t* x[COC_MAX_RANKS];     // T x h per rank
+    const uint16_t* x[COC_MAX_RANKS];     // tokens x h per rank
     uint16_t* xd[COC_MAX_RANKS];          // cap x h per destination rank
-    const int32_t* idx[COC_MAX_RANKS];
+    const int32_t* idx[COC_MAX_RANKS];    // T routing entries per rank (entry i: token i / k, slot i % k)
     const int32_t* dest;
-    int R, T, h, E, eloc;
+    int R, T, h, E, eloc, k;
+};
+// Top-k combine: out[r][t] = rne(sum_j gates[r][t*k+j] * y[q_j][dest_j]) in fp32, slots in order.
+struct MoeCombineArgs {
+    const uint16_t* y[COC_MAX_RANKS];     // cap x f expert outputs per destination rank
+    const int32_t* idx[COC_MAX_RANKS];    // tokens*k entries per rank
+    const float* gates[COC_MAX_RANKS];    // tokens*k per rank
+    const int32_t* dest;                  // R x tokens*k
+    uint16_t* out[COC_MAX_RANKS];         // tokens x f per rank
+    int R, tokens, k, f, E, eloc;
 };
 cudaError_t launch_moe_route(const MoeRouteArgs& a, cudaStream_t stream);
 cudaError_t launch_moe_permute(const MoePermuteArgs& a, int sm_count, cudaStream_t stream);
+cudaError_t launch_moe_combine(const MoeCombineArgs& a, bool bf16, int sm_count, cudaStream_t stream);
 
 // Host-side launch helpers implemented in coc_kernel.cu.  `pair` selects the
 // 2-SM variant (a cluster of two CTAs per 256-row tile; grid = 2 x pairs);

@@ -11,6 +11,9 @@
 //                     ranks' tokens: counts, offsets and every token's
 //                     destination row (deterministic, stable)
 // moe_permute_kernel  one warp per token row: the copy itself
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
 #include "coc_internal.h"
 
 namespace coc {
@@ -146,13 +149,90 @@ __global__ void __launch_bounds__(256) moe_permute_kernel(const __grid_constant_
         const int dst_row = __ldg(a.dest + w);
         if (dst_row < 0) continue;
         const int q = __ldg(a.idx[r] + t) / a.eloc;
-        const uint4* src = reinterpret_cast<const uint4*>(a.x[r] + static_cast<long long>(t) * a.h);
+        const uint4* src = reinterpret_cast<const uint4*>(a.x[r] + static_cast<long long>(t / a.k) * a.h);
         uint4* dst = reinterpret_cast<uint4*>(a.xd[q] + static_cast<long long>(dst_row) * a.h);
         for (int v = lane; v < vecs; v += 32) dst[v] = __ldg(src + v);
     }
 }
 
+// Top-k combine: one warp per token, lanes over 8-column chunks; the k expert
+// outputs are weighted and summed in fp32 in slot order, then rounded once.
+template <bool BF16>
+__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if constexpr (BF16) {
+            f[2 * i] = __uint_as_float(w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        } else {
+            const __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
+            const float2 t = __half22float2(h);
+            f[2 * i] = t.x;
+            f[2 * i + 1] = t.y;
+        }
+    }
+}
+template <bool BF16>
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if constexpr (BF16) {
+            const __nv_bfloat162 b = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+            w[i] = *reinterpret_cast<const uint32_t*>(&b);
+        } else {
+            const __half2 h = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
+            w[i] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(256) moe_combine_kernel(const __grid_constant__ MoeCombineArgs a) {
+    const long long ntok = static_cast<long long>(a.R) * a.tokens;
+    const int lane = threadIdx.x & 31;
+    const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+    const int vecs = a.f / 8;
+    const long long entries = static_cast<long long>(a.tokens) * a.k;
+    for (long long w = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); w < ntok;
+         w += warps) {
+        const int r = static_cast<int>(w / a.tokens);
+        const int t = static_cast<int>(w - static_cast<long long>(r) * a.tokens);
+        uint16_t* dst = a.out[r] + static_cast<long long>(t) * a.f;
+        for (int v = lane; v < vecs; v += 32) {
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int j = 0; j < a.k; ++j) {
+                const long long ent = static_cast<long long>(t) * a.k + j;
+                const int row = __ldg(a.dest + r * entries + ent);
+                if (row < 0) continue;
+                const int q = __ldg(a.idx[r] + ent) / a.eloc;
+                const float g = __ldg(a.gates[r] + ent);
+                float yv[8];
+                unpack8<BF16>(__ldg(reinterpret_cast<const uint4*>(a.y[q] + static_cast<long long>(row) * a.f) + v), yv);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[i] = __fmaf_rn(g, yv[i], acc[i]);
+            }
+            reinterpret_cast<uint4*>(dst)[v] = pack8<BF16>(acc);
+        }
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_moe_combine(const MoeCombineArgs& a, bool bf16, int sm_count, cudaStream_t stream) {
+    const long long rows = static_cast<long long>(a.R) * a.tokens;
+    if (rows <= 0) return cudaSuccess;
+    long long blocks = (rows + 7) / 8;
+    const long long cap = static_cast<long long>(sm_count > 0 ? sm_count : 1) * 8;
+    if (blocks > cap) blocks = cap;
+    if (bf16)
+        moe_combine_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a);
+    else
+        moe_combine_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_moe_route(const MoeRouteArgs& a, cudaStream_t stream) {
     moe_route_kernel<<<1, 32 * kRouteWarps, 0, stream>>>(a);

@@ -234,6 +234,22 @@ class MoEDispatch:
         p = w / w.sum()
         return [torch.from_numpy(g.choice(self.E, size=self.T, p=p).astype(np.int32)) for _ in range(self.R)]
 
+    def routing_topk(self, k: int):
+        """k distinct experts per token (Gumbel top-k over the skewed
+        popularity) and fp32 gates: positive, summing to 1 per token.
+        Returns (idxs, gates), each a list of (T x k) tensors."""
+        g = np.random.Generator(np.random.PCG64(self.seed * 7919 + 13))
+        w = (np.arange(self.E) + 1.0) ** (-self.skew)
+        logp = np.log(w[g.permutation(self.E)] / w.sum())
+        idxs, gates = [], []
+        for _ in range(self.R):
+            keys = logp[None, :] + g.gumbel(size=(self.T, self.E))
+            top = np.argsort(-keys, axis=1)[:, :k].astype(np.int32)
+            raw = g.random((self.T, k)).astype(np.float32) + np.float32(0.1)
+            idxs.append(torch.from_numpy(np.ascontiguousarray(top)))
+            gates.append(torch.from_numpy(raw / raw.sum(axis=1, keepdims=True)))
+        return idxs, gates
+
     def make(self):
         """Returns (xs, idxs, ws)."""
         xs = [to16(normal((self.T, self.h), 1.0, self.seed, 20 + r), self.dtype) for r in range(self.R)]

@@ -431,6 +431,40 @@ def test_moe_combine_per_token_matches_dispatch_and_numpy(oracle_mod, R, e_loc):
         assert _rel(per_tok[r], ref) < 1e-13
 
 
+def test_moe_topk_combine_pins(oracle_mod):
+    """Top-k combine: k = 1 with unit gates is the rounded per-token output
+    exactly; for k = 2 the result is within the rounding bound of the exact
+    gated sum computed by numpy; swapping the gates of the two slots is
+    detected."""
+    s = wl.MoEDispatch(R=2, T=31, h=16, f=24, e_loc=2, seed=50)
+    xs, _, ws = s.make()
+    xb, wb = [wl.bits16(x) for x in xs], [wl.bits16(w) for w in ws]
+    idx1, _ = s.routing_topk(1)
+    ones = [np.ones((s.T, 1), np.float32) for _ in range(s.R)]
+    got1 = oracle_mod.moe_topk_combine(oracle_mod.BF16, xb, [i.numpy() for i in idx1], ones, wb)
+    tok = oracle_mod.moe_token_outputs(oracle_mod.BF16, xb, [i.numpy()[:, 0] for i in idx1], wb)
+    for r in range(s.R):
+        assert np.array_equal(got1[r], oracle_mod.decode16(oracle_mod.encode_bf16(tok[r]), oracle_mod.BF16))
+    idx2, g2 = s.routing_topk(2)
+    i2, gg = [i.numpy() for i in idx2], [g.numpy() for g in g2]
+    for r in range(s.R):
+        assert np.all(i2[r][:, 0] != i2[r][:, 1]) and np.allclose(gg[r].sum(axis=1), 1.0, atol=1e-6)
+    got2 = oracle_mod.moe_topk_combine(oracle_mod.BF16, xb, i2, gg, wb)
+    for r in range(s.R):
+        X = _dec(xb[r], torch.bfloat16)
+        exact = np.zeros((s.T, s.f))
+        bound = np.zeros((s.T, s.f))
+        for t in range(s.T):
+            for j in range(2):
+                y = X[t] @ _dec(wb[i2[r][t, j]], torch.bfloat16)
+                exact[t] += np.float64(gg[r][t, j]) * y
+                bound[t] += np.float64(gg[r][t, j]) * np.abs(y) * 2.0 ** -8 + 1e-30   # half-ulp of bf16
+        assert np.all(np.abs(got2[r] - exact) <= bound)
+    swapped = [g[:, ::-1].copy() for g in gg]
+    bad = oracle_mod.moe_topk_combine(oracle_mod.BF16, xb, i2, swapped, wb)
+    assert not np.allclose(bad[0], got2[0])
+
+
 def test_moe_dispatch_mutants_rejected(oracle_mod):
     s = wl.MoEDispatch(R=3, T=20, h=8, f=8, e_loc=2, seed=9)
     _, idxs, _ = s.make()
