@@ -204,3 +204,20 @@ def test_moe_topk_parity(R, T, h, f, e_loc, k, dt):
     ref = orc.moe_topk_combine(CODE[dt], xb, [i.numpy() for i in idxs], [g.numpy() for g in gates], bits(ws))
     for r in range(R):
         assert_close(y_tok[r], ref[r], s.h, f"top-{k} combine rank {r}")
+
+
+@pytest.mark.parametrize("R,T,e_loc,f", [(8, 300, 8, 72), (8, 50, 32, 200)])
+def test_moe_many_experts(R, T, e_loc, f):
+    """64 and 256 experts (the maximum): most groups small or empty, f not a
+    multiple of the tile width; dispatch exact, dispatched outputs and the
+    combine against the oracle."""
+    s = wl.MoEDispatch(R=R, T=T, h=64, f=f, e_loc=e_loc, seed=T + e_loc)
+    xs, idxs, ws = s.make()
+    y, xd, counts, offsets = _run(s, xs, idxs, ws)
+    _check(s, xs, idxs, ws, y, xd, counts, offsets)
+    yt, _, _, _ = coc.moe_dispatch_grouped_matmul([x.to(DEV) for x in xs], [i.to(DEV) for i in idxs],
+                                                  torch.stack(ws).to(DEV), s.e_loc, combine=True)
+    coc.sync_status()
+    ref = orc.moe_token_outputs(CODE[s.dtype], bits(xs), [i.numpy() for i in idxs], bits(ws))
+    for r in range(R):
+        assert_close(yt[r], ref[r], s.h, f"combine rank {r}")
