@@ -11,7 +11,7 @@
 namespace coc {
 namespace {
 
-constexpr int kPrepassRows = 16;   // weight rows per thread: divides every group size (a multiple of 64)
+constexpr int kPrepassRows = 8;    // weight rows per thread: divides every group size (a multiple of 64)
 constexpr int kPrepassThreads = 256;
 
 // Thread i -> (rank, block of kPrepassRows rows, 16-column chunk), chunks
@@ -36,12 +36,19 @@ __global__ void __launch_bounds__(kPrepassThreads) w8_prepass_kernel(const __gri
         const int8_t* q = a.q[r] + static_cast<long long>(t0) * a.n + j0;
         uint16_t* o = a.out[r] + static_cast<long long>(t0) * a.n + j0;
         const int rows = min(kPrepassRows, a.k - t0);
-#pragma unroll 4
-        for (int t = 0; t < rows; ++t) {
-            const uint4 w = __ldg(reinterpret_cast<const uint4*>(q + static_cast<long long>(t) * a.n));
+        // every row's load in flight before the first conversion (the pass is
+        // bound by HBM latency x bytes in flight)
+        uint4 wv[kPrepassRows];
+#pragma unroll
+        for (int t = 0; t < kPrepassRows; ++t)
+            wv[t] = (t < rows) ? __ldg(reinterpret_cast<const uint4*>(q + static_cast<long long>(t) * a.n))
+                               : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int t = 0; t < kPrepassRows; ++t) {
+            if (t >= rows) break;
             uint4* dst = reinterpret_cast<uint4*>(o + static_cast<long long>(t) * a.n);
-            dst[0] = d0.convert(make_uint2(w.x, w.y));
-            dst[1] = d1.convert(make_uint2(w.z, w.w));
+            dst[0] = d0.convert(make_uint2(wv[t].x, wv[t].y));
+            dst[1] = d1.convert(make_uint2(wv[t].z, wv[t].w));
         }
     }
 }
@@ -52,8 +59,8 @@ cudaError_t launch_w8_prepass(const W8PrepassArgs& a, bool bf16, int sm_count, c
     const long long total = static_cast<long long>(a.n / 16) * ((a.k + kPrepassRows - 1) / kPrepassRows) * a.R;
     if (total <= 0) return cudaSuccess;
     long long blocks = (total + kPrepassThreads - 1) / kPrepassThreads;
-    const long long cap = static_cast<long long>(sm_count > 0 ? sm_count : 1) * 8;
-    if (blocks > cap) blocks = cap;   // grid-stride beyond 8 blocks per SM
+    const long long cap = static_cast<long long>(sm_count > 0 ? sm_count : 1) * 64;
+    if (blocks > cap) blocks = cap;   // grid-stride beyond 64 blocks per SM
     if (bf16)
         w8_prepass_kernel<true><<<static_cast<unsigned>(blocks), kPrepassThreads, 0, stream>>>(a);
     else

@@ -5,10 +5,11 @@ timing of one shape:
 
   python -m tensor_matmul_collective_gb300.run_case --op ag_v2 --R 8 --m 512 --n 1792 --k 8192 --iters 3
 
---op   ar | rs | ag | ag_v2 | w8a16 | plain
---m    rows (ar/rs/w8a16/plain: m; ag/ag_v2: m_shard)
---n    columns (ag/ag_v2: n_shard)
---k    contraction per shard (ag/ag_v2: full k)
+--op   ar | rs | ag | ag_v2 | w8a16 | plain | moe
+--m    rows (ar/rs/w8a16/plain: m; ag/ag_v2: m_shard; moe: tokens per rank)
+--n    columns (ag/ag_v2: n_shard; moe: f)
+--k    contraction per shard (ag/ag_v2: full k; moe: h)
+--eloc experts per rank (moe); --topk routing slots (moe, gated combine if > 1)
 """
 from __future__ import annotations
 
@@ -23,7 +24,7 @@ from tensor_matmul_collective_gb300 import workloads as wl
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--op", required=True, choices=["ar", "rs", "ag", "ag_v2", "w8a16", "plain"])
+    ap.add_argument("--op", required=True, choices=["ar", "rs", "ag", "ag_v2", "w8a16", "plain", "moe"])
     ap.add_argument("--R", type=int, default=8)
     ap.add_argument("--m", type=int, required=True)
     ap.add_argument("--n", type=int, required=True)
@@ -34,6 +35,8 @@ def main():
     ap.add_argument("--group", type=int, default=128)
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--zero", action="store_true", help="w8a16: int8 zero points (asymmetric weights)")
+    ap.add_argument("--eloc", type=int, default=1)
+    ap.add_argument("--topk", type=int, default=1)
     a = ap.parse_args()
 
     dev = torch.device("cuda:0")
@@ -50,6 +53,18 @@ def main():
         else:
             run = lambda: coc.all_gather_matmul(dx, dw, outs, chunks=a.chunks)  # noqa: E731
         flops = s.flops()
+    elif a.op == "moe":
+        s = wl.MoEDispatch(R=a.R, T=a.m, h=a.k, f=a.n, e_loc=a.eloc, seed=21, dtype=dt)
+        xs, idxs, ws = s.make()
+        dx, w = [x.to(dev) for x in xs], torch.stack(ws).to(dev)
+        if a.topk > 1:
+            ti, tg = s.routing_topk(a.topk)
+            ti, tg = [i.to(dev) for i in ti], [g.to(dev) for g in tg]
+            run = lambda: coc.moe_topk_grouped_matmul_combine(dx, ti, tg, w, a.eloc)  # noqa: E731
+        else:
+            di = [i.to(dev) for i in idxs]
+            run = lambda: coc.moe_dispatch_grouped_matmul(dx, di, w, a.eloc)  # noqa: E731
+        flops = s.flops() * a.topk
     elif a.op == "w8a16":
         s = wl.W8A16(R=a.R, m=a.m, n=a.n, k_shard=a.k, group=a.group, seed=3, dtype=dt)
         xs, wqs, scales = s.make(a.gran)
