@@ -511,6 +511,23 @@ def time_next_rows(ops, dev, t):
             name = f"w8a16_ar_channel_{'bf16' if dt == torch.bfloat16 else 'fp16'}_{'zp' if zero else 'sym'}"
             res[name] = {"ms": round(tm, 4), "tflops": round(s.flops() / tm / 1e9, 1)}
             del dx, dq, ds, dz, outs
+        # the suite's w8A16 layer through the fused in-kernel dequantisation
+        # (the path below 2048 rows) instead of the pre-pass, for comparison
+        s = base
+        xs, wqs, scales = s.make("channel")
+        dx, dq, ds = [x.to(dev) for x in xs], [w.to(dev) for w in wqs], [c.to(dev) for c in scales]
+        outs = [torch.empty(s.m, s.n, dtype=s.dtype, device=dev) for _ in range(s.R)]
+        prev = os.environ.get("COC_W8_PATH")
+        os.environ["COC_W8_PATH"] = "fused"
+        try:
+            tm = t(lambda: coc.matmul_all_reduce_w8a16(dx, dq, ds, "channel", s.group, outs))
+        finally:
+            if prev is None:
+                del os.environ["COC_W8_PATH"]
+            else:
+                os.environ["COC_W8_PATH"] = prev
+        res["w8a16_ar_channel_fp16_fused_dequant_path"] = {"ms": round(tm, 4), "tflops": round(s.flops() / tm / 1e9, 1)}
+        del dx, dq, ds, outs
     # MoE dispatch + GroupedMatMul (EP form of the fused operators): a
     # Mixtral-style layer on 8 EP ranks, one expert each, 4096 tokens per rank,
     # against one plain GEMM over the same number of rows

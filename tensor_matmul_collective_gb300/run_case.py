@@ -10,6 +10,7 @@ timing of one shape:
 --n    columns (ag/ag_v2: n_shard; moe: f)
 --k    contraction per shard (ag/ag_v2: full k; moe: h)
 --eloc experts per rank (moe); --topk routing slots (moe, gated combine if > 1)
+--deterministic  fixed rank-order reduction (ar/rs)
 """
 from __future__ import annotations
 
@@ -37,6 +38,7 @@ def main():
     ap.add_argument("--zero", action="store_true", help="w8a16: int8 zero points (asymmetric weights)")
     ap.add_argument("--eloc", type=int, default=1)
     ap.add_argument("--topk", type=int, default=1)
+    ap.add_argument("--deterministic", action="store_true", help="ar/rs: fixed rank-order reduction")
     a = ap.parse_args()
 
     dev = torch.device("cuda:0")
@@ -81,10 +83,12 @@ def main():
         dx, dw = [x.to(dev) for x in xs], [w.to(dev) for w in ws]
         if a.op == "ar":
             outs = [torch.empty(s.m, s.n, dtype=dt, device=dev) for _ in range(a.R)]
-            run = lambda: coc.matmul_all_reduce(dx, dw, outs, chunks=a.chunks)  # noqa: E731
+            run = lambda: coc.matmul_all_reduce(dx, dw, outs, chunks=a.chunks,  # noqa: E731
+                                                deterministic=a.deterministic)
         elif a.op == "rs":
             outs = [torch.empty(s.m // a.R, s.n, dtype=dt, device=dev) for _ in range(a.R)]
-            run = lambda: coc.matmul_reduce_scatter(dx, dw, outs, chunks=a.chunks)  # noqa: E731
+            run = lambda: coc.matmul_reduce_scatter(dx, dw, outs, chunks=a.chunks,  # noqa: E731
+                                                    deterministic=a.deterministic)
         else:
             out = torch.empty(s.m, s.n, dtype=dt, device=dev)
             run = lambda: coc.matmul(dx, dw, out)  # noqa: E731
