@@ -420,46 +420,46 @@ def time_context(ops, dev):
         out[op.name] = {"fused_ms": round(tf, 4), "all_gather_matmul_ms": round(t_ag, 4),
                         "plain_epilogue_ms": round(t_plain, 4), "fused_overhead": round(tf / t_plain - 1.0, 4),
                         "torch_unfused_ms": round(tu, 4)}
-    # The pages' Python-script CoC (CoC page, Python脚本层面实现): the left
-    # operand is cut along m into C chunks; each chunk's per-rank matmuls and
-    # reduction run on a compute stream while the previous chunk's
-    # "collective" (the reduced rows copied into every rank's buffer) runs on
-    # a second stream.  2 + R launches per chunk from the host.
+    # The pages' Python-script CoC (CoC page, Python脚本层面实现), module
+    # python_coc: each chunk's per-rank matmuls and reduction on a compute
+    # stream, its collective (copies into the rank buffers) on a second
+    # stream, 1 + 2R (AR/RS) or 2R + 1 (AG) host launches per chunk; against
+    # the fused kernel at the same chunk count.
+    from tensor_matmul_collective_gb300 import python_coc
+    streams = (torch.cuda.Stream(), torch.cuda.Stream())
+
+    def chunk_sweep(name, py, fused_call):
+        out[name] = {
+            "python_chunked_ms": {str(C): round(t(lambda C=C: py(C), 5), 4) for C in (1, 2, 4, 8)},
+            "fused_ms": {str(C): round(t(lambda C=C: fused_call(C)), 4) for C in (1, 2, 4, 8)}}
+
     ar7 = [o for o in ops if o.name == "bloom7b_ar"]
     if ar7:
         op = ar7[0]
         s = op.shape
         dx, dw = op.inputs[:s.R], op.inputs[s.R:2 * s.R]
         outs = op.outputs
-        comp, comm = torch.cuda.Stream(), torch.cuda.Stream()
-
-        def python_coc(C):
-            rows = s.m // C
-            cur = torch.cuda.current_stream()
-            comp.wait_stream(cur)
-            comm.wait_stream(cur)
-            for c in range(C):
-                sl = slice(c * rows, (c + 1) * rows)
-                with torch.cuda.stream(comp):
-                    acc = torch.matmul(dx[0][sl], dw[0]).float()
-                    for r in range(1, s.R):
-                        acc += torch.matmul(dx[r][sl], dw[r]).float()
-                    red = acc.to(s.dtype)
-                    ev = torch.cuda.Event()
-                    ev.record(comp)
-                with torch.cuda.stream(comm):
-                    comm.wait_event(ev)
-                    for r in range(s.R):
-                        outs[r][sl].copy_(red)
-                    red.record_stream(comm)
-            cur.wait_stream(comp)
-            cur.wait_stream(comm)
-        fused = {}
-        for C in (1, 2, 4, 8):
-            fused[C] = t(lambda C=C: coc.matmul_all_reduce(dx, dw, outs, chunks=C))
-        out["bloom7b_ar_python_chunking"] = {
-            "python_chunked_ms": {str(C): round(t(lambda C=C: python_coc(C), 5), 4) for C in (1, 2, 4, 8)},
-            "fused_ms": {str(C): round(v, 4) for C, v in fused.items()}}
+        chunk_sweep("bloom7b_ar_python_chunking",
+                    lambda C: python_coc.all_reduce(dx, dw, outs, C, *streams),
+                    lambda C: coc.matmul_all_reduce(dx, dw, outs, chunks=C))
+    rs = [o for o in ops if o.name == "llama70b_rs"]
+    if rs:
+        op = rs[0]
+        s = op.shape
+        dx, dw = op.inputs[:s.R], op.inputs[s.R:2 * s.R]
+        outs = op.outputs
+        chunk_sweep("llama70b_rs_python_chunking",
+                    lambda C: python_coc.reduce_scatter(dx, dw, outs, C, *streams),
+                    lambda C: coc.matmul_reduce_scatter(dx, dw, outs, chunks=C))
+    ag = [o for o in ops if o.kind == "ag_v2"]
+    if ag:
+        op = ag[0]
+        s = op.shape
+        dx, dw = op.inputs[:s.R], op.inputs[s.R:]
+        outs, gath = op.outputs[:s.R], op.outputs[s.R:2 * s.R]
+        chunk_sweep("llama70b_ag_v2_python_chunking",
+                    lambda C: python_coc.all_gather(dx, dw, outs, C, gath, *streams),
+                    lambda C: coc.all_gather_matmul_v2(dx, dw, outs, gath, chunks=C))
     out["next_rows"] = time_next_rows(ops, dev, t)
     return out
 
