@@ -500,7 +500,7 @@ def time_next_rows(ops, dev, t):
     w8 = [o for o in ops if o.kind == "w8a16_ar"]
     if w8:
         base = w8[0].shape
-        for dt, zero in ((torch.float16, True), (torch.bfloat16, False), (torch.bfloat16, True)):
+        for dt, zero in ((torch.float16, False), (torch.float16, True), (torch.bfloat16, False), (torch.bfloat16, True)):
             s = wl.W8A16(R=base.R, m=base.m, n=base.n, k_shard=base.k_shard, group=base.group, seed=base.seed,
                          dtype=dt)
             xs, wqs, scales = s.make("channel")
