@@ -726,12 +726,17 @@ def run_ours(args):
 
     e2e = None
     if args.e2e_steps > 0:
+        e2e_sampler = ClockSampler(bus)
+        e2e_sampler.start()
         wall, h2d, d2h = time_e2e(ops, args.e2e_steps, dev)
+        e2e_clocks = e2e_sampler.stop()
         wall_ms = max_over_ranks(wall * 1e3, dist, dev)
         e2e = {"value": job_value(step_flops, args.e2e_steps, world, wall_ms), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "h2d": "every operator's activation shards X_r from pinned host memory (weights resident)",
-               "d2h": "every distinct result tensor to pinned host memory"}
+               "d2h": "every distinct result tensor to pinned host memory",
+               # the SM clock of this leg (power-capped boxes settle differently per phase)
+               "sm_mhz": e2e_clocks["sm_mhz"] if e2e_clocks else None}
 
     context = None if args.no_context else time_context(ops, dev)
 
