@@ -48,10 +48,15 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--e2e-steps", type=int, default=30)
+    # the end-to-end leg runs as many steps as the timed region (30 at least),
+    # so that both legs see a power-capped GPU settle the same way
+    ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-context", action="store_true")
-    return ap.parse_args()
+    a = ap.parse_args()
+    if a.e2e_steps is None:
+        a.e2e_steps = max(30, a.steps)
+    return a
 
 
 def dist_env():
@@ -460,6 +465,21 @@ def time_context(ops, dev):
         chunk_sweep("llama70b_ag_v2_python_chunking",
                     lambda C: python_coc.all_gather(dx, dw, outs, C, gath, *streams),
                     lambda C: coc.all_gather_matmul_v2(dx, dw, outs, gath, chunks=C))
+    # the whole suite step captured once into a CUDA graph and replayed,
+    # against the same step launched eagerly (the host's launch cost)
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for op in ops:
+                op.run()
+        t_graph = t(g.replay, 20)
+        t_eager = t(lambda: [op.run() for op in ops], 20)
+        step_flops = sum(op.flops for op in ops)
+        out["suite_cuda_graph"] = {"graph_ms_per_step": round(t_graph, 4), "eager_ms_per_step": round(t_eager, 4),
+                                   "graph_tflops": round(step_flops / t_graph / 1e9, 1)}
+        del g
+    except RuntimeError as e:   # reported, not hidden: the operators are meant to be capturable
+        out["suite_cuda_graph"] = {"error": str(e)[:200]}
     out["next_rows"] = time_next_rows(ops, dev, t)
     return out
 

@@ -26,14 +26,19 @@
 //
 // Warp roles (one CTA per SM, persistent over work units):
 //   warp 0      TMA producer: A/B tiles into a STAGES-deep smem ring
-//   warp 1      TMEM owner + MMA issuer: tcgen05.mma 128x256x16, fp32 in TMEM
-//   warps 2-5   epilogue: tcgen05.ld -> round -> swizzled smem -> TMA store(s)
-//   warps 6-9   (w8A16 only) int8 -> fp16 dequantisation into the B stage
+//   warp 1      TMEM owner + MMA issuer: tcgen05.mma N=256, K=16, M=128 per CTA
+//               (M=256 over a cta_group::2 pair), fp32 accumulators in TMEM
+//   warps 2-5   epilogue: tcgen05.ld -> round -> swizzled smem -> TMA store and
+//               coalesced 16-byte stores to the other rank outputs
+//   warps 6-13  (w8A16 only) int8 -> fp16 dequantisation into the B stage, in
+//               two groups of 4 warps taking alternate k-blocks
 //
 // Every mbarrier wait is bounded (COC_WAIT_NS); a wait that runs out sets a
 // CTA-wide abort flag and the device status word, every role leaves its loop,
 // in-flight copies and MMAs are drained (again with bounded waits), TMEM is
 // freed and the kernel returns.
+#include <atomic>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -1052,12 +1057,25 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
     }
 }
 
+// The dynamic shared-memory limit of a kernel instance is raised once per
+// device (first launch there), not on every call: the call path then makes
+// only capture-safe API calls, so the operators can be recorded into CUDA
+// graphs after one eager call on the device.
+constexpr int kMaxDevices = 64;
+
 template <int OP, bool BF16, bool PAIR>
 cudaError_t launch_t(const KParams& p, int grid, cudaStream_t stream) {
     using C = Cfg<OP, PAIR>;
     auto kern = coc_fused_kernel<OP, BF16, PAIR>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    static std::atomic<unsigned char> smem_set[kMaxDevices];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices || !smem_set[dev].load(std::memory_order_acquire)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < kMaxDevices) smem_set[dev].store(1, std::memory_order_release);
+    }
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
