@@ -65,7 +65,12 @@
  *     bounded (about one second); a wait that runs out stops the kernel
  *     cleanly and records COC_ERR_TIMEOUT in the status buffer, which
  *     coc_sync_status() reports.  Results of a call that timed out are
- *     undefined.
+ *     undefined.  The bound is the build-time constant COC_WAIT_NS (ns);
+ *     raise it where the GPU is time-sliced between processes, since a
+ *     pause of the kernel counts against it.
+ *   - The first call on a device creates the library's per-device state
+ *     (status block, kernel attributes, workspace pool); after it, calls make
+ *     no synchronising CUDA call and can be captured into CUDA graphs.
  */
 #ifndef COC_H_
 #define COC_H_
