@@ -189,6 +189,20 @@ class Op:
         return self.outputs
 
 
+def algorithmic_bytes(op) -> int:
+    """Inputs read once plus outputs written once (every rank copy), bytes."""
+    s = op.shape
+    if op.kind in ("ar", "rs"):
+        out = s.R * s.m * s.n if op.kind == "ar" else s.m * s.n
+        return 2 * (s.m * s.K + s.K * s.n + out)
+    if op.kind == "ag_v2":
+        return 2 * (s.m * s.k + s.R * s.k * s.n_shard + s.R * s.m * s.n_shard + s.R * s.m * s.k)
+    if op.kind == "w8a16_ar":
+        scales = {"tensor": s.R, "channel": s.n, "group": (s.K // s.group) * s.n}[op.gran]
+        return 2 * s.m * s.K + s.K * s.n + 2 * scales + 2 * s.R * s.m * s.n
+    raise ValueError(op.kind)
+
+
 def build_suite(dev):
     """Device inputs/outputs for every operator of one step (inputs drawn on
     the host from the seeded generators, uploaded once)."""
@@ -425,6 +439,31 @@ def time_context(ops, dev):
         out[op.name] = {"fused_ms": round(tf, 4), "all_gather_matmul_ms": round(t_ag, 4),
                         "plain_epilogue_ms": round(t_plain, 4), "fused_overhead": round(tf / t_plain - 1.0, 4),
                         "torch_unfused_ms": round(tu, 4)}
+    # the unfused torch sequence for w8A16 (explicit dequantisation, then the
+    # AllReduce sequence), on the per-channel layer
+    w8c = [o for o in ops if o.name == "w8a16_ar_channel"]
+    w8t = [o for o in ops if o.name == "w8a16_ar_tensor"]
+    if w8c and w8t:
+        s = w8c[0].shape
+        dx, dq = w8t[0].inputs[:s.R], w8t[0].inputs[s.R:2 * s.R]
+        sc = w8c[0].inputs[0]
+
+        def w8_unfused(dx=dx, dq=dq, sc=sc, R=s.R):
+            wd = [(q.float() * sc.float()).half() for q in dq]
+            acc = torch.stack([torch.matmul(a, b) for a, b in zip(dx, wd)]).sum(0, dtype=torch.float32).half()
+            return [acc.clone() for _ in range(R)]
+        out["w8a16_ar_channel"] = {"fused_ms": round(t(w8c[0].run), 4), "torch_unfused_ms": round(t(w8_unfused, 3), 4)}
+    # the tiny AllReduce configuration (R = 2, 64 x 128 x 256 fp16, chunks 2):
+    # latency-bound, reported in microseconds per call
+    from tensor_matmul_collective_gb300 import workloads as wl
+    ts = wl.TINY_AR
+    txs, tws = ts.make()
+    tx, tw = [x.to(dev) for x in txs], [w.to(dev) for w in tws]
+    to = [torch.empty(ts.m, ts.n, dtype=ts.dtype, device=dev) for _ in range(ts.R)]
+    out["tiny_ar_r2_64x128_k256"] = {
+        "us_per_call": round(1e3 * t(lambda: coc.matmul_all_reduce(tx, tw, to, chunks=2), 200), 2),
+        "deterministic_us_per_call": round(1e3 * t(lambda: coc.matmul_all_reduce(tx, tw, to, chunks=2,
+                                                                                  deterministic=True), 200), 2)}
     # The pages' Python-script CoC (CoC page, Python脚本层面实现), module
     # python_coc: each chunk's per-rank matmuls and reduction on a compute
     # stream, its collective (copies into the rank buffers) on a second
@@ -741,7 +780,11 @@ def run_ours(args):
     chunks_of = {w.name: w.chunks for w in wl.TP8_SUITE}
     traffic = load_traffic(ops[dom].name, chunks_of.get(ops[dom].name, chunks_of.get("w8a16_ar", 1)))
     per_op_json = {op.name: {"ms": round(t, 4), "tflops": round(op.flops / (t / 1e3) / 1e12, 1),
-                             "frac_of_peak": round(op.flops / (t / 1e3) / 1e12 / peak, 4)}
+                             "frac_of_peak": round(op.flops / (t / 1e3) / 1e12 / peak, 4),
+                             # achieved algorithmic HBM bandwidth, against the measured copy bandwidth
+                             "algorithmic_gb": round(algorithmic_bytes(op) / 1e9, 4),
+                             "hbm_gbs": round(algorithmic_bytes(op) / (t / 1e3) / 1e9, 1),
+                             "hbm_frac": round(algorithmic_bytes(op) / (t / 1e3) / 1e9 / peaks["hbm_gbs"], 4)}
                    for op, t in zip(ops, per_op)}
 
     e2e = None
@@ -765,6 +808,7 @@ def run_ours(args):
         rows = 16
         t, flops, cores = oracle_sample(host, rows, None)
         cpu = {"value": flops / t / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "extrapolated_step_s": round(t * step_flops / flops, 1),
                "sample": f"{rows} seeded output rows (all columns) of every operator of one suite step "
                          f"({flops / 1e9:.1f} GFLOP in {t:.1f} s)"}
 
