@@ -504,6 +504,27 @@ def time_context(ops, dev):
         chunk_sweep("llama70b_ag_v2_python_chunking",
                     lambda C: python_coc.all_gather(dx, dw, outs, C, gath, *streams),
                     lambda C: coc.all_gather_matmul_v2(dx, dw, outs, gath, chunks=C))
+    # decode-sized AllReduce (8 ranks, n 8192, K 8 x 1024, bf16): weight-stream
+    # bound, so reported as us per call (20 calls replayed from a CUDA graph)
+    # and algorithmic HBM GB/s (W read once, X read, R output copies)
+    dec = {}
+    for m in (1, 16, 64, 128):
+        ds_ = wl.RowParallel(R=8, m=m, n=8192, k_shard=1024, dtype=torch.bfloat16, x_dist="normal(0,1)",
+                             w_dist="normal(0,0.02)", seed=1)
+        dxs, dws = ds_.make()
+        ddx, ddw = [x.to(dev) for x in dxs], [w.to(dev) for w in dws]
+        dout = [torch.empty(m, ds_.n, dtype=ds_.dtype, device=dev) for _ in range(ds_.R)]
+        coc.matmul_all_reduce(ddx, ddw, dout)
+        torch.cuda.synchronize()
+        gd = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gd):
+            for _ in range(20):
+                coc.matmul_all_reduce(ddx, ddw, dout)
+        us = 1e3 * t(gd.replay, 10) / 20
+        byts = 2 * (ds_.K * ds_.n + m * ds_.K + ds_.R * m * ds_.n)
+        dec[str(m)] = {"us_per_call": round(us, 1), "hbm_gbs": round(byts / us / 1e3, 0)}
+        del gd, ddx, ddw, dout
+    out["decode_ar_r8_n8192_k8192_cuda_graph"] = dec
     # the whole suite step captured once into a CUDA graph and replayed,
     # against the same step launched eagerly (the host's launch cost)
     try:

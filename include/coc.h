@@ -53,9 +53,13 @@
  *     (TMA requirement), see the per-call alignment notes.
  *   - Array-of-pointer arguments (`x`, `w`, `out`, ...) are HOST arrays of R
  *     device pointers, read before the call returns.
- *   - The library allocates nothing per call.  On the first call on a device
- *     it allocates a small status buffer (a few words) that coc_shutdown()
- *     frees.
+ *   - On the first call on a device the library allocates a small status
+ *     buffer (a few words) and creates a stream-ordered memory pool, both
+ *     released by coc_shutdown().  Per-call scratch comes from that pool,
+ *     allocated and freed on the call's stream (no call synchronises; the pool
+ *     keeps freed memory for reuse): the w8A16 pre-pass's dequantised weight,
+ *     the MoE routing tables, and the fp32 parts of a rank-split AllReduce /
+ *     ReduceScatter (below).  coc_matmul_all_reduce_noalloc takes none.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
  *     default stream).  Outputs must not alias inputs or each other.
  *   - Argument errors are detected on the host before any CUDA call and are
@@ -136,6 +140,17 @@ typedef struct CUstream_st* coc_stream_t;
  * Alignment: k_shard % 8 == 0 and n % 8 == 0 (16-byte rows), pointers 16-byte
  * aligned.  m, n, k_shard in [0, 2^31); m == 0 or n == 0 is a no-op and
  * k_shard == 0 writes zeros.
+ *
+ * Rank split (this call, coc_matmul_reduce_scatter, coc_matmul and
+ * coc_fused_matmul's AllReduce / ReduceScatter): for m <= 128 (decode-sized
+ * m) with at most half as many 128 x 256 output tiles as the GPU has SMs,
+ * each tile's R shards are cut into ksplit parts (the largest power of two
+ * dividing R that keeps tiles x ksplit within one wave), each a work unit of
+ * its own, and the parts' fp32 sums are added in part order 0..ksplit-1
+ * before the one rounding.  (Not for w8A16 or the no-alloc call.)
+ * ksplit depends on the shape and the GPU only, so results stay bitwise
+ * reproducible across calls and chunk counts; they can differ in the last
+ * bit from the same sums taken in one accumulator.
  */
 coc_status_t coc_matmul_all_reduce(int R, int64_t m, int64_t n, int64_t k_shard,
                                    const void* const* x, const void* const* w,

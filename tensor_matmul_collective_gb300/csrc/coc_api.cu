@@ -213,13 +213,40 @@ coc_status_t launch_checked(int op, bool bf16, bool pair, KParams& p, DeviceStat
     return COC_OK;
 }
 
+coc_status_t device_pool(DeviceState* ds, cudaMemPool_t* out);
+
+// Rank split (AllReduce, ReduceScatter, single-CTA tiles: m <= 128): with at
+// most half as many output tiles as SMs (decode-sized m), each tile's R shards
+// are cut into ksplit parts of R / ksplit shards, one work unit each, so the
+// weight stream is spread over ksplit times more SMs; ksplit is the largest
+// power of two dividing R that keeps the units within one wave.  It depends
+// on the shape only (never on chunks), so results stay bitwise
+// chunk-independent.  Measured (8 ranks, n 8192, k_shard 1024, bf16, one
+// call in a CUDA graph): m 1 / 16 / 64 / 128 take 48 / 42 / 42 / 49 us split
+// in 4 against 70 / 62 / 55 / 60 us unsplit; for 256-row tiles (m > 128)
+// splitting gained nothing (m 256: 54 us either way), so they are not split.
+int rank_split(int op, int R, int64_t ks, int64_t tiles, bool pair, int sm_count) {
+    int ksplit = 1;
+    if ((op == OP_AR || op == OP_RS) && ks > 0 && R > 1) {
+        const char* e = std::getenv("COC_KSPLIT");   // forces the part count (tuning and tests only)
+        if (e != nullptr) {
+            const int f = std::atoi(e);
+            while (ksplit * 2 <= f && ksplit < R) ksplit *= 2;
+            return ksplit;
+        }
+        if (pair) return 1;
+        while (ksplit < R && tiles * ksplit * 2 <= sm_count) ksplit *= 2;
+    }
+    return ksplit;
+}
+
 // ---- row-parallel family: AR, RS, W8, plain ----------------------------------
 // w_nk: each W shard is stored n x k_shard (Megatron's [out, in]) instead of
 // k_shard x n; the kernel then reads B K-major.
 coc_status_t row_parallel(int op, int R, int64_t m, int64_t n, int64_t ks, const void* const* x,
                           const void* const* w, void* const* out, int n_out, coc_dtype_t dt, int chunks,
                           const void* const* scale, coc_scale_t gran, int64_t group, cudaStream_t stream,
-                          bool w_nk = false, const void* const* zero = nullptr) {
+                          bool w_nk = false, const void* const* zero = nullptr, bool allow_split = true) {
     KParams p;
     std::memset(&p, 0, sizeof p);
     p.b_kmajor = w_nk ? 1 : 0;
@@ -286,7 +313,29 @@ coc_status_t row_parallel(int op, int R, int64_t m, int64_t n, int64_t ks, const
         for (int o = 0; o < n_out; ++o) p.outp[o] = static_cast<uint16_t*>(out[o]);
         p.replica_stores = 1;
     }
-    return launch_checked(op, dt == COC_BF16, pair, p, ds, stream);
+    const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
+    const int ksplit = allow_split ? rank_split(op, R, ks, tiles, pair, ds->sm_count) : 1;
+    if (ksplit == 1) return launch_checked(op, dt == COC_BF16, pair, p, ds, stream);
+
+    // rank split: fp32 parts and arrival counters in a stream-ordered workspace
+    p.ksplit = ksplit;
+    p.units = static_cast<int>(tiles * ksplit);
+    for (int o = 0; o < (op == OP_RS ? R : n_out); ++o) p.outp[o] = static_cast<uint16_t*>(out[o]);
+    const size_t part_bytes = static_cast<size_t>(tiles) * ksplit * tile_m * BN * sizeof(float);
+    const size_t cnt_bytes = static_cast<size_t>(tiles) * (pair ? 2 : 1) * NUM_EPI_WARPS * sizeof(unsigned);
+    cudaMemPool_t pool = nullptr;
+    if ((st = device_pool(ds, &pool)) != COC_OK) return st;
+    void* ws = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, part_bytes + cnt_bytes, pool, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMallocFromPoolAsync (rank-split parts)");
+    p.part = static_cast<float*>(ws);
+    p.part_cnt = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + part_bytes);
+    e = cudaMemsetAsync(p.part_cnt, 0, cnt_bytes, stream);
+    st = (e != cudaSuccess) ? cuda_fail(e, "cudaMemsetAsync (rank-split counters)")
+                            : launch_checked(op, dt == COC_BF16, pair, p, ds, stream);
+    const cudaError_t ef = cudaFreeAsync(ws, stream);
+    if (st == COC_OK && ef != cudaSuccess) st = cuda_fail(ef, "cudaFreeAsync (rank-split parts)");
+    return st;
 }
 
 coc_status_t validate_row_parallel(int R, int64_t m, int64_t n, int64_t ks, const void* const* x, const void* const* w,
@@ -376,7 +425,9 @@ coc_status_t w8_prepass_all_reduce(int R, int64_t m, int64_t n, int64_t ks, cons
     a.group = static_cast<int>(group);
     e = launch_w8_prepass(a, dt == COC_BF16, ds->sm_count, stream);
     if (e != cudaSuccess) st = cuda_fail(e, "w8A16 pre-pass launch");
-    else st = row_parallel(OP_AR, R, m, n, ks, x, wd, out, R, dt, chunks, nullptr, COC_SCALE_TENSOR, 0, stream);
+    // (unsplit, like the fused w8A16 kernel: both paths give the same bits)
+    else st = row_parallel(OP_AR, R, m, n, ks, x, wd, out, R, dt, chunks, nullptr, COC_SCALE_TENSOR, 0, stream, false,
+                           nullptr, false);
     const cudaError_t ef = cudaFreeAsync(ws, stream);
     if (st == COC_OK && ef != cudaSuccess) st = cuda_fail(ef, "cudaFreeAsync (w8A16 workspace)");
     return st;

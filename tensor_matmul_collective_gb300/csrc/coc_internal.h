@@ -73,6 +73,14 @@ struct KParams {
                                  // token r * gmm_T + t of each dispatched row, -1 for padding; NULL: no combine
     int gmm_T;                   // combine: tokens per rank
     int replica_stores; // AllReduce: write the n_out outputs with plain stores (outp) instead of TMA
+    // Split by rank (AllReduce / ReduceScatter with few output tiles): each
+    // tile's contraction is cut into ksplit unit-sized parts of R / ksplit
+    // shards each; a part's fp32 sum goes to part, and per epilogue-warp row
+    // slab the last part to arrive (part_cnt) adds the ksplit parts in order
+    // 0..ksplit-1 and writes the outputs.  ksplit <= 1: off.
+    int ksplit;
+    float* part;          // tiles x ksplit x TILE_M x BN fp32
+    unsigned* part_cnt;   // tiles x (CTAs per tile) x NUM_EPI_WARPS arrival counters, zero at launch
 };
 
 // Argument checks of coc_matmul_all_reduce and the per-thread error text

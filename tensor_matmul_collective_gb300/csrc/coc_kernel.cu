@@ -484,6 +484,24 @@ __device__ __forceinline__ void gather_slice_warp(const KParams& p, int r, int m
     }
 }
 
+// Rank split, end of a part: one epilogue warp has written its 32-row slab of
+// the part to the scratch.  Count the part; true for the warp whose part
+// completes the slab, which then adds the parts and stores the outputs.  No
+// warp waits for another: the last to arrive does the work, and the fences
+// make every counted part's writes visible to its reads.
+__device__ __forceinline__ bool split_last(const KParams& p, int ksplit, int tile_id, uint32_t rank, int q, int lane,
+                                           int npair) {
+    __threadfence();
+    __syncwarp();
+    unsigned* cnt = p.part_cnt + (static_cast<long long>(tile_id) * npair + rank) * NUM_EPI_WARPS + q;
+    unsigned prev = 0;
+    if (lane == 0) prev = atomicAdd(cnt, 1u);
+    prev = __shfl_sync(0xffffffffu, prev, 0);
+    const bool last = (prev == static_cast<unsigned>(ksplit - 1));
+    if (last) __threadfence();
+    return last;
+}
+
 // ------------------------------------------------------------ the kernel ---
 
 // Shared-memory rings.  AR/RS/AG: one ring of SA stages holding an A and a B
@@ -593,13 +611,17 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int total_kb = p.num_kshards * p.kblocks;
+    // split by rank: a unit is part u % ksplit of tile u / ksplit and sums
+    // R / ksplit shards (AllReduce / ReduceScatter only)
+    const int ksplit = ((OP == OP_AR || OP == OP_RS) && p.ksplit > 1) ? p.ksplit : 1;
+    const int unit_kb = total_kb / ksplit;   // k-blocks one unit accumulates
     // work units: fixed by the host, except for the grouped GEMM whose expert
     // group sizes the routing kernel wrote to device memory
     int n_units = p.units;
     if constexpr (OP == OP_GMM) n_units = gmm_units(p, TILE_M);
     auto decode = [&](int u, int& r, int& mt, int& nt) {
         if constexpr (OP == OP_GMM) gmm_decode(p, u, TILE_M, r, mt, nt);
-        else decode_unit<OP>(p, u, r, mt, nt);
+        else decode_unit<OP>(p, ksplit > 1 ? u / ksplit : u, r, mt, nt);
     };
 
     if (warp == 0) {
@@ -614,13 +636,14 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
         constexpr uint32_t kFullBytes = NPAIR * (A_STAGE_BYTES + (W8 ? 0 : C::B_BYTES));
         const uint64_t pol_a = make_l2_policy(p.a_hint), pol_b = make_l2_policy(p.b_hint);
         bool ok = true;
+        int ks_lo = 0, ks_hi = p.num_kshards;   // the unit's shards (all but with the rank split)
         // One unit's k-loop.  issue_a / issue_b put the unit's A and B boxes of
         // one k-block into a stage; they are chosen once per unit (below), so
         // the loop that runs per k-block has no layout branches: measured,
         // deciding the AllGather A-box layout inside this loop cost ~13% on the
         // LLaMA2-70B AG layer.
         auto unit_loop = [&](int col_base, auto&& issue_a, auto&& issue_b) {
-            for (int ks = 0; ok && ks < p.num_kshards; ++ks) {
+            for (int ks = ks_lo; ok && ks < ks_hi; ++ks) {
                 for (int kb = 0; kb < p.kblocks; ++kb) {
                     ok = warp_wait(smem_u32(&empty[stage]), phase ^ 1u, ctl, 0x100u + stage);
                     if (!ok) break;
@@ -661,6 +684,11 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
         for (int u = first_unit; ok && u < n_units; u += unit_step) {
             int r, mt, nt;
             decode(u, r, mt, nt);
+            if (ksplit > 1) {
+                const int per = p.num_kshards / ksplit;
+                ks_lo = (u % ksplit) * per;
+                ks_hi = ks_lo + per;
+            }
             const int row_base = mt * TILE_M + static_cast<int>(rank) * BM;   // this CTA's first A row
             const int col_base = nt * BN + static_cast<int>(rank) * C::BN_CTA;  // this CTA's first B column
             // A: one 128-row box (AllGather: from the shard holding the rows,
@@ -758,7 +786,7 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + buf * BN;
-                for (int i = 0; i < total_kb; ++i) {
+                for (int i = 0; i < unit_kb; ++i) {
                     ok = warp_wait<PAIR>(smem_u32(&full[stage]), phase, ctl, 0x210u + stage);
                     if (W8 && ok) ok = warp_wait<PAIR>(smem_u32(&bfull[bstage]), bphase, ctl, 0x220u + bstage);
                     if (!ok) break;
@@ -821,28 +849,19 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
             if (!ok) break;
             tc_fence_after();
             const int row0 = mt * TILE_M + static_cast<int>(rank) * BM + 32 * q;
+            const int tile_id = mt * p.n_tiles + nt;
+            const int part_s = (ksplit > 1) ? u % ksplit : 0;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + buf * BN;
-            for (int sub = 0; sub < BN / EPI_COLS; ++sub) {
-                uint32_t va[32], vb[32];
-                if (total_kb > 0) {
-                    tmem_ld_32cols(t_row + sub * EPI_COLS, va);
-                    tmem_ld_32cols(t_row + sub * EPI_COLS + 32, vb);
-                    tmem_wait_ld();
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) { va[i] = 0u; vb[i] = 0u; }
-                }
-                if (sub == BN / EPI_COLS - 1) {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) {
-                        const uint32_t ab = acce_base + buf * static_cast<uint32_t>(sizeof(uint64_t));
-                        if constexpr (PAIR) mbar_arrive_cluster(ab);
-                        else mbar_arrive(ab);
-                    }
-                }
+            // this warp's 32-row slab of part sp of the tile (rank split scratch)
+            auto part_slab = [&](int sp) {
+                return p.part + (((static_cast<long long>(tile_id) * ksplit + sp) * NPAIR + rank) * NUM_EPI_WARPS + q) *
+                                    (32LL * BN);
+            };
+            // Round one 32-row x 64-column sub-tile (fp32 bits, lane = row) and
+            // store it: staged once in swizzled shared memory, then the
+            // operator's stores.
+            auto emit = [&](int sub, const uint32_t (&va)[32], const uint32_t (&vb)[32]) {
                 const int col = nt * BN + sub * EPI_COLS;
-                if (col >= p.n || row0 >= p.m) continue;   // sub-tile entirely outside the output
                 uint8_t* sbuf = my_epi + (sb_i % C::EPI_NBUF) * EPI_BUF_BYTES;
                 ++sb_i;
                 // the stores that last read this buffer are done
@@ -932,7 +951,70 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
                         }
                     }
                 }
+            };
+            for (int sub = 0; sub < BN / EPI_COLS; ++sub) {
+                uint32_t va[32], vb[32];
+                if (unit_kb > 0) {
+                    tmem_ld_32cols(t_row + sub * EPI_COLS, va);
+                    tmem_ld_32cols(t_row + sub * EPI_COLS + 32, vb);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) { va[i] = 0u; vb[i] = 0u; }
+                }
+                if (sub == BN / EPI_COLS - 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        const uint32_t ab = acce_base + buf * static_cast<uint32_t>(sizeof(uint64_t));
+                        if constexpr (PAIR) mbar_arrive_cluster(ab);
+                        else mbar_arrive(ab);
+                    }
+                }
+                if (row0 >= p.m || nt * BN + sub * EPI_COLS >= p.n) continue;   // sub-tile outside the output
+                if (ksplit > 1) {
+                    // rank split: this part's fp32 sums into the slab's scratch, laid
+                    // out so that a warp access is 512 contiguous bytes
+                    float* dst = part_slab(part_s) + static_cast<long long>(sub) * (16 * 32 * 4) + lane * 4;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const uint32_t* v = (j < 8) ? (va + 4 * j) : (vb + 4 * (j - 8));
+                        *reinterpret_cast<uint4*>(dst + j * (32 * 4)) = make_uint4(v[0], v[1], v[2], v[3]);
+                    }
+                    continue;
+                }
+                emit(sub, va, vb);
                 __syncwarp();
+            }
+            if (ksplit > 1 && row0 < p.m && split_last(p, ksplit, tile_id, rank, q, lane, NPAIR)) {
+                // the last part of this slab to arrive: add the parts in part order
+                // (part 0 taken as is), then round and store as an unsplit tile
+                for (int sub = 0; sub < BN / EPI_COLS; ++sub) {
+                    if (nt * BN + sub * EPI_COLS >= p.n) break;
+                    uint32_t va[32], vb[32];
+                    const float* src = part_slab(0) + static_cast<long long>(sub) * (16 * 32 * 4) + lane * 4;
+                    const long long pstride = 32LL * BN * NUM_EPI_WARPS * NPAIR;   // between parts
+                    for (int sp = 0; sp < ksplit; ++sp, src += pstride) {
+                        float4 v[16];   // one part's 64 columns: all loads in flight together
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) v[j] = __ldcg(reinterpret_cast<const float4*>(src + j * (32 * 4)));
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            uint32_t* d = (j < 8) ? (va + 4 * j) : (vb + 4 * (j - 8));
+                            if (sp == 0) {
+                                d[0] = __float_as_uint(v[j].x); d[1] = __float_as_uint(v[j].y);
+                                d[2] = __float_as_uint(v[j].z); d[3] = __float_as_uint(v[j].w);
+                            } else {
+                                d[0] = __float_as_uint(__uint_as_float(d[0]) + v[j].x);
+                                d[1] = __float_as_uint(__uint_as_float(d[1]) + v[j].y);
+                                d[2] = __float_as_uint(__uint_as_float(d[2]) + v[j].z);
+                                d[3] = __float_as_uint(__uint_as_float(d[3]) + v[j].w);
+                            }
+                        }
+                    }
+                    emit(sub, va, vb);
+                    __syncwarp();
+                }
             }
             ++acc_i;
             if constexpr (OP == OP_AG) {
