@@ -64,8 +64,9 @@ def test_side_stream_orders_after_the_callers_work():
 
 
 def _graph_suite():
-    """Static buffers for AR, RS, AG-V2, w8A16 (pre-pass and fused paths) and
-    MoE top-2 with the gated combine, and a function that runs all of them."""
+    """Static buffers for AR, RS, AG-V2, w8A16 (pre-pass and fused paths),
+    MoE top-2 with the gated combine and a decode-sized AR, and a function
+    that runs all of them."""
     R = 4
     xs, ws = _rp(R, 512, 384, 256, BF16, 32)
     ar_x, ar_w = [x.to(DEV) for x in xs], [w.to(DEV) for w in ws]
@@ -90,8 +91,11 @@ def _graph_suite():
     mo_i, mo_g = [i.to(DEV) for i in ti], [g.to(DEV) for g in tg]
     mo_w = torch.stack(mws).to(DEV)
     mo = list(coc.moe_topk_grouped_matmul_combine(mo_x, mo_i, mo_g, mo_w, ms.e_loc))   # buffers
-    inputs = ar_x + ag_x + [t for m in w8 for t in w8[m][0]] + mo_x
-    outputs = ar_out + rs_out + ag_out + ag_g + [t for m in w8 for t in w8[m][3]] + mo[0] + [mo[3]]
+    dxs, dws = _rp(R, 16, 512, 128, BF16, 39)   # decode-sized: the rank-split path and its scratch
+    dec_x, dec_w = [x.to(DEV) for x in dxs], [w.to(DEV) for w in dws]
+    dec_out = [torch.empty(16, 512, dtype=BF16, device=DEV) for _ in range(R)]
+    inputs = ar_x + ag_x + [t for m in w8 for t in w8[m][0]] + mo_x + dec_x
+    outputs = ar_out + rs_out + ag_out + ag_g + [t for m in w8 for t in w8[m][3]] + mo[0] + [mo[3]] + dec_out
 
     def run():
         coc.matmul_all_reduce(ar_x, ar_w, ar_out, chunks=2)
@@ -102,6 +106,7 @@ def _graph_suite():
             coc.matmul_all_reduce_w8a16(x8, q8, c8, "group", 64, o8)
         coc.moe_topk_grouped_matmul_combine(mo_x, mo_i, mo_g, mo_w, ms.e_loc, xd=mo[2], y=mo[1], y_tok=mo[0],
                                             counts=mo[3], offsets=mo[4])
+        coc.matmul_all_reduce(dec_x, dec_w, dec_out)
     return run, inputs, outputs
 
 
