@@ -75,6 +75,12 @@
  *   - The first call on a device creates the library's per-device state
  *     (status block, kernel attributes, workspace pool); after it, calls make
  *     no synchronising CUDA call and can be captured into CUDA graphs.
+ *   - Environment variables that force a schedule (tuning and tests only;
+ *     every value gives correct results): COC_PAIR=0|1 (single-CTA or 2-SM
+ *     tiles), COC_W8_PATH=fused|prepass (w8A16 dequantisation inside the
+ *     GEMM kernel or in a pre-pass), COC_KSPLIT=<n> (rank-split part count,
+ *     rounded down to a power of two dividing R).  Forcing one can change
+ *     the last bit of results (a different summation grouping).
  */
 #ifndef COC_H_
 #define COC_H_
