@@ -133,6 +133,28 @@ def test_forced_part_counts(R, m, n, ks, forced, monkeypatch):
         assert torch.equal(torch.cat(rs, 0), outs[0])
 
 
+def test_split_nk_weights_match_kn_bits():
+    """Megatron's n x k weight storage takes the same split and gives the
+    same bits as k x n (the B operand read K-major instead of MN-major)."""
+    R, m, n, ks = 8, 16, 2048, 128
+    xs, ws = _data(R, m, n, ks, BF16, 17)
+    dx, dw = to_dev(xs), to_dev(ws)
+    wnk = [w.t().contiguous() for w in dw]
+    kn = coc.matmul_all_reduce(dx, dw)
+    nk = coc.fused_matmul("all_reduce", dx, wnk, w_layout="nk")
+    coc.sync_status()
+    for a, b in zip(kn, nk):
+        assert torch.equal(a, b)
+    m2 = 128   # ReduceScatter needs m / R in 8-row blocks
+    xs2, ws2 = _data(R, m2, n, ks, BF16, 18)
+    dx2, dw2 = to_dev(xs2), to_dev(ws2)
+    rs = coc.matmul_reduce_scatter(dx2, dw2)
+    rs_nk = coc.fused_matmul("reduce_scatter", dx2, [w.t().contiguous() for w in dw2], w_layout="nk")
+    coc.sync_status()
+    for a, b in zip(rs, rs_nk):
+        assert torch.equal(a, b)
+
+
 def test_r1_and_zero_k_are_not_split():
     xs, ws = _data(1, 16, 256, 64, BF16, 9)
     out = coc.matmul_all_reduce(to_dev(xs), to_dev(ws))
