@@ -155,9 +155,19 @@ def _prep(xs, ws):
     x0, w0 = xs[0], ws[0]
     if x0.dim() != 2 or w0.dim() != 2:
         raise ValueError("X and W shards must be 2-D")
-    if x0.device.type != "cuda":
-        raise ValueError("inputs must be CUDA tensors")
+    _check_device(x0)
     return R, x0, w0
+
+
+def _check_device(t):
+    """The library works on the current CUDA device: tensors of another one
+    would be addressed from the wrong context, so they are rejected here."""
+    if t.device.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    cur = torch.cuda.current_device()
+    if t.device.index is not None and t.device.index != cur:
+        raise ValueError(f"inputs are on {t.device} but the current device is cuda:{cur}; "
+                         f"call inside `with torch.cuda.device({t.device}):`")
 
 
 def _outs(outs, R, shape, dtype, device):
@@ -357,6 +367,7 @@ def moe_dispatch_grouped_matmul(xs, idxs, w, experts_per_rank: int, xd=None, y=N
     T, h = x0.shape
     if x0.dtype not in (torch.float16, torch.bfloat16):
         raise ValueError("tokens must be fp16 or bf16")
+    _check_device(x0)
     dt = x0.dtype
     _check_list(xs, "xs", (T, h), dt, x0.device)
     _check_list(idxs, "idxs", (T,), torch.int32, x0.device)
@@ -391,6 +402,7 @@ def moe_topk_grouped_matmul_combine(xs, idxs, gates, w, experts_per_rank: int, x
     T, h = x0.shape
     if x0.dtype not in (torch.float16, torch.bfloat16):
         raise ValueError("tokens must be fp16 or bf16")
+    _check_device(x0)
     dt = x0.dtype
     k = idxs[0].shape[1] if idxs[0].dim() == 2 else 1
     _check_list(xs, "xs", (T, h), dt, x0.device)
