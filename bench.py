@@ -404,6 +404,28 @@ def time_context(ops, dev):
         torch.cuda.synchronize()
         return a.elapsed_time(b) / it
 
+    def t_pair(fa, fb, it=16):
+        """Two calls timed alternately (a, b, b, a, ...) so that clock and
+        power drift hit both alike; trimmed means in ms."""
+        for _ in range(3):
+            fa()
+            fb()
+        torch.cuda.synchronize()
+        ev = {0: [], 1: []}
+        for i in range(it):
+            for k in ((0, 1) if i % 2 == 0 else (1, 0)):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                (fa if k == 0 else fb)()
+                b.record()
+                ev[k].append((a, b))
+        torch.cuda.synchronize()
+        res = []
+        for k in (0, 1):
+            ts = sorted(a.elapsed_time(b) for a, b in ev[k])[2:-2]
+            res.append(sum(ts) / len(ts))
+        return res
+
     out = {}
     for op in ops:
         if op.kind not in ("ar", "rs"):
@@ -414,8 +436,7 @@ def time_context(ops, dev):
             prev = [o for o in ops if o.name == "bloom176b_det_ar"][0]
             dx, dw = prev.inputs[:s.R], prev.inputs[s.R:2 * s.R]
         plain = torch.empty(s.m, s.n, dtype=s.dtype, device=dev)
-        tf = t(op.run)
-        tp = t(lambda: coc.matmul(dx, dw, plain))
+        tf, tp = t_pair(op.run, lambda: coc.matmul(dx, dw, plain))
 
         def unfused(dx=dx, dw=dw, R=s.R, kind=op.kind, m=s.m):
             acc = torch.stack([torch.matmul(a, b) for a, b in zip(dx, dw)]).sum(0, dtype=torch.float32).to(dx[0].dtype)
@@ -432,9 +453,8 @@ def time_context(ops, dev):
         dx, dw = op.inputs[:s.R], op.inputs[s.R:]
         outs = op.outputs[:s.R]
         xg = op.outputs[s.R]
-        tf = t(op.run)
+        tf, t_plain = t_pair(op.run, lambda: [coc.matmul([xg], [dw[r]], outs[r]) for r in range(s.R)])
         t_ag = t(lambda: coc.all_gather_matmul(dx, dw, outs, chunks=1))
-        t_plain = t(lambda: [coc.matmul([xg], [dw[r]], outs[r]) for r in range(s.R)])
         tu = t(lambda: [torch.matmul(torch.cat(dx, 0), dw[r]) for r in range(s.R)], 3)
         out[op.name] = {"fused_ms": round(tf, 4), "all_gather_matmul_ms": round(t_ag, 4),
                         "plain_epilogue_ms": round(t_plain, 4), "fused_overhead": round(tf / t_plain - 1.0, 4),
