@@ -24,6 +24,11 @@
 // one tile's epilogue (the "communication") run while the next tile's
 // mainloop runs.
 //
+// At decode-sized m (few output tiles) AllReduce and ReduceScatter cut each
+// tile's R shards into groups run as separate units (the rank split); the
+// epilogue warp whose group completes a row slab adds the groups' fp32 sums
+// in group order and stores the slab.
+//
 // Warp roles (one CTA per SM, persistent over work units):
 //   warp 0      TMA producer: A/B tiles into a STAGES-deep smem ring
 //   warp 1      TMEM owner + MMA issuer: tcgen05.mma N=256, K=16, M=128 per CTA
