@@ -1,0 +1,109 @@
+"""Seeded random shapes for every operator against the fp64 oracle.
+
+Each case draws the rank count, sizes (ragged against the 128 / 256-row,
+256-column and 64-deep tiles, from decode-sized m to several tiles), dtype
+and chunk count from a fixed seed, within the operators' documented
+constraints, so that unit decoding, the 2-SM / single-CTA choice, the rank
+split, row groups and chunk orders meet combinations the hand-picked cases
+do not."""
+import random
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle as orc
+from tensor_matmul_collective_gb300 import coc
+from tensor_matmul_collective_gb300 import workloads as wl
+
+from gpu_util import assert_close, bits, to_dev
+
+pytestmark = pytest.mark.gpu
+BF16, F16 = torch.bfloat16, torch.float16
+CODE = {F16: orc.F16, BF16: orc.BF16}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from tensor_matmul_collective_gb300 import build
+    build.build()
+    coc.lib()
+    yield
+    coc.sync_status()
+
+
+def _chunks(rng, m):
+    return rng.choice([c for c in (1, 2, 4, 8) if m % c == 0])
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_random_row_parallel(seed):
+    rng = random.Random(1000 + seed)
+    R = rng.choice([1, 2, 4, 8])
+    dt = rng.choice([BF16, F16])
+    n = 8 * rng.randint(1, 80)                       # up to 640 columns
+    ks = 8 * rng.randint(1, 40)                      # up to 320 per shard
+    m = rng.choice([1, 8, 16, 64, 100, 128, 136, 200, 256, 264, 384, 520])
+    xs, ws = wl.RowParallel(R=R, m=m, n=n, k_shard=ks, dtype=dt, x_dist="normal(0,1)", w_dist="normal(0,0.02)",
+                            seed=seed).make()
+    dx, dw = to_dev(xs), to_dev(ws)
+    c = _chunks(rng, m)
+    det = rng.random() < 0.5
+    outs = coc.matmul_all_reduce(dx, dw, chunks=c, deterministic=det)
+    coc.sync_status()
+    ref = orc.matmul_all_reduce(CODE[dt], bits(xs), bits(ws))
+    what = f"AR R={R} m={m} n={n} ks={ks} {dt} chunks={c}"
+    for r in range(R):
+        assert_close(outs[r], ref, R * ks, what)
+        assert torch.equal(outs[r], outs[0])
+    if m % (8 * R) == 0:                             # ReduceScatter: m / R in 8-row blocks
+        rs = coc.matmul_reduce_scatter(dx, dw, chunks=c, deterministic=det)
+        coc.sync_status()
+        assert torch.equal(torch.cat(rs, 0), outs[0]), what + " RS concat"
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_all_gather_v2(seed):
+    rng = random.Random(2000 + seed)
+    R = rng.choice([1, 2, 4, 8])
+    dt = rng.choice([BF16, F16])
+    ms = rng.choice([8, 16, 24, 64, 72, 128, 136])
+    ns = 8 * rng.randint(1, 48)
+    k = 8 * rng.randint(1, 40)
+    s = wl.ColumnParallelSP(R=R, m_shard=ms, n_shard=ns, k=k, dtype=dt, x_dist="normal(0,1)",
+                            w_dist="normal(0,0.02)", seed=seed)
+    xs, ws = s.make()
+    c = _chunks(rng, R * ms)
+    outs, gathered = coc.all_gather_matmul_v2(to_dev(xs), to_dev(ws), chunks=c)
+    coc.sync_status()
+    xg = orc.all_gather(bits(xs))
+    what = f"AG-V2 R={R} ms={ms} ns={ns} k={k} {dt} chunks={c}"
+    for r in range(R):
+        assert_close(outs[r], orc.all_gather_matmul(CODE[dt], bits(xs), bits(ws), r), k, what)
+        assert np.array_equal(wl.bits16(gathered[r].cpu()), xg), what + " gathered"
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_random_w8a16(seed):
+    rng = random.Random(3000 + seed)
+    R = rng.choice([1, 2, 4, 8])
+    group = rng.choice([64, 128])
+    ks = group * rng.randint(1, 3)
+    n = 16 * rng.randint(1, 24)
+    m = rng.choice([1, 16, 100, 128, 200, 264])
+    gran = rng.choice(["tensor", "channel", "group"])
+    dt = rng.choice([F16, BF16])
+    zero = rng.random() < 0.5
+    s = wl.W8A16(R=R, m=m, n=n, k_shard=ks, group=group, seed=seed, dtype=dt)
+    xs, wqs, scales = s.make(gran)
+    zs = s.zeros(gran) if zero else None
+    outs = coc.matmul_all_reduce_w8a16(to_dev(xs), to_dev(wqs), to_dev(scales), gran, group,
+                                       zeros=to_dev(zs) if zs is not None else None, chunks=_chunks(rng, m))
+    coc.sync_status()
+    code = {"tensor": 0, "channel": 1, "group": 2}[gran]
+    ref = orc.matmul_all_reduce_w8a16(bits(xs), [w.numpy() for w in wqs], bits(scales), code, group,
+                                      zeros=[z.numpy() for z in zs] if zs is not None else None, dtype=CODE[dt])
+    for r in range(R):
+        assert_close(outs[r], ref, s.K, f"w8A16 R={R} m={m} n={n} ks={ks} {gran} {dt} zero={zero}")
