@@ -1,4 +1,5 @@
-"""Seeded random shapes for every operator against the fp64 oracle.
+"""Seeded random shapes for every operator against the fp64 oracle (AllReduce,
+ReduceScatter, AllGather-V2, w8A16, MoE dispatch + GroupedMatMul + combine).
 
 Each case draws the rank count, sizes (ragged against the 128 / 256-row,
 256-column and 64-deep tiles, from decode-sized m to several tiles), dtype
@@ -107,3 +108,32 @@ def test_random_w8a16(seed):
                                       zeros=[z.numpy() for z in zs] if zs is not None else None, dtype=CODE[dt])
     for r in range(R):
         assert_close(outs[r], ref, s.K, f"w8A16 R={R} m={m} n={n} ks={ks} {gran} {dt} zero={zero}")
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_random_moe(seed):
+    """MoE dispatch + GroupedMatMul + combine: top-1 through the fused combine,
+    top-2 / top-3 through the gated combine."""
+    rng = random.Random(4000 + seed)
+    R = rng.choice([1, 2, 4, 8])
+    e_loc = rng.choice([1, 2, 3, 4])
+    T = rng.randint(1, 300)
+    h = 64 * rng.randint(1, 4)                       # the operator takes h in 64-column steps
+    f = 8 * rng.randint(1, 40)
+    dt = rng.choice([BF16, F16])
+    k = min(rng.choice([1, 1, 2, 3]), R * e_loc)   # k distinct experts
+    s = wl.MoEDispatch(R=R, T=T, h=h, f=f, e_loc=e_loc, seed=seed, dtype=dt)
+    xs, idxs, ws = s.make()
+    dx, w = to_dev(xs), torch.stack(ws).cuda()
+    what = f"MoE R={R} T={T} h={h} f={f} e_loc={e_loc} top-{k} {dt}"
+    if k == 1:
+        y, _, _, _ = coc.moe_dispatch_grouped_matmul(dx, to_dev(idxs), w, e_loc, combine=True)
+        coc.sync_status()
+        ref = orc.moe_token_outputs(CODE[dt], bits(xs), [i.numpy() for i in idxs], bits(ws))
+    else:
+        ti, tg = s.routing_topk(k)
+        y, _, _, _, _ = coc.moe_topk_grouped_matmul_combine(dx, to_dev(ti), to_dev(tg), w, e_loc)
+        coc.sync_status()
+        ref = orc.moe_topk_combine(CODE[dt], bits(xs), [i.numpy() for i in ti], [g.numpy() for g in tg], bits(ws))
+    for r in range(R):
+        assert_close(y[r], ref[r], h, what)
