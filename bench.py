@@ -16,6 +16,7 @@ value = algorithmic FLOPs (2 m n K per operator) of all steps on all ranks /
 wall time of the timed steps (CUDA events, max over ranks), in TFLOP/s.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py --case ar|rs|ag|ag_v2|w8a16|plain|moe --m M --n N --k K [...]   (one operator)
 
 Under torchrun (N > 1) every rank runs the whole suite on its own GPU
 (replicas; the path has no cross-GPU exchange), rank 0 prints the line.
@@ -53,6 +54,22 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-context", action="store_true")
+    # --case: one operator on seeded synthetic data of a chosen size, timed
+    # over --iters calls (the command the profiles/ captures run)
+    ap.add_argument("--case", choices=["ar", "rs", "ag", "ag_v2", "w8a16", "plain", "moe"], default=None)
+    ap.add_argument("--R", type=int, default=8)
+    ap.add_argument("--m", type=int, help="rows (ar/rs/w8a16/plain: m; ag/ag_v2: m_shard; moe: tokens per rank)")
+    ap.add_argument("--n", type=int, help="columns (ag/ag_v2: n_shard; moe: f)")
+    ap.add_argument("--k", type=int, help="contraction per shard (ag/ag_v2: full k; moe: h)")
+    ap.add_argument("--dtype", choices=["bf16", "fp16"], default="bf16")
+    ap.add_argument("--chunks", type=int, default=1)
+    ap.add_argument("--gran", choices=["tensor", "channel", "group"], default="group")
+    ap.add_argument("--group", type=int, default=128)
+    ap.add_argument("--iters", type=int, default=3)
+    ap.add_argument("--zero", action="store_true", help="w8a16: int8 zero points")
+    ap.add_argument("--eloc", type=int, default=1, help="moe: experts per rank")
+    ap.add_argument("--topk", type=int, default=1, help="moe: routing slots (gated combine if > 1)")
+    ap.add_argument("--deterministic", action="store_true")
     a = ap.parse_args()
     if a.e2e_steps is None:
         a.e2e_steps = max(30, a.steps)
@@ -87,8 +104,10 @@ def load_peaks():
     if os.path.exists(path):
         d = json.load(open(path))
         return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
-                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
-    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "sustained_sm_mhz": (d.get("clocks_under_load") or {}).get("sm_mhz_median"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "sustained_sm_mhz": None,
+            "source": "fallback"}
 
 
 def kernel_source_hash() -> str:
@@ -116,7 +135,90 @@ def load_traffic(op: str, chunks: int):
 
 # ------------------------------------------------------------------ clocks ---
 
-class ClockSampler:
+class NvmlSampler:
+    """SM clock, power draw and clock-event reasons of one GPU, sampled
+    through NVML (libnvidia-ml, reached with ctypes; read-only queries)
+    every `period_s` seconds by a background thread while the timed region
+    runs.  Falls back to `nvidia-smi -lms 100` where NVML cannot be loaded."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, bus_id: str | None, index: int = 0, period_s: float = 0.005):
+        self.bus, self.index, self.period = bus_id, index, period_s
+        self.samples, self.thread, self.stop_evt, self.lib, self.handle = [], None, None, None, None
+        self.fallback = None
+        self.max_mhz = None
+
+    def _open(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit_v2 failed")
+        h = ctypes.c_void_p()
+        ok = False
+        if self.bus:
+            for fmt in (self.bus, "0000" + self.bus):
+                if lib.nvmlDeviceGetHandleByPciBusId_v2(fmt.encode(), ctypes.byref(h)) == 0:
+                    ok = True
+                    break
+        if not ok and lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.index), ctypes.byref(h)) != 0:
+            raise OSError("no NVML handle")
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+            self.max_mhz = float(mx.value)
+        self.lib, self.handle = lib, h
+        self.reason_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+
+    def _loop(self):
+        import ctypes
+        mhz, mw, mask = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        i = 0
+        while not self.stop_evt.is_set():
+            t = time.perf_counter()
+            a = self.lib.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(mhz))
+            b = self.reason_fn(self.handle, ctypes.byref(mask))
+            p = self.lib.nvmlDeviceGetPowerUsage(self.handle, ctypes.byref(mw)) if i % 10 == 0 else 1
+            self.samples.append((t, mhz.value if a == 0 else None, mask.value if b == 0 else None,
+                                 mw.value / 1000.0 if p == 0 else None))
+            i += 1
+            self.stop_evt.wait(self.period)
+
+    def start(self):
+        import threading
+        try:
+            self._open()
+        except (OSError, AttributeError):
+            self.fallback = SmiSampler(self.bus)
+            self.fallback.start()
+            return
+        self.samples, self.stop_evt = [], threading.Event()
+        self.thread = threading.Thread(target=self._loop, daemon=True)
+        self.thread.start()
+
+    def stop(self):
+        if self.fallback is not None:
+            return self.fallback.stop()
+        if self.thread is None:
+            return None
+        self.stop_evt.set()
+        self.thread.join()
+        try:
+            self.lib.nvmlShutdown()
+        except Exception:
+            pass
+        sm = [x[1] for x in self.samples if x[1] is not None]
+        reasons = sorted({name for x in self.samples if x[2] is not None
+                          for bit, name in self.REASONS.items() if x[2] & bit})
+        power = [x[3] for x in self.samples if x[3] is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples": len(sm), "sm_mhz_min": min(sm) if sm else None, "sm_mhz_max": max(sm) if sm else None,
+                "power_w_max": max(power) if power else None,
+                "sampler": f"NVML in-process, every {self.period * 1e3:.0f} ms"}
+
+
+class SmiSampler:
     FIELDS = ("pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -124,7 +226,6 @@ class ClockSampler:
     def __init__(self, bus_id: str | None):
         self.bus = (bus_id or "").lower()
         self.proc = None
-        self.lines = []
 
     def start(self):
         try:
@@ -154,7 +255,8 @@ class ClockSampler:
         reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
         power = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows), "power_w_max": max(power) if power else None}
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(power) if power else None,
+                "sampler": "nvidia-smi -lms 100"}
 
 
 # ------------------------------------------------------------------- suite ---
@@ -306,20 +408,28 @@ def time_device(ops, steps, warmup, dist, sampler):
     sampler.start()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
+    for i in range(len(ops)):
+        coc.clock_read(i)            # clear the in-kernel clock slots
     t_start.record(stream)
     for s in range(steps):
         ev[s][0].record(stream)
         for i, op in enumerate(ops):
+            coc.clock_probe(i)       # host-side flag: this operator's kernels record into slot i
             op.run()
             ev[s][i + 1].record(stream)
     t_end.record(stream)
+    coc.clock_probe(-1)
     torch.cuda.synchronize()
     clocks = sampler.stop()
+    mhz = [coc.clock_mhz(i) for i in range(len(ops))]
+    if clocks is not None:
+        clocks["sm_mhz_in_kernel"] = {op.name: m for op, m in zip(ops, mhz)}
     if dist is not None:
         dist.barrier()
     coc.sync_status()
     total_ms = t_start.elapsed_time(t_end)
-    per_op = [statistics.mean(ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(steps)) for i in range(len(ops))]
+    # every operator's time in every timed step (events recorded between launches)
+    per_op = [[ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(steps)] for i in range(len(ops))]
     return total_ms, per_op, clocks
 
 
@@ -384,49 +494,65 @@ def time_e2e(ops, steps, dev):
     return wall, h2d, d2h
 
 
-def time_context(ops, dev):
-    """Context numbers measured outside the timed region: the same contraction
-    with a plain one-buffer epilogue (fused overhead) and the unfused torch
-    sequence (per-shard torch.matmul, then a separate reduction/copy)."""
+def interleaved(fns: dict, it: int = 20, warm: int = 3) -> dict:
+    """The one timing protocol of every context figure: each call of `fns`
+    (name -> callable) is bracketed by its own CUDA events on the current
+    stream, and the calls are taken round-robin (a, b, c, a, b, c, ...) so
+    that clock and power drift under the power cap hit every variant alike.
+    Returns {name: {"median_ms", "min_ms", "max_ms"}} over `it` calls each,
+    after `warm` untimed rounds."""
     import torch
 
     from tensor_matmul_collective_gb300 import coc
 
-    def t(fn, it=10):
-        for _ in range(3):
-            fn()
-        torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        for _ in range(it):
-            fn()
-        b.record()
-        torch.cuda.synchronize()
-        return a.elapsed_time(b) / it
-
-    def t_pair(fa, fb, it=16):
-        """Two calls timed alternately (a, b, b, a, ...) so that clock and
-        power drift hit both alike; trimmed means in ms."""
-        for _ in range(3):
-            fa()
-            fb()
-        torch.cuda.synchronize()
-        ev = {0: [], 1: []}
-        for i in range(it):
-            for k in ((0, 1) if i % 2 == 0 else (1, 0)):
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record()
-                (fa if k == 0 else fb)()
-                b.record()
-                ev[k].append((a, b))
-        torch.cuda.synchronize()
-        res = []
-        for k in (0, 1):
-            ts = sorted(a.elapsed_time(b) for a, b in ev[k])[2:-2]
-            res.append(sum(ts) / len(ts))
-        return res
-
+    names = list(fns)
+    for _ in range(warm):
+        for n in names:
+            fns[n]()
+    torch.cuda.synchronize()
+    probe = len(names) <= 8          # one in-kernel clock slot per variant
+    if probe:
+        for j in range(len(names)):
+            coc.clock_read(j)
+    ev = {n: [] for n in names}
+    for i in range(it):
+        order = names if i % 2 == 0 else names[::-1]
+        for n in order:
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            if probe:
+                coc.clock_probe(names.index(n))
+            a.record()
+            fns[n]()
+            b.record()
+            ev[n].append((a, b))
+    coc.clock_probe(-1)
+    torch.cuda.synchronize()
     out = {}
+    for j, n in enumerate(names):
+        ts = [a.elapsed_time(b) for a, b in ev[n]]
+        out[n] = {"median_ms": round(statistics.median(ts), 4), "min_ms": round(min(ts), 4),
+                  "max_ms": round(max(ts), 4)}
+        if probe:
+            out[n]["sm_mhz_in_kernel"] = coc.clock_mhz(j)
+    return out
+
+
+def time_context(ops, dev, bus=None, index=0):
+    """Context numbers measured outside the timed region, all with the same
+    protocol (interleaved, per-call CUDA events, median and min): each
+    operator against the same kernel with a plain one-buffer epilogue (fused
+    overhead) and against the unfused torch sequence (per-shard torch.matmul,
+    then a separate reduction / copy); the Python-script chunking against the
+    fused kernel at C = 1/2/4/8; a decode-sized AllReduce; the suite as one
+    CUDA graph; and the rows built beyond the suite."""
+    import torch
+
+    from tensor_matmul_collective_gb300 import coc
+
+    sampler = NvmlSampler(bus, index)
+    sampler.start()
+    out = {"protocol": "interleaved round-robin calls, each between its own CUDA events; median / min of 20 "
+                       "calls per variant after 3 untimed rounds (torch and Python-chunked sequences: 6 calls)"}
     for op in ops:
         if op.kind not in ("ar", "rs"):
             continue
@@ -436,16 +562,17 @@ def time_context(ops, dev):
             prev = [o for o in ops if o.name == "bloom176b_det_ar"][0]
             dx, dw = prev.inputs[:s.R], prev.inputs[s.R:2 * s.R]
         plain = torch.empty(s.m, s.n, dtype=s.dtype, device=dev)
-        tf, tp = t_pair(op.run, lambda: coc.matmul(dx, dw, plain))
 
         def unfused(dx=dx, dw=dw, R=s.R, kind=op.kind, m=s.m):
             acc = torch.stack([torch.matmul(a, b) for a, b in zip(dx, dw)]).sum(0, dtype=torch.float32).to(dx[0].dtype)
             if kind == "ar":
                 return [acc.clone() for _ in range(R)]
             return [acc[r * (m // R):(r + 1) * (m // R)].clone() for r in range(R)]
-        tu = t(unfused, 3)
-        out[op.name] = {"fused_ms": round(tf, 4), "plain_epilogue_ms": round(tp, 4),
-                        "fused_overhead": round(tf / tp - 1.0, 4), "torch_unfused_ms": round(tu, 4)}
+        r = interleaved({"fused": op.run, "plain": lambda dx=dx, dw=dw, o=plain: coc.matmul(dx, dw, o)})
+        u = interleaved({"torch": unfused}, it=6)
+        out[op.name] = {"fused_ms": r["fused"], "plain_epilogue_ms": r["plain"],
+                        "fused_overhead": round(r["fused"]["median_ms"] / r["plain"]["median_ms"] - 1.0, 4),
+                        "torch_unfused_ms": u["torch"]}
     ag = [o for o in ops if o.kind == "ag_v2"]
     if ag:
         op = ag[0]
@@ -453,12 +580,14 @@ def time_context(ops, dev):
         dx, dw = op.inputs[:s.R], op.inputs[s.R:]
         outs = op.outputs[:s.R]
         xg = op.outputs[s.R]
-        tf, t_plain = t_pair(op.run, lambda: [coc.matmul([xg], [dw[r]], outs[r]) for r in range(s.R)])
-        t_ag = t(lambda: coc.all_gather_matmul(dx, dw, outs, chunks=1))
-        tu = t(lambda: [torch.matmul(torch.cat(dx, 0), dw[r]) for r in range(s.R)], 3)
-        out[op.name] = {"fused_ms": round(tf, 4), "all_gather_matmul_ms": round(t_ag, 4),
-                        "plain_epilogue_ms": round(t_plain, 4), "fused_overhead": round(tf / t_plain - 1.0, 4),
-                        "torch_unfused_ms": round(tu, 4)}
+        r = interleaved({"fused_v2": op.run,
+                         "plain": lambda: [coc.matmul([xg], [dw[q]], outs[q]) for q in range(s.R)],
+                         "all_gather_matmul": lambda: coc.all_gather_matmul(dx, dw, outs, chunks=1)})
+        u = interleaved({"torch": lambda: [torch.matmul(torch.cat(dx, 0), dw[q]) for q in range(s.R)]}, it=6)
+        out[op.name] = {"fused_ms": r["fused_v2"], "all_gather_matmul_ms": r["all_gather_matmul"],
+                        "plain_epilogue_ms": r["plain"],
+                        "fused_overhead": round(r["fused_v2"]["median_ms"] / r["plain"]["median_ms"] - 1.0, 4),
+                        "torch_unfused_ms": u["torch"]}
     # the unfused torch sequence for w8A16 (explicit dequantisation, then the
     # AllReduce sequence), on the per-channel layer
     w8c = [o for o in ops if o.name == "w8a16_ar_channel"]
@@ -472,7 +601,9 @@ def time_context(ops, dev):
             wd = [(q.float() * sc.float()).half() for q in dq]
             acc = torch.stack([torch.matmul(a, b) for a, b in zip(dx, wd)]).sum(0, dtype=torch.float32).half()
             return [acc.clone() for _ in range(R)]
-        out["w8a16_ar_channel"] = {"fused_ms": round(t(w8c[0].run), 4), "torch_unfused_ms": round(t(w8_unfused, 3), 4)}
+        r = interleaved({"fused": w8c[0].run})
+        u = interleaved({"torch": w8_unfused}, it=6)
+        out["w8a16_ar_channel"] = {"fused_ms": r["fused"], "torch_unfused_ms": u["torch"]}
     # the tiny AllReduce configuration (R = 2, 64 x 128 x 256 fp16, chunks 2):
     # latency-bound, reported in microseconds per call
     from tensor_matmul_collective_gb300 import workloads as wl
@@ -480,10 +611,10 @@ def time_context(ops, dev):
     txs, tws = ts.make()
     tx, tw = [x.to(dev) for x in txs], [w.to(dev) for w in tws]
     to = [torch.empty(ts.m, ts.n, dtype=ts.dtype, device=dev) for _ in range(ts.R)]
-    out["tiny_ar_r2_64x128_k256"] = {
-        "us_per_call": round(1e3 * t(lambda: coc.matmul_all_reduce(tx, tw, to, chunks=2), 200), 2),
-        "deterministic_us_per_call": round(1e3 * t(lambda: coc.matmul_all_reduce(tx, tw, to, chunks=2,
-                                                                                  deterministic=True), 200), 2)}
+    r = interleaved({"det0": lambda: coc.matmul_all_reduce(tx, tw, to, chunks=2),
+                     "det1": lambda: coc.matmul_all_reduce(tx, tw, to, chunks=2, deterministic=True)}, it=200)
+    out["tiny_ar_r2_64x128_k256"] = {"us_per_call_median": round(1e3 * r["det0"]["median_ms"], 2),
+                                     "deterministic_us_per_call_median": round(1e3 * r["det1"]["median_ms"], 2)}
     # The pages' Python-script CoC (CoC page, Python脚本层面实现), module
     # python_coc: each chunk's per-rank matmuls and reduction on a compute
     # stream, its collective (copies into the rank buffers) on a second
@@ -493,9 +624,10 @@ def time_context(ops, dev):
     streams = (torch.cuda.Stream(), torch.cuda.Stream())
 
     def chunk_sweep(name, py, fused_call):
-        out[name] = {
-            "python_chunked_ms": {str(C): round(t(lambda C=C: py(C), 5), 4) for C in (1, 2, 4, 8)},
-            "fused_ms": {str(C): round(t(lambda C=C: fused_call(C)), 4) for C in (1, 2, 4, 8)}}
+        r = interleaved({f"py{C}": (lambda C=C: py(C)) for C in (1, 2, 4, 8)}, it=6)
+        f = interleaved({f"fused{C}": (lambda C=C: fused_call(C)) for C in (1, 2, 4, 8)})
+        out[name] = {"python_chunked_ms": {str(C): r[f"py{C}"]["median_ms"] for C in (1, 2, 4, 8)},
+                     "fused_ms": {str(C): f[f"fused{C}"]["median_ms"] for C in (1, 2, 4, 8)}}
 
     ar7 = [o for o in ops if o.name == "bloom7b_ar"]
     if ar7:
@@ -527,7 +659,7 @@ def time_context(ops, dev):
     # decode-sized AllReduce (8 ranks, n 8192, K 8 x 1024, bf16): weight-stream
     # bound, so reported as us per call (20 calls replayed from a CUDA graph)
     # and algorithmic HBM GB/s (W read once, X read, R output copies)
-    dec = {}
+    graphs, keep, byts = {}, [], {}
     for m in (1, 16, 64, 128):
         ds_ = wl.RowParallel(R=8, m=m, n=8192, k_shard=1024, dtype=torch.bfloat16, x_dist="normal(0,1)",
                              w_dist="normal(0,0.02)", seed=1)
@@ -540,11 +672,14 @@ def time_context(ops, dev):
         with torch.cuda.graph(gd):
             for _ in range(20):
                 coc.matmul_all_reduce(ddx, ddw, dout)
-        us = 1e3 * t(gd.replay, 10) / 20
-        byts = 2 * (ds_.K * ds_.n + m * ds_.K + ds_.R * m * ds_.n)
-        dec[str(m)] = {"us_per_call": round(us, 1), "hbm_gbs": round(byts / us / 1e3, 0)}
-        del gd, ddx, ddw, dout
-    out["decode_ar_r8_n8192_k8192_cuda_graph"] = dec
+        graphs[str(m)] = gd.replay
+        keep.append((gd, ddx, ddw, dout))
+        byts[str(m)] = 2 * (ds_.K * ds_.n + m * ds_.K + ds_.R * m * ds_.n)
+    r = interleaved(graphs, it=10)
+    out["decode_ar_r8_n8192_k8192_cuda_graph"] = {
+        m: {"us_per_call": round(1e3 * r[m]["median_ms"] / 20, 1),
+            "hbm_gbs": round(byts[m] / (1e3 * r[m]["median_ms"] / 20) / 1e3, 0)} for m in graphs}
+    del keep, graphs
     # the whole suite step captured once into a CUDA graph and replayed,
     # against the same step launched eagerly (the host's launch cost)
     try:
@@ -552,22 +687,24 @@ def time_context(ops, dev):
         with torch.cuda.graph(g):
             for op in ops:
                 op.run()
-        t_graph = t(g.replay, 20)
-        t_eager = t(lambda: [op.run() for op in ops], 20)
+        r = interleaved({"graph": g.replay, "eager": lambda: [op.run() for op in ops]}, it=10)
         step_flops = sum(op.flops for op in ops)
-        out["suite_cuda_graph"] = {"graph_ms_per_step": round(t_graph, 4), "eager_ms_per_step": round(t_eager, 4),
-                                   "graph_tflops": round(step_flops / t_graph / 1e9, 1)}
+        out["suite_cuda_graph"] = {"graph_ms_per_step": r["graph"]["median_ms"],
+                                   "eager_ms_per_step": r["eager"]["median_ms"],
+                                   "graph_tflops": round(step_flops / r["graph"]["median_ms"] / 1e9, 1)}
         del g
     except RuntimeError as e:   # reported, not hidden: the operators are meant to be capturable
         out["suite_cuda_graph"] = {"error": str(e)[:200]}
-    out["next_rows"] = time_next_rows(ops, dev, t)
+    out["next_rows"] = time_next_rows(ops, dev)
+    out["clocks"] = sampler.stop()
     return out
 
 
-def time_next_rows(ops, dev, t):
+def time_next_rows(ops, dev):
     """The rows built beyond the headline suite, on the suite's layer shapes:
     Megatron's n x k weight and the weight-gradient pass (LLaMA2-70B layers),
-    and the w8A16 extensions (bf16 activations, int8 zero points)."""
+    the w8A16 extensions (bf16 activations, int8 zero points) and the MoE
+    expert-parallel layer, each with the interleaved protocol."""
     import torch
 
     from tensor_matmul_collective_gb300 import coc
@@ -581,10 +718,10 @@ def time_next_rows(ops, dev, t):
         dx, dw = op.inputs[:s.R], op.inputs[s.R:2 * s.R]
         wnk = [w.t().contiguous() for w in dw]
         outs = [torch.empty(s.m // s.R, s.n, dtype=s.dtype, device=dev) for _ in range(s.R)]
-        tk = t(op.run)
-        tn = t(lambda: coc.fused_matmul("reduce_scatter", dx, wnk, w_layout="nk", outs=outs))
-        res["llama70b_rs_weight_nk"] = {"kn_ms": round(tk, 4), "nk_ms": round(tn, 4),
-                                        "nk_tflops": round(s.flops() / tn / 1e9, 1)}
+        r = interleaved({"kn": op.run, "nk": lambda: coc.fused_matmul("reduce_scatter", dx, wnk, w_layout="nk",
+                                                                      outs=outs)})
+        res["llama70b_rs_weight_nk"] = {"kn_ms": r["kn"]["median_ms"], "nk_ms": r["nk"]["median_ms"],
+                                        "nk_tflops": round(s.flops() / r["nk"]["median_ms"] / 1e9, 1)}
         del wnk, outs
     ag = [o for o in ops if o.kind == "ag_v2"]
     if ag:
@@ -593,13 +730,15 @@ def time_next_rows(ops, dev, t):
         dys = op.outputs[:s.R]                 # tokens x n_shard per rank (stands in for dY)
         xgs = op.outputs[s.R:2 * s.R]          # the gathered X V2 returned, per rank (tokens x k)
         dws = [torch.empty(s.n_shard, s.k, dtype=s.dtype, device=dev) for _ in range(s.R)]
-        tw = t(lambda: coc.weight_grad(dys, xgs, dws), 5)
+        r = interleaved({"wgrad": lambda: coc.weight_grad(dys, xgs, dws)}, it=10)
         flops = 2.0 * s.m * s.n_shard * s.k * s.R
-        res["llama70b_weight_grad"] = {"ms": round(tw, 4), "tflops": round(flops / tw / 1e9, 1)}
+        res["llama70b_weight_grad"] = {"ms": r["wgrad"]["median_ms"],
+                                       "tflops": round(flops / r["wgrad"]["median_ms"] / 1e9, 1)}
         del dws
     w8 = [o for o in ops if o.kind == "w8a16_ar"]
     if w8:
         base = w8[0].shape
+        fns, flops, keep = {}, {}, []
         for dt, zero in ((torch.float16, False), (torch.float16, True), (torch.bfloat16, False), (torch.bfloat16, True)):
             s = wl.W8A16(R=base.R, m=base.m, n=base.n, k_shard=base.k_shard, group=base.group, seed=base.seed,
                          dtype=dt)
@@ -607,27 +746,15 @@ def time_next_rows(ops, dev, t):
             dx, dq, ds = [x.to(dev) for x in xs], [w.to(dev) for w in wqs], [c.to(dev) for c in scales]
             dz = [z.to(dev) for z in s.zeros("channel")] if zero else None
             outs = [torch.empty(s.m, s.n, dtype=dt, device=dev) for _ in range(s.R)]
-            tm = t(lambda: coc.matmul_all_reduce_w8a16(dx, dq, ds, "channel", s.group, outs, zeros=dz))
             name = f"w8a16_ar_channel_{'bf16' if dt == torch.bfloat16 else 'fp16'}_{'zp' if zero else 'sym'}"
-            res[name] = {"ms": round(tm, 4), "tflops": round(s.flops() / tm / 1e9, 1)}
-            del dx, dq, ds, dz, outs
-        # the suite's w8A16 layer through the fused in-kernel dequantisation
-        # (the path below 2048 rows) instead of the pre-pass, for comparison
-        s = base
-        xs, wqs, scales = s.make("channel")
-        dx, dq, ds = [x.to(dev) for x in xs], [w.to(dev) for w in wqs], [c.to(dev) for c in scales]
-        outs = [torch.empty(s.m, s.n, dtype=s.dtype, device=dev) for _ in range(s.R)]
-        prev = os.environ.get("COC_W8_PATH")
-        os.environ["COC_W8_PATH"] = "fused"
-        try:
-            tm = t(lambda: coc.matmul_all_reduce_w8a16(dx, dq, ds, "channel", s.group, outs))
-        finally:
-            if prev is None:
-                del os.environ["COC_W8_PATH"]
-            else:
-                os.environ["COC_W8_PATH"] = prev
-        res["w8a16_ar_channel_fp16_fused_dequant_path"] = {"ms": round(tm, 4), "tflops": round(s.flops() / tm / 1e9, 1)}
-        del dx, dq, ds, outs
+            fns[name] = lambda dx=dx, dq=dq, ds=ds, dz=dz, outs=outs, g=s.group: coc.matmul_all_reduce_w8a16(
+                dx, dq, ds, "channel", g, outs, zeros=dz)
+            flops[name] = s.flops()
+            keep.append((dx, dq, ds, dz, outs))
+        r = interleaved(fns, it=10)
+        for name in fns:
+            res[name] = {"ms": r[name]["median_ms"], "tflops": round(flops[name] / r[name]["median_ms"] / 1e9, 1)}
+        del keep, fns
     # MoE dispatch + GroupedMatMul (EP form of the fused operators): a
     # Mixtral-style layer on 8 EP ranks, one expert each, 4096 tokens per rank,
     # against one plain GEMM over the same number of rows
@@ -635,24 +762,25 @@ def time_next_rows(ops, dev, t):
     xs, idxs, ws = s.make()
     dx, di, w = [x.to(dev) for x in xs], [i.to(dev) for i in idxs], torch.stack(ws).to(dev)
     y, xd, cnt, off = coc.moe_dispatch_grouped_matmul(dx, di, w, s.e_loc)
-    tm = t(lambda: coc.moe_dispatch_grouped_matmul(dx, di, w, s.e_loc, xd=xd, y=y, counts=cnt, offsets=off), 5)
     xg = torch.cat(dx, 0)
     og = torch.empty(xg.shape[0], s.f, dtype=s.dtype, device=dev)
-    tp = t(lambda: coc.matmul([xg], [w[0]], og), 5)
-    res["moe_dispatch_grouped_matmul_mixtral_ep8"] = {
-        "ms": round(tm, 4), "tflops": round(s.flops() / tm / 1e9, 1), "plain_gemm_same_rows_ms": round(tp, 4),
-        "tokens_per_expert": [int(v) for v in cnt.cpu().tolist()]}
-    del y, xd, xg, og
-    # the same layer with Mixtral's top-2 routing and the gated combine
     ti, tg = s.routing_topk(2)
     ti, tg = [i.to(dev) for i in ti], [g.to(dev) for g in tg]
     yt, y2, xd2, cnt2, off2 = coc.moe_topk_grouped_matmul_combine(dx, ti, tg, w, s.e_loc)
-    tk = t(lambda: coc.moe_topk_grouped_matmul_combine(dx, ti, tg, w, s.e_loc, xd=xd2, y=y2, y_tok=yt, counts=cnt2,
-                                                       offsets=off2), 5)
+    r = interleaved({"moe": lambda: coc.moe_dispatch_grouped_matmul(dx, di, w, s.e_loc, xd=xd, y=y, counts=cnt,
+                                                                    offsets=off),
+                     "plain": lambda: coc.matmul([xg], [w[0]], og),
+                     "top2": lambda: coc.moe_topk_grouped_matmul_combine(dx, ti, tg, w, s.e_loc, xd=xd2, y=y2,
+                                                                         y_tok=yt, counts=cnt2, offsets=off2)},
+                    it=10)
+    res["moe_dispatch_grouped_matmul_mixtral_ep8"] = {
+        "ms": r["moe"]["median_ms"], "tflops": round(s.flops() / r["moe"]["median_ms"] / 1e9, 1),
+        "plain_gemm_same_rows_ms": r["plain"]["median_ms"],
+        "tokens_per_expert": [int(v) for v in cnt.cpu().tolist()]}
     res["moe_top2_grouped_matmul_combine_mixtral_ep8"] = {
-        "ms": round(tk, 4), "tflops": round(2 * s.flops() / tk / 1e9, 1),
+        "ms": r["top2"]["median_ms"], "tflops": round(2 * s.flops() / r["top2"]["median_ms"] / 1e9, 1),
         "entries_per_expert": [int(v) for v in cnt2.cpu().tolist()]}
-    del dx, di, w, ti, tg, yt, y2, xd2
+    del dx, di, w, ti, tg, yt, y2, xd2, y, xd, xg, og
     return res
 
 
@@ -782,6 +910,49 @@ def run_reference(args):
     return 0
 
 
+def op_stats(op, ts, peaks):
+    """Median / min / max of one operator's per-step times, its TFLOP/s at the
+    median and min, fractions of the measured tensor peaks, and its achieved
+    algorithmic HBM bandwidth."""
+    med, lo, hi = statistics.median(ts), min(ts), max(ts)
+    tf = op.flops / (med / 1e3) / 1e12
+    ab = algorithmic_bytes(op)
+    return {"ms_median": round(med, 4), "ms_min": round(lo, 4), "ms_max": round(hi, 4),
+            "spread": round((hi - lo) / med, 4), "samples": len(ts),
+            "tflops": round(tf, 1), "tflops_at_min": round(op.flops / (lo / 1e3) / 1e12, 1),
+            "frac_burst": round(tf / peaks["bf16_tflops"], 4),
+            "frac_sustained": round(tf / peaks["bf16_tflops_sustained"], 4),
+            "algorithmic_gb": round(ab / 1e9, 4), "hbm_gbs": round(ab / (med / 1e3) / 1e9, 1),
+            "hbm_frac": round(ab / (med / 1e3) / 1e9 / peaks["hbm_gbs"], 4)}
+
+
+def roofline_obj(op, ts, peaks, clocks, traffic):
+    """The dominant kernel against the dense bf16 tensor roofline.  frac (the
+    headline) divides by the measured BURST peak, the right denominator for a
+    sub-second timed region; frac_clock_normalised scales the measured
+    sustained peak by the SM clock this kernel ran at (measured inside the
+    kernel: SM cycles over %globaltimer ns) over the clock that peak was
+    measured at, i.e. the kernel's per-clock efficiency against cuBLAS's."""
+    med = statistics.median(ts)
+    tf = op.flops / (med / 1e3) / 1e12
+    burst, sus = peaks["bf16_tflops"], peaks["bf16_tflops_sustained"]
+    kern_mhz = ((clocks or {}).get("sm_mhz_in_kernel") or {}).get(op.name)
+    line_mhz, peak_mhz = (clocks or {}).get("sm_mhz"), peaks.get("sustained_sm_mhz")
+    norm = None
+    if kern_mhz and peak_mhz:
+        norm = round(tf / (sus * kern_mhz / peak_mhz), 4)
+    return {"bound": "tensor", "kernel": op.name, "achieved": round(tf, 1), "peak": burst, "unit": UNIT,
+            "frac": round(tf / burst, 4), "traffic": traffic,
+            "frac_burst": round(tf / burst, 4), "frac_sustained": round(tf / sus, 4),
+            "frac_clock_normalised": norm,
+            "sm_mhz_samples": (clocks or {}).get("samples"), "sm_mhz_line": line_mhz,
+            "sm_mhz_in_kernel": kern_mhz, "sm_mhz_of_sustained_peak": peak_mhz,
+            "headline": "frac = frac_burst (measured burst bf16 peak, of measured)",
+            "achieved_from": f"median over {len(ts)} timed steps of the kernel's CUDA-event duration "
+                             f"on the launching stream; algorithmic 2mnK FLOPs",
+            "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json: burst {burst}, sustained {sus} TFLOP/s)"}
+
+
 def run_ours(args):
     import torch
 
@@ -803,10 +974,10 @@ def run_ours(args):
     bus = None
     try:
         props = torch.cuda.get_device_properties(dev)
-        bus = "%02x:%02x." % (props.pci_bus_id, props.pci_device_id)
+        bus = "%04x:%02x:%02x.0" % (getattr(props, "pci_domain_id", 0), props.pci_bus_id, props.pci_device_id)
     except Exception:
         bus = None
-    sampler = ClockSampler(bus)
+    sampler = NvmlSampler(bus, local)
     total_ms, per_op, clocks = time_device(ops, args.steps, args.warmup, dist, sampler)
 
     total_ms = max_over_ranks(total_ms, dist, dev)
@@ -814,23 +985,17 @@ def run_ours(args):
     value = job_value(step_flops, args.steps, world, total_ms)
 
     peaks = load_peaks()
-    peak = peaks["bf16_tflops_sustained"]
-    dom = max(range(len(ops)), key=lambda i: per_op[i])
-    dom_tf = ops[dom].flops / (per_op[dom] / 1e3) / 1e12
+    dom = max(range(len(ops)), key=lambda i: statistics.median(per_op[i]))
     from tensor_matmul_collective_gb300 import workloads as wl
     chunks_of = {w.name: w.chunks for w in wl.TP8_SUITE}
     traffic = load_traffic(ops[dom].name, chunks_of.get(ops[dom].name, chunks_of.get("w8a16_ar", 1)))
-    per_op_json = {op.name: {"ms": round(t, 4), "tflops": round(op.flops / (t / 1e3) / 1e12, 1),
-                             "frac_of_peak": round(op.flops / (t / 1e3) / 1e12 / peak, 4),
-                             # achieved algorithmic HBM bandwidth, against the measured copy bandwidth
-                             "algorithmic_gb": round(algorithmic_bytes(op) / 1e9, 4),
-                             "hbm_gbs": round(algorithmic_bytes(op) / (t / 1e3) / 1e9, 1),
-                             "hbm_frac": round(algorithmic_bytes(op) / (t / 1e3) / 1e9 / peaks["hbm_gbs"], 4)}
-                   for op, t in zip(ops, per_op)}
+    per_op_json = {op.name: op_stats(op, ts, peaks) for op, ts in zip(ops, per_op)}
+    for op in ops:
+        per_op_json[op.name]["sm_mhz_in_kernel"] = ((clocks or {}).get("sm_mhz_in_kernel") or {}).get(op.name)
 
     e2e = None
     if args.e2e_steps > 0:
-        e2e_sampler = ClockSampler(bus)
+        e2e_sampler = NvmlSampler(bus, local)
         e2e_sampler.start()
         wall, h2d, d2h = time_e2e(ops, args.e2e_steps, dev)
         e2e_clocks = e2e_sampler.stop()
@@ -842,7 +1007,7 @@ def run_ours(args):
                # the SM clock of this leg (power-capped boxes settle differently per phase)
                "sm_mhz": e2e_clocks["sm_mhz"] if e2e_clocks else None}
 
-    context = None if args.no_context else time_context(ops, dev)
+    context = None if args.no_context else time_context(ops, dev, bus, local)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -857,12 +1022,11 @@ def run_ours(args):
         line = base_line(world, args.steps, args.warmup)
         line.update({
             "value": value, "ms_per_step": total_ms / args.steps, "config": config_dict(world),
-            "pct_of_peak": round(100.0 * value / world / peak, 2),
-            "peak": {"bf16_tflops_sustained": peak, "bf16_tflops_burst": peaks["bf16_tflops"],
-                     "source": peaks["source"]},
-            "roofline": {"bound": "tensor", "kernel": ops[dom].name, "achieved": round(dom_tf, 1), "peak": peak,
-                         "unit": UNIT, "frac": round(dom_tf / peak, 4), "traffic": traffic,
-                         "peak_source": f"{peaks['source']} sustained bf16 (kernel timed inside a long step)"},
+            "pct_of_peak_burst": round(100.0 * value / world / peaks["bf16_tflops"], 2),
+            "pct_of_peak_sustained": round(100.0 * value / world / peaks["bf16_tflops_sustained"], 2),
+            "peak": {"bf16_tflops_burst": peaks["bf16_tflops"], "bf16_tflops_sustained": peaks["bf16_tflops_sustained"],
+                     "hbm_gbs": peaks["hbm_gbs"], "source": peaks["source"]},
+            "roofline": roofline_obj(ops[dom], per_op[dom], peaks, clocks, traffic),
             "per_op": per_op_json,
             "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
             "gpu_launches": sum(o.launches for o in ops) * args.steps,
@@ -875,8 +1039,86 @@ def run_ours(args):
     return 0
 
 
+def run_case(a):
+    """One operator on seeded synthetic data, timed over a.iters calls (CUDA
+    events, after one untimed call); prints one JSON line."""
+    import torch
+
+    from tensor_matmul_collective_gb300 import build as cbuild
+    from tensor_matmul_collective_gb300 import coc
+    from tensor_matmul_collective_gb300 import workloads as wl
+    cbuild.build()
+    dev = torch.device("cuda:0")
+    dt = torch.bfloat16 if a.dtype == "bf16" else torch.float16
+    if a.case in ("ag", "ag_v2"):
+        s = wl.ColumnParallelSP(R=a.R, m_shard=a.m, n_shard=a.n, k=a.k, dtype=dt, x_dist="normal(0,1)",
+                                w_dist="normal(0,0.02)", seed=2)
+        xs, ws = s.make()
+        dx, dw = [x.to(dev) for x in xs], [w.to(dev) for w in ws]
+        outs = [torch.empty(s.m, s.n_shard, dtype=dt, device=dev) for _ in range(a.R)]
+        if a.case == "ag_v2":
+            g = [torch.empty(s.m, s.k, dtype=dt, device=dev) for _ in range(a.R)]
+            run = lambda: coc.all_gather_matmul_v2(dx, dw, outs, g, chunks=a.chunks)  # noqa: E731
+        else:
+            run = lambda: coc.all_gather_matmul(dx, dw, outs, chunks=a.chunks)  # noqa: E731
+        flops = s.flops()
+    elif a.case == "moe":
+        s = wl.MoEDispatch(R=a.R, T=a.m, h=a.k, f=a.n, e_loc=a.eloc, seed=21, dtype=dt)
+        xs, idxs, ws = s.make()
+        dx, w = [x.to(dev) for x in xs], torch.stack(ws).to(dev)
+        if a.topk > 1:
+            ti, tg = s.routing_topk(a.topk)
+            ti, tg = [i.to(dev) for i in ti], [g.to(dev) for g in tg]
+            run = lambda: coc.moe_topk_grouped_matmul_combine(dx, ti, tg, w, a.eloc)  # noqa: E731
+        else:
+            di = [i.to(dev) for i in idxs]
+            run = lambda: coc.moe_dispatch_grouped_matmul(dx, di, w, a.eloc)  # noqa: E731
+        flops = s.flops() * a.topk
+    elif a.case == "w8a16":
+        s = wl.W8A16(R=a.R, m=a.m, n=a.n, k_shard=a.k, group=a.group, seed=3, dtype=dt)
+        xs, wqs, scales = s.make(a.gran)
+        dx, dw, dsc = [x.to(dev) for x in xs], [w.to(dev) for w in wqs], [t.to(dev) for t in scales]
+        dz = [z.to(dev) for z in s.zeros(a.gran)] if a.zero else None
+        outs = [torch.empty(s.m, s.n, dtype=dt, device=dev) for _ in range(a.R)]
+        run = lambda: coc.matmul_all_reduce_w8a16(dx, dw, dsc, a.gran, a.group, outs, chunks=a.chunks,  # noqa: E731
+                                                  zeros=dz)
+        flops = s.flops()
+    else:
+        s = wl.RowParallel(R=a.R, m=a.m, n=a.n, k_shard=a.k, dtype=dt, x_dist="normal(0,1)",
+                           w_dist="normal(0,0.02)", seed=1)
+        xs, ws = s.make()
+        dx, dw = [x.to(dev) for x in xs], [w.to(dev) for w in ws]
+        if a.case == "ar":
+            outs = [torch.empty(s.m, s.n, dtype=dt, device=dev) for _ in range(a.R)]
+            run = lambda: coc.matmul_all_reduce(dx, dw, outs, chunks=a.chunks,  # noqa: E731
+                                                deterministic=a.deterministic)
+        elif a.case == "rs":
+            outs = [torch.empty(s.m // a.R, s.n, dtype=dt, device=dev) for _ in range(a.R)]
+            run = lambda: coc.matmul_reduce_scatter(dx, dw, outs, chunks=a.chunks,  # noqa: E731
+                                                    deterministic=a.deterministic)
+        else:
+            out = torch.empty(s.m, s.n, dtype=dt, device=dev)
+            run = lambda: coc.matmul(dx, dw, out)  # noqa: E731
+        flops = s.flops()
+    run()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(a.iters):
+        run()
+    e1.record()
+    torch.cuda.synchronize()
+    coc.sync_status()
+    ms = e0.elapsed_time(e1) / a.iters
+    print(json.dumps({"case": a.case, "R": a.R, "m": a.m, "n": a.n, "k": a.k, "chunks": a.chunks, "ms": ms,
+                      "tflops": flops / (ms / 1e3) / 1e12}), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
+    if args.case is not None:
+        return run_case(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -33,18 +33,28 @@
  * Chunking.  Following the page's CoC idea (section 解决思路: split compute
  * and communication into smaller sub-tasks and pipeline them; the left
  * matmul operand is split along m into 2/4/8 parts and m must be a multiple
- * of the split count), `chunks` in {1, 2, 4, 8} splits the output rows into
- * equal chunks processed in chunk order; one chunk's reduce/scatter/gather
- * epilogue overlaps the next chunk's matmul mainloop.  chunks = 1 means no
- * chunking.  The result never depends on `chunks`.
+ * of the split count), `chunks` in {1, 2, 4, 8} cuts the output rows into C
+ * equal chunks and sets the order in which the kernel issues its output
+ * tiles: every tile of chunk c before any tile of chunk c+1.  When a chunk
+ * boundary falls inside a tile (m / C not a multiple of the tile height:
+ * 128 rows up to m = 128, 256 rows above), the tiles are issued in plain row
+ * order instead, which keeps the chunk order at tile granularity (a tile
+ * that straddles two chunks is issued with the earlier one).  chunks = 1
+ * means no chunking.  The overlap of communication with compute does not
+ * depend on `chunks`: the accumulator is double-buffered in tensor memory,
+ * so every tile's reduce/scatter/gather epilogue runs while the next tile's
+ * mainloop runs.  The result never depends on `chunks`.
  *
- * Deterministic mode (same section: "及其确定性计算").  With deterministic != 0
- * the output is bitwise reproducible for identical inputs on the same GPU and
- * library build, across runs and across chunk counts: each output element is
- * accumulated in fp32 in the fixed order rank 0..R-1, k ascending, with no
- * split-K, atomics or arrival-order reduction, and rounded once
- * (round-to-nearest-even) to the output type.  The current kernels use this
- * order in both modes, so deterministic = 0 gives the same bits.
+ * Deterministic mode (same section: "及其确定性计算").  Every call is
+ * bitwise reproducible for identical inputs on the same GPU and library
+ * build, across runs and across chunk counts: each output element is
+ * accumulated in fp32 in the fixed order rank 0..R-1, k ascending, and
+ * rounded once (round-to-nearest-even) to the output type.  No call combines
+ * partial sums with atomics or in arrival order; the one split of the
+ * contraction, the rank split of decode-sized AllReduce / ReduceScatter
+ * (below), depends on the shape only and adds its parts in a fixed order.
+ * There is no faster non-deterministic schedule, so `deterministic` is
+ * accepted and has no effect: deterministic = 0 gives the same bits.
  *
  * Conventions for every entry point:
  *   - All matrices are row-major and densely packed, in device memory the
@@ -53,13 +63,21 @@
  *     (TMA requirement), see the per-call alignment notes.
  *   - Array-of-pointer arguments (`x`, `w`, `out`, ...) are HOST arrays of R
  *     device pointers, read before the call returns.
- *   - On the first call on a device the library allocates a small status
- *     buffer (a few words) and creates a stream-ordered memory pool, both
- *     released by coc_shutdown().  Per-call scratch comes from that pool,
- *     allocated and freed on the call's stream (no call synchronises; the pool
- *     keeps freed memory for reuse): the w8A16 pre-pass's dequantised weight,
- *     the MoE routing tables, and the fp32 parts of a rank-split AllReduce /
- *     ReduceScatter (below).  coc_matmul_all_reduce_noalloc takes none.
+ *   - Library-owned device memory.  The first call on a device allocates a
+ *     small status buffer (a few words).  Calls that need scratch (the fp32
+ *     parts of a rank-split AllReduce / ReduceScatter, the MoE routing
+ *     tables, the w8A16 pre-pass's dequantised weight) take it from a
+ *     workspace the library keeps per stream: allocated by the first such
+ *     call on the stream and grown only when a later call needs more (the
+ *     growing call waits for the earlier users of the old buffer first), so
+ *     repeated calls of the same shapes make no allocating call at all
+ *     (coc_debug_alloc_count counts them).  One call takes at most 4 GiB of
+ *     scratch (COC_ERR_SHAPE beyond).  Calls captured into a CUDA graph take
+ *     their scratch as stream-ordered allocations from a device pool, which
+ *     become memory nodes of the graph, so graph replays allocate nothing
+ *     either.  coc_shutdown() frees all of it.  Calls on different streams
+ *     use different workspaces and may overlap freely.
+ *     coc_matmul_all_reduce_noalloc takes none of this memory.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
  *     default stream).  Outputs must not alias inputs or each other.
  *   - Argument errors are detected on the host before any CUDA call and are
@@ -73,8 +91,10 @@
  *     raise it where the GPU is time-sliced between processes, since a
  *     pause of the kernel counts against it.
  *   - The first call on a device creates the library's per-device state
- *     (status block, kernel attributes, workspace pool); after it, calls make
- *     no synchronising CUDA call and can be captured into CUDA graphs.
+ *     (status block, kernel attributes), and the first call on a stream
+ *     that needs scratch sizes that stream's workspace (synchronising CUDA
+ *     calls).  After them, calls make no synchronising CUDA call and can be
+ *     captured into CUDA graphs.
  *   - Environment variables that force a schedule (tuning and tests only;
  *     every value gives correct results): COC_PAIR=0|1 (single-CTA or 2-SM
  *     tiles), COC_W8_PATH=fused|prepass (w8A16 dequantisation inside the
@@ -295,9 +315,10 @@ coc_status_t coc_matmul_all_reduce_w8a16_ex(int R, int64_t m, int64_t n, int64_t
  * Shape: h a positive multiple of 64; f * 2 % 16 == 0; E <= 256.
  * Alignment: x, xd, y, w 16-byte aligned; idx, counts, offsets 4-byte.
  * Ownership: all buffers are the caller's device memory; a routing table of
- * R x tokens int32 is taken from the library's stream-ordered pool for the
- * duration of the call.  Runs on `stream` (three kernels: routing, token
- * copy, grouped GEMM); no host synchronisation.
+ * R x tokens int32 lives in the stream's workspace (see the conventions
+ * above) for the duration of the call.  Runs on `stream` (three kernels:
+ * routing, token copy, grouped GEMM); no host synchronisation once the
+ * workspace is sized.
  */
 coc_status_t coc_moe_dispatch_grouped_matmul(int R, int64_t tokens, int64_t h, int64_t f, int experts_per_rank,
                                              const void* const* x, const int32_t* const* idx, const void* w,
@@ -316,7 +337,7 @@ coc_status_t coc_moe_dispatch_grouped_matmul(int R, int64_t tokens, int64_t h, i
  *           tokens with an out-of-range expert id are not written.
  * Other arguments as coc_moe_dispatch_grouped_matmul (xd still receives the
  * dispatched tokens).  The routing table grows by R x capacity int32 (the
- * source token of each dispatched row), from the same pool.
+ * source token of each dispatched row), in the same workspace.
  */
 coc_status_t coc_moe_dispatch_grouped_matmul_combine(int R, int64_t tokens, int64_t h, int64_t f, int experts_per_rank,
                                                      const void* const* x, const int32_t* const* idx, const void* w,
@@ -409,19 +430,24 @@ coc_status_t coc_matmul(int R, int64_t m, int64_t n, int64_t k_shard,
  * through a custom allocator.
  *
  * Same arguments, results and checks as coc_matmul_all_reduce.  The library
- * makes no cudaMalloc/cudaFree or other allocating call here.  The kernel's
+ * makes no cudaMalloc/cudaFree or other allocating call here (it never takes
+ * the rank split, whose fp32 parts would need a workspace).  The kernel's
  * only scratch (its 32-byte status block) lives in a fixed 256-byte
  * __device__ array that every GPU loading the library holds until the
  * process exits; this scratch does not grow with m, n or k, and a need
  * beyond 256 bytes would be rejected with COC_ERR_SHAPE.
  *   - The first call on a device looks up that array's device address
- *     (cudaGetSymbolAddress) with the device current; make that first call
- *     before any stream capture.
- *   - Every call shares the array.  Each call clears the status block in
- *     stream order before its kernel; calls whose kernels overlap on the GPU
- *     (different streams) race on it.
- *   - The status block is not read by coc_sync_status(): a bounded wait that
- *     runs out here still stops the kernel cleanly, but is not reported.
+ *     (cudaGetSymbolAddress) with the device current and clears it; make
+ *     that first call before any stream capture.
+ *   - Every call shares the array.  Kernels only ever set bits in it (a
+ *     bounded wait that runs out records COC_ERR_TIMEOUT there), so calls
+ *     whose kernels overlap on the GPU (different streams) may both record a
+ *     timeout, and the report cannot tell which of them it came from.
+ *   - coc_sync_status() reads this block too (without allocating) and clears
+ *     it when it reports a timeout; until then the timeout stays recorded,
+ *     whatever calls follow.
+ *   - coc_shutdown() forgets the looked-up address; call it before a
+ *     cudaDeviceReset if calls continue afterwards.
  */
 coc_status_t coc_matmul_all_reduce_noalloc(int R, int64_t m, int64_t n, int64_t k_shard,
                                            const void* const* x, const void* const* w,
@@ -430,9 +456,12 @@ coc_status_t coc_matmul_all_reduce_noalloc(int R, int64_t m, int64_t n, int64_t 
 
 /*
  * Waits for `stream`, then returns and clears the device-side status of
- * this library on the current device: COC_ERR_TIMEOUT if a kernel's bounded
- * wait ran out since the last check, COC_ERR_CUDA if the stream reports an
- * error, COC_OK otherwise.
+ * this library on the current device (the status buffer of the allocating
+ * entry points and the static block of coc_matmul_all_reduce_noalloc):
+ * COC_ERR_TIMEOUT if a kernel's bounded wait ran out since the last check,
+ * COC_ERR_INVALID_ARG if a MoE dispatch met an expert id out of range,
+ * COC_ERR_CUDA if the stream reports an error, COC_OK otherwise.  It creates
+ * no library state and allocates nothing.
  */
 coc_status_t coc_sync_status(coc_stream_t stream);
 
@@ -453,7 +482,29 @@ int coc_version(void);
  */
 coc_status_t coc_debug_inject_timeout(int enable);
 
-/* Frees the per-device status buffers.  Further calls re-create them. */
+/*
+ * Test and audit hook: the number of device allocations (cudaMalloc, and
+ * stream-ordered allocations of captured calls) the library has made in
+ * this process.  Steady-state calls of unchanged shapes on a stream leave it
+ * unchanged.
+ */
+int64_t coc_debug_alloc_count(void);
+
+/*
+ * Measurement hook: while `slot` (0..7) is selected, block 0 of every fused
+ * kernel launched afterwards adds the SM clock cycles and the nanoseconds
+ * (%globaltimer) it ran for to that slot of the device status buffer; -1
+ * stops it.  coc_debug_clock_read waits for the device, returns a slot's two
+ * sums and clears them: cycles / ns is the SM clock the kernels actually ran
+ * at, which the driver's sampled clock does not show on a power-capped GPU.
+ * (The allocation-free entry point never records.)
+ */
+coc_status_t coc_debug_clock_probe(int slot);
+coc_status_t coc_debug_clock_read(int slot, int64_t* cycles, int64_t* ns);
+
+/* Frees the per-device status buffers, the per-stream workspaces and the
+ * graph-capture pool; forgets the allocation-free entry point's set-up.
+ * Further calls re-create what they need. */
 coc_status_t coc_shutdown(void);
 
 #ifdef __cplusplus

@@ -29,7 +29,8 @@ EXPORTS = (
     "coc_sync_status", "coc_status_string", "coc_last_error", "coc_version",
     "coc_debug_inject_timeout", "coc_shutdown", "coc_matmul_all_reduce_noalloc",
     "coc_fused_matmul", "coc_matmul_all_reduce_w8a16_ex", "coc_moe_dispatch_grouped_matmul", "coc_moe_capacity",
-    "coc_moe_dispatch_grouped_matmul_combine", "coc_moe_topk_grouped_matmul_combine",
+    "coc_moe_dispatch_grouped_matmul_combine", "coc_moe_topk_grouped_matmul_combine", "coc_debug_alloc_count",
+    "coc_debug_clock_probe", "coc_debug_clock_read",
 )
 
 OP_ALL_REDUCE, OP_REDUCE_SCATTER, OP_ALL_GATHER, OP_ALL_GATHER_V2, OP_WEIGHT_GRAD = range(5)
@@ -97,6 +98,12 @@ def lib() -> ctypes.CDLL:
             L.coc_debug_inject_timeout.argtypes = [i32]
             L.coc_debug_inject_timeout.restype = i32
             L.coc_shutdown.restype = i32
+            L.coc_debug_alloc_count.argtypes = []
+            L.coc_debug_alloc_count.restype = i64
+            L.coc_debug_clock_probe.argtypes = [i32]
+            L.coc_debug_clock_probe.restype = i32
+            L.coc_debug_clock_read.argtypes = [i32, ctypes.POINTER(i64), ctypes.POINTER(i64)]
+            L.coc_debug_clock_read.restype = i32
             _lib = L
     return _lib
 
@@ -189,6 +196,21 @@ def matmul_all_reduce(xs, ws, outs=None, chunks: int = 1, deterministic: bool = 
     outs = _outs(outs, R, (m, n), x0.dtype, x0.device)
     _check(lib().coc_matmul_all_reduce(R, m, n, ks, _ptrs(xs), _ptrs(ws), _ptrs(outs), _dtype_code(x0.dtype),
                                        int(chunks), int(bool(deterministic)), _stream(stream)))
+    return outs
+
+
+def matmul_all_reduce_noalloc(xs, ws, outs=None, chunks: int = 1, deterministic: bool = False, stream=None):
+    """MATMUL_ALL_REDUCE through the allocation-free entry point (the library
+    allocates no device memory for this call; `outs` None allocates the
+    outputs here, through PyTorch)."""
+    R, x0, w0 = _prep(xs, ws)
+    m, ks = x0.shape
+    n = w0.shape[1]
+    _check_list(xs, "xs", (m, ks), x0.dtype, x0.device)
+    _check_list(ws, "ws", (ks, n), x0.dtype, x0.device)
+    outs = _outs(outs, R, (m, n), x0.dtype, x0.device)
+    _check(lib().coc_matmul_all_reduce_noalloc(R, m, n, ks, _ptrs(xs), _ptrs(ws), _ptrs(outs), _dtype_code(x0.dtype),
+                                               int(chunks), int(bool(deterministic)), _stream(stream)))
     return outs
 
 
@@ -453,6 +475,31 @@ def sync_status(stream=None) -> None:
 def inject_timeout(enable: bool) -> None:
     """Test hook: make subsequently launched kernels stop with COC_ERR_TIMEOUT."""
     _check(lib().coc_debug_inject_timeout(int(bool(enable))))
+
+
+def alloc_count() -> int:
+    """Device allocations the library has made in this process (an audit hook)."""
+    return int(lib().coc_debug_alloc_count())
+
+
+def clock_probe(slot: int) -> None:
+    """Fused kernels launched from now on add their block-0 SM cycles and ns
+    to clock slot `slot` (0..7); -1 stops recording."""
+    _check(lib().coc_debug_clock_probe(int(slot)))
+
+
+def clock_read(slot: int):
+    """(cycles, ns) accumulated in a clock slot since its last read (waits for
+    the device); cycles / ns * 1e3 is the SM clock in MHz."""
+    c, n = ctypes.c_int64(), ctypes.c_int64()
+    _check(lib().coc_debug_clock_read(int(slot), ctypes.byref(c), ctypes.byref(n)))
+    return c.value, n.value
+
+
+def clock_mhz(slot: int):
+    """The SM clock (MHz) the kernels recorded in `slot` ran at, None if none ran."""
+    c, n = clock_read(slot)
+    return round(1e3 * c / n, 1) if n > 0 else None
 
 
 def shutdown() -> None:

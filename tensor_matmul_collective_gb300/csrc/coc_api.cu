@@ -32,13 +32,29 @@ coc_status_t cuda_fail(cudaError_t e, const char* what) {
 }
 
 std::atomic<int> g_inject{0};
+std::atomic<int> g_clock_slot{-1};         // coc_debug_clock_probe
+std::atomic<long long> g_alloc_calls{0};   // device allocations made by the library (coc_debug_alloc_count)
+
+// Scratch owned by the library for the calls made on one stream: the
+// rank-split fp32 parts, the MoE routing tables, the w8A16 pre-pass weight.
+// Allocated at the first call on the stream that needs it and grown only when
+// a call needs more, so steady-state calls allocate nothing.  `last_use` is
+// recorded after every call that used it and waited on by the next one, so a
+// stream handle that is reused after cudaStreamDestroy can never overlap the
+// previous owner's kernels.
+struct Workspace {
+    void* ptr = nullptr;
+    size_t bytes = 0;
+    cudaEvent_t last_use = nullptr;
+};
 
 struct DeviceState {
     int sm_count = 0;
     int cc_major = 0, cc_minor = 0;
     unsigned* status = nullptr;
     int max_pairs[NUM_OPS][2] = {{-1, -1}, {-1, -1}, {-1, -1}, {-1, -1}, {-1, -1}};   // per op, per bf16; -1 = not queried
-    cudaMemPool_t pool = nullptr;   // stream-ordered workspace (w8A16 pre-pass), kept between calls
+    cudaMemPool_t pool = nullptr;   // stream-ordered allocations of calls captured into CUDA graphs
+    std::unordered_map<cudaStream_t, Workspace> ws;   // per-stream scratch of eager calls
 };
 
 std::mutex g_mu;
@@ -68,12 +84,30 @@ coc_status_t device_state(DeviceState** out) {
             return fail(COC_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a", dev,
                         st.cc_major, st.cc_minor);
         void* p = nullptr;
-        if ((e = cudaMalloc(&p, STATUS_WORDS * sizeof(unsigned))) != cudaSuccess) return cuda_fail(e, "cudaMalloc(status)");
-        if ((e = cudaMemset(p, 0, STATUS_WORDS * sizeof(unsigned))) != cudaSuccess) {
+        g_alloc_calls.fetch_add(1);
+        if ((e = cudaMalloc(&p, STATUS_BLOCK_WORDS * sizeof(unsigned))) != cudaSuccess) return cuda_fail(e, "cudaMalloc(status)");
+        if ((e = cudaMemset(p, 0, STATUS_BLOCK_WORDS * sizeof(unsigned))) != cudaSuccess) {
             cudaFree(p);
             return cuda_fail(e, "cudaMemset(status)");
         }
         st.status = static_cast<unsigned*>(p);
+    }
+    if (st.pool == nullptr) {
+        // the pool that captured calls allocate their scratch from; created
+        // here, by the first call on the device, because creating it while a
+        // stream is being captured would invalidate the capture
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t pool = nullptr;
+        if ((e = cudaMemPoolCreate(&pool, &props)) != cudaSuccess) return cuda_fail(e, "cudaMemPoolCreate");
+        uint64_t keep = UINT64_MAX;   // keep freed memory for the next replay / capture
+        if ((e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep)) != cudaSuccess) {
+            cudaMemPoolDestroy(pool);
+            return cuda_fail(e, "cudaMemPoolSetAttribute");
+        }
+        st.pool = pool;
     }
     *out = &st;
     return COC_OK;
@@ -200,6 +234,7 @@ CUtensorMapDataType tma_dtype(coc_dtype_t dt) {
 coc_status_t launch_checked(int op, bool bf16, bool pair, KParams& p, DeviceState* ds, cudaStream_t stream) {
     p.status = ds->status;
     p.inject_timeout = g_inject.load();
+    p.clock_slot = g_clock_slot.load();
     int grid;
     if (pair) {
         const int pairs = pairs_available(ds, op, bf16);
@@ -214,6 +249,21 @@ coc_status_t launch_checked(int op, bool bf16, bool pair, KParams& p, DeviceStat
 }
 
 coc_status_t device_pool(DeviceState* ds, cudaMemPool_t* out);
+
+// Scratch for one call (see Workspace): a region of at least `bytes` bytes,
+// usable by the kernels the call puts on `stream`.  Eager calls get the
+// stream's persistent workspace (allocated or grown only when too small);
+// calls captured into a CUDA graph get a stream-ordered allocation from the
+// device pool, which becomes a memory node of the graph, so graph replays
+// call no allocator either.  scratch_release ends the call's use.
+struct Scratch {
+    void* ptr = nullptr;
+    bool captured = false;
+    Workspace* w = nullptr;
+};
+constexpr size_t kWorkspaceCap = size_t(4) << 30;   // largest scratch one call may take
+coc_status_t scratch_acquire(DeviceState* ds, cudaStream_t stream, size_t bytes, Scratch* out);
+coc_status_t scratch_release(cudaStream_t stream, Scratch& sc, coc_status_t st);
 
 // Rank split (AllReduce, ReduceScatter, single-CTA tiles: m <= 128): with at
 // most half as many output tiles as SMs (decode-sized m), each tile's R shards
@@ -323,19 +373,14 @@ coc_status_t row_parallel(int op, int R, int64_t m, int64_t n, int64_t ks, const
     for (int o = 0; o < (op == OP_RS ? R : n_out); ++o) p.outp[o] = static_cast<uint16_t*>(out[o]);
     const size_t part_bytes = static_cast<size_t>(tiles) * ksplit * tile_m * BN * sizeof(float);
     const size_t cnt_bytes = static_cast<size_t>(tiles) * (pair ? 2 : 1) * NUM_EPI_WARPS * sizeof(unsigned);
-    cudaMemPool_t pool = nullptr;
-    if ((st = device_pool(ds, &pool)) != COC_OK) return st;
-    void* ws = nullptr;
-    cudaError_t e = cudaMallocFromPoolAsync(&ws, part_bytes + cnt_bytes, pool, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMallocFromPoolAsync (rank-split parts)");
-    p.part = static_cast<float*>(ws);
-    p.part_cnt = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + part_bytes);
-    e = cudaMemsetAsync(p.part_cnt, 0, cnt_bytes, stream);
+    Scratch sc;
+    if ((st = scratch_acquire(ds, stream, part_bytes + cnt_bytes, &sc)) != COC_OK) return st;
+    p.part = static_cast<float*>(sc.ptr);
+    p.part_cnt = reinterpret_cast<unsigned*>(static_cast<char*>(sc.ptr) + part_bytes);
+    const cudaError_t e = cudaMemsetAsync(p.part_cnt, 0, cnt_bytes, stream);
     st = (e != cudaSuccess) ? cuda_fail(e, "cudaMemsetAsync (rank-split counters)")
                             : launch_checked(op, dt == COC_BF16, pair, p, ds, stream);
-    const cudaError_t ef = cudaFreeAsync(ws, stream);
-    if (st == COC_OK && ef != cudaSuccess) st = cuda_fail(ef, "cudaFreeAsync (rank-split parts)");
-    return st;
+    return scratch_release(stream, sc, st);
 }
 
 coc_status_t validate_row_parallel(int R, int64_t m, int64_t n, int64_t ks, const void* const* x, const void* const* w,
@@ -373,41 +418,82 @@ bool w8_use_prepass(int64_t m) {
 
 coc_status_t device_pool(DeviceState* ds, cudaMemPool_t* out) {
     std::lock_guard<std::mutex> lk(g_mu);
-    if (ds->pool == nullptr) {
-        int dev = 0;
-        cudaError_t e = cudaGetDevice(&dev);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-        cudaMemPoolProps props = {};
-        props.allocType = cudaMemAllocationTypePinned;
-        props.location.type = cudaMemLocationTypeDevice;
-        props.location.id = dev;
-        cudaMemPool_t pool = nullptr;
-        if ((e = cudaMemPoolCreate(&pool, &props)) != cudaSuccess) return cuda_fail(e, "cudaMemPoolCreate");
-        uint64_t keep = UINT64_MAX;   // keep freed workspace for the next call
-        if ((e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep)) != cudaSuccess) {
-            cudaMemPoolDestroy(pool);
-            return cuda_fail(e, "cudaMemPoolSetAttribute");
-        }
-        ds->pool = pool;
-    }
+    if (ds->pool == nullptr) return fail(COC_ERR_CUDA, "no memory pool on this device (coc_shutdown during a capture?)");
     *out = ds->pool;
     return COC_OK;
 }
 
-// Pre-pass path: dequantise all ranks' weights into a stream-ordered
-// workspace, run the AllReduce on it, release the workspace on the stream.
+coc_status_t scratch_acquire(DeviceState* ds, cudaStream_t stream, size_t bytes, Scratch* out) {
+    *out = Scratch{};
+    if (bytes == 0) return COC_OK;
+    if (bytes > kWorkspaceCap)
+        return fail(COC_ERR_SHAPE, "the call needs %zu bytes of scratch, above the %zu-byte cap", bytes, kWorkspaceCap);
+    bytes = (bytes + 255) & ~size_t(255);
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(stream, &cap);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+    if (cap != cudaStreamCaptureStatusNone) {
+        cudaMemPool_t pool = nullptr;
+        coc_status_t st = device_pool(ds, &pool);
+        if (st != COC_OK) return st;
+        g_alloc_calls.fetch_add(1);
+        if ((e = cudaMallocFromPoolAsync(&out->ptr, bytes, pool, stream)) != cudaSuccess)
+            return cuda_fail(e, "cudaMallocFromPoolAsync (scratch of a captured call)");
+        out->captured = true;
+        return COC_OK;
+    }
+    std::lock_guard<std::mutex> lk(g_mu);
+    Workspace& w = ds->ws[stream];
+    if (w.last_use == nullptr && (e = cudaEventCreateWithFlags(&w.last_use, cudaEventDisableTiming)) != cudaSuccess) {
+        w.last_use = nullptr;
+        return cuda_fail(e, "cudaEventCreateWithFlags (workspace)");
+    }
+    if (w.bytes < bytes) {
+        // grow: the previous buffer is freed once every kernel that used it is done
+        if (w.ptr != nullptr) {
+            if ((e = cudaEventSynchronize(w.last_use)) != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize (workspace)");
+            if ((e = cudaFree(w.ptr)) != cudaSuccess) return cuda_fail(e, "cudaFree (workspace)");
+            w.ptr = nullptr;
+            w.bytes = 0;
+        }
+        const size_t want = std::max(bytes, (size_t(1) << 20));
+        g_alloc_calls.fetch_add(1);
+        if ((e = cudaMalloc(&w.ptr, want)) != cudaSuccess) {
+            w.ptr = nullptr;
+            return cuda_fail(e, "cudaMalloc (workspace)");
+        }
+        w.bytes = want;
+    }
+    // after the previous user of this workspace (this stream, or a destroyed
+    // stream whose handle this one reuses)
+    if ((e = cudaStreamWaitEvent(stream, w.last_use, 0)) != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent (workspace)");
+    out->ptr = w.ptr;
+    out->w = &w;
+    return COC_OK;
+}
+
+coc_status_t scratch_release(cudaStream_t stream, Scratch& sc, coc_status_t st) {
+    cudaError_t e = cudaSuccess;
+    if (sc.captured && sc.ptr != nullptr) e = cudaFreeAsync(sc.ptr, stream);
+    else if (sc.w != nullptr) e = cudaEventRecord(sc.w->last_use, stream);
+    sc = Scratch{};
+    if (st == COC_OK && e != cudaSuccess) st = cuda_fail(e, "releasing the call's scratch");
+    return st;
+}
+
+// Pre-pass path: dequantise all ranks' weights into the call's scratch, run
+// the AllReduce on it, release the scratch in stream order.
 coc_status_t w8_prepass_all_reduce(int R, int64_t m, int64_t n, int64_t ks, const void* const* x, const void* const* w,
                                    const void* const* scale, const void* const* zero, coc_scale_t gran, int64_t group,
                                    void* const* out, coc_dtype_t dt, int chunks, cudaStream_t stream) {
     DeviceState* ds = nullptr;
     coc_status_t st = device_state(&ds);
     if (st != COC_OK) return st;
-    cudaMemPool_t pool = nullptr;
-    if ((st = device_pool(ds, &pool)) != COC_OK) return st;
     const size_t per_rank = static_cast<size_t>(ks) * static_cast<size_t>(n);   // elements
-    void* ws = nullptr;
-    cudaError_t e = cudaMallocFromPoolAsync(&ws, per_rank * 2 * R, pool, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMallocFromPoolAsync (w8A16 workspace)");
+    Scratch sc;
+    if ((st = scratch_acquire(ds, stream, per_rank * 2 * R, &sc)) != COC_OK) return st;
+    void* ws = sc.ptr;
+    cudaError_t e;
     W8PrepassArgs a;
     std::memset(&a, 0, sizeof a);
     const void* wd[COC_MAX_RANKS] = {};
@@ -428,9 +514,7 @@ coc_status_t w8_prepass_all_reduce(int R, int64_t m, int64_t n, int64_t ks, cons
     // (unsplit, like the fused w8A16 kernel: both paths give the same bits)
     else st = row_parallel(OP_AR, R, m, n, ks, x, wd, out, R, dt, chunks, nullptr, COC_SCALE_TENSOR, 0, stream, false,
                            nullptr, false);
-    const cudaError_t ef = cudaFreeAsync(ws, stream);
-    if (st == COC_OK && ef != cudaSuccess) st = cuda_fail(ef, "cudaFreeAsync (w8A16 workspace)");
-    return st;
+    return scratch_release(stream, sc, st);
 }
 
 // Rows each destination buffer of the MoE dispatch needs in the worst case:
@@ -768,20 +852,18 @@ static coc_status_t moe_impl(int R, int64_t tokens, int k, int64_t h, int64_t f,
     MoeRouteArgs ra;
     std::memset(&ra, 0, sizeof ra);
     void* ws = nullptr;
-    cudaMemPool_t pool = nullptr;
+    Scratch sc;
     // routing table: R x tokens destination rows, then (combine) R x capacity source tokens
     const bool fused_combine = y_tok != nullptr && gates == nullptr;
     const size_t dest_ints = static_cast<size_t>(R) * entries;
     const size_t src_ints = fused_combine ? static_cast<size_t>(R) * capacity : 0;
     if (tokens > 0) {
-        if ((st = device_pool(ds, &pool)) != COC_OK) return st;
-        cudaError_t e = cudaMallocFromPoolAsync(&ws, (dest_ints + src_ints) * sizeof(int32_t), pool, s);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaMallocFromPoolAsync (MoE routing table)");
+        if ((st = scratch_acquire(ds, s, (dest_ints + src_ints) * sizeof(int32_t), &sc)) != COC_OK) return st;
+        ws = sc.ptr;
+        cudaError_t e;
         if (src_ints > 0 &&
-            (e = cudaMemsetAsync(static_cast<int32_t*>(ws) + dest_ints, 0xFF, src_ints * sizeof(int32_t), s)) != cudaSuccess) {
-            cudaFreeAsync(ws, s);
-            return cuda_fail(e, "cudaMemsetAsync (MoE source map)");
-        }
+            (e = cudaMemsetAsync(static_cast<int32_t*>(ws) + dest_ints, 0xFF, src_ints * sizeof(int32_t), s)) != cudaSuccess)
+            return scratch_release(s, sc, cuda_fail(e, "cudaMemsetAsync (MoE source map)"));
     }
     for (int r = 0; r < R; ++r) ra.idx[r] = tokens > 0 ? idx[r] : nullptr;
     ra.dest = static_cast<int32_t*>(ws);
@@ -875,11 +957,7 @@ static coc_status_t moe_impl(int R, int64_t tokens, int k, int64_t h, int64_t f,
         e = launch_moe_combine(ca, dt == COC_BF16, ds->sm_count, s);
         if (e != cudaSuccess) st = cuda_fail(e, "MoE top-k combine launch");
     }
-    if (ws != nullptr) {
-        const cudaError_t ef = cudaFreeAsync(ws, s);
-        if (st == COC_OK && ef != cudaSuccess) st = cuda_fail(ef, "cudaFreeAsync (MoE routing table)");
-    }
-    return st;
+    return scratch_release(s, sc, st);
 }
 
 COC_API coc_status_t coc_moe_dispatch_grouped_matmul(int R, int64_t tokens, int64_t h, int64_t f, int experts_per_rank,
@@ -914,21 +992,42 @@ COC_API coc_status_t coc_moe_topk_grouped_matmul_combine(int R, int64_t tokens, 
                     dt, stream);
 }
 
+// Status words of the current device's library state, read and cleared; all
+// zero (and nothing created) when no allocating call has run on the device.
+static coc_status_t take_library_status(unsigned (&words)[STATUS_WORDS]) {
+    std::memset(words, 0, sizeof words);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    unsigned* status = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto it = g_dev.find(dev);
+        if (it != g_dev.end()) status = it->second.status;
+    }
+    if (status == nullptr) return COC_OK;
+    if ((e = cudaMemcpy(words, status, sizeof words, cudaMemcpyDeviceToHost)) != cudaSuccess)
+        return cuda_fail(e, "cudaMemcpy(status)");
+    if (words[0] != 0 && (e = cudaMemset(status, 0, sizeof words)) != cudaSuccess) return cuda_fail(e, "cudaMemset(status)");
+    return COC_OK;
+}
+
 COC_API coc_status_t coc_sync_status(coc_stream_t stream) {
     cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
-    DeviceState* ds = nullptr;
-    coc_status_t st = device_state(&ds);
+    // both status blocks: the library's (allocating entry points) and the
+    // static one of the allocation-free entry point; neither read allocates
+    unsigned lib_words[STATUS_WORDS], na_words[STATUS_WORDS];
+    coc_status_t st = take_library_status(lib_words);
     if (st != COC_OK) return st;
-    unsigned words[STATUS_WORDS] = {0};
-    if ((e = cudaMemcpy(words, ds->status, sizeof words, cudaMemcpyDeviceToHost)) != cudaSuccess)
-        return cuda_fail(e, "cudaMemcpy(status)");
+    if ((st = noalloc_take_status(na_words)) != COC_OK) return st;
+    const unsigned* words = lib_words[0] != 0 ? lib_words : na_words;
     if (words[0] != 0) {
-        if ((e = cudaMemset(ds->status, 0, sizeof words)) != cudaSuccess) return cuda_fail(e, "cudaMemset(status)");
         if (words[0] == DEV_ERR_BAD_INDEX)
             return fail(COC_ERR_INVALID_ARG, "MoE dispatch: an expert id was outside [0, E); those tokens were not dispatched");
-        return fail(COC_ERR_TIMEOUT, "device wait timed out (flags 0x%x, first wait site 0x%x, block %u)", words[0],
-                    words[1], words[2] ? words[2] - 1 : 0);
+        return fail(COC_ERR_TIMEOUT, "device wait timed out%s (flags 0x%x, first wait site 0x%x, block %u)",
+                    words == na_words ? " in the allocation-free AllReduce" : "", words[0], words[1],
+                    words[2] ? words[2] - 1 : 0);
     }
     return COC_OK;
 }
@@ -955,12 +1054,56 @@ COC_API coc_status_t coc_debug_inject_timeout(int enable) {
     return COC_OK;
 }
 
+COC_API int64_t coc_debug_alloc_count(void) { return static_cast<int64_t>(g_alloc_calls.load()); }
+
+COC_API coc_status_t coc_debug_clock_probe(int slot) {
+    if (slot < -1 || slot >= CLOCK_SLOTS) return fail(COC_ERR_INVALID_ARG, "clock slot %d outside [-1, %d)", slot, CLOCK_SLOTS);
+    g_clock_slot.store(slot);
+    return COC_OK;
+}
+
+COC_API coc_status_t coc_debug_clock_read(int slot, int64_t* cycles, int64_t* ns) {
+    if (slot < 0 || slot >= CLOCK_SLOTS || cycles == nullptr || ns == nullptr)
+        return fail(COC_ERR_INVALID_ARG, "clock slot %d outside [0, %d) or NULL output", slot, CLOCK_SLOTS);
+    *cycles = 0;
+    *ns = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    unsigned* status = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto it = g_dev.find(dev);
+        if (it != g_dev.end()) status = it->second.status;
+    }
+    if (status == nullptr) return COC_OK;
+    if ((e = cudaDeviceSynchronize()) != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    unsigned long long v[2] = {0, 0};
+    unsigned long long* src = reinterpret_cast<unsigned long long*>(status + STATUS_WORDS) + 2 * slot;
+    if ((e = cudaMemcpy(v, src, sizeof v, cudaMemcpyDeviceToHost)) != cudaSuccess) return cuda_fail(e, "cudaMemcpy(clock)");
+    if ((e = cudaMemset(src, 0, sizeof v)) != cudaSuccess) return cuda_fail(e, "cudaMemset(clock)");
+    *cycles = static_cast<int64_t>(v[0]);
+    *ns = static_cast<int64_t>(v[1]);
+    return COC_OK;
+}
+
 COC_API coc_status_t coc_shutdown(void) {
     std::lock_guard<std::mutex> lk(g_mu);
     int cur = 0;
     const bool have_cur = cudaGetDevice(&cur) == cudaSuccess;
     coc_status_t st = COC_OK;
     for (auto& kv : g_dev) {
+        if (!kv.second.ws.empty() && cudaSetDevice(kv.first) == cudaSuccess) {
+            for (auto& w : kv.second.ws) {
+                if (w.second.last_use != nullptr) {
+                    cudaEventSynchronize(w.second.last_use);
+                    cudaEventDestroy(w.second.last_use);
+                }
+                if (w.second.ptr != nullptr && cudaFree(w.second.ptr) != cudaSuccess)
+                    st = fail(COC_ERR_CUDA, "could not free a workspace of device %d", kv.first);
+            }
+            kv.second.ws.clear();
+        }
         if (kv.second.pool != nullptr) {
             if (cudaSetDevice(kv.first) == cudaSuccess && cudaMemPoolDestroy(kv.second.pool) == cudaSuccess)
                 kv.second.pool = nullptr;
@@ -976,6 +1119,7 @@ COC_API coc_status_t coc_shutdown(void) {
     }
     if (have_cur) cudaSetDevice(cur);
     g_dev.clear();
+    noalloc_forget_devices();
     return st;
 }
 
@@ -989,5 +1133,7 @@ coc_status_t validate_all_reduce_args(int R, int64_t m, int64_t n, int64_t k_sha
 }
 
 coc_status_t report_error(coc_status_t st, const char* msg) { return fail(st, "%s", msg); }
+
+int inject_timeout_enabled() { return g_inject.load(); }
 
 }  // namespace coc

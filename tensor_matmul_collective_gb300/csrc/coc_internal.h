@@ -31,6 +31,12 @@ constexpr int NUM_OPS = 5;
 // Device status words (per device, zero when healthy).
 enum : unsigned { DEV_ERR_TIMEOUT = 1u, DEV_ERR_BAD_INDEX = 2u };
 constexpr int STATUS_WORDS = 8;   // [0] error bits, [1] first "where" code, [2] block
+// After the status words, CLOCK_SLOTS clock-probe slots of two uint64 each
+// (SM cycles, ns) accumulated by block 0 of every fused-kernel launch made
+// while coc_debug_clock_probe selects that slot: the clock the kernels
+// actually ran at is cycles / ns.
+constexpr int CLOCK_SLOTS = 8;
+constexpr int STATUS_BLOCK_WORDS = STATUS_WORDS + 4 * CLOCK_SLOTS;
 
 struct KParams {
     CUtensorMap tm_a[COC_MAX_RANKS];    // A operand (X shards), K-major, 128B swizzle
@@ -61,6 +67,7 @@ struct KParams {
     int gran;          // w8A16 scale granularity
     int group;         // w8A16 group size (rows of K)
     int inject_timeout;
+    int clock_slot;    // clock-probe slot this launch accumulates into; -1: none
     int has_gather;    // AG-V2
     int a_hint, b_hint;  // L2 policy of A / B loads: 0 evict_normal, 1 evict_first, 2 evict_last
     int b_kmajor;      // W stored n x k (K-major B operand) instead of k x n
@@ -89,6 +96,14 @@ coc_status_t validate_all_reduce_args(int R, int64_t m, int64_t n, int64_t k_sha
                                       const void* const* w, void* const* out, coc_dtype_t dt, int chunks,
                                       int deterministic);
 coc_status_t report_error(coc_status_t st, const char* msg);
+// coc_debug_inject_timeout's flag, for kernels launched outside coc_api.cu.
+int inject_timeout_enabled();
+// Allocation-free entry point (coc_noalloc.cu): read and clear its static
+// status block on the current device (all zero if it never ran there), and
+// forget the per-device set-up (coc_shutdown, so a later call after a device
+// reset looks the block's address up again).
+coc_status_t noalloc_take_status(unsigned (&words)[STATUS_WORDS]);
+void noalloc_forget_devices();
 
 // w8A16 streaming pre-pass (coc_w8_prepass.cu): dequantise every rank's int8
 // weight once, Wd = rne((q - z) * s) in the activation type, into a 16-bit

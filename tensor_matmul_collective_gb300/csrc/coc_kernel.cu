@@ -615,6 +615,13 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
     else __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // clock probe: block 0 measures the SM cycles and nanoseconds it spends
+    const bool probe = p.clock_slot >= 0 && blockIdx.x == 0 && threadIdx.x == 0;
+    uint64_t probe_clk = 0, probe_ns = 0;
+    if (probe) {
+        probe_clk = clock64();
+        probe_ns = globaltimer();
+    }
     const int total_kb = p.num_kshards * p.kblocks;
     // split by rank: a unit is part u % ksplit of tile u / ksplit and sums
     // R / ksplit shards (AllReduce / ReduceScatter only)
@@ -1141,6 +1148,12 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
             tc_fence_after();
             tmem_dealloc(tmem_base, 2 * BN);
         }
+    }
+    if (probe) {
+        unsigned long long* slot =
+            reinterpret_cast<unsigned long long*>(p.status + STATUS_WORDS) + 2 * p.clock_slot;
+        atomicAdd(slot, static_cast<unsigned long long>(clock64() - probe_clk));
+        atomicAdd(slot + 1, static_cast<unsigned long long>(globaltimer() - probe_ns));
     }
 }
 

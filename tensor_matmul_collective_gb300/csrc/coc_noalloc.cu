@@ -25,9 +25,9 @@
 
 #include "coc_internal.h"
 
-// 256 bytes: room for the kernel's status block (STATUS_WORDS words).
+// 256 bytes: room for the kernel's status block (STATUS_BLOCK_WORDS words).
 constexpr int kNoallocScratchWords = 64;
-static_assert(coc::STATUS_WORDS <= kNoallocScratchWords, "status block must fit the static scratch");
+static_assert(coc::STATUS_BLOCK_WORDS <= kNoallocScratchWords, "status block must fit the static scratch");
 
 static __device__ __align__(256) unsigned g_noalloc_scratch[kNoallocScratchWords];
 
@@ -79,6 +79,10 @@ coc_status_t setup(NoallocDevice** out) {
         void* p = nullptr;
         if ((e = cudaGetSymbolAddress(&p, g_noalloc_scratch)) != cudaSuccess)
             return cuda_error(e, "cudaGetSymbolAddress(scratch)");
+        // the status block starts at zero; after this it is cleared only when
+        // coc_sync_status reads a non-zero status, so a timeout stays visible
+        // until it is reported (later calls do not wipe it)
+        if ((e = cudaMemset(p, 0, sizeof g_noalloc_scratch)) != cudaSuccess) return cuda_error(e, "cudaMemset(scratch)");
         d.scratch = static_cast<unsigned*>(p);
         d.ready = true;
     }
@@ -144,11 +148,40 @@ extern "C" __attribute__((visibility("default"))) coc_status_t coc_matmul_all_re
         }
         if ((st = encode_2d(&p.tm_out[r], tdt, out[r], n, m, n * 2, EPI_COLS, p.store_rows)) != COC_OK) return st;
     }
-    // The status words must start at zero; clear them in stream order.
-    cudaError_t e = cudaMemsetAsync(d->scratch, 0, STATUS_WORDS * sizeof(unsigned), s);
-    if (e != cudaSuccess) return cuda_error(e, "cudaMemsetAsync(scratch)");
     p.status = d->scratch;
+    p.inject_timeout = inject_timeout_enabled();
+    p.clock_slot = -1;
     const int grid = p.units < d->sm_count ? p.units : d->sm_count;
-    if ((e = launch(OP_AR, dt == COC_BF16, false, p, grid, s)) != cudaSuccess) return cuda_error(e, "kernel launch");
+    const cudaError_t e = launch(OP_AR, dt == COC_BF16, false, p, grid, s);
+    if (e != cudaSuccess) return cuda_error(e, "kernel launch");
     return COC_OK;
 }
+
+namespace coc {
+
+coc_status_t noalloc_take_status(unsigned (&words)[STATUS_WORDS]) {
+    for (int i = 0; i < STATUS_WORDS; ++i) words[i] = 0u;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_error(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return COC_OK;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!g_devices[dev].ready) return COC_OK;   // never ran here: nothing to report, nothing set up
+    }
+    if ((e = cudaMemcpyFromSymbol(words, g_noalloc_scratch, sizeof words)) != cudaSuccess)
+        return cuda_error(e, "cudaMemcpyFromSymbol(scratch)");
+    if (words[0] != 0u) {
+        const unsigned zero[STATUS_WORDS] = {};
+        if ((e = cudaMemcpyToSymbol(g_noalloc_scratch, zero, sizeof zero)) != cudaSuccess)
+            return cuda_error(e, "cudaMemcpyToSymbol(scratch)");
+    }
+    return COC_OK;
+}
+
+void noalloc_forget_devices() {
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (NoallocDevice& d : g_devices) d = NoallocDevice{};
+}
+
+}  // namespace coc
