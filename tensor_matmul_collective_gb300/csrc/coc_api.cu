@@ -53,6 +53,8 @@ struct DeviceState {
     int cc_major = 0, cc_minor = 0;
     unsigned* status = nullptr;
     int max_pairs[NUM_OPS][2] = {{-1, -1}, {-1, -1}, {-1, -1}, {-1, -1}, {-1, -1}};   // per op, per bf16; -1 = not queried
+    int ts_pairs[2] = {-1, -1};     // co-resident pairs of the w8A16 tensor-memory kernel, per bf16
+    int split_clusters[2][2][2] = {{{-1, -1}, {-1, -1}}, {{-1, -1}, {-1, -1}}};   // [RS][bf16][ksplit 4]: co-resident
     cudaMemPool_t pool = nullptr;   // stream-ordered allocations of calls captured into CUDA graphs
     std::unordered_map<cudaStream_t, Workspace> ws;   // per-stream scratch of eager calls
 };
@@ -275,6 +277,14 @@ coc_status_t scratch_release(cudaStream_t stream, Scratch& sc, coc_status_t st);
 // call in a CUDA graph): m 1 / 16 / 64 / 128 take 48 / 42 / 42 / 49 us split
 // in 4 against 70 / 62 / 55 / 60 us unsplit; for 256-row tiles (m > 128)
 // splitting gained nothing (m 256: 54 us either way), so they are not split.
+// COC_SPLIT_PATH=scratch forces the rank split through global scratch
+// instead of a cluster's shared memory (tests and tuning only; both give the
+// same bits: the same parts added in the same order).
+bool split_cluster_allowed() {
+    const char* e = std::getenv("COC_SPLIT_PATH");
+    return !(e != nullptr && std::strcmp(e, "scratch") == 0);
+}
+
 int rank_split(int op, int R, int64_t ks, int64_t tiles, bool pair, int sm_count) {
     int ksplit = 1;
     if ((op == OP_AR || op == OP_RS) && ks > 0 && R > 1) {
@@ -367,10 +377,31 @@ coc_status_t row_parallel(int op, int R, int64_t m, int64_t n, int64_t ks, const
     const int ksplit = allow_split ? rank_split(op, R, ks, tiles, pair, ds->sm_count) : 1;
     if (ksplit == 1) return launch_checked(op, dt == COC_BF16, pair, p, ds, stream);
 
-    // rank split: fp32 parts and arrival counters in a stream-ordered workspace
     p.ksplit = ksplit;
     p.units = static_cast<int>(tiles * ksplit);
     for (int o = 0; o < (op == OP_RS ? R : n_out); ++o) p.outp[o] = static_cast<uint16_t*>(out[o]);
+    // rank split through distributed shared memory: the ksplit part-CTAs of a
+    // tile are one cluster, one unit per CTA (all tiles' clusters co-resident)
+    if (!pair && (ksplit == 2 || ksplit == 4) && split_cluster_allowed()) {
+        int clusters = 0;
+        {
+            std::lock_guard<std::mutex> lk(g_mu);
+            int& v = ds->split_clusters[op == OP_RS ? 1 : 0][dt == COC_BF16 ? 1 : 0][ksplit == 4 ? 1 : 0];
+            if (v < 0) v = max_split_clusters(op, dt == COC_BF16, ksplit);
+            clusters = v;
+        }
+        if (clusters >= tiles) {
+            p.split_cluster = 1;
+            p.status = ds->status;
+            p.inject_timeout = g_inject.load();
+            p.clock_slot = g_clock_slot.load();
+            const cudaError_t e = launch_split(op, dt == COC_BF16, p, p.units, ksplit, stream);
+            return e == cudaSuccess ? COC_OK : cuda_fail(e, "kernel launch (rank split in clusters)");
+        }
+    }
+
+    // rank split through global memory: fp32 parts and arrival counters in the
+    // stream's workspace, the last part to arrive adds them
     const size_t part_bytes = static_cast<size_t>(tiles) * ksplit * tile_m * BN * sizeof(float);
     const size_t cnt_bytes = static_cast<size_t>(tiles) * (pair ? 2 : 1) * NUM_EPI_WARPS * sizeof(unsigned);
     Scratch sc;
@@ -400,20 +431,23 @@ coc_status_t validate_row_parallel(int R, int64_t m, int64_t n, int64_t ks, cons
     return COC_OK;
 }
 
-// w8A16 path choice.  The fused kernel dequantises each weight tile in shared
-// memory once per 256-row tile; the pre-pass dequantises every weight element
-// once through HBM (1 byte read, 2 written) and then runs the AllReduce
-// kernel.  The pre-pass costs about 3 K n / HBM bandwidth against the fused
-// path's ~20% of the GEMM time (measured: 14.5% conversion traffic in shared
-// memory plus the extra barrier handshake), so it wins from roughly m = 1700
-// rows.  COC_W8_PATH=fused|prepass forces a path (tests, tuning).
+// w8A16 schedule.  Three kernels compute the same bits: the persistent fused
+// kernel whose dequant warps write the 16-bit weight tile to shared memory
+// ("fused"), a streaming pre-pass that dequantises every weight element once
+// into the stream's workspace followed by the fp16 AllReduce kernel
+// ("prepass"), and one launch of the kernel that keeps the dequantised weight
+// in tensor memory ("ts", coc_w8_ts.cu).  Default: the fused kernel below
+// kW8PrepassMinRows rows, the pre-pass from there (it repeats no conversion
+// per row tile); COC_W8_PATH=fused|prepass|ts forces one (tests, tuning).
+enum class W8Path { TS, Fused, Prepass };
 constexpr int64_t kW8PrepassMinRows = 2048;
 
-bool w8_use_prepass(int64_t m) {
+W8Path w8_path(int64_t m) {
     const char* e = std::getenv("COC_W8_PATH");
-    if (e != nullptr && std::strcmp(e, "fused") == 0) return false;
-    if (e != nullptr && std::strcmp(e, "prepass") == 0) return true;
-    return m >= kW8PrepassMinRows;
+    if (e != nullptr && std::strcmp(e, "fused") == 0) return W8Path::Fused;
+    if (e != nullptr && std::strcmp(e, "prepass") == 0) return W8Path::Prepass;
+    if (e != nullptr && std::strcmp(e, "ts") == 0) return W8Path::TS;
+    return m >= kW8PrepassMinRows ? W8Path::Prepass : W8Path::Fused;
 }
 
 coc_status_t device_pool(DeviceState* ds, cudaMemPool_t* out) {
@@ -517,6 +551,73 @@ coc_status_t w8_prepass_all_reduce(int R, int64_t m, int64_t n, int64_t ks, cons
     return scratch_release(stream, sc, st);
 }
 
+// The default w8A16 path: Y^T = Wd^T X^T in one launch, the int8 weight
+// dequantised in registers into tensor memory (the MMA's A operand).
+coc_status_t w8_ts_all_reduce(int R, int64_t m, int64_t n, int64_t ks, const void* const* x, const void* const* w,
+                              const void* const* scale, const void* const* zero, coc_scale_t gran, int64_t group,
+                              void* const* out, coc_dtype_t dt, int chunks, cudaStream_t stream) {
+    DeviceState* ds = nullptr;
+    coc_status_t st = device_state(&ds);
+    if (st != COC_OK) return st;
+    KParams p;
+    std::memset(&p, 0, sizeof p);
+    p.R = R;
+    p.n_out = R;
+    p.m = static_cast<int>(m);
+    p.n = static_cast<int>(n);
+    p.k = static_cast<int>(ks);
+    p.num_kshards = R;
+    p.kblocks = static_cast<int>((ks + BK - 1) / BK);
+    // rows per unit (the MMA's N): the smallest power of two >= m in [32, 256],
+    // so that decode-sized m does not pay for 256-row tiles
+    int nr = 32;
+    while (nr < TS_MAX_ROWS && nr < m) nr *= 2;
+    p.unit_rows = nr;
+    p.m_tiles = static_cast<int>((m + nr - 1) / nr);
+    p.n_tiles = static_cast<int>((n + TS_UNIT_COLS - 1) / TS_UNIT_COLS);
+    p.units = p.m_tiles * p.n_tiles;
+    p.chunk_mt = chunk_m_tiles(m, chunks, nr);
+    p.gran = static_cast<int>(gran);
+    p.group = static_cast<int>(group);
+    int pairs = 0;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        int& v = ds->ts_pairs[dt == COC_BF16 ? 1 : 0];
+        if (v < 0) v = w8_ts_max_pairs(dt == COC_BF16);
+        pairs = v;
+    }
+    if (pairs <= 0) return fail(COC_ERR_CUDA, "no co-resident CTA pair of the w8A16 kernel fits on this device");
+    {
+        const int64_t k_total = static_cast<int64_t>(R) * ks;
+        p.group_mt = row_group(p.chunk_mt, p.n_tiles, int64_t(nr) * k_total * 2, int64_t(TS_UNIT_COLS) * k_total, pairs);
+        if (p.group_mt > 0) p.a_hint = 2;   // the group's X rows stay in L2 while W streams past
+    }
+    const CUtensorMapDataType adt = tma_dtype(dt);
+    for (int r = 0; r < R; ++r) {
+        if (ks > 0) {
+            if ((st = encode(&p.tm_a[r], adt, x[r], ks, m, ks * 2, BK, nr / 2, CU_TENSOR_MAP_SWIZZLE_128B)) != COC_OK)
+                return st;
+            if ((st = encode(&p.tm_b[r], CU_TENSOR_MAP_DATA_TYPE_UINT8, w[r], n, ks, n, TS_UNIT_COLS / 2, BK,
+                             CU_TENSOR_MAP_SWIZZLE_128B)) != COC_OK)
+                return st;
+        }
+        p.scale[r] = static_cast<const uint16_t*>(scale[r]);
+        p.outp[r] = static_cast<uint16_t*>(out[r]);
+    }
+    if (zero != nullptr) {
+        p.has_zero = 1;
+        for (int r = 0; r < R; ++r) p.zero[r] = static_cast<const int8_t*>(zero[r]);
+    }
+    p.replica_stores = 1;
+    p.status = ds->status;
+    p.inject_timeout = g_inject.load();
+    p.clock_slot = g_clock_slot.load();
+    const int grid = 2 * (p.units < pairs ? p.units : pairs);
+    const cudaError_t e = launch_w8_ts(p, dt == COC_BF16, grid, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "w8A16 kernel launch");
+    return COC_OK;
+}
+
 // Rows each destination buffer of the MoE dispatch needs in the worst case:
 // all tokens of all ranks, each of the rank's eloc expert groups padded to a
 // 256-row boundary.
@@ -594,7 +695,11 @@ COC_API coc_status_t coc_matmul_all_reduce_w8a16_ex(int R, int64_t m, int64_t n,
                         (long long)group_size);
     }
     if (empty) return COC_OK;
-    if (k_shard > 0 && w8_use_prepass(m))
+    const W8Path path = w8_path(m);
+    if (path == W8Path::TS)
+        return w8_ts_all_reduce(R, m, n, k_shard, x, w, scale, zero, gran, group_size, out, dt, chunks,
+                                reinterpret_cast<cudaStream_t>(stream));
+    if (k_shard > 0 && path == W8Path::Prepass)
         return w8_prepass_all_reduce(R, m, n, k_shard, x, w, scale, zero, gran, group_size, out, dt, chunks,
                                      reinterpret_cast<cudaStream_t>(stream));
     return row_parallel(OP_W8, R, m, n, k_shard, x, w, out, R, dt, chunks, scale, gran, group_size,

@@ -68,6 +68,7 @@ struct KParams {
     int group;         // w8A16 group size (rows of K)
     int inject_timeout;
     int clock_slot;    // clock-probe slot this launch accumulates into; -1: none
+    int unit_rows;     // w8A16 tensor-memory kernel: activation rows per unit (32, 64, 128 or 256)
     int has_gather;    // AG-V2
     int a_hint, b_hint;  // L2 policy of A / B loads: 0 evict_normal, 1 evict_first, 2 evict_last
     int b_kmajor;      // W stored n x k (K-major B operand) instead of k x n
@@ -88,6 +89,12 @@ struct KParams {
     int ksplit;
     float* part;          // tiles x ksplit x TILE_M x BN fp32
     unsigned* part_cnt;   // tiles x (CTAs per tile) x NUM_EPI_WARPS arrival counters, zero at launch
+    // Rank split through distributed shared memory (single-CTA tiles, ksplit 2
+    // or 4, one unit per CTA): the ksplit part-CTAs of a tile are one cluster;
+    // each drains its fp32 part into its own shared memory, and CTA j adds
+    // all parts (in part order) of columns [j BN / ksplit, (j+1) BN / ksplit)
+    // read from the cluster's shared memory.  part / part_cnt are unused.
+    int split_cluster;
 };
 
 // Argument checks of coc_matmul_all_reduce and the per-thread error text
@@ -116,6 +123,19 @@ struct W8PrepassArgs {
     int R, k, n, gran, group;
 };
 cudaError_t launch_w8_prepass(const W8PrepassArgs& a, bool bf16, int sm_count, cudaStream_t stream);
+
+// w8A16 AllReduce with the dequantised weight in tensor memory
+// (coc_w8_ts.cu), run by CTA pairs: a unit is TS_UNIT_COLS weight columns
+// (TS_UNIT_COLS / 2 per CTA) x p.unit_rows activation rows (half per CTA).
+// p as for the fused kernel's w8A16 operator, with n_tiles counting
+// TS_UNIT_COLS-column tiles, m_tiles unit_rows-row tiles, the X maps boxed
+// BK x unit_rows / 2 (128-byte swizzle), the int8 weight maps boxed
+// TS_UNIT_COLS / 2 x BK (128-byte swizzle), and the R outputs in outp.
+// grid = 2 x min(units, w8_ts_max_pairs()).
+constexpr int TS_UNIT_COLS = 256;
+constexpr int TS_MAX_ROWS = 256;
+cudaError_t launch_w8_ts(const KParams& p, bool bf16, int grid, cudaStream_t stream);
+int w8_ts_max_pairs(bool bf16);
 
 // MoE dispatch (coc_moe.cu): the routing kernel counts each rank's tokens per
 // expert and gives every token its row in its expert's (256-row aligned)
@@ -158,6 +178,11 @@ cudaError_t launch_moe_combine(const MoeCombineArgs& a, bool bf16, int sm_count,
 // 2-SM variant (a cluster of two CTAs per 256-row tile; grid = 2 x pairs);
 // otherwise one CTA per 128-row tile.
 cudaError_t launch(int op, bool bf16, bool pair, const KParams& p, int grid, cudaStream_t stream);
+// Single-CTA kernel launched in clusters of `cluster` CTAs (the rank split
+// through distributed shared memory, p.split_cluster), and the number of such
+// clusters that can be co-resident.
+cudaError_t launch_split(int op, bool bf16, const KParams& p, int grid, int cluster, cudaStream_t stream);
+int max_split_clusters(int op, bool bf16, int cluster);
 // Co-resident CTA pairs the 2-SM variant can have on the current device.
 int max_pairs(int op, bool bf16);
 

@@ -49,349 +49,10 @@
 
 #include "coc_dequant.cuh"
 #include "coc_internal.h"
+#include "coc_ptx.cuh"
 
 namespace coc {
 namespace {
-
-#ifndef COC_WAIT_NS
-#define COC_WAIT_NS 1000000000ull   // one second
-#endif
-constexpr unsigned long long kDrainNs = 20000000ull;  // 20 ms for post-abort drains
-
-// ------------------------------------------------------------ PTX helpers ---
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ uint64_t globaltimer() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// TMA tile load into shared memory with an L2 eviction-priority policy for the loaded lines.
-__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map, int c0, int c1,
-                                                 uint32_t bar, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
-        : "memory");
-}
-
-// L2 policies: 0 evict_normal, 1 evict_first (streamed once), 2 evict_last (reused).
-__device__ __forceinline__ uint64_t make_l2_policy(int kind) {
-    uint64_t pol;
-    if (kind == 1) asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-    else if (kind == 2) asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
-    else asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
-    return pol;
-}
-
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int c0, int c1) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
-            reinterpret_cast<uint64_t>(map)),
-        "r"(c0), "r"(c1), "r"(src)
-        : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void bulk_wait_read() {
-    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
-
-// ---- tcgen05 ----
-
-__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
-                 "r"(ncols)
-                 : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish() {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-                 : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                           uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-        : "memory");
-}
-
-// 32 lanes x 32 consecutive fp32 columns: thread t receives lane (base + t).
-__device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&v)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
-          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
-          "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
-          "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
-          "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
-        : "r"(taddr)
-        : "memory");
-}
-__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
-// ---- CTA pairs (2-SM tcgen05 MMA) ----
-//
-// A cluster of two CTAs on neighbouring SMs computes one 256-row tile: each
-// CTA holds 128 rows of A and 128 of the 256 B columns in its own shared
-// memory and 128 accumulator lanes in its own TMEM; the even CTA ("leader")
-// issues the MMAs for both.  The peer's TMA loads complete on the leader's
-// barriers, the leader's commits arrive on both CTAs' barriers.
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ uint32_t cluster_id() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ uint32_t cluster_count() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// Address of the same shared-memory location in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-    return r;
-}
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-// TMA load into this CTA's shared memory, completing on a barrier that may
-// live in the peer CTA (cluster address).
-__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int c0, int c1,
-                                                 uint32_t bar_cluster, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar_cluster), "l"(policy)
-        : "memory");
-}
-// Bulk copy from this CTA's shared memory to a (peer) CTA's shared memory,
-// completing `bytes` of transaction count on a barrier in the destination CTA.
-// Used as an async-proxy "ready" signal that follows a fence.proxy.async.
-__device__ __forceinline__ void bulk_copy_s2s_signal(uint32_t dst_cluster, uint32_t src, uint32_t bytes,
-                                                     uint32_t bar_cluster) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            dst_cluster),
-        "r"(src), "r"(bytes), "r"(bar_cluster)
-        : "memory");
-}
-__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
-                 : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish_pair() {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-__device__ __forceinline__ void tc_mma_f16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                                uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-// Arrive on the barrier at this offset in both CTAs of the pair once the
-// issuing thread's MMAs are complete.
-__device__ __forceinline__ void tc_commit_pair_both(uint32_t bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            bar),
-        "h"(static_cast<uint16_t>(3))
-        : "memory");
-}
-__device__ __forceinline__ void tc_commit_pair_local(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
-
-// Instruction descriptor, kind::f16: D fp32, A/B both fp16 or both bf16,
-// A K-major, B MN-major ("transposed"), N >> 3 at bit 17, M >> 4 at bit 24.
-__host__ __device__ constexpr uint32_t make_idesc(bool bf16, int M, int N) {
-    return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | (0u << 15) | (1u << 16) |
-           (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
-}
-
-// Shared-memory matrix descriptor: start >> 4 [0,14), LBO >> 4 [16,30),
-// SBO >> 4 [32,46), fixed 0b001 at [46,49), swizzle mode 2 (128-byte) at [61,64).
-__device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-    return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(lbo >> 4) << 16) |
-           (static_cast<uint64_t>(sbo >> 4) << 32) | (1ull << 46) | (2ull << 61);
-}
-
-// ------------------------------------------------------------ bounded waits ---
-
-struct Ctl {
-    volatile uint32_t* abort_flag;   // shared memory, CTA-wide
-    unsigned* status;                // global status words
-};
-
-__device__ __noinline__ void raise_timeout(const Ctl& c, unsigned where) {
-    *c.abort_flag = 1u;
-    atomicOr(c.status, DEV_ERR_TIMEOUT);
-    atomicCAS(c.status + 1, 0u, where);
-    atomicCAS(c.status + 2, 0u, blockIdx.x + 1u);
-}
-
-template <bool CLUSTER>
-__device__ __forceinline__ bool try_wait_scoped(uint32_t bar, uint32_t parity) {
-    if constexpr (CLUSTER) return mbar_try_wait_cluster(bar, parity);
-    else return mbar_try_wait(bar, parity);
-}
-
-// Wait for phase `parity` of `bar`.  False if the CTA is aborting or the wait
-// ran out (which starts the abort).  CLUSTER: acquire at cluster scope (the
-// phase may have been completed by the peer CTA).
-template <bool CLUSTER = false>
-__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const Ctl& c,
-                                             unsigned where, unsigned long long limit_ns) {
-    if (try_wait_scoped<CLUSTER>(bar, parity)) return true;
-    const uint64_t t0 = globaltimer();
-    while (!try_wait_scoped<CLUSTER>(bar, parity)) {
-        if (*c.abort_flag) return false;
-        if (globaltimer() - t0 > limit_ns) {
-            raise_timeout(c, where);
-            return false;
-        }
-    }
-    return true;
-}
-
-// Post-abort drain: wait for a phase that is known to complete (an issued
-// copy or MMA) regardless of the abort flag, for at most limit_ns.
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
-    if (mbar_try_wait(bar, parity)) return;
-    const uint64_t t0 = globaltimer();
-    while (!mbar_try_wait(bar, parity)) {
-        if (globaltimer() - t0 > limit_ns) return;
-    }
-}
-
-// Whole-warp wait with a warp-uniform outcome.
-template <bool CLUSTER = false>
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const Ctl& c, unsigned where) {
-    const bool ok = wait_bounded<CLUSTER>(bar, parity, c, where, COC_WAIT_NS);
-    return __all_sync(0xffffffffu, ok);
-}
-
-// ------------------------------------------------------------ scheduling ---
-
-// Work unit -> (rank r for AllGather, m-tile, n-tile).  Units go chunk by
-// chunk; inside a chunk, m-tiles are taken in groups of group_mt (an L2-sized
-// slice of the A rows), and inside a group the m-tiles of one (rank, n-tile)
-// column are adjacent, so concurrently running CTAs share their B tiles and
-// the group's A rows stay in L2 while the columns stream past.  Odd groups
-// walk the columns backwards, starting on the W columns the previous group
-// read last.
-template <int OP>
-__device__ __forceinline__ void decode_unit(const KParams& p, int u, int& r, int& mt, int& nt) {
-    const int rg = (OP == OP_AG) ? p.R : 1;
-    const int ncols = p.n_tiles * rg;   // (rank, n-tile) columns
-    if (p.chunk_mt > 0) {
-        const int per_chunk = p.chunk_mt * ncols;
-        const int c = u / per_chunk;
-        int v = u - c * per_chunk;
-        const int G = p.group_mt > 0 ? p.group_mt : p.chunk_mt;
-        const int per_group = G * ncols;
-        const int g = v / per_group;
-        v -= g * per_group;
-        const int mi = v % G;
-        int col = v / G;
-        if (g & 1) col = ncols - 1 - col;
-        nt = col % p.n_tiles;
-        r = col / p.n_tiles;
-        mt = c * p.chunk_mt + g * G + mi;
-    } else {
-        mt = u / ncols;
-        const int v = u - mt * ncols;
-        nt = v % p.n_tiles;
-        r = v / p.n_tiles;
-    }
-}
 
 // Grouped GEMM (MoE dispatch): unit -> (expert e, global row tile mt, n-tile
 // nt).  Experts in order; inside an expert, its row tiles are taken in L2
@@ -564,7 +225,8 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
     uint64_t* acce = accf + 2;         // [2]  accumulator drained by the epilogue (leader: both CTAs)
     uint64_t* never = acce + 2;        // [1]  nothing arrives here (fault-injection test)
     uint64_t* drain = never + 1;       // [1]  MMA drain before TMEM release
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* red_ready = drain + 1;   // [1]  rank split in a cluster: every part-CTA's fp32 part is in its smem
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red_ready + 1);
     uint32_t* abort_word = tmem_slot + 1;
     // w8A16 pair: 16-byte landing slots for the peer's per-stage "B half ready" copies
     uint8_t* sig_slots = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(abort_word + 1) + 15) & ~uintptr_t(15));
@@ -596,6 +258,10 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
         }
         mbar_init(smem_u32(never), 1);
         mbar_init(smem_u32(drain), 1);
+        // rank split in a cluster: one arrival per part-CTA and epilogue warp
+        // holding output rows (the split runs on one row tile of m <= 128 rows)
+        const int active_warps = min(NUM_EPI_WARPS, (min(p.m, BM) + 31) / 32);
+        mbar_init(smem_u32(red_ready), p.split_cluster ? p.ksplit * active_warps : 1);
         *abort_word = 0u;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         fence_proxy_async_smem();
@@ -610,8 +276,11 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
             tmem_relinquish();
         }
     }
+    // split in a cluster (single-CTA tiles): the cluster's barriers must all
+    // exist before any part-CTA arrives remotely
+    const bool csplit = !PAIR && (OP == OP_AR || OP == OP_RS) && p.split_cluster && p.ksplit > 1;
     tc_fence_before();
-    if constexpr (PAIR) cluster_sync();   // both CTAs' barriers exist before any cross-CTA traffic
+    if (PAIR || csplit) cluster_sync();   // both CTAs' barriers exist before any cross-CTA traffic
     else __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
@@ -983,6 +652,24 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
                         else mbar_arrive(ab);
                     }
                 }
+                if (csplit) {
+                    // rank split in a cluster: this part's fp32 sums into this CTA's
+                    // reduction area (the operand ring, idle once the only unit's
+                    // MMAs are done): warp q's 32 rows x 256 columns, row = lane,
+                    // 16-byte chunk c of a row at chunk c ^ (row & 7)
+                    if (row0 < p.m) {
+                        const uint32_t rb = smem_u32(a_st) + q * (32 * BN * 4) + lane * (BN * 4);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const uint32_t* v = (j < 8) ? (va + 4 * j) : (vb + 4 * (j - 8));
+                            const uint32_t cidx = static_cast<uint32_t>(sub * 16 + j);
+                            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(rb + ((cidx ^ (lane & 7)) << 4)),
+                                         "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3])
+                                         : "memory");
+                        }
+                    }
+                    continue;
+                }
                 if (row0 >= p.m || nt * BN + sub * EPI_COLS >= p.n) continue;   // sub-tile outside the output
                 if (ksplit > 1) {
                     // rank split: this part's fp32 sums into the slab's scratch, laid
@@ -998,7 +685,52 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
                 emit(sub, va, vb);
                 __syncwarp();
             }
-            if (ksplit > 1 && row0 < p.m && split_last(p, ksplit, tile_id, rank, q, lane, NPAIR)) {
+            if (csplit && row0 < p.m) {
+                // every part of this warp's rows is in its part-CTA's shared memory
+                // once each part-CTA's active warps arrived on every red_ready
+                __syncwarp();
+                if (lane == 0)
+                    for (int j = 0; j < ksplit; ++j) mbar_arrive_cluster(map_to_rank(smem_u32(red_ready), j));
+                ok = warp_wait<true>(smem_u32(red_ready), 0, ctl, 0x330u);
+                if (!ok) break;
+                // this CTA (part `me`) adds, for its columns, the ksplit parts in part
+                // order (part 0 taken as is), read from the cluster's shared memory
+                const uint32_t me = cluster_rank();
+                const int nsub = (BN / EPI_COLS) / ksplit;
+                const uint32_t rb = smem_u32(a_st) + q * (32 * BN * 4) + lane * (BN * 4);
+                for (int s = 0; s < nsub; ++s) {
+                    const int sub = static_cast<int>(me) * nsub + s;
+                    if (nt * BN + sub * EPI_COLS >= p.n) break;
+                    uint32_t va[32], vb[32];
+                    for (int sp = 0; sp < ksplit; ++sp) {
+                        uint4 v[16];   // one part's 64 columns of this row: all loads in flight together
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const uint32_t cidx = static_cast<uint32_t>(sub * 16 + j);
+                            const uint32_t a = map_to_rank(rb + ((cidx ^ (lane & 7)) << 4), static_cast<uint32_t>(sp));
+                            asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                         : "=r"(v[j].x), "=r"(v[j].y), "=r"(v[j].z), "=r"(v[j].w)
+                                         : "r"(a)
+                                         : "memory");
+                        }
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            uint32_t* d = (j < 8) ? (va + 4 * j) : (vb + 4 * (j - 8));
+                            if (sp == 0) {
+                                d[0] = v[j].x; d[1] = v[j].y; d[2] = v[j].z; d[3] = v[j].w;
+                            } else {
+                                d[0] = __float_as_uint(__uint_as_float(d[0]) + __uint_as_float(v[j].x));
+                                d[1] = __float_as_uint(__uint_as_float(d[1]) + __uint_as_float(v[j].y));
+                                d[2] = __float_as_uint(__uint_as_float(d[2]) + __uint_as_float(v[j].z));
+                                d[3] = __float_as_uint(__uint_as_float(d[3]) + __uint_as_float(v[j].w));
+                            }
+                        }
+                    }
+                    emit(sub, va, vb);
+                    __syncwarp();
+                }
+            }
+            if (!csplit && ksplit > 1 && row0 < p.m && split_last(p, ksplit, tile_id, rank, q, lane, NPAIR)) {
                 // the last part of this slab to arrive: add the parts in part order
                 // (part 0 taken as is), then round and store as an unsplit tile
                 for (int sub = 0; sub < BN / EPI_COLS; ++sub) {
@@ -1143,7 +875,9 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
             tmem_dealloc_pair(tmem_base, 2 * BN);
         }
     } else {
-        __syncthreads();
+        // split in a cluster: no CTA may leave while the others read its shared memory
+        if (csplit) cluster_sync();
+        else __syncthreads();
         if (warp == 1) {
             tc_fence_after();
             tmem_dealloc(tmem_base, 2 * BN);
@@ -1164,7 +898,7 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
 constexpr int kMaxDevices = 64;
 
 template <int OP, bool BF16, bool PAIR>
-cudaError_t launch_t(const KParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch_t(const KParams& p, int grid, cudaStream_t stream, int cluster = 1) {
     using C = Cfg<OP, PAIR>;
     auto kern = coc_fused_kernel<OP, BF16, PAIR>;
     static std::atomic<unsigned char> smem_set[kMaxDevices];
@@ -1184,15 +918,36 @@ cudaError_t launch_t(const KParams& p, int grid, cudaStream_t stream) {
     cfg.stream = stream;
     cfg.attrs = nullptr;
     cfg.numAttrs = 0;
-    if constexpr (PAIR) {
+    if (PAIR || cluster > 1) {
         attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.x = PAIR ? 2 : cluster;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
     return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+template <int OP, bool BF16>
+int max_split_clusters_t(int cluster) {
+    using C = Cfg<OP, false>;
+    auto kern = coc_fused_kernel<OP, BF16, false>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess) return 0;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cluster, 1, 1);
+    cfg.blockDim = dim3(C::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) return 0;
+    return n;
 }
 
 template <int OP, bool BF16>
@@ -1230,6 +985,24 @@ cudaError_t launch(int op, bool bf16, bool pair, const KParams& p, int grid, cud
         default: return cudaErrorInvalidValue;
     }
 #undef COC_LAUNCH
+}
+
+cudaError_t launch_split(int op, bool bf16, const KParams& p, int grid, int cluster, cudaStream_t stream) {
+    switch (op) {
+        case OP_AR: return bf16 ? launch_t<OP_AR, true, false>(p, grid, stream, cluster)
+                                : launch_t<OP_AR, false, false>(p, grid, stream, cluster);
+        case OP_RS: return bf16 ? launch_t<OP_RS, true, false>(p, grid, stream, cluster)
+                                : launch_t<OP_RS, false, false>(p, grid, stream, cluster);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+int max_split_clusters(int op, bool bf16, int cluster) {
+    switch (op) {
+        case OP_AR: return bf16 ? max_split_clusters_t<OP_AR, true>(cluster) : max_split_clusters_t<OP_AR, false>(cluster);
+        case OP_RS: return bf16 ? max_split_clusters_t<OP_RS, true>(cluster) : max_split_clusters_t<OP_RS, false>(cluster);
+        default: return 0;
+    }
 }
 
 int max_pairs(int op, bool bf16) {

@@ -8,6 +8,8 @@ it.  The library counts every device allocation it makes
 (coc_debug_alloc_count); after one warm-up call of every operator, further
 calls of the same shapes on the same stream must leave the count unchanged,
 and so must replays of a CUDA graph that captured them."""
+import os
+
 import pytest
 import torch
 
@@ -63,13 +65,28 @@ def _calls():
     calls["ag_v2"] = lambda: coc.all_gather_matmul_v2(ax, aw, ago, agg)
     dws = [torch.empty(264, 192, dtype=BF16, device=DEV) for _ in range(4)]
     calls["wgrad"] = lambda: coc.weight_grad(ago, agg, dws)
-    # w8A16 through both dequantisation paths (the schedule is chosen by m)
-    for name, m in (("w8_fused", 256), ("w8_prepass", 2048)):
+    # w8A16: the schedules without scratch (in-kernel dequantisation to shared
+    # or to tensor memory) and the pre-pass schedule, whose dequantised weight
+    # lives in the stream's workspace
+    for name, m, path in (("w8_fused", 256, "fused"), ("w8_ts", 256, "ts"), ("w8_prepass", 2048, "prepass")):
         w8 = wl.W8A16(R=4, m=m, n=256, k_shard=256, group=128, seed=4)
         x8, q8, sc8 = w8.make("group")
         x8, q8, sc8 = to_dev(x8), to_dev(q8), to_dev(sc8)
         o8 = [torch.empty(m, 256, dtype=F16, device=DEV) for _ in range(4)]
-        calls[name] = lambda x8=x8, q8=q8, sc8=sc8, o8=o8: coc.matmul_all_reduce_w8a16(x8, q8, sc8, "group", 128, o8)
+
+        def w8call(x8=x8, q8=q8, sc8=sc8, o8=o8, path=path):
+            prev = os.environ.get("COC_W8_PATH")
+            if path is not None:
+                os.environ["COC_W8_PATH"] = path
+            try:
+                coc.matmul_all_reduce_w8a16(x8, q8, sc8, "group", 128, o8)
+            finally:
+                if path is not None:
+                    if prev is None:
+                        del os.environ["COC_W8_PATH"]
+                    else:
+                        os.environ["COC_W8_PATH"] = prev
+        calls[name] = w8call
     # MoE: dispatch + GroupedMatMul, the fused top-1 combine, top-2 with the gated combine
     moe = wl.MoEDispatch(R=4, T=200, h=128, f=264, e_loc=2, seed=5)
     mx, mi, mw = moe.make()

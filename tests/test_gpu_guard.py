@@ -205,7 +205,8 @@ def test_all_gather_v2_skipped_copies_leave_buffers_alone():
         assert np.all(raw == CANARY), f"skipped gather buffer {r} was written"
 
 
-@pytest.mark.parametrize("gran,path", [("channel", "fused"), ("group", "fused"), ("tensor", "prepass")])
+@pytest.mark.parametrize("gran,path", [("channel", "fused"), ("group", "fused"), ("tensor", "prepass"),
+                                       ("channel", "ts"), ("group", "ts")])
 def test_w8a16_guards(gran, path, monkeypatch):
     monkeypatch.setenv("COC_W8_PATH", path)
     R, m, n, ks, group = 4, 200, 272, 128, 64

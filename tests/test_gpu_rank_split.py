@@ -164,3 +164,27 @@ def test_r1_and_zero_k_are_not_split():
                               [torch.empty(0, 256, dtype=BF16, device="cuda")] * 4)
     coc.sync_status()
     assert all(torch.count_nonzero(o) == 0 for o in z)
+
+
+@pytest.mark.parametrize("R,m,n,ks,dt", [(8, 16, 8192, 128, BF16), (8, 64, 1000, 72, F16), (4, 100, 520, 200, BF16),
+                                         (2, 128, 256, 64, F16), (8, 128, 4096, 64, BF16)])
+def test_cluster_and_scratch_split_give_the_same_bits(R, m, n, ks, dt, monkeypatch):
+    """The rank split runs its parts as one cluster that adds them through
+    distributed shared memory, or (COC_SPLIT_PATH=scratch) through a global
+    workspace with arrival counters: the same parts added in the same order,
+    so the same bits, for AllReduce and ReduceScatter."""
+    xs, ws = _data(R, m, n, ks, dt, 19 * m + n)
+    dx, dw = to_dev(xs), to_dev(ws)
+    a = [t.clone() for t in coc.matmul_all_reduce(dx, dw)]
+    rs_ok = m % (8 * R) == 0
+    ra = [t.clone() for t in coc.matmul_reduce_scatter(dx, dw)] if rs_ok else None
+    monkeypatch.setenv("COC_SPLIT_PATH", "scratch")
+    b = coc.matmul_all_reduce(dx, dw)
+    rb = coc.matmul_reduce_scatter(dx, dw) if rs_ok else None
+    coc.sync_status()
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    if rs_ok:
+        for x, y in zip(ra, rb):
+            assert torch.equal(x, y)
+    assert_close(a[0], orc.matmul_all_reduce(CODE[dt], bits(xs), bits(ws)), R * ks, "cluster split")

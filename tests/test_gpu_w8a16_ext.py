@@ -98,10 +98,13 @@ def _force_path(monkeypatch, path):
 @pytest.mark.parametrize("dt", [torch.float16, torch.bfloat16], ids=["fp16", "bf16"])
 @pytest.mark.parametrize("zero", [False, True], ids=["sym", "zp"])
 @pytest.mark.parametrize("gran", ["tensor", "channel", "group"])
-def test_prepass_and_fused_paths_give_the_same_bits(monkeypatch, dt, zero, gran):
-    """Large m dequantises the weight once in a pre-pass and runs the AllReduce
-    kernel; small m dequantises per tile inside the fused kernel.  Both use the
-    same conversion and the same accumulation order: identical outputs."""
+def test_all_schedules_give_the_same_bits(monkeypatch, dt, zero, gran):
+    """Three schedules of the same operator: the default kernel with the
+    dequantised weight in tensor memory (Y^T = Wd^T X^T), the fused kernel
+    with dequant warps writing the weight tile to shared memory, and the
+    pre-pass that dequantises once before the fp16 AllReduce kernel.  All
+    use the same conversion and the same accumulation order (rank 0..R-1, k
+    ascending, 16 k per MMA): identical outputs."""
     shape = wl.W8A16(R=4, m=512, n=272, k_shard=192, group=64, seed=31, dtype=dt)
     xs, wqs, scales = shape.make(gran)
     zs = shape.zeros(gran) if zero else None
@@ -111,9 +114,12 @@ def test_prepass_and_fused_paths_give_the_same_bits(monkeypatch, dt, zero, gran)
     a = coc.matmul_all_reduce_w8a16(*args, **kw)
     _force_path(monkeypatch, "prepass")
     b = coc.matmul_all_reduce_w8a16(*args, **kw)
+    _force_path(monkeypatch, "ts")
+    c = coc.matmul_all_reduce_w8a16(*args, **kw)
     coc.sync_status()
-    for x, y in zip(a, b):
+    for x, y, z in zip(a, b, c):
         assert torch.equal(x, y)
+        assert torch.equal(z, y), "tensor-memory schedule differs from the pre-pass schedule"
     ref = orc.matmul_all_reduce_w8a16(bits(xs), [w.numpy() for w in wqs], bits(scales), GRAN[gran], 64,
                                       zeros=[z.numpy() for z in zs] if zs is not None else None, dtype=CODE[dt])
     assert_close(b[0], ref, shape.K, f"pre-pass {dt} zero={zero} {gran}")
