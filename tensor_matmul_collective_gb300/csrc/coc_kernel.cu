@@ -225,8 +225,9 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
     uint64_t* acce = accf + 2;         // [2]  accumulator drained by the epilogue (leader: both CTAs)
     uint64_t* never = acce + 2;        // [1]  nothing arrives here (fault-injection test)
     uint64_t* drain = never + 1;       // [1]  MMA drain before TMEM release
-    uint64_t* red_ready = drain + 1;   // [1]  rank split in a cluster: every part-CTA's fp32 part is in its smem
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red_ready + 1);
+    uint64_t* red_ready = drain + 1;   // [1]  rank split in a cluster: every part-CTA pushed its slices here
+    uint64_t* ring_free = red_ready + 1;   // [1]  rank split in a cluster: every part-CTA's MMAs are done
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ring_free + 1);
     uint32_t* abort_word = tmem_slot + 1;
     // w8A16 pair: 16-byte landing slots for the peer's per-stage "B half ready" copies
     uint8_t* sig_slots = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(abort_word + 1) + 15) & ~uintptr_t(15));
@@ -259,9 +260,16 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
         mbar_init(smem_u32(never), 1);
         mbar_init(smem_u32(drain), 1);
         // rank split in a cluster: one arrival per part-CTA and epilogue warp
-        // holding output rows (the split runs on one row tile of m <= 128 rows)
-        const int active_warps = min(NUM_EPI_WARPS, (min(p.m, BM) + 31) / 32);
+        // holding output rows of this CTA's row tile (one unit per CTA; the
+        // cluster's CTAs share the tile)
+        int active_warps = NUM_EPI_WARPS;
+        if (p.split_cluster && p.ksplit > 1) {
+            int r_, mt_, nt_;
+            decode_unit<OP>(p, static_cast<int>(blockIdx.x) / p.ksplit, r_, mt_, nt_);
+            active_warps = min(NUM_EPI_WARPS, (min(p.m - mt_ * BM, BM) + 31) / 32);
+        }
         mbar_init(smem_u32(red_ready), p.split_cluster ? p.ksplit * active_warps : 1);
+        mbar_init(smem_u32(ring_free), p.split_cluster ? p.ksplit : 1);
         *abort_word = 0u;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         fence_proxy_async_smem();
@@ -530,6 +538,16 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
             if (!ok) break;
             tc_fence_after();
             const int row0 = mt * TILE_M + static_cast<int>(rank) * BM + 32 * q;
+            if (csplit) {
+                // this CTA's MMAs are done, so its operand ring is idle: tell every
+                // part-CTA of the cluster, and push only once all rings are idle
+                if (q == 0 && lane == 0)
+                    for (int j = 0; j < ksplit; ++j) mbar_arrive_cluster(map_to_rank(smem_u32(ring_free), j));
+                if (row0 < p.m) {
+                    ok = warp_wait<true>(smem_u32(ring_free), 0, ctl, 0x320u);
+                    if (!ok) break;
+                }
+            }
             const int tile_id = mt * p.n_tiles + nt;
             const int part_s = (ksplit > 1) ? u % ksplit : 0;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + buf * BN;
@@ -653,17 +671,24 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
                     }
                 }
                 if (csplit) {
-                    // rank split in a cluster: this part's fp32 sums into this CTA's
-                    // reduction area (the operand ring, idle once the only unit's
-                    // MMAs are done): warp q's 32 rows x 256 columns, row = lane,
-                    // 16-byte chunk c of a row at chunk c ^ (row & 7)
+                    // rank split in a cluster: the sub-tile's 64 columns belong to part-CTA
+                    // `owner`; push this part's fp32 sums straight into the owner's
+                    // reception area (its operand ring, idle once ring_free completed):
+                    // slot [part][q][row = lane] of (BN / ksplit) columns, 16-byte chunk
+                    // c of a row at chunk c ^ (row & 7)
                     if (row0 < p.m) {
-                        const uint32_t rb = smem_u32(a_st) + q * (32 * BN * 4) + lane * (BN * 4);
+                        const int nsub = (BN / EPI_COLS) / ksplit;
+                        const uint32_t owner = static_cast<uint32_t>(sub / nsub);
+                        const uint32_t row_bytes = static_cast<uint32_t>(BN * 4 / ksplit);
+                        const uint32_t rb = smem_u32(a_st) +
+                                            ((static_cast<uint32_t>(part_s) * NUM_EPI_WARPS + q) * 32 + lane) * row_bytes;
+                        const uint32_t rb_owner = map_to_rank(rb, owner);
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
                             const uint32_t* v = (j < 8) ? (va + 4 * j) : (vb + 4 * (j - 8));
-                            const uint32_t cidx = static_cast<uint32_t>(sub * 16 + j);
-                            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(rb + ((cidx ^ (lane & 7)) << 4)),
+                            const uint32_t cidx = static_cast<uint32_t>((sub % nsub) * 16 + j);
+                            asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};"
+                                         ::"r"(rb_owner + ((cidx ^ (lane & 7)) << 4)),
                                          "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3])
                                          : "memory");
                         }
@@ -686,31 +711,33 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
                 __syncwarp();
             }
             if (csplit && row0 < p.m) {
-                // every part of this warp's rows is in its part-CTA's shared memory
-                // once each part-CTA's active warps arrived on every red_ready
+                // every part of this warp's rows is in this CTA's ring once each
+                // part-CTA's active warps pushed their slices and arrived here
                 __syncwarp();
                 if (lane == 0)
                     for (int j = 0; j < ksplit; ++j) mbar_arrive_cluster(map_to_rank(smem_u32(red_ready), j));
                 ok = warp_wait<true>(smem_u32(red_ready), 0, ctl, 0x330u);
                 if (!ok) break;
                 // this CTA (part `me`) adds, for its columns, the ksplit parts in part
-                // order (part 0 taken as is), read from the cluster's shared memory
+                // order (part 0 taken as is), from its own shared memory
                 const uint32_t me = cluster_rank();
                 const int nsub = (BN / EPI_COLS) / ksplit;
-                const uint32_t rb = smem_u32(a_st) + q * (32 * BN * 4) + lane * (BN * 4);
+                const uint32_t row_bytes = static_cast<uint32_t>(BN * 4 / ksplit);
                 for (int s = 0; s < nsub; ++s) {
                     const int sub = static_cast<int>(me) * nsub + s;
                     if (nt * BN + sub * EPI_COLS >= p.n) break;
                     uint32_t va[32], vb[32];
                     for (int sp = 0; sp < ksplit; ++sp) {
-                        uint4 v[16];   // one part's 64 columns of this row: all loads in flight together
+                        // part sp's 64 columns of this row, pushed into this CTA's ring
+                        const uint32_t rb = smem_u32(a_st) +
+                                            ((static_cast<uint32_t>(sp) * NUM_EPI_WARPS + q) * 32 + lane) * row_bytes;
+                        uint4 v[16];
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
-                            const uint32_t cidx = static_cast<uint32_t>(sub * 16 + j);
-                            const uint32_t a = map_to_rank(rb + ((cidx ^ (lane & 7)) << 4), static_cast<uint32_t>(sp));
-                            asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+                            const uint32_t cidx = static_cast<uint32_t>(s * 16 + j);
+                            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                                          : "=r"(v[j].x), "=r"(v[j].y), "=r"(v[j].z), "=r"(v[j].w)
-                                         : "r"(a)
+                                         : "r"(rb + ((cidx ^ (lane & 7)) << 4))
                                          : "memory");
                         }
 #pragma unroll
