@@ -11,7 +11,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libcoc.so")
-SOURCES = ["coc_api.cu", "coc_kernel.cu", "coc_w8_ts.cu", "coc_noalloc.cu", "coc_w8_prepass.cu", "coc_moe.cu"]
+SOURCES = ["coc_api.cu", "coc_kernel.cu", "coc_slab.cu", "coc_w8_ts.cu", "coc_noalloc.cu", "coc_w8_prepass.cu", "coc_moe.cu"]
 HEADERS = ["coc_internal.h", "coc_dequant.cuh", "coc_ptx.cuh", os.path.join("..", "..", "include", "coc.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

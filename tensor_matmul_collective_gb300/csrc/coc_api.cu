@@ -55,6 +55,7 @@ struct DeviceState {
     int max_pairs[NUM_OPS][2] = {{-1, -1}, {-1, -1}, {-1, -1}, {-1, -1}, {-1, -1}};   // per op, per bf16; -1 = not queried
     int ts_pairs[2] = {-1, -1};     // co-resident pairs of the w8A16 tensor-memory kernel, per bf16
     int split_clusters[2][2][2] = {{{-1, -1}, {-1, -1}}, {{-1, -1}, {-1, -1}}};   // [RS][bf16][ksplit 4]: co-resident
+    std::unordered_map<long long, int> slab_clusters;   // column-slab clusters co-resident, by launch shape
     cudaMemPool_t pool = nullptr;   // stream-ordered allocations of calls captured into CUDA graphs
     std::unordered_map<cudaStream_t, Workspace> ws;   // per-stream scratch of eager calls
 };
@@ -130,6 +131,20 @@ coc_status_t encode(CUtensorMap* map, CUtensorMapDataType dt, const void* base, 
                     static_cast<unsigned long long>(rows), static_cast<unsigned long long>(cols),
                     static_cast<unsigned long long>(pitch_bytes));
     return COC_OK;
+}
+
+// 3-D view of a row-major matrix for stage-sized boxes: element (i, r, j) at
+// base + (j d0 + i) * elem + r pitch, i.e. dims (d0 = one block of the inner
+// dimension, rows, blocks), strides (pitch, d0 * elem).  Returns the driver's
+// result without reporting (the caller falls back to 2-D boxes).
+CUresult encode_blocked(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t d0, uint64_t rows,
+                        uint64_t blocks, uint64_t pitch_bytes, uint32_t box0, uint32_t box_rows, uint32_t box_blocks) {
+    const cuuint64_t dims[3] = {d0, rows, blocks};
+    const cuuint64_t strides[2] = {pitch_bytes, d0 * 2};
+    const cuuint32_t box[3] = {box0, box_rows, box_blocks};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return g_encode(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1024;
@@ -300,6 +315,119 @@ int rank_split(int op, int R, int64_t ks, int64_t tiles, bool pair, int sm_count
     return ksplit;
 }
 
+// Column-slab kernel (coc_slab.cu) for decode-sized m (m <= kSlabMaxRows;
+// above that the X rows every slab re-reads from L2 cost more than the rank
+// split's reduction).  Plan: 128-column slabs (256-byte weight rows: measured
+// faster than 64 columns, whose 128-byte rows moved 30% less per SM), two
+// k-blocks per stage (one TMA operation per 64-column group and one for X),
+// and, while the slabs fill at most half of the SMs, each slab's contraction
+// split over a cluster of 2 or 4 CTAs.  No plan (boxes 0) when the CTAs would
+// fill less than half of the SMs: the persistent kernel's rank split takes
+// those shapes.  COC_SLAB=0 turns the kernel off; COC_SLAB=1 takes it for
+// every m <= 128, with COC_SLAB_BOXES, COC_SLAB_KPS and COC_SLAB_SPLIT
+// overriding the plan (tests and tuning only).
+constexpr int64_t kSlabMaxRows = 64;
+struct SlabPlan {
+    int boxes = 0, split = 1, kps = 1;
+};
+int env_int(const char* name, int dflt) {
+    const char* e = std::getenv(name);
+    return e == nullptr ? dflt : std::atoi(e);
+}
+SlabPlan slab_plan(int op, int R, int64_t m, int64_t n, int64_t ks, int sm_count) {
+    SlabPlan pl;
+    if ((op != OP_AR && op != OP_RS) || ks <= 0 || m <= 0 || m > BM) return pl;
+    const int forced = env_int("COC_SLAB", -1);
+    if (forced == 0 || (forced != 1 && m > kSlabMaxRows)) return pl;
+    const int boxes = env_int("COC_SLAB_BOXES", 2) == 1 ? 1 : 2;
+    const int64_t kblocks = (ks + BK - 1) / BK;
+    int kps = env_int("COC_SLAB_KPS", boxes == 1 ? 4 : 2);
+    kps = kps >= 4 ? 4 : kps >= 2 ? 2 : 1;
+    while (kps > 1 && kblocks % kps != 0) kps /= 2;
+    const int64_t slabs = (n + 64 * boxes - 1) / (64 * boxes);
+    const int64_t spu = static_cast<int64_t>(R) * (kblocks / kps);   // stages per slab
+    int split = 1;
+    // (each part finalises 64 boxes / split >= 32 columns and sums at least one stage)
+    const int max_split = boxes == 2 ? 4 : 2;
+    if (m <= kSlabMaxRows) {
+        while (split < max_split && slabs * split * 2 <= sm_count && split * 2 <= spu) split *= 2;
+        const int fs = env_int("COC_SLAB_SPLIT", 0);
+        if ((fs == 1 || fs == 2 || fs == 4) && fs <= max_split && fs <= spu) split = fs;
+    }
+    if (forced != 1 && slabs * split * 2 < sm_count) return pl;
+    pl.boxes = boxes;
+    pl.split = split;
+    pl.kps = kps;
+    return pl;
+}
+
+coc_status_t slab_row_parallel(int op, int R, int64_t m, int64_t n, int64_t ks, const void* const* x,
+                               const void* const* w, void* const* out, int n_out, coc_dtype_t dt, const SlabPlan& pl,
+                               DeviceState* ds, cudaStream_t stream, bool w_nk) {
+    KParams p;
+    std::memset(&p, 0, sizeof p);
+    p.R = R;
+    p.n_out = n_out;
+    p.m = static_cast<int>(m);
+    p.n = static_cast<int>(n);
+    p.k = static_cast<int>(ks);
+    p.num_kshards = R;
+    p.kblocks = static_cast<int>((ks + BK - 1) / BK);
+    p.m_tiles = 1;
+    p.n_tiles = static_cast<int>((n + 64 * pl.boxes - 1) / (64 * pl.boxes));
+    p.units = p.n_tiles;
+    p.rows_per_rank = static_cast<int>(m / R);
+    p.a_box_rows = static_cast<int>((m + 7) / 8 * 8);
+    const int kps = pl.kps, boxes = pl.boxes;
+    // A split slab takes one cluster for its whole life (the parts' reception
+    // areas are not reused), so every slab needs a resident cluster; else
+    // the slabs run unsplit.
+    int split = pl.split, clusters = 0;
+    if (split > 1) {
+        const int smem = slab_smem_bytes(slab_stages(p.a_box_rows, boxes, kps, split), p.a_box_rows, boxes, kps, split);
+        const long long key = (static_cast<long long>(dt == COC_BF16) << 40) | (static_cast<long long>(split) << 32) | smem;
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto it = ds->slab_clusters.find(key);
+        if (it == ds->slab_clusters.end())
+            it = ds->slab_clusters.emplace(key, slab_max_clusters(dt == COC_BF16, split, smem)).first;
+        clusters = it->second;
+        if (clusters < p.units) split = 1;
+    }
+    p.slab_boxes = boxes;
+    p.slab_kps = kps;
+    p.slab_split = split;
+    p.slab_stages = slab_stages(p.a_box_rows, boxes, kps, split);
+    p.b_kmajor = w_nk ? 1 : 0;
+    const CUtensorMapDataType adt = tma_dtype(dt);
+    coc_status_t st;
+    // 3-D maps (one A box per stage; n x k B likewise) where the k-blocks tile
+    // k_shard exactly, so that no box reads past a row's end
+    bool a3d = kps > 1 && ks % BK == 0;
+    for (int r = 0; a3d && r < R; ++r) {
+        a3d = encode_blocked(&p.tm_a[r], adt, x[r], BK, m, ks / BK, ks * 2, BK, p.a_box_rows, kps) == CUDA_SUCCESS;
+        if (a3d && w_nk)
+            a3d = encode_blocked(&p.tm_b[r], adt, w[r], BK, n, ks / BK, ks * 2, BK, 64 * boxes, kps) == CUDA_SUCCESS;
+    }
+    p.slab_a3d = a3d ? 1 : 0;
+    for (int r = 0; r < R; ++r) {
+        if (!a3d) {
+            if ((st = encode(&p.tm_a[r], adt, x[r], ks, m, ks * 2, BK, p.a_box_rows, CU_TENSOR_MAP_SWIZZLE_128B)) != COC_OK)
+                return st;
+            if (w_nk && (st = encode(&p.tm_b[r], adt, w[r], ks, n, ks * 2, BK, 64 * boxes, CU_TENSOR_MAP_SWIZZLE_128B)) != COC_OK)
+                return st;
+        }
+        if (!w_nk && (st = encode(&p.tm_b[r], adt, w[r], n, ks, n * 2, 64, BK * kps, CU_TENSOR_MAP_SWIZZLE_128B)) != COC_OK)
+            return st;
+    }
+    for (int o = 0; o < (op == OP_RS ? R : n_out); ++o) p.outp[o] = static_cast<uint16_t*>(out[o]);
+    p.status = ds->status;
+    p.inject_timeout = g_inject.load();
+    p.clock_slot = g_clock_slot.load();
+    const int grid = split > 1 ? split * p.units : (p.units < ds->sm_count ? p.units : ds->sm_count);
+    const cudaError_t e = launch_slab(op, dt == COC_BF16, p, grid, stream);
+    return e == cudaSuccess ? COC_OK : cuda_fail(e, "kernel launch (column slabs)");
+}
+
 // ---- row-parallel family: AR, RS, W8, plain ----------------------------------
 // w_nk: each W shard is stored n x k_shard (Megatron's [out, in]) instead of
 // k_shard x n; the kernel then reads B K-major.
@@ -333,6 +461,10 @@ coc_status_t row_parallel(int op, int R, int64_t m, int64_t n, int64_t ks, const
     DeviceState* ds = nullptr;
     coc_status_t st = device_state(&ds);
     if (st != COC_OK) return st;
+    if (allow_split) {
+        const SlabPlan pl = slab_plan(op, R, m, n, ks, ds->sm_count);
+        if (pl.boxes > 0) return slab_row_parallel(op, R, m, n, ks, x, w, out, n_out, dt, pl, ds, stream, w_nk);
+    }
 
     const bool w8 = (op == OP_W8);
     const CUtensorMapDataType adt = tma_dtype(dt);

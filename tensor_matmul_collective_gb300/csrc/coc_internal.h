@@ -95,6 +95,19 @@ struct KParams {
     // all parts (in part order) of columns [j BN / ksplit, (j+1) BN / ksplit)
     // read from the cluster's shared memory.  part / part_cnt are unused.
     int split_cluster;
+    // Column-slab kernel (decode-sized m): 64-column groups per slab (1 or
+    // 2), operand stages, k-blocks per stage (1, 2 or 4, dividing kblocks),
+    // and whether the A (and n x k B) maps are 3-D (k in block, row, k-block)
+    // so that one box holds a stage; a_box_rows is then the rows of X per
+    // k-block.
+    int slab_boxes;
+    int slab_stages;
+    int slab_kps;
+    int slab_a3d;
+    // CTAs per slab (1, 2 or 4, one cluster): part j sums the j-th of
+    // slab_split contiguous ranges of the contraction's stages and finalises
+    // the j-th of slab_split column ranges, adding the parts in part order.
+    int slab_split;
 };
 
 // Argument checks of coc_matmul_all_reduce and the per-thread error text
@@ -182,6 +195,25 @@ cudaError_t launch(int op, bool bf16, bool pair, const KParams& p, int grid, cud
 // through distributed shared memory, p.split_cluster), and the number of such
 // clusters that can be co-resident.
 cudaError_t launch_split(int op, bool bf16, const KParams& p, int grid, int cluster, cudaStream_t stream);
+
+// Column-slab kernel (coc_slab.cu), AllReduce and ReduceScatter at
+// decode-sized m: one unit per slab of 64 x slab_boxes output columns, all m
+// rows (m <= 128), the whole contraction in one CTA.  Launched with grid =
+// min(units, SMs), slab_smem_bytes of dynamic shared memory.  128-byte
+// swizzle everywhere.  A maps: BK x a_box_rows boxes (2-D), or dims (BK, m,
+// kblocks) with boxes (BK, a_box_rows, slab_kps) (3-D, slab_a3d).  B maps,
+// k x n storage: 64 x (slab_kps BK) boxes; n x k storage (b_kmajor): BK x
+// 64 slab_boxes boxes (2-D) or dims (BK, n, kblocks) with boxes (BK, 64
+// slab_boxes, slab_kps) (3-D, slab_a3d).  outp holds the n_out outputs
+// (AllReduce) or the R rank outputs (ReduceScatter).  With slab_split > 1
+// (m <= 64) the grid is slab_split x the slabs run at once, in clusters of
+// slab_split CTAs.
+constexpr int kSlabMaxStages = 32;
+constexpr int kSlabSmemCap = 227 * 1024;                       // dynamic shared memory per CTA
+int slab_stages(int a_rows, int boxes, int kps, int split);    // most stages that fit (at least 2)
+int slab_smem_bytes(int stages, int a_rows, int boxes, int kps, int split);
+cudaError_t launch_slab(int op, bool bf16, const KParams& p, int grid, cudaStream_t stream);
+int slab_max_clusters(bool bf16, int split, int smem);         // clusters of `split` resident at once
 int max_split_clusters(int op, bool bf16, int cluster);
 // Co-resident CTA pairs the 2-SM variant can have on the current device.
 int max_pairs(int op, bool bf16);

@@ -92,20 +92,6 @@ __device__ __forceinline__ int gmm_units(const KParams& p, int tile_m) {
     return acc;
 }
 
-// ------------------------------------------------------------ conversions ---
-
-template <bool BF16>
-__device__ __forceinline__ uint32_t pack2(uint32_t lo_bits, uint32_t hi_bits) {
-    const float lo = __uint_as_float(lo_bits), hi = __uint_as_float(hi_bits);
-    if constexpr (BF16) {
-        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-        return *reinterpret_cast<uint32_t*>(&h);
-    } else {
-        __half2 h = __floats2half2_rn(lo, hi);
-        return *reinterpret_cast<uint32_t*>(&h);
-    }
-}
-
 // ALL_GATHER_MATMUL_V2: copy this unit's share of the m-tile's gathered rows
 // to every rank's gather buffer.  The tile's rows are one contiguous run of
 // the gathered matrix; it is cut into R * n_tiles equal pieces, one per work
@@ -240,6 +226,11 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
     const int unit_step = PAIR ? static_cast<int>(cluster_count()) : static_cast<int>(gridDim.x);
     constexpr int NPAIR = PAIR ? 2 : 1;
 
+    // the operand maps' descriptors start loading at once, in parallel
+    if (warp == 0 && lane < p.num_kshards && lane < COC_MAX_RANKS) {
+        prefetch_tmap(&p.tm_a[lane]);
+        prefetch_tmap(&p.tm_b[lane]);
+    }
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::SA; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
@@ -287,11 +278,27 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
     // split in a cluster (single-CTA tiles): the cluster's barriers must all
     // exist before any part-CTA arrives remotely
     const bool csplit = !PAIR && (OP == OP_AR || OP == OP_RS) && p.split_cluster && p.ksplit > 1;
+    // Single-CTA tiles: the producer warp (whose lane 0 initialised the
+    // barriers) needs nothing the others set up, so it only arrives and
+    // starts its loads while TMEM is allocated; it waits for the cluster
+    // barrier at the end, before the teardown.  CTA pairs: the peer's loads
+    // complete on the leader's barriers, so everyone waits.
+    constexpr uint32_t kSetupBar = 3;   // named barrier (1 and 2: the dequant groups' votes)
+    const bool early_producer = !PAIR && warp == 0;
     tc_fence_before();
-    if (PAIR || csplit) cluster_sync();   // both CTAs' barriers exist before any cross-CTA traffic
-    else __syncthreads();
+    if (early_producer) __syncwarp();   // lane 0's barrier initialisation is visible to the warp
+    if (PAIR) {
+        cluster_sync();   // both CTAs' barriers exist before any cross-CTA traffic
+    } else if (csplit) {
+        cluster_arrive();   // the cluster's barriers exist before any part-CTA arrives remotely
+        if (!early_producer) cluster_wait();
+    } else if (early_producer) {
+        named_arrive(kSetupBar, C::THREADS);
+    } else {
+        named_sync(kSetupBar, C::THREADS);
+    }
     tc_fence_after();
-    const uint32_t tmem_base = *tmem_slot;
+    const uint32_t tmem_base = early_producer ? 0u : *tmem_slot;
     // clock probe: block 0 measures the SM cycles and nanoseconds it spends
     const bool probe = p.clock_slot >= 0 && blockIdx.x == 0 && threadIdx.x == 0;
     uint64_t probe_clk = 0, probe_ns = 0;
@@ -315,9 +322,6 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
 
     if (warp == 0) {
         // ================================================= TMA producer ===
-        if (lane == 0) {
-            for (int i = 0; i < p.num_kshards && i < COC_MAX_RANKS; ++i) prefetch_tmap(&p.tm_a[i]);
-        }
         uint32_t stage = 0, phase = 0, rstage = 0, rphase = 0;
         uint32_t filled = 0, fill_parity = 0;     // per-stage bit masks of the last fill (A ring)
         uint32_t rfilled = 0, rfill_parity = 0;   // same for the raw int8 ring
@@ -903,8 +907,12 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
         }
     } else {
         // split in a cluster: no CTA may leave while the others read its shared memory
-        if (csplit) cluster_sync();
-        else __syncthreads();
+        if (csplit) {
+            if (early_producer) cluster_wait();   // the setup phase this warp only arrived at
+            cluster_sync();
+        } else {
+            __syncthreads();
+        }
         if (warp == 1) {
             tc_fence_after();
             tmem_dealloc(tmem_base, 2 * BN);

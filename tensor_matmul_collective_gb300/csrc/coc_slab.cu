@@ -1,0 +1,518 @@
+// Column-slab kernel: MATMUL_ALL_REDUCE and MATMUL_REDUCE_SCATTER at
+// decode-sized m (CoC page, 融合算子实现: the same two operators as the
+// persistent kernel, for the few-row activations of token generation).
+//
+// At m <= 64 the operator reads the R weight shards (R x k_shard x n) once
+// and does almost no arithmetic per weight byte, so its time is the weight
+// stream.  The persistent kernel's 128 x 256 tiles are too few to spread that
+// stream over the SMs, and cutting K across CTAs (the rank split) costs a
+// cross-CTA reduction after the last weight byte arrives.  Here a work unit
+// is one column slab of the output instead: all m rows by SN = 64 or 128
+// columns, accumulated over the whole contraction (rank 0..R-1, k ascending)
+// in one CTA, so n / SN units cover the SMs and nothing is reduced across
+// CTAs.
+//
+//   stage          kps = 1, 2 or 4 k-blocks of 64 k, in as few TMA operations
+//                  as the layouts allow: measured, a CTA's weight stream is
+//                  bound by the TMA operations it has in flight, not by their
+//                  bytes (one 8 KiB box per 64 k moved 26 GB/s per SM; the
+//                  stream of the same weight in 32 KiB boxes is several times
+//                  faster).
+//   A (X shards)   per k-block a_rows = roundup(m, 8) rows x 64 k (128-byte
+//                  swizzle, K-major): one 3-D box (k within the block, row,
+//                  k-block) for the whole stage when k_shard % 64 == 0, else
+//                  one 2-D box per k-block.  The MMA is M = 128, so it also
+//                  reads the 128 - a_rows rows after a k-block's rows, which
+//                  belong to the next k-blocks: those accumulator rows are
+//                  never read back.
+//   B (W shards)   k x n storage (MN-major): per 64-column group one box of
+//                  64 columns x kps * 64 k; n x k storage (K-major): per
+//                  k-block SN rows x 64 k, as one 3-D box for the stage when
+//                  k_shard % 64 == 0.
+//   stages         as many as fit in shared memory (up to kSlabMaxStages).
+//   accumulator    two TMEM buffers of SN fp32 columns, so a CTA with a
+//                  second unit overlaps its epilogue with the next mainloop.
+//
+// Warp roles (192 threads, one CTA per SM, persistent over slabs):
+//   warp 0      TMA producer; it initialised the barriers, so it starts
+//               loading without waiting for the TMEM allocation
+//   warp 1      TMEM owner + MMA issuer (tcgen05.mma kind::f16, M 128, N SN)
+//   warps 2-5   epilogue: warp q drains accumulator lanes 32q..32q+31 (rows)
+//               when they hold output rows, rounds them, transposes them
+//               through a swizzled shared-memory buffer and writes coalesced
+//               128-byte row segments: every rank output (AllReduce) or the
+//               rank owning each row (ReduceScatter).
+//
+// Every mbarrier wait is bounded (COC_WAIT_NS); a wait that runs out sets
+// the CTA abort flag and the device status word, every role leaves its loop,
+// issued copies and MMAs are drained, TMEM is freed and the kernel returns.
+#include <atomic>
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "coc_internal.h"
+#include "coc_ptx.cuh"
+
+namespace coc {
+namespace {
+
+constexpr int SLAB_THREADS = 192;
+constexpr uint32_t kSlabBoxBytes = 64 * BK * 2;   // one 64 x 64 16-bit box
+constexpr uint32_t kSlabStageBar = 3;             // named barrier of the set-up phase
+static_assert(kSlabMaxStages <= 32, "the producer's fill masks hold one bit per stage");
+
+__host__ __device__ constexpr uint32_t slab_bar_bytes(int stages) {
+    return static_cast<uint32_t>(8 * (2 * stages + 7) + 16);
+}
+// Reception area of a slab split over `split` CTAs: per other part, per row
+// quadrant (m <= 64: two) 32 rows of the (64 boxes / split) fp32 columns this
+// CTA finalises.
+__host__ __device__ constexpr uint32_t slab_recv_bytes(int boxes, int split) {
+    return split > 1 ? static_cast<uint32_t>((split - 1) * 2 * 32 * (64 * boxes / split) * 4) : 0u;
+}
+
+template <int OP, bool BF16>
+__global__ void __launch_bounds__(SLAB_THREADS, 1) coc_slab_kernel(const __grid_constant__ KParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // every kernel parameter the roles need, read once up front (the first
+    // read of each parameter line is a long-latency miss)
+    const int S = p.slab_stages;
+    const int nb = p.slab_boxes;          // 64-column groups per slab
+    const int kps = p.slab_kps;           // k-blocks per stage (divides kblocks)
+    const int csplit = p.slab_split;      // CTAs (one cluster) per slab
+    const int a_rows = p.a_box_rows;
+    const int R = p.num_kshards;
+    const int kblocks = p.kblocks;
+    const int units = p.units;
+    const int m = p.m, n = p.n;
+    const uint32_t a_kb = static_cast<uint32_t>(a_rows) * 128u;                 // A bytes per k-block
+    const uint32_t a_stage = static_cast<uint32_t>(kps) * a_kb;
+    const uint32_t b_group = static_cast<uint32_t>(kps) * kSlabBoxBytes;       // one 64-column group's k x 64
+    const uint32_t b_stage = static_cast<uint32_t>(nb) * b_group;
+    const int W = nb * 64;                // slab width
+    const int ow = W / csplit;            // columns this CTA finalises (split: its share of the slab)
+
+    uint8_t* a_st = smem;                          // S x a_stage
+    uint8_t* b_st = a_st + S * a_stage;            // S x b_stage
+    uint8_t* stg = b_st + S * b_stage;             // 4 epilogue warps x 4 KiB
+    uint8_t* recv = stg + NUM_EPI_WARPS * EPI_BUF_BYTES;   // split: the other parts' sums of this CTA's columns
+    uint64_t* full = reinterpret_cast<uint64_t*>(recv + slab_recv_bytes(nb, csplit));   // [S]
+    uint64_t* empty = full + S;                    // [S]
+    uint64_t* accf = empty + S;                    // [2] accumulator ready for the epilogue
+    uint64_t* acce = accf + 2;                     // [2] accumulator drained (4 epilogue warps)
+    uint64_t* never = acce + 2;                    // [1] nothing arrives here (fault-injection test)
+    uint64_t* drain = never + 1;                   // [1] MMA drain before TMEM release
+    uint64_t* red_full = drain + 1;                // [1] split: every other part pushed its sums here
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red_full + 1);
+    uint32_t* abort_word = tmem_slot + 1;
+    const Ctl ctl{abort_word, p.status};
+    const int nq = min(NUM_EPI_WARPS, (m + 31) / 32);   // epilogue warps holding output rows
+
+    if (warp == 0 && lane < R && lane < COC_MAX_RANKS) {
+        prefetch_tmap(&p.tm_a[lane]);
+        prefetch_tmap(&p.tm_b[lane]);
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&accf[b]), 1);
+            mbar_init(smem_u32(&acce[b]), NUM_EPI_WARPS);
+        }
+        mbar_init(smem_u32(never), 1);
+        mbar_init(smem_u32(drain), 1);
+        mbar_init(smem_u32(red_full), csplit > 1 ? (csplit - 1) * nq : 1);
+        *abort_word = 0u;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        fence_proxy_async_smem();
+    }
+    const uint32_t tmem_cols = nb == 1 ? 128u : 256u;   // two W-column accumulators
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), tmem_cols);
+        tmem_relinquish();
+    }
+    // The producer warp (whose lane 0 initialised the barriers) only arrives
+    // and starts loading; it waits for the cluster barrier at the end.  Split:
+    // the cluster's barriers exist before any part pushes remotely.
+    tc_fence_before();
+    if (warp == 0) __syncwarp();
+    if (csplit > 1) {
+        cluster_arrive();
+        if (warp != 0) cluster_wait();
+    } else if (warp == 0) {
+        named_arrive(kSlabStageBar, SLAB_THREADS);
+    } else {
+        named_sync(kSlabStageBar, SLAB_THREADS);
+    }
+    tc_fence_after();
+    const uint32_t tmem_base = warp == 0 ? 0u : *tmem_slot;
+    const bool probe = p.clock_slot >= 0 && blockIdx.x == 0 && threadIdx.x == 0;
+    uint64_t probe_clk = 0, probe_ns = 0;
+    if (probe) {
+        probe_clk = clock64();
+        probe_ns = globaltimer();
+    }
+    // a unit is one slab (stage s of its contraction: shard s / spk, k-blocks
+    // from (s % spk) kps).  Unsplit, CTA b takes slabs b, b + grid, ...;
+    // split, cluster c takes slab c alone (the host launches one cluster per
+    // slab: the reception areas are never reused), and its part `part` sums
+    // stages [st_lo, st_hi), the parts adding up to the whole contraction.
+    const uint32_t part = csplit > 1 ? cluster_rank() : 0u;
+    const int first_u = static_cast<int>(blockIdx.x) / csplit;
+    const int u_step = static_cast<int>(gridDim.x) / csplit;
+    const int spk = kblocks / kps;            // stages per shard
+    const int spu = R * spk;                  // stages per unit
+    const int st_lo = (spu * static_cast<int>(part)) / csplit;
+    const int st_hi = (spu * (static_cast<int>(part) + 1)) / csplit;
+
+    if (warp == 0) {
+        // ================================================= TMA producer ===
+        const bool b_kmajor = p.b_kmajor != 0;
+        const bool a3d = p.slab_a3d != 0;
+        const uint64_t pol_a = make_l2_policy(2), pol_b = make_l2_policy(1);   // X reused, W streamed once
+        uint32_t stage = 0, phase = 0, filled = 0, fill_parity = 0;
+        bool ok = true;
+        for (int u = first_u; ok && u < units; u += u_step) {
+            const int col0 = u * W;
+            for (int s = st_lo; s < st_hi; ++s) {
+                const int ks = s / spk;
+                const int kb = (s - ks * spk) * kps;
+                ok = warp_wait(smem_u32(&empty[stage]), phase ^ 1u, ctl, 0x500u + stage);
+                if (!ok) break;
+                if (lane == 0) {
+                    const CUtensorMap* am = &p.tm_a[ks];
+                    const CUtensorMap* bm = &p.tm_b[ks];
+                    const uint32_t fb = smem_u32(&full[stage]);
+                    mbar_expect_tx(fb, a_stage + b_stage);
+                    const uint32_t adst = smem_u32(a_st + stage * a_stage);
+                    if (a3d) {
+                        tma_load_3d_hint(adst, am, 0, 0, kb, fb, pol_a);
+                    } else {
+                        for (int t = 0; t < kps; ++t) tma_load_2d_hint(adst + t * a_kb, am, (kb + t) * BK, 0, fb, pol_a);
+                    }
+                    const uint32_t bdst = smem_u32(b_st + stage * b_stage);
+                    if (b_kmajor) {
+                        if (a3d) {
+                            tma_load_3d_hint(bdst, bm, 0, col0, kb, fb, pol_b);
+                        } else {
+                            for (int t = 0; t < kps; ++t)
+                                tma_load_2d_hint(bdst + t * (b_stage / kps), bm, (kb + t) * BK, col0, fb, pol_b);
+                        }
+                    } else {
+                        for (int j = 0; j < nb; ++j)
+                            tma_load_2d_hint(bdst + j * b_group, bm, col0 + 64 * j, kb * BK, fb, pol_b);
+                    }
+                    filled |= 1u << stage;
+                    fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
+                }
+                __syncwarp();
+                if (++stage == static_cast<uint32_t>(S)) { stage = 0; phase ^= 1u; }
+            }
+        }
+        if (!ok && lane == 0) {
+            // leave no TMA load in flight into shared memory
+            for (int s = 0; s < S; ++s)
+                if (filled & (1u << s)) drain_wait(smem_u32(&full[s]), (fill_parity >> s) & 1u, kDrainNs);
+        }
+    } else if (warp == 1) {
+        // ================================================= MMA issuer ===
+        // B MN-major (k x n storage): 64-column groups b_group apart, k-block t
+        // at +8 KiB t, +2 KiB per 16-k step; B K-major (n x k storage): k-block
+        // t at +W x 128 bytes t, +32 bytes per 16-k step, and the "B
+        // transposed" bit cleared
+        const bool b_kmajor = p.b_kmajor != 0;
+        const uint32_t idesc = make_idesc(BF16, BM, W) & (b_kmajor ? ~(1u << 16) : ~0u);
+        const uint32_t b_lbo = b_kmajor ? 16u : b_group;
+        const uint64_t b_step = b_kmajor ? 2u : 128u;
+        const uint32_t b_kb = b_kmajor ? static_cast<uint32_t>(W) * 128u : kSlabBoxBytes;
+        uint32_t stage = 0, phase = 0;
+        int acc_i = 0;
+        bool ok = true;
+        for (int u = first_u; ok && u < units; u += u_step) {
+            const int buf = acc_i & 1;
+            ok = warp_wait(smem_u32(&acce[buf]), ((acc_i >> 1) & 1) ^ 1u, ctl, 0x520u + buf);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * W);
+            for (int i = 0; i < st_hi - st_lo; ++i) {
+                ok = warp_wait(smem_u32(&full[stage]), phase, ctl, 0x540u + stage);
+                if (!ok) break;
+                tc_fence_after();
+                if (lane == 0) {
+                    for (int t = 0; t < kps; ++t) {
+                        const uint64_t ad = make_sdesc(smem_u32(a_st + stage * a_stage + t * a_kb), 16u, 1024u);
+                        const uint64_t bd = make_sdesc(smem_u32(b_st + stage * b_stage + t * b_kb), b_lbo, 1024u);
+#pragma unroll
+                        for (int kk = 0; kk < BK / UMMA_K; ++kk)
+                            tc_mma_f16(d_tmem, ad + static_cast<uint64_t>(kk) * 2u,
+                                       bd + static_cast<uint64_t>(kk) * b_step, idesc,
+                                       (i > 0 || t > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    tc_commit(smem_u32(&empty[stage]));
+                }
+                __syncwarp();
+                if (++stage == static_cast<uint32_t>(S)) { stage = 0; phase ^= 1u; }
+            }
+            if (!ok) break;
+            if (lane == 0) tc_commit(smem_u32(&accf[buf]));
+            __syncwarp();
+            ++acc_i;
+        }
+        // every issued MMA must finish before TMEM is released
+        if (lane == 0) {
+            tc_commit(smem_u32(drain));
+            drain_wait(smem_u32(drain), 0, kDrainNs);
+        }
+        __syncwarp();
+    } else {
+        // ================================================= epilogue ===
+        const int q = warp & 3;                  // TMEM lane quadrant this warp may read
+        const int row0 = 32 * q;
+        const bool active = q < nq;
+        uint8_t* buf_s = stg + (warp - 2) * EPI_BUF_BYTES;
+        const int n_out = p.n_out, rpr = p.rows_per_rank;
+        const uint32_t row_bytes = static_cast<uint32_t>(ow) * 4u;   // one row of a reception slot
+        // Round 32 columns of this warp's rows (fp32 bits, lane = row) and
+        // store them: row = lane into the staging buffer (64 bytes, 16-byte
+        // chunk j at j ^ (row / 2 % 4)), read back so that lane l holds chunk
+        // l % 4 of rows l / 4 + 8 i, then 16-byte stores to every rank output
+        // (AllReduce) or to the rank owning the row (ReduceScatter).
+        auto emit32 = [&](int col, const uint32_t (&v)[32]) {
+            uint8_t* rowp = buf_s + lane * 64;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint4 w4;
+                w4.x = pack2<BF16>(v[8 * j + 0], v[8 * j + 1]);
+                w4.y = pack2<BF16>(v[8 * j + 2], v[8 * j + 3]);
+                w4.z = pack2<BF16>(v[8 * j + 4], v[8 * j + 5]);
+                w4.w = pack2<BF16>(v[8 * j + 6], v[8 * j + 7]);
+                *reinterpret_cast<uint4*>(rowp + ((j ^ ((lane >> 1) & 3)) << 4)) = w4;
+            }
+            __syncwarp();
+            const int ch = lane & 3;
+            uint4 rv[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int rr = (lane >> 2) + 8 * i;
+                rv[i] = *reinterpret_cast<const uint4*>(buf_s + rr * 64 + ((ch ^ ((rr >> 1) & 3)) << 4));
+            }
+            __syncwarp();   // the buffer is free for the next 32 columns
+            const int c = col + ch * 8;   // n % 8 == 0: a chunk is wholly inside or outside
+            if (c >= n) return;
+            if constexpr (OP == OP_RS) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int g = row0 + (lane >> 2) + 8 * i;
+                    if (g < m) {
+                        const int dst = g / rpr;
+                        *reinterpret_cast<uint4*>(p.outp[dst] + static_cast<long long>(g - dst * rpr) * n + c) = rv[i];
+                    }
+                }
+            } else {
+                for (int o = 0; o < n_out; ++o) {
+                    uint16_t* base = p.outp[o] + c;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int g = row0 + (lane >> 2) + 8 * i;
+                        if (g < m) *reinterpret_cast<uint4*>(base + static_cast<long long>(g) * n) = rv[i];
+                    }
+                }
+            }
+        };
+        // reception slot row of source part `src` (not this CTA) for this warp's lane
+        auto recv_row = [&](uint32_t src, uint32_t dst_part) {
+            const uint32_t sidx = src < dst_part ? src : src - 1u;
+            return smem_u32(recv) + ((sidx * 2u + static_cast<uint32_t>(q)) * 32u + static_cast<uint32_t>(lane)) * row_bytes;
+        };
+        int acc_i = 0;
+        bool ok = true;
+        if (p.inject_timeout) ok = warp_wait(smem_u32(never), 0, ctl, 0x560u);
+        for (int u = first_u; ok && u < units; u += u_step) {
+            const int buf = acc_i & 1;
+            ok = warp_wait(smem_u32(&accf[buf]), (acc_i >> 1) & 1, ctl, 0x570u + buf);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(row0) << 16) + static_cast<uint32_t>(buf * W);
+            if (active && csplit > 1) {
+                // push this part's sums of every other part's columns into that
+                // part's reception area (16-byte chunk c of a row at c ^ (row % 8))
+                for (int j = 0; j < csplit; ++j) {
+                    if (j == static_cast<int>(part)) continue;
+                    const uint32_t dst = map_to_rank(recv_row(part, static_cast<uint32_t>(j)), static_cast<uint32_t>(j));
+                    for (int cc = 0; cc < ow; cc += 32) {
+                        uint32_t v[32];
+                        tmem_ld_32cols(t_row + j * ow + cc, v);
+                        tmem_wait_ld();
+                        if (row0 + lane < m) {
+#pragma unroll
+                            for (int jj = 0; jj < 8; ++jj) {
+                                const uint32_t chunk = static_cast<uint32_t>(cc / 4 + jj);
+                                asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};"
+                                             ::"r"(dst + ((chunk ^ (lane & 7)) << 4)), "r"(v[4 * jj]), "r"(v[4 * jj + 1]),
+                                               "r"(v[4 * jj + 2]), "r"(v[4 * jj + 3])
+                                             : "memory");
+                            }
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0)
+                    for (int j = 0; j < csplit; ++j)
+                        if (j != static_cast<int>(part))
+                            mbar_arrive_cluster(map_to_rank(smem_u32(red_full), static_cast<uint32_t>(j)));
+                ok = warp_wait<true>(smem_u32(red_full), acc_i & 1, ctl, 0x580u);
+                if (!ok) break;
+            }
+            // this CTA's columns: the parts added in part order (its own from
+            // TMEM), 32 at a time
+            for (int cc = 0; cc < ow; cc += 32) {
+                uint32_t v[32];
+                if (active) {
+                    tmem_ld_32cols(t_row + static_cast<int>(part) * ow + cc, v);
+                    tmem_wait_ld();
+                }
+                if (cc + 32 >= ow) {
+                    // the accumulator is free for the unit after next
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&acce[buf]));
+                }
+                const int col = u * W + static_cast<int>(part) * ow + cc;
+                if (!active || col >= n) continue;
+                if (csplit > 1) {
+                    uint32_t own[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) own[i] = v[i];
+                    for (int sp = 0; sp < csplit; ++sp) {
+                        uint32_t w[32];
+                        if (sp == static_cast<int>(part)) {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) w[i] = own[i];
+                        } else {
+                            const uint32_t rb = recv_row(static_cast<uint32_t>(sp), part);
+#pragma unroll
+                            for (int jj = 0; jj < 8; ++jj) {
+                                const uint32_t chunk = static_cast<uint32_t>(cc / 4 + jj);
+                                asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                             : "=r"(w[4 * jj]), "=r"(w[4 * jj + 1]), "=r"(w[4 * jj + 2]), "=r"(w[4 * jj + 3])
+                                             : "r"(rb + ((chunk ^ (lane & 7)) << 4))
+                                             : "memory");
+                            }
+                        }
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            v[i] = sp == 0 ? w[i] : __float_as_uint(__uint_as_float(v[i]) + __uint_as_float(w[i]));
+                    }
+                }
+                emit32(col, v);
+            }
+            ++acc_i;
+        }
+    }
+
+    if (csplit > 1) {
+        // no CTA leaves while a part may still push into its shared memory
+        if (warp == 0) cluster_wait();   // the set-up phase this warp only arrived at
+        tc_fence_before();
+        cluster_sync();
+    } else {
+        tc_fence_before();
+        __syncthreads();
+    }
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, tmem_cols);
+    }
+    if (probe) {
+        unsigned long long* slot = reinterpret_cast<unsigned long long*>(p.status + STATUS_WORDS) + 2 * p.clock_slot;
+        atomicAdd(slot, static_cast<unsigned long long>(clock64() - probe_clk));
+        atomicAdd(slot + 1, static_cast<unsigned long long>(globaltimer() - probe_ns));
+    }
+}
+
+constexpr int kMaxDevices = 64;
+
+template <int OP, bool BF16>
+cudaError_t launch_slab_t(const KParams& p, int grid, cudaStream_t stream) {
+    auto kern = coc_slab_kernel<OP, BF16>;
+    static std::atomic<unsigned char> smem_set[kMaxDevices];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices || !smem_set[dev].load(std::memory_order_acquire)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSlabSmemCap);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < kMaxDevices) smem_set[dev].store(1, std::memory_order_release);
+    }
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(SLAB_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = slab_smem_bytes(p.slab_stages, p.a_box_rows, p.slab_boxes, p.slab_kps, p.slab_split);
+    cfg.stream = stream;
+    if (p.slab_split > 1) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = p.slab_split;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+template <int OP, bool BF16>
+int slab_max_clusters_t(int split, int smem) {
+    auto kern = coc_slab_kernel<OP, BF16>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSlabSmemCap) != cudaSuccess) return 0;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = split;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(split, 1, 1);
+    cfg.blockDim = dim3(SLAB_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int v = 0;
+    if (cudaOccupancyMaxActiveClusters(&v, kern, &cfg) != cudaSuccess) return 0;
+    return v;
+}
+
+}  // namespace
+
+int slab_stages(int a_rows, int boxes, int kps, int split) {
+    int s = kSlabMaxStages;
+    while (s > 2 && slab_smem_bytes(s, a_rows, boxes, kps, split) > kSlabSmemCap) --s;
+    return s;
+}
+
+int slab_smem_bytes(int stages, int a_rows, int boxes, int kps, int split) {
+    return 1024 + stages * kps * (a_rows * 128 + boxes * static_cast<int>(kSlabBoxBytes)) +
+           NUM_EPI_WARPS * EPI_BUF_BYTES + static_cast<int>(slab_recv_bytes(boxes, split)) +
+           static_cast<int>(slab_bar_bytes(stages));
+}
+
+cudaError_t launch_slab(int op, bool bf16, const KParams& p, int grid, cudaStream_t stream) {
+    switch (op) {
+        case OP_AR: return bf16 ? launch_slab_t<OP_AR, true>(p, grid, stream) : launch_slab_t<OP_AR, false>(p, grid, stream);
+        case OP_RS: return bf16 ? launch_slab_t<OP_RS, true>(p, grid, stream) : launch_slab_t<OP_RS, false>(p, grid, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+int slab_max_clusters(bool bf16, int split, int smem) {
+    // the kernel's resources do not depend on the operator; ask one instance
+    return bf16 ? slab_max_clusters_t<OP_AR, true>(split, smem) : slab_max_clusters_t<OP_AR, false>(split, smem);
+}
+
+}  // namespace coc

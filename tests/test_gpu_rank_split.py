@@ -31,6 +31,13 @@ def _lib():
     coc.sync_status()
 
 
+@pytest.fixture(autouse=True)
+def _no_slab(monkeypatch):
+    # decode-sized shapes whose column slabs cover the SMs would otherwise go
+    # to the column-slab kernel, which needs no split
+    monkeypatch.setenv("COC_SLAB", "0")
+
+
 def _data(R, m, n, ks, dt, seed):
     return wl.RowParallel(R=R, m=m, n=n, k_shard=ks, dtype=dt, x_dist="normal(0,1)", w_dist="normal(0,0.02)",
                           seed=seed).make()
