@@ -684,10 +684,28 @@ def time_context(ops, dev, bus=None, index=0):
         graphs[str(m)] = gd.replay
         keep.append((gd, ddx, ddw, dout))
         byts[str(m)] = 2 * (ds_.K * ds_.n + m * ds_.K + ds_.R * m * ds_.n)
+    # the suite's other decode layers at m 16: BLOOM-7B (n 4096, K 8 x 2048) and
+    # BLOOM-176B (n 14336, K 8 x 7168)
+    for name, n_, ks_ in (("bloom7b_m16", 4096, 2048), ("bloom176b_m16", 14336, 7168)):
+        ds_ = wl.RowParallel(R=8, m=16, n=n_, k_shard=ks_, dtype=torch.bfloat16, x_dist="normal(0,1)",
+                             w_dist="normal(0,0.02)", seed=1)
+        dxs, dws = ds_.make()
+        ddx, ddw = [x.to(dev) for x in dxs], [w.to(dev) for w in dws]
+        dout = [torch.empty(16, ds_.n, dtype=ds_.dtype, device=dev) for _ in range(ds_.R)]
+        coc.matmul_all_reduce(ddx, ddw, dout)
+        torch.cuda.synchronize()
+        gd = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gd):
+            for _ in range(20):
+                coc.matmul_all_reduce(ddx, ddw, dout)
+        graphs[name] = gd.replay
+        keep.append((gd, ddx, ddw, dout))
+        byts[name] = 2 * (ds_.K * ds_.n + 16 * ds_.K + ds_.R * 16 * ds_.n)
     r = interleaved(graphs, it=10)
-    out["decode_ar_r8_n8192_k8192_cuda_graph"] = {
-        m: {"us_per_call": round(1e3 * r[m]["median_ms"] / 20, 1),
-            "hbm_gbs": round(byts[m] / (1e3 * r[m]["median_ms"] / 20) / 1e3, 0)} for m in graphs}
+    per_call = {m: {"us_per_call": round(1e3 * r[m]["median_ms"] / 20, 1),
+                    "hbm_gbs": round(byts[m] / (1e3 * r[m]["median_ms"] / 20) / 1e3, 0)} for m in graphs}
+    out["decode_ar_r8_n8192_k8192_cuda_graph"] = {m: v for m, v in per_call.items() if not m.startswith("bloom")}
+    out["decode_ar_layers_cuda_graph"] = {m: v for m, v in per_call.items() if m.startswith("bloom")}
     del keep, graphs
     # the whole suite step captured once into a CUDA graph and replayed,
     # against the same step launched eagerly (the host's launch cost)

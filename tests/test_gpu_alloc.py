@@ -44,6 +44,25 @@ def _calls():
         xs, ws = map(to_dev, rp(R, m, n, ks))
         outs = [torch.empty(m, n, dtype=BF16, device=DEV) for _ in range(R)]
         calls[name] = lambda xs=xs, ws=ws, o=outs: coc.matmul_all_reduce(xs, ws, o, chunks=2)
+    # the column-slab kernel (decode-sized m), unsplit and split over clusters
+    for name, plan in (("ar_slab", (2, 1, 2)), ("ar_slab_split", (2, 2, 2))):
+        xs, ws = map(to_dev, rp(8, 16, 2048, 256))
+        outs = [torch.empty(16, 2048, dtype=BF16, device=DEV) for _ in range(8)]
+
+        def slab_call(xs=xs, ws=ws, o=outs, plan=plan):
+            env = {"COC_SLAB": "1", "COC_SLAB_BOXES": str(plan[0]), "COC_SLAB_SPLIT": str(plan[1]),
+                   "COC_SLAB_KPS": str(plan[2])}
+            prev = {k: os.environ.get(k) for k in env}
+            os.environ.update(env)
+            try:
+                coc.matmul_all_reduce(xs, ws, o)
+            finally:
+                for k, v in prev.items():
+                    if v is None:
+                        del os.environ[k]
+                    else:
+                        os.environ[k] = v
+        calls[name] = slab_call
     xs, ws = map(to_dev, rp(8, 64, 1024, 256))
     rso = [torch.empty(8, 1024, dtype=BF16, device=DEV) for _ in range(8)]
     calls["rs_split"] = lambda: coc.matmul_reduce_scatter(xs, ws, rso)

@@ -3,7 +3,7 @@
 Every fused operator writes R rank buffers, and several of its store paths
 compute their addresses by hand instead of going through a bounds-clipped TMA
 store: the AllReduce replica stores, the rank-split slab stores, the
-ALL_GATHER_MATMUL_V2 gather copy, the MoE token permute and combine scatter,
+column-slab kernel's stores, the ALL_GATHER_MATMUL_V2 gather copy, the MoE token permute and combine scatter,
 and the w8A16 and allocation-free AllReduce paths.  A store that runs past a
 buffer would land in the next rank's buffer, which only an element-wise
 check of that row would notice.
@@ -110,6 +110,39 @@ def test_allreduce_guards(R, m, n, ks, dt, chunks):
     for r, o in enumerate(slab.views):
         Slab.assert_written(o, f"AllReduce rank {r}")
         assert_close(o, ref, R * ks, f"AllReduce rank {r}")
+
+
+# The column-slab kernel (decode-sized m): plain 16-byte stores of every
+# slab's rows to every rank output (AllReduce) or to the owning rank
+# (ReduceScatter), slabs split over clusters of 2 and 4, ragged last slab.
+SLAB_CASES = [
+    # op, R, m, n, k_shard, dtype, (boxes, split, kps)
+    ("ar", 8, 40, 1000, 200, BF16, (2, 2, 1)),    # k_shard ends inside a k-block
+    ("ar", 4, 17, 520, 128, F16, (2, 4, 2)),      # clusters of 4, 3-D X boxes
+    ("ar", 2, 100, 264, 64, BF16, (1, 1, 1)),     # 64-column slabs, m > 64 (no split)
+    ("rs", 8, 64, 1000, 72, BF16, (2, 2, 1)),     # 8 rows per rank
+    ("rs", 4, 32, 520, 128, F16, (1, 2, 2)),      # 64-column slabs split in two
+]
+
+
+@pytest.mark.parametrize("op,R,m,n,ks,dt,plan", SLAB_CASES)
+def test_column_slab_guards(op, R, m, n, ks, dt, plan, monkeypatch):
+    b, sp, kps = plan
+    for k, v in (("COC_SLAB", 1), ("COC_SLAB_BOXES", b), ("COC_SLAB_SPLIT", sp), ("COC_SLAB_KPS", kps)):
+        monkeypatch.setenv(k, str(v))
+    xs, ws = _rp(R, m, n, ks, dt, seed=550 + m)
+    rows = m if op == "ar" else m // R
+    slab = Slab([(rows, n)] * R, [dt] * R)
+    if op == "ar":
+        coc.matmul_all_reduce(to_dev(xs), to_dev(ws), slab.views)
+    else:
+        coc.matmul_reduce_scatter(to_dev(xs), to_dev(ws), slab.views)
+    coc.sync_status()
+    slab.check_guards(f"column slab {op}")
+    ref = orc.matmul_all_reduce(CODE[dt], bits(xs), bits(ws))
+    for r, o in enumerate(slab.views):
+        Slab.assert_written(o, f"column slab {op} rank {r}")
+        assert_close(o, ref if op == "ar" else ref[r * rows:(r + 1) * rows], R * ks, f"column slab {op} rank {r}")
 
 
 def test_allreduce_noalloc_guards():
