@@ -315,18 +315,18 @@ int rank_split(int op, int R, int64_t ks, int64_t tiles, bool pair, int sm_count
     return ksplit;
 }
 
-// Column-slab kernel (coc_slab.cu) for decode-sized m (m <= kSlabMaxRows;
-// above that the X rows every slab re-reads from L2 cost more than the rank
-// split's reduction).  Plan: 128-column slabs (256-byte weight rows: measured
-// faster than 64 columns, whose 128-byte rows moved 30% less per SM), two
-// k-blocks per stage (one TMA operation per 64-column group and one for X),
-// and, while the slabs fill at most half of the SMs, each slab's contraction
-// split over a cluster of 2 or 4 CTAs.  No plan (boxes 0) when the CTAs would
-// fill less than half of the SMs: the persistent kernel's rank split takes
-// those shapes.  COC_SLAB=0 turns the kernel off; COC_SLAB=1 takes it for
-// every m <= 128, with COC_SLAB_BOXES, COC_SLAB_KPS and COC_SLAB_SPLIT
-// overriding the plan (tests and tuning only).
-constexpr int64_t kSlabMaxRows = 64;
+// Column-slab kernel (coc_slab.cu) for decode-sized m (m <= 128, one row
+// tile).  Plan: 128-column slabs (256-byte weight rows: measured faster than
+// 64 columns, whose 128-byte rows moved 30% less per SM), two k-blocks per
+// stage (one TMA operation per 64-column group and one for X), and, while the
+// slabs fill at most half of the SMs, each slab's contraction split over a
+// cluster of 2 or 4 CTAs.  No plan (boxes 0) when the CTAs would fill less
+// than half of the SMs: the persistent kernel's rank split takes those
+// shapes.  Measured (8 ranks, K 8 x 1024, bf16, CUDA graph): n 8192 at m 16 /
+// 64 / 96 / 128 takes 27.0 / 27.7 / 30.0 / 37.1 us against 34.1 / 34.4 /
+// 37.0 / 41.5 us for the rank split.  COC_SLAB=0 turns the kernel off;
+// COC_SLAB=1 takes it whenever m <= 128, with COC_SLAB_BOXES, COC_SLAB_KPS
+// and COC_SLAB_SPLIT overriding the plan (tests and tuning only).
 struct SlabPlan {
     int boxes = 0, split = 1, kps = 1;
 };
@@ -338,9 +338,12 @@ SlabPlan slab_plan(int op, int R, int64_t m, int64_t n, int64_t ks, int sm_count
     SlabPlan pl;
     if ((op != OP_AR && op != OP_RS) || ks <= 0 || m <= 0 || m > BM) return pl;
     const int forced = env_int("COC_SLAB", -1);
-    if (forced == 0 || (forced != 1 && m > kSlabMaxRows)) return pl;
+    if (forced == 0) return pl;
     const int boxes = env_int("COC_SLAB_BOXES", 2) == 1 ? 1 : 2;
     const int64_t kblocks = (ks + BK - 1) / BK;
+    // k-blocks per stage: 4 for 64-column slabs, 2 for 128 (measured best; at
+    // m = 128 two stages of 2 k-blocks beat five of 1: fewer TMA operations
+    // in flight matter more than ring depth)
     int kps = env_int("COC_SLAB_KPS", boxes == 1 ? 4 : 2);
     kps = kps >= 4 ? 4 : kps >= 2 ? 2 : 1;
     while (kps > 1 && kblocks % kps != 0) kps /= 2;
@@ -349,11 +352,9 @@ SlabPlan slab_plan(int op, int R, int64_t m, int64_t n, int64_t ks, int sm_count
     int split = 1;
     // (each part finalises 64 boxes / split >= 32 columns and sums at least one stage)
     const int max_split = boxes == 2 ? 4 : 2;
-    if (m <= kSlabMaxRows) {
-        while (split < max_split && slabs * split * 2 <= sm_count && split * 2 <= spu) split *= 2;
-        const int fs = env_int("COC_SLAB_SPLIT", 0);
-        if ((fs == 1 || fs == 2 || fs == 4) && fs <= max_split && fs <= spu) split = fs;
-    }
+    while (split < max_split && slabs * split * 2 <= sm_count && split * 2 <= spu) split *= 2;
+    const int fs = env_int("COC_SLAB_SPLIT", 0);
+    if ((fs == 1 || fs == 2 || fs == 4) && fs <= max_split && fs <= spu) split = fs;
     if (forced != 1 && slabs * split * 2 < sm_count) return pl;
     pl.boxes = boxes;
     pl.split = split;

@@ -206,7 +206,7 @@ cudaError_t launch_split(int op, bool bf16, const KParams& p, int grid, int clus
 // 64 slab_boxes boxes (2-D) or dims (BK, n, kblocks) with boxes (BK, 64
 // slab_boxes, slab_kps) (3-D, slab_a3d).  outp holds the n_out outputs
 // (AllReduce) or the R rank outputs (ReduceScatter).  With slab_split > 1
-// (m <= 64) the grid is slab_split x the slabs run at once, in clusters of
+// the grid is slab_split x the slabs run at once, in clusters of
 // slab_split CTAs.
 constexpr int kSlabMaxStages = 32;
 constexpr int kSlabSmemCap = 227 * 1024;                       // dynamic shared memory per CTA

@@ -2,9 +2,9 @@
 // decode-sized m (CoC page, 融合算子实现: the same two operators as the
 // persistent kernel, for the few-row activations of token generation).
 //
-// At m <= 64 the operator reads the R weight shards (R x k_shard x n) once
-// and does almost no arithmetic per weight byte, so its time is the weight
-// stream.  The persistent kernel's 128 x 256 tiles are too few to spread that
+// At m <= 128 (one row tile) the operator reads the R weight shards (R x
+// k_shard x n) once and does little arithmetic per weight byte, so its time
+// is the weight stream.  The persistent kernel's 128 x 256 tiles are too few to spread that
 // stream over the SMs, and cutting K across CTAs (the rank split) costs a
 // cross-CTA reduction after the last weight byte arrives.  Here a work unit
 // is one column slab of the output instead: all m rows by SN = 64 or 128
@@ -66,10 +66,10 @@ __host__ __device__ constexpr uint32_t slab_bar_bytes(int stages) {
     return static_cast<uint32_t>(8 * (2 * stages + 7) + 16);
 }
 // Reception area of a slab split over `split` CTAs: per other part, per row
-// quadrant (m <= 64: two) 32 rows of the (64 boxes / split) fp32 columns this
-// CTA finalises.
-__host__ __device__ constexpr uint32_t slab_recv_bytes(int boxes, int split) {
-    return split > 1 ? static_cast<uint32_t>((split - 1) * 2 * 32 * (64 * boxes / split) * 4) : 0u;
+// quadrant holding output rows (a_rows / 32 rounded up), 32 rows of the (64
+// boxes / split) fp32 columns this CTA finalises.
+__host__ __device__ constexpr uint32_t slab_recv_bytes(int boxes, int split, int a_rows) {
+    return split > 1 ? static_cast<uint32_t>((split - 1) * ((a_rows + 31) / 32) * 32 * (64 * boxes / split) * 4) : 0u;
 }
 
 template <int OP, bool BF16>
@@ -101,7 +101,7 @@ __global__ void __launch_bounds__(SLAB_THREADS, 1) coc_slab_kernel(const __grid_
     uint8_t* b_st = a_st + S * a_stage;            // S x b_stage
     uint8_t* stg = b_st + S * b_stage;             // 4 epilogue warps x 4 KiB
     uint8_t* recv = stg + NUM_EPI_WARPS * EPI_BUF_BYTES;   // split: the other parts' sums of this CTA's columns
-    uint64_t* full = reinterpret_cast<uint64_t*>(recv + slab_recv_bytes(nb, csplit));   // [S]
+    uint64_t* full = reinterpret_cast<uint64_t*>(recv + slab_recv_bytes(nb, csplit, a_rows));   // [S]
     uint64_t* empty = full + S;                    // [S]
     uint64_t* accf = empty + S;                    // [2] accumulator ready for the epilogue
     uint64_t* acce = accf + 2;                     // [2] accumulator drained (4 epilogue warps)
@@ -329,7 +329,8 @@ __global__ void __launch_bounds__(SLAB_THREADS, 1) coc_slab_kernel(const __grid_
         // reception slot row of source part `src` (not this CTA) for this warp's lane
         auto recv_row = [&](uint32_t src, uint32_t dst_part) {
             const uint32_t sidx = src < dst_part ? src : src - 1u;
-            return smem_u32(recv) + ((sidx * 2u + static_cast<uint32_t>(q)) * 32u + static_cast<uint32_t>(lane)) * row_bytes;
+            return smem_u32(recv) +
+                   ((sidx * static_cast<uint32_t>(nq) + static_cast<uint32_t>(q)) * 32u + static_cast<uint32_t>(lane)) * row_bytes;
         };
         int acc_i = 0;
         bool ok = true;
@@ -498,7 +499,7 @@ int slab_stages(int a_rows, int boxes, int kps, int split) {
 
 int slab_smem_bytes(int stages, int a_rows, int boxes, int kps, int split) {
     return 1024 + stages * kps * (a_rows * 128 + boxes * static_cast<int>(kSlabBoxBytes)) +
-           NUM_EPI_WARPS * EPI_BUF_BYTES + static_cast<int>(slab_recv_bytes(boxes, split)) +
+           NUM_EPI_WARPS * EPI_BUF_BYTES + static_cast<int>(slab_recv_bytes(boxes, split, a_rows)) +
            static_cast<int>(slab_bar_bytes(stages));
 }
 

@@ -119,7 +119,8 @@ SLAB_CASES = [
     # op, R, m, n, k_shard, dtype, (boxes, split, kps)
     ("ar", 8, 40, 1000, 200, BF16, (2, 2, 1)),    # k_shard ends inside a k-block
     ("ar", 4, 17, 520, 128, F16, (2, 4, 2)),      # clusters of 4, 3-D X boxes
-    ("ar", 2, 100, 264, 64, BF16, (1, 1, 1)),     # 64-column slabs, m > 64 (no split)
+    ("ar", 2, 100, 264, 64, BF16, (1, 1, 1)),     # 64-column slabs, unsplit
+    ("ar", 4, 120, 1000, 128, BF16, (2, 2, 1)),   # four row quadrants pushed between two parts
     ("rs", 8, 64, 1000, 72, BF16, (2, 2, 1)),     # 8 rows per rank
     ("rs", 4, 32, 520, 128, F16, (1, 2, 2)),      # 64-column slabs split in two
 ]

@@ -56,7 +56,9 @@ CASES = [
     (8, 5, 9792, 200, F16, (1, 1, 4)),       # k_shard ends inside a k-block: 2-D X boxes
     (4, 33, 6000, 72, BF16, (2, 4, 1)),      # rows in two TMEM lane quadrants, clusters of 4
     (8, 64, 4864, 64, F16, (1, 2, 1)),       # 64-column slabs split in two (32 columns per part)
-    (2, 128, 4096, 64, BF16, (2, 1, 1)),     # all four epilogue warps (no split above 64 rows)
+    (2, 128, 4096, 64, BF16, (2, 1, 1)),     # all four epilogue warps, unsplit
+    (4, 100, 6000, 128, BF16, (2, 2, 1)),    # four row quadrants pushed between two parts
+    (8, 128, 4096, 256, F16, (2, 4, 1)),     # four row quadrants, clusters of 4
     (2, 16, 40000, 64, BF16, (2, 1, 1)),     # several slabs per CTA (both accumulator buffers)
     (8, 16, 4096, 1024, BF16, (2, 4, 2)),    # the 4096-column decode layer: clusters of 4
     (8, 48, 8192, 256, F16, (2, 2, 4)),      # four k-blocks per stage with 128-column slabs
