@@ -336,7 +336,7 @@ int env_int(const char* name, int dflt) {
 }
 SlabPlan slab_plan(int op, int R, int64_t m, int64_t n, int64_t ks, int sm_count) {
     SlabPlan pl;
-    if ((op != OP_AR && op != OP_RS) || ks <= 0 || m <= 0 || m > BM) return pl;
+    if ((op != OP_AR && op != OP_RS && op != OP_W8) || ks <= 0 || m <= 0 || m > BM) return pl;
     const int forced = env_int("COC_SLAB", -1);
     if (forced == 0) return pl;
     const int boxes = env_int("COC_SLAB_BOXES", 2) == 1 ? 1 : 2;
@@ -356,15 +356,25 @@ SlabPlan slab_plan(int op, int R, int64_t m, int64_t n, int64_t ks, int sm_count
     const int fs = env_int("COC_SLAB_SPLIT", 0);
     if ((fs == 1 || fs == 2 || fs == 4) && fs <= max_split && fs <= spu) split = fs;
     if (forced != 1 && slabs * split * 2 < sm_count) return pl;
+    // two stages at least must fit in shared memory (w8A16 also holds the
+    // 16-bit ring): fewer k-blocks per stage where they do not
+    const bool w8 = (op == OP_W8);
+    const int a_rows = static_cast<int>((m + 7) / 8 * 8);
+    while (kps > 1 && slab_smem_bytes(2, a_rows, boxes, kps, split, w8) > kSlabSmemCap) kps /= 2;
+    if (slab_smem_bytes(2, a_rows, boxes, kps, split, w8) > kSlabSmemCap) return pl;
     pl.boxes = boxes;
     pl.split = split;
     pl.kps = kps;
     return pl;
 }
 
+// op OP_W8: the w8A16 AllReduce (int8 w, scales / zero points as for the
+// persistent kernel).
 coc_status_t slab_row_parallel(int op, int R, int64_t m, int64_t n, int64_t ks, const void* const* x,
                                const void* const* w, void* const* out, int n_out, coc_dtype_t dt, const SlabPlan& pl,
-                               DeviceState* ds, cudaStream_t stream, bool w_nk) {
+                               DeviceState* ds, cudaStream_t stream, bool w_nk, const void* const* scale,
+                               coc_scale_t gran, int64_t group, const void* const* zero) {
+    const bool w8 = (op == OP_W8);
     KParams p;
     std::memset(&p, 0, sizeof p);
     p.R = R;
@@ -385,19 +395,23 @@ coc_status_t slab_row_parallel(int op, int R, int64_t m, int64_t n, int64_t ks, 
     // the slabs run unsplit.
     int split = pl.split, clusters = 0;
     if (split > 1) {
-        const int smem = slab_smem_bytes(slab_stages(p.a_box_rows, boxes, kps, split), p.a_box_rows, boxes, kps, split);
-        const long long key = (static_cast<long long>(dt == COC_BF16) << 40) | (static_cast<long long>(split) << 32) | smem;
+        const int smem =
+            slab_smem_bytes(slab_stages(p.a_box_rows, boxes, kps, split, w8), p.a_box_rows, boxes, kps, split, w8);
+        const long long key = (static_cast<long long>(w8) << 41) | (static_cast<long long>(dt == COC_BF16) << 40) |
+                              (static_cast<long long>(split) << 32) | smem;
         std::lock_guard<std::mutex> lk(g_mu);
         auto it = ds->slab_clusters.find(key);
         if (it == ds->slab_clusters.end())
-            it = ds->slab_clusters.emplace(key, slab_max_clusters(dt == COC_BF16, split, smem)).first;
+            it = ds->slab_clusters.emplace(key, slab_max_clusters(dt == COC_BF16, w8, split, smem)).first;
         clusters = it->second;
         if (clusters < p.units) split = 1;
     }
     p.slab_boxes = boxes;
     p.slab_kps = kps;
     p.slab_split = split;
-    p.slab_stages = slab_stages(p.a_box_rows, boxes, kps, split);
+    p.slab_stages = slab_stages(p.a_box_rows, boxes, kps, split, w8);
+    if (slab_smem_bytes(p.slab_stages, p.a_box_rows, boxes, kps, split, w8) > kSlabSmemCap)
+        return fail(COC_ERR_SHAPE, "column-slab schedule does not fit in shared memory (m = %lld)", (long long)m);
     p.b_kmajor = w_nk ? 1 : 0;
     const CUtensorMapDataType adt = tma_dtype(dt);
     coc_status_t st;
@@ -417,15 +431,31 @@ coc_status_t slab_row_parallel(int op, int R, int64_t m, int64_t n, int64_t ks, 
             if (w_nk && (st = encode(&p.tm_b[r], adt, w[r], ks, n, ks * 2, BK, 64 * boxes, CU_TENSOR_MAP_SWIZZLE_128B)) != COC_OK)
                 return st;
         }
-        if (!w_nk && (st = encode(&p.tm_b[r], adt, w[r], n, ks, n * 2, 64, BK * kps, CU_TENSOR_MAP_SWIZZLE_128B)) != COC_OK)
+        if (w8) {
+            // int8 W: one box of the slab's columns x the stage's k-blocks, unswizzled
+            st = encode(&p.tm_b[r], CU_TENSOR_MAP_DATA_TYPE_UINT8, w[r], n, ks, n, 64 * boxes, BK * kps,
+                        CU_TENSOR_MAP_SWIZZLE_NONE);
+            if (st != COC_OK) return st;
+        } else if (!w_nk &&
+                   (st = encode(&p.tm_b[r], adt, w[r], n, ks, n * 2, 64, BK * kps, CU_TENSOR_MAP_SWIZZLE_128B)) != COC_OK) {
             return st;
+        }
+    }
+    if (w8) {
+        p.gran = static_cast<int>(gran);
+        p.group = static_cast<int>(group);
+        for (int r = 0; r < R; ++r) p.scale[r] = static_cast<const uint16_t*>(scale[r]);
+        if (zero != nullptr) {
+            p.has_zero = 1;
+            for (int r = 0; r < R; ++r) p.zero[r] = static_cast<const int8_t*>(zero[r]);
+        }
     }
     for (int o = 0; o < (op == OP_RS ? R : n_out); ++o) p.outp[o] = static_cast<uint16_t*>(out[o]);
     p.status = ds->status;
     p.inject_timeout = g_inject.load();
     p.clock_slot = g_clock_slot.load();
     const int grid = split > 1 ? split * p.units : (p.units < ds->sm_count ? p.units : ds->sm_count);
-    const cudaError_t e = launch_slab(op, dt == COC_BF16, p, grid, stream);
+    const cudaError_t e = launch_slab(w8 ? OP_AR : op, dt == COC_BF16, w8, p, grid, stream);
     return e == cudaSuccess ? COC_OK : cuda_fail(e, "kernel launch (column slabs)");
 }
 
@@ -464,7 +494,8 @@ coc_status_t row_parallel(int op, int R, int64_t m, int64_t n, int64_t ks, const
     if (st != COC_OK) return st;
     if (allow_split) {
         const SlabPlan pl = slab_plan(op, R, m, n, ks, ds->sm_count);
-        if (pl.boxes > 0) return slab_row_parallel(op, R, m, n, ks, x, w, out, n_out, dt, pl, ds, stream, w_nk);
+        if (pl.boxes > 0)
+            return slab_row_parallel(op, R, m, n, ks, x, w, out, n_out, dt, pl, ds, stream, w_nk, scale, gran, group, zero);
     }
 
     const bool w8 = (op == OP_W8);
@@ -569,10 +600,14 @@ coc_status_t validate_row_parallel(int R, int64_t m, int64_t n, int64_t ks, cons
 // ("fused"), a streaming pre-pass that dequantises every weight element once
 // into the stream's workspace followed by the fp16 AllReduce kernel
 // ("prepass"), and one launch of the kernel that keeps the dequantised weight
-// in tensor memory ("ts", coc_w8_ts.cu).  Default: the fused kernel below
-// kW8PrepassMinRows rows, the pre-pass from there (it repeats no conversion
-// per row tile); COC_W8_PATH=fused|prepass|ts forces one (tests, tuning).
-enum class W8Path { TS, Fused, Prepass };
+// in tensor memory ("ts", coc_w8_ts.cu).  At m <= 128 the column-slab kernel
+// ("slab", coc_slab.cu) streams the int8 weight over all SMs with its own
+// dequant warps (the same bits unsplit; split over a cluster, the parts add
+// in part order).  Default: the slab kernel up to 128 rows where its plan fits
+// the shape, the fused kernel below kW8PrepassMinRows rows, the pre-pass from
+// there (it repeats no conversion per row tile); COC_W8_PATH=
+// fused|prepass|ts|slab forces one (tests, tuning).
+enum class W8Path { TS, Fused, Prepass, Slab };
 constexpr int64_t kW8PrepassMinRows = 2048;
 
 W8Path w8_path(int64_t m) {
@@ -580,7 +615,9 @@ W8Path w8_path(int64_t m) {
     if (e != nullptr && std::strcmp(e, "fused") == 0) return W8Path::Fused;
     if (e != nullptr && std::strcmp(e, "prepass") == 0) return W8Path::Prepass;
     if (e != nullptr && std::strcmp(e, "ts") == 0) return W8Path::TS;
-    return m >= kW8PrepassMinRows ? W8Path::Prepass : W8Path::Fused;
+    if (e != nullptr && std::strcmp(e, "slab") == 0) return W8Path::Slab;
+    if (m >= kW8PrepassMinRows) return W8Path::Prepass;
+    return m <= BM ? W8Path::Slab : W8Path::Fused;
 }
 
 coc_status_t device_pool(DeviceState* ds, cudaMemPool_t* out) {
@@ -835,8 +872,9 @@ COC_API coc_status_t coc_matmul_all_reduce_w8a16_ex(int R, int64_t m, int64_t n,
     if (k_shard > 0 && path == W8Path::Prepass)
         return w8_prepass_all_reduce(R, m, n, k_shard, x, w, scale, zero, gran, group_size, out, dt, chunks,
                                      reinterpret_cast<cudaStream_t>(stream));
+    // (the column-slab kernel where its plan fits the shape, else the fused kernel)
     return row_parallel(OP_W8, R, m, n, k_shard, x, w, out, R, dt, chunks, scale, gran, group_size,
-                        reinterpret_cast<cudaStream_t>(stream), false, zero);
+                        reinterpret_cast<cudaStream_t>(stream), false, zero, path == W8Path::Slab);
 }
 
 COC_API coc_status_t coc_matmul_all_reduce_w8a16(int R, int64_t m, int64_t n, int64_t k_shard, const void* const* x,

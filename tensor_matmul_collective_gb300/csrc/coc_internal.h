@@ -208,12 +208,17 @@ cudaError_t launch_split(int op, bool bf16, const KParams& p, int grid, int clus
 // (AllReduce) or the R rank outputs (ReduceScatter).  With slab_split > 1
 // the grid is slab_split x the slabs run at once, in clusters of
 // slab_split CTAs.
+// w8A16 (AllReduce, w8 true): the B maps are the int8 weights, boxed 64
+// slab_boxes x (slab_kps BK) without swizzle; scale / zero / gran / group as
+// for the persistent kernel; the kernel dequantises into kSlabW8BStages
+// 16-bit B stages.
 constexpr int kSlabMaxStages = 32;
-constexpr int kSlabSmemCap = 227 * 1024;                       // dynamic shared memory per CTA
-int slab_stages(int a_rows, int boxes, int kps, int split);    // most stages that fit (at least 2)
-int slab_smem_bytes(int stages, int a_rows, int boxes, int kps, int split);
-cudaError_t launch_slab(int op, bool bf16, const KParams& p, int grid, cudaStream_t stream);
-int slab_max_clusters(bool bf16, int split, int smem);         // clusters of `split` resident at once
+constexpr int kSlabW8BStages = 3;
+constexpr int kSlabSmemCap = 227 * 1024;                                // dynamic shared memory per CTA
+int slab_stages(int a_rows, int boxes, int kps, int split, bool w8);    // most stages that fit (at least 2)
+int slab_smem_bytes(int stages, int a_rows, int boxes, int kps, int split, bool w8);
+cudaError_t launch_slab(int op, bool bf16, bool w8, const KParams& p, int grid, cudaStream_t stream);
+int slab_max_clusters(bool bf16, bool w8, int split, int smem);         // clusters of `split` resident at once
 int max_split_clusters(int op, bool bf16, int cluster);
 // Co-resident CTA pairs the 2-SM variant can have on the current device.
 int max_pairs(int op, bool bf16);

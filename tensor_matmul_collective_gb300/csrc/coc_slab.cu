@@ -51,19 +51,23 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "coc_dequant.cuh"
 #include "coc_internal.h"
 #include "coc_ptx.cuh"
 
 namespace coc {
 namespace {
 
-constexpr int SLAB_THREADS = 192;
+constexpr int SLAB_DQ_WARPS = 8;                  // w8A16: dequantisation warps
+// warps: producer, MMA, 4 epilogue; w8A16 adds the dequant warps and one X loader
+__host__ __device__ constexpr int slab_threads(bool w8) { return (6 + (w8 ? SLAB_DQ_WARPS + 1 : 0)) * 32; }
+constexpr int SLAB_XLOAD_WARP = 6 + SLAB_DQ_WARPS;   // w8A16: loads X into the A and B ring
 constexpr uint32_t kSlabBoxBytes = 64 * BK * 2;   // one 64 x 64 16-bit box
 constexpr uint32_t kSlabStageBar = 3;             // named barrier of the set-up phase
 static_assert(kSlabMaxStages <= 32, "the producer's fill masks hold one bit per stage");
 
-__host__ __device__ constexpr uint32_t slab_bar_bytes(int stages) {
-    return static_cast<uint32_t>(8 * (2 * stages + 7) + 16);
+__host__ __device__ constexpr uint32_t slab_bar_bytes(int stages, bool w8) {
+    return static_cast<uint32_t>(8 * (2 * stages + (w8 ? 3 * kSlabW8BStages : 0) + 7) + 16);
 }
 // Reception area of a slab split over `split` CTAs: per other part, per row
 // quadrant holding output rows (a_rows / 32 rounded up), 32 rows of the (64
@@ -72,8 +76,39 @@ __host__ __device__ constexpr uint32_t slab_recv_bytes(int boxes, int split, int
     return split > 1 ? static_cast<uint32_t>((split - 1) * ((a_rows + 31) / 32) * 32 * (64 * boxes / split) * 4) : 0u;
 }
 
-template <int OP, bool BF16>
-__global__ void __launch_bounds__(SLAB_THREADS, 1) coc_slab_kernel(const __grid_constant__ KParams p) {
+template <int V>
+struct IntC {
+    static constexpr int value = V;
+};
+
+// w8A16: one dequant thread's share of a stage of NB 64-column groups x KPS
+// k-blocks: chunk cc (8 columns) of rows kr0, kr0 + R_STEP, ... of every
+// k-block, from the int8 stage `raw` (rows of 64 NB bytes) into the 16-bit B
+// stage (NB groups of KPS k-blocks x 64 rows x 128 bytes, 16-byte chunks
+// XOR-ed with row % 8).  All loads are issued before the first conversion.
+template <bool BF16, int NB, int KPS>
+__device__ __forceinline__ void dequant_stage(const uint8_t* raw, uint8_t* bst, int kr0, int cc, int c16, Dq<BF16>& dq,
+                                              const W8Layout& w8l, const uint16_t* sc, const int8_t* zp, int kb, int j0,
+                                              bool per_group) {
+    constexpr int W = 64 * NB;
+    constexpr int R_STEP = (SLAB_DQ_WARPS * 32) / (W / 8);
+    constexpr int RPK = BK / R_STEP;   // rows per k-block
+    constexpr int ROWS = KPS * RPK;
+    uint2 q8[ROWS];
+#pragma unroll
+    for (int i = 0; i < ROWS; ++i)
+        q8[i] = *reinterpret_cast<const uint2*>(raw + ((i / RPK) * BK + kr0 + (i % RPK) * R_STEP) * W + cc * 8);
+#pragma unroll
+    for (int i = 0; i < ROWS; ++i) {
+        if (per_group && i % RPK == 0) dq.load(w8l, sc, zp, (kb + i / RPK) * BK, j0);
+        const int kk = (i / RPK) * BK + kr0 + (i % RPK) * R_STEP;   // row of the stage
+        *reinterpret_cast<uint4*>(bst + kk * 128 + ((c16 ^ (kk & 7)) << 4)) = dq.convert(q8[i]);
+    }
+}
+
+template <int OP, bool BF16, bool W8>
+__global__ void __launch_bounds__(slab_threads(W8), 1) coc_slab_kernel(const __grid_constant__ KParams p) {
+    constexpr int THREADS = slab_threads(W8);
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5;
@@ -96,14 +131,26 @@ __global__ void __launch_bounds__(SLAB_THREADS, 1) coc_slab_kernel(const __grid_
     const uint32_t b_stage = static_cast<uint32_t>(nb) * b_group;
     const int W = nb * 64;                // slab width
     const int ow = W / csplit;            // columns this CTA finalises (split: its share of the slab)
+    const uint32_t raw_stage = W8 ? static_cast<uint32_t>(kps * 64 * W) : 0u;   // w8A16: int8 W of a stage
+    // w8A16: the producer's ring carries only the int8 W (freed by the dequant
+    // warps, so it runs as far ahead as it is deep); X and the 16-bit W share
+    // a second ring of SB stages (X loaded by the dequant warps, freed by the MMA)
+    constexpr int SB = W8 ? kSlabW8BStages : 0;
+    const int SAB = W8 ? SB : S;                               // stages of the A and B rings
 
-    uint8_t* a_st = smem;                          // S x a_stage
-    uint8_t* b_st = a_st + S * a_stage;            // S x b_stage
-    uint8_t* stg = b_st + S * b_stage;             // 4 epilogue warps x 4 KiB
+    // A ring first: the MMA reads 128 rows from a k-block's start, past the
+    // last A stage into the B ring (>= 16 KiB), never past the allocation
+    uint8_t* a_st = smem;                                      // SAB x a_stage
+    uint8_t* b_st = a_st + SAB * a_stage;                      // SAB x b_stage
+    uint8_t* raw_st = b_st + SAB * b_stage;                    // w8A16: S x raw_stage
+    uint8_t* stg = raw_st + S * raw_stage;                     // 4 epilogue warps x 4 KiB
     uint8_t* recv = stg + NUM_EPI_WARPS * EPI_BUF_BYTES;   // split: the other parts' sums of this CTA's columns
     uint64_t* full = reinterpret_cast<uint64_t*>(recv + slab_recv_bytes(nb, csplit, a_rows));   // [S]
-    uint64_t* empty = full + S;                    // [S]
-    uint64_t* accf = empty + S;                    // [2] accumulator ready for the epilogue
+    uint64_t* empty = full + S;                    // [S]  (w8A16: int8 stage read by every dequant warp)
+    uint64_t* bfull = empty + S;                   // [SB] w8A16: 16-bit B stage written (every dequant warp)
+    uint64_t* bempty = bfull + SB;                 // [SB] w8A16: A and B stage consumed by the MMA
+    uint64_t* afull = bempty + SB;                 // [SB] w8A16: X of the stage landed
+    uint64_t* accf = afull + SB;                   // [2] accumulator ready for the epilogue
     uint64_t* acce = accf + 2;                     // [2] accumulator drained (4 epilogue warps)
     uint64_t* never = acce + 2;                    // [1] nothing arrives here (fault-injection test)
     uint64_t* drain = never + 1;                   // [1] MMA drain before TMEM release
@@ -120,7 +167,12 @@ __global__ void __launch_bounds__(SLAB_THREADS, 1) coc_slab_kernel(const __grid_
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
-            mbar_init(smem_u32(&empty[s]), 1);
+            mbar_init(smem_u32(&empty[s]), W8 ? SLAB_DQ_WARPS : 1);
+        }
+        for (int b = 0; b < SB; ++b) {
+            mbar_init(smem_u32(&bfull[b]), SLAB_DQ_WARPS);
+            mbar_init(smem_u32(&bempty[b]), 1);
+            mbar_init(smem_u32(&afull[b]), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&accf[b]), 1);
@@ -147,9 +199,9 @@ __global__ void __launch_bounds__(SLAB_THREADS, 1) coc_slab_kernel(const __grid_
         cluster_arrive();
         if (warp != 0) cluster_wait();
     } else if (warp == 0) {
-        named_arrive(kSlabStageBar, SLAB_THREADS);
+        named_arrive(kSlabStageBar, THREADS);
     } else {
-        named_sync(kSlabStageBar, SLAB_THREADS);
+        named_sync(kSlabStageBar, THREADS);
     }
     tc_fence_after();
     const uint32_t tmem_base = warp == 0 ? 0u : *tmem_slot;
@@ -190,15 +242,21 @@ __global__ void __launch_bounds__(SLAB_THREADS, 1) coc_slab_kernel(const __grid_
                     const CUtensorMap* am = &p.tm_a[ks];
                     const CUtensorMap* bm = &p.tm_b[ks];
                     const uint32_t fb = smem_u32(&full[stage]);
-                    mbar_expect_tx(fb, a_stage + b_stage);
-                    const uint32_t adst = smem_u32(a_st + stage * a_stage);
-                    if (a3d) {
-                        tma_load_3d_hint(adst, am, 0, 0, kb, fb, pol_a);
-                    } else {
-                        for (int t = 0; t < kps; ++t) tma_load_2d_hint(adst + t * a_kb, am, (kb + t) * BK, 0, fb, pol_a);
+                    mbar_expect_tx(fb, W8 ? raw_stage : a_stage + b_stage);
+                    if constexpr (!W8) {
+                        const uint32_t adst = smem_u32(a_st + stage * a_stage);
+                        if (a3d) {
+                            tma_load_3d_hint(adst, am, 0, 0, kb, fb, pol_a);
+                        } else {
+                            for (int t = 0; t < kps; ++t)
+                                tma_load_2d_hint(adst + t * a_kb, am, (kb + t) * BK, 0, fb, pol_a);
+                        }
                     }
                     const uint32_t bdst = smem_u32(b_st + stage * b_stage);
-                    if (b_kmajor) {
+                    if constexpr (W8) {
+                        // the int8 W of the stage: W columns x kps k-blocks, one box
+                        tma_load_2d_hint(smem_u32(raw_st + stage * raw_stage), bm, col0, kb * BK, fb, pol_b);
+                    } else if (b_kmajor) {
                         if (a3d) {
                             tma_load_3d_hint(bdst, bm, 0, col0, kb, fb, pol_b);
                         } else {
@@ -232,7 +290,7 @@ __global__ void __launch_bounds__(SLAB_THREADS, 1) coc_slab_kernel(const __grid_
         const uint32_t b_lbo = b_kmajor ? 16u : b_group;
         const uint64_t b_step = b_kmajor ? 2u : 128u;
         const uint32_t b_kb = b_kmajor ? static_cast<uint32_t>(W) * 128u : kSlabBoxBytes;
-        uint32_t stage = 0, phase = 0;
+        uint32_t stage = 0, phase = 0, bstage = 0, bphase = 0;
         int acc_i = 0;
         bool ok = true;
         for (int u = first_u; ok && u < units; u += u_step) {
@@ -242,23 +300,31 @@ __global__ void __launch_bounds__(SLAB_THREADS, 1) coc_slab_kernel(const __grid_
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * W);
             for (int i = 0; i < st_hi - st_lo; ++i) {
-                ok = warp_wait(smem_u32(&full[stage]), phase, ctl, 0x540u + stage);
+                if constexpr (W8) {
+                    ok = warp_wait(smem_u32(&afull[bstage]), bphase, ctl, 0x590u + bstage);
+                    if (ok) ok = warp_wait(smem_u32(&bfull[bstage]), bphase, ctl, 0x598u + bstage);
+                } else {
+                    ok = warp_wait(smem_u32(&full[stage]), phase, ctl, 0x540u + stage);
+                }
                 if (!ok) break;
                 tc_fence_after();
                 if (lane == 0) {
+                    const uint32_t bs = W8 ? bstage : stage;   // stage of the A and B rings
                     for (int t = 0; t < kps; ++t) {
-                        const uint64_t ad = make_sdesc(smem_u32(a_st + stage * a_stage + t * a_kb), 16u, 1024u);
-                        const uint64_t bd = make_sdesc(smem_u32(b_st + stage * b_stage + t * b_kb), b_lbo, 1024u);
+                        const uint64_t ad = make_sdesc(smem_u32(a_st + bs * a_stage + t * a_kb), 16u, 1024u);
+                        const uint64_t bd = make_sdesc(smem_u32(b_st + bs * b_stage + t * b_kb), b_lbo, 1024u);
 #pragma unroll
                         for (int kk = 0; kk < BK / UMMA_K; ++kk)
                             tc_mma_f16(d_tmem, ad + static_cast<uint64_t>(kk) * 2u,
                                        bd + static_cast<uint64_t>(kk) * b_step, idesc,
                                        (i > 0 || t > 0 || kk > 0) ? 1u : 0u);
                     }
-                    tc_commit(smem_u32(&empty[stage]));
+                    if (W8) tc_commit(smem_u32(&bempty[bstage]));
+                    else tc_commit(smem_u32(&empty[stage]));
                 }
                 __syncwarp();
-                if (++stage == static_cast<uint32_t>(S)) { stage = 0; phase ^= 1u; }
+                if (!W8 && ++stage == static_cast<uint32_t>(S)) { stage = 0; phase ^= 1u; }
+                if (W8 && ++bstage == static_cast<uint32_t>(SB)) { bstage = 0; bphase ^= 1u; }
             }
             if (!ok) break;
             if (lane == 0) tc_commit(smem_u32(&accf[buf]));
@@ -271,7 +337,7 @@ __global__ void __launch_bounds__(SLAB_THREADS, 1) coc_slab_kernel(const __grid_
             drain_wait(smem_u32(drain), 0, kDrainNs);
         }
         __syncwarp();
-    } else {
+    } else if (warp < 2 + NUM_EPI_WARPS) {
         // ================================================= epilogue ===
         const int q = warp & 3;                  // TMEM lane quadrant this warp may read
         const int row0 = 32 * q;
@@ -418,6 +484,110 @@ __global__ void __launch_bounds__(SLAB_THREADS, 1) coc_slab_kernel(const __grid_
         }
     }
 
+    if constexpr (W8) {
+        if (warp >= 2 + NUM_EPI_WARPS && warp < SLAB_XLOAD_WARP) {
+            // ================================================= w8A16 dequant ===
+            // Per stage: once the MMA has freed the A and B stage (bempty) and the
+            // int8 stage has landed (full), thread tt, which owns 8 consecutive
+            // columns (chunk cc) of the slab and the stage rows kr0, kr0 + r_step, ..., reads
+            // their int8 bytes, dequantises them (coc_dequant.cuh, the fused
+            // kernel's and the pre-pass's conversion) and writes the 16-bit B
+            // stage in the MMA's MN-major 128-byte-swizzled layout.  Every warp
+            // then arrives on the B stage's `bfull` and the int8 stage's `empty`.
+            const int tt = (warp - 2 - NUM_EPI_WARPS) * 32 + lane;
+            const int chunks = W / 8;
+            const int cc = tt % chunks;
+            const int kr0 = tt / chunks;
+            const int r_step = (SLAB_DQ_WARPS * 32) / chunks;
+            const W8Layout w8l{p.gran, p.group, p.n};
+            uint32_t stage = 0, phase = 0, bstage = 0, bphase = 0;
+            bool ok = true;
+            for (int u = first_u; ok && u < units; u += u_step) {
+                const int j0 = u * W + cc * 8;   // this thread's first output column
+                int dq_ks = -1;
+                Dq<BF16> dq;
+                for (int s = st_lo; s < st_hi; ++s) {
+                    const int ks = s / spk;
+                    const int kb = (s - ks * spk) * kps;
+                    const uint16_t* sc = p.scale[ks];
+                    const int8_t* zp = p.has_zero ? p.zero[ks] : nullptr;
+                    if (ks != dq_ks && p.gran != COC_SCALE_GROUP) dq.load(w8l, sc, zp, 0, j0);   // once per shard
+                    dq_ks = ks;
+                    ok = warp_wait(smem_u32(&bempty[bstage]), bphase ^ 1u, ctl, 0x5C0u + bstage);
+                    if (ok) ok = warp_wait(smem_u32(&full[stage]), phase, ctl, 0x5A0u + stage);
+                    if (!ok) break;
+                    const uint8_t* raw = raw_st + stage * raw_stage;
+                    uint8_t* bst = b_st + bstage * b_stage + (cc >> 3) * b_group;
+                    const int c16 = cc & 7;
+                    // this thread's rows of the stage, all loads first, then convert
+                    // and store (slab width and stage depth fixed at compile time)
+                    auto run = [&](auto nb_c, auto kps_c) {
+                        dequant_stage<BF16, decltype(nb_c)::value, decltype(kps_c)::value>(
+                            raw, bst, kr0, cc, c16, dq, w8l, sc, zp, kb, j0, p.gran == COC_SCALE_GROUP);
+                    };
+                    if (nb == 2) {
+                        if (kps == 4) run(IntC<2>{}, IntC<4>{});
+                        else if (kps == 2) run(IntC<2>{}, IntC<2>{});
+                        else run(IntC<2>{}, IntC<1>{});
+                    } else {
+                        if (kps == 4) run(IntC<1>{}, IntC<4>{});
+                        else if (kps == 2) run(IntC<1>{}, IntC<2>{});
+                        else run(IntC<1>{}, IntC<1>{});
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(smem_u32(&bfull[bstage]));
+                        mbar_arrive(smem_u32(&empty[stage]));
+                    }
+                    if (++stage == static_cast<uint32_t>(S)) { stage = 0; phase ^= 1u; }
+                    if (++bstage == static_cast<uint32_t>(SB)) { bstage = 0; bphase ^= 1u; }
+                }
+            }
+        }
+    }
+    if constexpr (W8) {
+        if (warp == SLAB_XLOAD_WARP) {
+            // ================================================= w8A16 X loads ===
+            // once the MMA has freed an A and B stage (bempty), X of the stage it
+            // will hold next into its A part (afull); the int8 stream never waits
+            // behind these loads
+            const bool a3d = p.slab_a3d != 0;
+            const uint64_t pol_a = make_l2_policy(2);   // X: reused by every slab
+            uint32_t bstage = 0, bphase = 0, a_filled = 0, a_parity = 0;
+            bool ok = true;
+            for (int u = first_u; ok && u < units; u += u_step) {
+                for (int s = st_lo; s < st_hi; ++s) {
+                    const int ks = s / spk;
+                    const int kb = (s - ks * spk) * kps;
+                    ok = warp_wait(smem_u32(&bempty[bstage]), bphase ^ 1u, ctl, 0x5E0u + bstage);
+                    if (!ok) break;
+                    if (lane == 0) {
+                        const CUtensorMap* am = &p.tm_a[ks];
+                        const uint32_t ab = smem_u32(&afull[bstage]);
+                        const uint32_t adst = smem_u32(a_st + bstage * a_stage);
+                        mbar_expect_tx(ab, a_stage);
+                        if (a3d) {
+                            tma_load_3d_hint(adst, am, 0, 0, kb, ab, pol_a);
+                        } else {
+                            for (int t = 0; t < kps; ++t)
+                                tma_load_2d_hint(adst + t * a_kb, am, (kb + t) * BK, 0, ab, pol_a);
+                        }
+                        a_filled |= 1u << bstage;
+                        a_parity = (a_parity & ~(1u << bstage)) | (bphase << bstage);
+                    }
+                    __syncwarp();
+                    if (++bstage == static_cast<uint32_t>(SB)) { bstage = 0; bphase ^= 1u; }
+                }
+            }
+            if (!ok && lane == 0) {
+                // leave no X load in flight into shared memory
+                for (int b = 0; b < SB; ++b)
+                    if (a_filled & (1u << b)) drain_wait(smem_u32(&afull[b]), (a_parity >> b) & 1u, kDrainNs);
+            }
+        }
+    }
+
     if (csplit > 1) {
         // no CTA leaves while a part may still push into its shared memory
         if (warp == 0) cluster_wait();   // the set-up phase this warp only arrived at
@@ -440,9 +610,9 @@ __global__ void __launch_bounds__(SLAB_THREADS, 1) coc_slab_kernel(const __grid_
 
 constexpr int kMaxDevices = 64;
 
-template <int OP, bool BF16>
+template <int OP, bool BF16, bool W8>
 cudaError_t launch_slab_t(const KParams& p, int grid, cudaStream_t stream) {
-    auto kern = coc_slab_kernel<OP, BF16>;
+    auto kern = coc_slab_kernel<OP, BF16, W8>;
     static std::atomic<unsigned char> smem_set[kMaxDevices];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -455,8 +625,8 @@ cudaError_t launch_slab_t(const KParams& p, int grid, cudaStream_t stream) {
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
-    cfg.blockDim = dim3(SLAB_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = slab_smem_bytes(p.slab_stages, p.a_box_rows, p.slab_boxes, p.slab_kps, p.slab_split);
+    cfg.blockDim = dim3(slab_threads(W8), 1, 1);
+    cfg.dynamicSmemBytes = slab_smem_bytes(p.slab_stages, p.a_box_rows, p.slab_boxes, p.slab_kps, p.slab_split, W8);
     cfg.stream = stream;
     if (p.slab_split > 1) {
         attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -469,9 +639,9 @@ cudaError_t launch_slab_t(const KParams& p, int grid, cudaStream_t stream) {
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-template <int OP, bool BF16>
+template <int OP, bool BF16, bool W8>
 int slab_max_clusters_t(int split, int smem) {
-    auto kern = coc_slab_kernel<OP, BF16>;
+    auto kern = coc_slab_kernel<OP, BF16, W8>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSlabSmemCap) != cudaSuccess) return 0;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -480,7 +650,7 @@ int slab_max_clusters_t(int split, int smem) {
     attr[0].val.clusterDim.z = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(split, 1, 1);
-    cfg.blockDim = dim3(SLAB_THREADS, 1, 1);
+    cfg.blockDim = dim3(slab_threads(W8), 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
@@ -491,29 +661,41 @@ int slab_max_clusters_t(int split, int smem) {
 
 }  // namespace
 
-int slab_stages(int a_rows, int boxes, int kps, int split) {
+int slab_stages(int a_rows, int boxes, int kps, int split, bool w8) {
     int s = kSlabMaxStages;
-    while (s > 2 && slab_smem_bytes(s, a_rows, boxes, kps, split) > kSlabSmemCap) --s;
+    while (s > 2 && slab_smem_bytes(s, a_rows, boxes, kps, split, w8) > kSlabSmemCap) --s;
     return s;
 }
 
-int slab_smem_bytes(int stages, int a_rows, int boxes, int kps, int split) {
-    return 1024 + stages * kps * (a_rows * 128 + boxes * static_cast<int>(kSlabBoxBytes)) +
+int slab_smem_bytes(int stages, int a_rows, int boxes, int kps, int split, bool w8) {
+    const int b_stage = boxes * kps * static_cast<int>(kSlabBoxBytes);   // 16-bit B of a stage
+    const int raw_stage = kps * 64 * 64 * boxes;                          // w8A16: int8 W of a stage
+    const int a_stage = kps * a_rows * 128;
+    return 1024 + (w8 ? stages * raw_stage + kSlabW8BStages * (a_stage + b_stage) : stages * (a_stage + b_stage)) +
            NUM_EPI_WARPS * EPI_BUF_BYTES + static_cast<int>(slab_recv_bytes(boxes, split, a_rows)) +
-           static_cast<int>(slab_bar_bytes(stages));
+           static_cast<int>(slab_bar_bytes(stages, w8));
 }
 
-cudaError_t launch_slab(int op, bool bf16, const KParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch_slab(int op, bool bf16, bool w8, const KParams& p, int grid, cudaStream_t stream) {
+    if (w8) {
+        if (op != OP_AR) return cudaErrorInvalidValue;
+        return bf16 ? launch_slab_t<OP_AR, true, true>(p, grid, stream) : launch_slab_t<OP_AR, false, true>(p, grid, stream);
+    }
     switch (op) {
-        case OP_AR: return bf16 ? launch_slab_t<OP_AR, true>(p, grid, stream) : launch_slab_t<OP_AR, false>(p, grid, stream);
-        case OP_RS: return bf16 ? launch_slab_t<OP_RS, true>(p, grid, stream) : launch_slab_t<OP_RS, false>(p, grid, stream);
+        case OP_AR:
+            return bf16 ? launch_slab_t<OP_AR, true, false>(p, grid, stream)
+                        : launch_slab_t<OP_AR, false, false>(p, grid, stream);
+        case OP_RS:
+            return bf16 ? launch_slab_t<OP_RS, true, false>(p, grid, stream)
+                        : launch_slab_t<OP_RS, false, false>(p, grid, stream);
         default: return cudaErrorInvalidValue;
     }
 }
 
-int slab_max_clusters(bool bf16, int split, int smem) {
+int slab_max_clusters(bool bf16, bool w8, int split, int smem) {
     // the kernel's resources do not depend on the operator; ask one instance
-    return bf16 ? slab_max_clusters_t<OP_AR, true>(split, smem) : slab_max_clusters_t<OP_AR, false>(split, smem);
+    if (w8) return bf16 ? slab_max_clusters_t<OP_AR, true, true>(split, smem) : slab_max_clusters_t<OP_AR, false, true>(split, smem);
+    return bf16 ? slab_max_clusters_t<OP_AR, true, false>(split, smem) : slab_max_clusters_t<OP_AR, false, false>(split, smem);
 }
 
 }  // namespace coc
