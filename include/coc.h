@@ -50,9 +50,10 @@
  * build, across runs and across chunk counts: each output element is
  * accumulated in fp32 in the fixed order rank 0..R-1, k ascending, and
  * rounded once (round-to-nearest-even) to the output type.  No call combines
- * partial sums with atomics or in arrival order; the one split of the
- * contraction, the rank split of decode-sized AllReduce / ReduceScatter
- * (below), depends on the shape only and adds its parts in a fixed order.
+ * partial sums with atomics or in arrival order; the splits of the
+ * contraction at decode-sized m (the column-slab split and the rank split,
+ * below) depend on the shape and the GPU only and add their parts in a
+ * fixed order.
  * There is no faster non-deterministic schedule, so `deterministic` is
  * accepted and has no effect: deterministic = 0 gives the same bits.
  *
@@ -97,10 +98,15 @@
  *     captured into CUDA graphs.
  *   - Environment variables that force a schedule (tuning and tests only;
  *     every value gives correct results): COC_PAIR=0|1 (single-CTA or 2-SM
- *     tiles), COC_W8_PATH=fused|prepass (w8A16 dequantisation inside the
- *     GEMM kernel or in a pre-pass), COC_KSPLIT=<n> (rank-split part count,
- *     rounded down to a power of two dividing R).  Forcing one can change
- *     the last bit of results (a different summation grouping).
+ *     tiles), COC_W8_PATH=fused|prepass|ts|slab (w8A16 dequantisation in the
+ *     GEMM kernel's shared memory, in a pre-pass, in tensor memory, or the
+ *     column-slab kernel), COC_KSPLIT=<n> (rank-split part count, rounded
+ *     down to a power of two dividing R), COC_SPLIT_PATH=scratch (rank split
+ *     through global memory), COC_SLAB=0|1 (column-slab kernel off / for
+ *     every m <= 128) with COC_SLAB_BOXES=1|2, COC_SLAB_SPLIT=1|2|4 and
+ *     COC_SLAB_KPS=1|2|4 (its slab width in 64-column groups, CTAs per
+ *     slab, k-blocks per stage).  Forcing one can change the last bit of
+ *     results (a different summation grouping).
  */
 #ifndef COC_H_
 #define COC_H_
@@ -167,9 +173,17 @@ typedef struct CUstream_st* coc_stream_t;
  * aligned.  m, n, k_shard in [0, 2^31); m == 0 or n == 0 is a no-op and
  * k_shard == 0 writes zeros.
  *
- * Rank split (this call, coc_matmul_reduce_scatter, coc_matmul and
- * coc_fused_matmul's AllReduce / ReduceScatter): for m <= 128 (decode-sized
- * m) with at most half as many 128 x 256 output tiles as the GPU has SMs,
+ * Decode-sized m (this call, coc_matmul_reduce_scatter, coc_matmul,
+ * coc_fused_matmul's AllReduce / ReduceScatter, and the w8A16 AllReduce):
+ * for m <= 128 a column-slab kernel streams the weights over all SMs in
+ * slabs of 128 output columns (all m rows), each summed over the whole
+ * contraction by one CTA (the same bits as one accumulator) or, while the
+ * slabs fill at most half of the SMs, by a cluster of 2 or 4 CTAs that each
+ * sum a fixed contiguous range of it and add the ranges in order.  Shapes
+ * with too few slabs to fill half of the SMs take the rank split instead.
+ *
+ * Rank split (the same operators except w8A16): for m <= 128 with at most
+ * half as many 128 x 256 output tiles as the GPU has SMs,
  * each tile's R shards are cut into ksplit parts (the largest power of two
  * dividing R that keeps tiles x ksplit within one wave), each a work unit of
  * its own, and the parts' fp32 sums are added in part order 0..ksplit-1
