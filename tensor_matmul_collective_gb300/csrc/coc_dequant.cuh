@@ -89,6 +89,10 @@ struct Dq<false> {
         load_w8_scale_words(L, sc, row, j0, w);
         int z[8];
         load_w8_zeros(L, zp, row, j0, z);
+        set(w, z);
+    }
+    // from the 8 scales (four words of two) and the 8 zero points
+    __device__ __forceinline__ void set(const uint32_t (&w)[4], const int (&z)[8]) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             s[e] = *reinterpret_cast<const __half2*>(&w[e]);
@@ -120,6 +124,10 @@ struct Dq<true> {
         load_w8_scale_words(L, sc, row, j0, w);
         int z[8];
         load_w8_zeros(L, zp, row, j0, z);
+        set(w, z);
+    }
+    // from the 8 scales (four words of two) and the 8 zero points
+    __device__ __forceinline__ void set(const uint32_t (&w)[4], const int (&z)[8]) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             s[2 * e] = __uint_as_float(w[e] << 16);

@@ -76,6 +76,13 @@ __host__ __device__ constexpr uint32_t slab_recv_bytes(int boxes, int split, int
     return split > 1 ? static_cast<uint32_t>((split - 1) * ((a_rows + 31) / 32) * 32 * (64 * boxes / split) * 4) : 0u;
 }
 
+// w8A16: bytes of one int8 stage: the weight (kps k-blocks x 64 rows x 64
+// boxes columns) and its scale / zero-point table rows (kps rows of 64 boxes
+// 16-bit scales, then kps rows of int8 zero points), rounded to 1 KiB.
+__host__ __device__ constexpr int slab_raw_stage(int kps, int boxes) {
+    return (kps * 64 * 64 * boxes + kps * 64 * boxes * 3 + 1023) / 1024 * 1024;
+}
+
 template <int V>
 struct IntC {
     static constexpr int value = V;
@@ -86,10 +93,31 @@ struct IntC {
 // k-block, from the int8 stage `raw` (rows of 64 NB bytes) into the 16-bit B
 // stage (NB groups of KPS k-blocks x 64 rows x 128 bytes, 16-byte chunks
 // XOR-ed with row % 8).  All loads are issued before the first conversion.
+// The scale and zero points of this thread's 8 columns from table slot
+// `tab` of the stage (16-bit scales at tab, int8 zero points at ztab; zero
+// points 0 when there are none, scales 0 past n, as for the global tables).
+template <bool BF16>
+__device__ __forceinline__ void dq_from_slot(Dq<BF16>& dq, const uint8_t* tab, const uint8_t* ztab, int cc, bool valid) {
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+    int z[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    if (valid) {
+        const uint4 s4 = *reinterpret_cast<const uint4*>(tab + cc * 16);
+        w[0] = s4.x; w[1] = s4.y; w[2] = s4.z; w[3] = s4.w;
+        if (ztab != nullptr) {
+            const uint2 z8 = *reinterpret_cast<const uint2*>(ztab + cc * 8);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                z[e] = static_cast<int8_t>((z8.x >> (8 * e)) & 0xFFu);
+                z[4 + e] = static_cast<int8_t>((z8.y >> (8 * e)) & 0xFFu);
+            }
+        }
+    }
+    dq.set(w, z);
+}
+
 template <bool BF16, int NB, int KPS>
 __device__ __forceinline__ void dequant_stage(const uint8_t* raw, uint8_t* bst, int kr0, int cc, int c16, Dq<BF16>& dq,
-                                              const W8Layout& w8l, const uint16_t* sc, const int8_t* zp, int kb, int j0,
-                                              bool per_group) {
+                                              const uint8_t* tab, const uint8_t* ztab, bool valid, bool per_group) {
     constexpr int W = 64 * NB;
     constexpr int R_STEP = (SLAB_DQ_WARPS * 32) / (W / 8);
     constexpr int RPK = BK / R_STEP;   // rows per k-block
@@ -100,7 +128,8 @@ __device__ __forceinline__ void dequant_stage(const uint8_t* raw, uint8_t* bst, 
         q8[i] = *reinterpret_cast<const uint2*>(raw + ((i / RPK) * BK + kr0 + (i % RPK) * R_STEP) * W + cc * 8);
 #pragma unroll
     for (int i = 0; i < ROWS; ++i) {
-        if (per_group && i % RPK == 0) dq.load(w8l, sc, zp, (kb + i / RPK) * BK, j0);
+        if (per_group && i % RPK == 0)
+            dq_from_slot<BF16>(dq, tab + (i / RPK) * W * 2, ztab != nullptr ? ztab + (i / RPK) * W : nullptr, cc, valid);
         const int kk = (i / RPK) * BK + kr0 + (i % RPK) * R_STEP;   // row of the stage
         *reinterpret_cast<uint4*>(bst + kk * 128 + ((c16 ^ (kk & 7)) << 4)) = dq.convert(q8[i]);
     }
@@ -131,7 +160,7 @@ __global__ void __launch_bounds__(slab_threads(W8), 1) coc_slab_kernel(const __g
     const uint32_t b_stage = static_cast<uint32_t>(nb) * b_group;
     const int W = nb * 64;                // slab width
     const int ow = W / csplit;            // columns this CTA finalises (split: its share of the slab)
-    const uint32_t raw_stage = W8 ? static_cast<uint32_t>(kps * 64 * W) : 0u;   // w8A16: int8 W of a stage
+    const uint32_t raw_stage = W8 ? static_cast<uint32_t>(slab_raw_stage(kps, nb)) : 0u;   // w8A16: int8 stage
     // w8A16: the producer's ring carries only the int8 W (freed by the dequant
     // warps, so it runs as far ahead as it is deep); X and the 16-bit W share
     // a second ring of SB stages (X loaded by the dequant warps, freed by the MMA)
@@ -242,7 +271,16 @@ __global__ void __launch_bounds__(slab_threads(W8), 1) coc_slab_kernel(const __g
                     const CUtensorMap* am = &p.tm_a[ks];
                     const CUtensorMap* bm = &p.tm_b[ks];
                     const uint32_t fb = smem_u32(&full[stage]);
-                    mbar_expect_tx(fb, W8 ? raw_stage : a_stage + b_stage);
+                    // w8A16 per-group: the int8 box plus the in-range columns of the
+                    // scale and zero-point rows of the stage's k-blocks (measured:
+                    // per-group 50.9 -> 42.8 us at m 16; the per-tensor and
+                    // per-channel constants change only per shard and come from
+                    // global memory there, which measured faster than an extra
+                    // copy per stage or per shard)
+                    const int tab_cols = W8 ? min(W, n - col0) : 0;
+                    const int tab_rows = (W8 && p.gran == COC_SCALE_GROUP) ? kps : 0;
+                    const uint32_t tab_bytes = static_cast<uint32_t>(tab_rows * tab_cols * (p.has_zero ? 3 : 2));
+                    mbar_expect_tx(fb, W8 ? static_cast<uint32_t>(kps * 64 * W) + tab_bytes : a_stage + b_stage);
                     if constexpr (!W8) {
                         const uint32_t adst = smem_u32(a_st + stage * a_stage);
                         if (a3d) {
@@ -255,7 +293,18 @@ __global__ void __launch_bounds__(slab_threads(W8), 1) coc_slab_kernel(const __g
                     const uint32_t bdst = smem_u32(b_st + stage * b_stage);
                     if constexpr (W8) {
                         // the int8 W of the stage: W columns x kps k-blocks, one box
-                        tma_load_2d_hint(smem_u32(raw_st + stage * raw_stage), bm, col0, kb * BK, fb, pol_b);
+                        uint8_t* rs = raw_st + stage * raw_stage;
+                        tma_load_2d_hint(smem_u32(rs), bm, col0, kb * BK, fb, pol_b);
+                        uint8_t* tab = rs + kps * 64 * W;   // scale rows, then zero-point rows
+                        for (int t = 0; t < tab_rows; ++t) {
+                            const long long row =
+                                (p.gran == COC_SCALE_GROUP) ? static_cast<long long>((kb + t) * BK / p.group) * n : 0LL;
+                            bulk_load_g2s(smem_u32(tab + t * W * 2), p.scale[ks] + row + col0,
+                                          static_cast<uint32_t>(tab_cols * 2), fb);
+                            if (p.has_zero)
+                                bulk_load_g2s(smem_u32(tab + kps * W * 2 + t * W), p.zero[ks] + row + col0,
+                                              static_cast<uint32_t>(tab_cols), fb);
+                        }
                     } else if (b_kmajor) {
                         if (a3d) {
                             tma_load_3d_hint(bdst, bm, 0, col0, kb, fb, pol_b);
@@ -506,24 +555,26 @@ __global__ void __launch_bounds__(slab_threads(W8), 1) coc_slab_kernel(const __g
                 const int j0 = u * W + cc * 8;   // this thread's first output column
                 int dq_ks = -1;
                 Dq<BF16> dq;
+                const bool valid = j0 + 8 <= n;   // this thread's columns lie inside the output
                 for (int s = st_lo; s < st_hi; ++s) {
                     const int ks = s / spk;
-                    const int kb = (s - ks * spk) * kps;
-                    const uint16_t* sc = p.scale[ks];
-                    const int8_t* zp = p.has_zero ? p.zero[ks] : nullptr;
-                    if (ks != dq_ks && p.gran != COC_SCALE_GROUP) dq.load(w8l, sc, zp, 0, j0);   // once per shard
+                    // per-tensor / per-channel: the shard's constants from global memory
+                    if (ks != dq_ks && p.gran != COC_SCALE_GROUP)
+                        dq.load(w8l, p.scale[ks], p.has_zero ? p.zero[ks] : nullptr, 0, j0);
                     dq_ks = ks;
                     ok = warp_wait(smem_u32(&bempty[bstage]), bphase ^ 1u, ctl, 0x5C0u + bstage);
                     if (ok) ok = warp_wait(smem_u32(&full[stage]), phase, ctl, 0x5A0u + stage);
                     if (!ok) break;
                     const uint8_t* raw = raw_st + stage * raw_stage;
+                    const uint8_t* tab = raw + kps * 64 * W;
+                    const uint8_t* ztab = p.has_zero ? tab + kps * W * 2 : nullptr;
                     uint8_t* bst = b_st + bstage * b_stage + (cc >> 3) * b_group;
                     const int c16 = cc & 7;
                     // this thread's rows of the stage, all loads first, then convert
                     // and store (slab width and stage depth fixed at compile time)
                     auto run = [&](auto nb_c, auto kps_c) {
                         dequant_stage<BF16, decltype(nb_c)::value, decltype(kps_c)::value>(
-                            raw, bst, kr0, cc, c16, dq, w8l, sc, zp, kb, j0, p.gran == COC_SCALE_GROUP);
+                            raw, bst, kr0, cc, c16, dq, tab, ztab, valid, p.gran == COC_SCALE_GROUP);
                     };
                     if (nb == 2) {
                         if (kps == 4) run(IntC<2>{}, IntC<4>{});
@@ -669,7 +720,7 @@ int slab_stages(int a_rows, int boxes, int kps, int split, bool w8) {
 
 int slab_smem_bytes(int stages, int a_rows, int boxes, int kps, int split, bool w8) {
     const int b_stage = boxes * kps * static_cast<int>(kSlabBoxBytes);   // 16-bit B of a stage
-    const int raw_stage = kps * 64 * 64 * boxes;                          // w8A16: int8 W of a stage
+    const int raw_stage = slab_raw_stage(kps, boxes);                     // w8A16: int8 stage with its tables
     const int a_stage = kps * a_rows * 128;
     return 1024 + (w8 ? stages * raw_stage + kSlabW8BStages * (a_stage + b_stage) : stages * (a_stage + b_stage)) +
            NUM_EPI_WARPS * EPI_BUF_BYTES + static_cast<int>(slab_recv_bytes(boxes, split, a_rows)) +
