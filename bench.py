@@ -707,6 +707,29 @@ def time_context(ops, dev, bus=None, index=0):
     out["decode_ar_r8_n8192_k8192_cuda_graph"] = {m: v for m, v in per_call.items() if not m.startswith("bloom")}
     out["decode_ar_layers_cuda_graph"] = {m: v for m, v in per_call.items() if m.startswith("bloom")}
     del keep, graphs
+    # w8A16 at the same decode shape (m 16, fp16, int8 weights: 64 MiB read)
+    graphs, keep, byts = {}, [], {}
+    for gran in ("channel", "group"):
+        ws_ = wl.W8A16(R=8, m=16, n=8192, k_shard=1024, group=128, seed=3, dtype=torch.float16)
+        wxs, wqs, wsc = ws_.make(gran)
+        dxs, dqs, dsc = [x.to(dev) for x in wxs], [q.to(dev) for q in wqs], [t.to(dev) for t in wsc]
+        dout = [torch.empty(16, 8192, dtype=torch.float16, device=dev) for _ in range(8)]
+        call = (lambda dxs=dxs, dqs=dqs, dsc=dsc, dout=dout, gran=gran:
+                coc.matmul_all_reduce_w8a16(dxs, dqs, dsc, gran, 128, dout))
+        call()
+        torch.cuda.synchronize()
+        gd = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gd):
+            for _ in range(20):
+                call()
+        graphs[gran] = gd.replay
+        keep.append((gd, dxs, dqs, dsc, dout))
+        byts[gran] = 8 * 1024 * 8192 + 2 * (16 * 8192 + 8 * 16 * 8192)
+    r = interleaved(graphs, it=10)
+    out["decode_w8a16_r8_m16_n8192_k8192_cuda_graph"] = {
+        g: {"us_per_call": round(1e3 * r[g]["median_ms"] / 20, 1),
+            "hbm_gbs": round(byts[g] / (1e3 * r[g]["median_ms"] / 20) / 1e3, 0)} for g in graphs}
+    del keep, graphs
     # the whole suite step captured once into a CUDA graph and replayed,
     # against the same step launched eagerly (the host's launch cost)
     try:
