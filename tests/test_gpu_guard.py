@@ -96,6 +96,10 @@ AR_CASES = [
     (8, 200, 136, 72, BF16, 1),      # 2-SM pair, ragged m/n/k
     (2, 520, 1000, 64, F16, 4),      # several pair tiles, ragged tail in both dimensions
     (1, 130, 264, 64, BF16, 1),      # R = 1
+    # n a multiple of 16 (the cases above end 8 columns into a 16-column group)
+    (8, 200, 144, 72, BF16, 1),      # one partial pair tile, 144 = two sub-tiles + 16 columns
+    (2, 520, 1008, 64, F16, 4),      # the last sub-tile 48 columns wide
+    (4, 300, 4096, 64, BF16, 2),     # whole tiles in n, ragged m
 ]
 
 
