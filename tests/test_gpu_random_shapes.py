@@ -1,5 +1,6 @@
 """Seeded random shapes for every operator against the fp64 oracle (AllReduce,
-ReduceScatter, AllGather-V2, w8A16, MoE dispatch + GroupedMatMul + combine).
+ReduceScatter, AllGather-V2, w8A16, MoE dispatch + GroupedMatMul + combine,
+and the column-slab kernel under random schedules).
 
 Each case draws the rank count, sizes (ragged against the 128 / 256-row,
 256-column and 64-deep tiles, from decode-sized m to several tiles), dtype
@@ -108,6 +109,61 @@ def test_random_w8a16(seed):
                                       zeros=[z.numpy() for z in zs] if zs is not None else None, dtype=CODE[dt])
     for r in range(R):
         assert_close(outs[r], ref, s.K, f"w8A16 R={R} m={m} n={n} ks={ks} {gran} {dt} zero={zero}")
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_random_column_slab(seed, monkeypatch):
+    """The column-slab kernel (decode-sized m), taken whatever the SM count,
+    with a random schedule (slab width, cluster split, k-blocks per stage;
+    the library reduces what does not fit) on AllReduce, ReduceScatter and
+    w8A16 shapes: ragged slabs, k_shard ending inside a k-block, one to
+    several slabs per CTA."""
+    rng = random.Random(5000 + seed)
+    R = rng.choice([1, 2, 4, 8])
+    m = rng.choice([1, 3, 8, 16, 31, 32, 33, 64, 96, 100, 127, 128])
+    kind = rng.choice(["ar", "rs", "w8"])
+    if kind == "rs" and m % (8 * R) != 0:
+        kind = "ar"
+    n = 16 * rng.randint(1, 400)                     # up to 6400 columns
+    plan = (rng.choice([1, 2]), rng.choice([1, 2, 4]), rng.choice([1, 2, 4]))
+    for k, v in zip(("COC_SLAB", "COC_SLAB_BOXES", "COC_SLAB_SPLIT", "COC_SLAB_KPS", "COC_W8_PATH"),
+                    (1,) + plan + ("slab",)):
+        monkeypatch.setenv(k, str(v))
+    dt = rng.choice([F16, BF16])
+    c = _chunks(rng, m)
+    what = f"{kind} R={R} m={m} n={n} {dt} plan={plan} chunks={c}"
+    if kind == "w8":
+        gran = rng.choice(["tensor", "channel", "group"])
+        group = rng.choice([64, 128, 256])
+        ks = group * rng.randint(1, 3) if gran == "group" else 8 * rng.randint(1, 64)
+        zero = rng.random() < 0.5
+        sh = wl.W8A16(R=R, m=m, n=n, k_shard=ks, group=group, seed=seed, dtype=dt)
+        xs, wqs, scales = sh.make(gran)
+        zs = sh.zeros(gran) if zero else None
+        outs = coc.matmul_all_reduce_w8a16(to_dev(xs), to_dev(wqs), to_dev(scales), gran, group,
+                                           zeros=to_dev(zs) if zs is not None else None, chunks=c)
+        coc.sync_status()
+        code = {"tensor": 0, "channel": 1, "group": 2}[gran]
+        ref = orc.matmul_all_reduce_w8a16(bits(xs), [w.numpy() for w in wqs], bits(scales), code, group,
+                                          zeros=[z.numpy() for z in zs] if zs is not None else None,
+                                          dtype=CODE[dt])
+        for r in range(R):
+            assert_close(outs[r], ref, sh.K, f"{what} ks={ks} {gran} zero={zero}")
+            assert torch.equal(outs[r], outs[0])
+        return
+    ks = 8 * rng.randint(1, 64)                      # up to 512 per shard
+    xs, ws = wl.RowParallel(R=R, m=m, n=n, k_shard=ks, dtype=dt, x_dist="normal(0,1)", w_dist="normal(0,0.02)",
+                            seed=seed).make()
+    dx, dw = to_dev(xs), to_dev(ws)
+    ar = coc.matmul_all_reduce(dx, dw, chunks=c)
+    rs = coc.matmul_reduce_scatter(dx, dw, chunks=c) if kind == "rs" else None
+    coc.sync_status()
+    ref = orc.matmul_all_reduce(CODE[dt], bits(xs), bits(ws))
+    for r in range(R):
+        assert_close(ar[r], ref, R * ks, f"{what} ks={ks} AR rank {r}")
+        assert torch.equal(ar[r], ar[0])
+    if rs is not None:
+        assert torch.equal(torch.cat(rs, 0), ar[0]), what + " concat(RS) != AR"
 
 
 @pytest.mark.parametrize("seed", range(16))
