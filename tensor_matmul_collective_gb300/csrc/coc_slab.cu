@@ -538,7 +538,7 @@ __global__ void __launch_bounds__(slab_threads(W8), 1) coc_slab_kernel(const __g
             // ================================================= w8A16 dequant ===
             // Per stage: once the MMA has freed the A and B stage (bempty) and the
             // int8 stage has landed (full), thread tt, which owns 8 consecutive
-            // columns (chunk cc) of the slab and the stage rows kr0, kr0 + r_step, ..., reads
+            // columns (chunk cc) of the slab and the stage rows kr0, kr0 + R_STEP, ... (dequant_stage), reads
             // their int8 bytes, dequantises them (coc_dequant.cuh, the fused
             // kernel's and the pre-pass's conversion) and writes the 16-bit B
             // stage in the MMA's MN-major 128-byte-swizzled layout.  Every warp
@@ -547,7 +547,6 @@ __global__ void __launch_bounds__(slab_threads(W8), 1) coc_slab_kernel(const __g
             const int chunks = W / 8;
             const int cc = tt % chunks;
             const int kr0 = tt / chunks;
-            const int r_step = (SLAB_DQ_WARPS * 32) / chunks;
             const W8Layout w8l{p.gran, p.group, p.n};
             uint32_t stage = 0, phase = 0, bstage = 0, bphase = 0;
             bool ok = true;
