@@ -9,6 +9,7 @@
 #include <cstring>
 #include <mutex>
 #include <unordered_map>
+#include <utility>
 
 #include <cudaTypedefs.h>
 
@@ -334,31 +335,27 @@ int env_int(const char* name, int dflt) {
     const char* e = std::getenv(name);
     return e == nullptr ? dflt : std::atoi(e);
 }
-SlabPlan slab_plan(int op, int R, int64_t m, int64_t n, int64_t ks, int sm_count) {
+// The column-slab schedule of one slab width (64 boxes columns) and kps0
+// k-blocks per stage (fewer where they do not divide the k-blocks or two
+// stages do not fit); boxes = 0 where the slabs would not fill the SMs.
+SlabPlan slab_plan_for(int op, int R, int64_t m, int64_t n, int64_t ks, int sm_count, int boxes, int kps0,
+                       bool forced) {
     SlabPlan pl;
-    if ((op != OP_AR && op != OP_RS && op != OP_W8) || ks <= 0 || m <= 0 || m > BM) return pl;
-    const int forced = env_int("COC_SLAB", -1);
-    if (forced == 0) return pl;
-    const int boxes = env_int("COC_SLAB_BOXES", 2) == 1 ? 1 : 2;
+    const bool w8 = (op == OP_W8);
     const int64_t kblocks = (ks + BK - 1) / BK;
-    // k-blocks per stage: 4 for 64-column slabs, 2 for 128 (measured best; at
-    // m = 128 two stages of 2 k-blocks beat five of 1: fewer TMA operations
-    // in flight matter more than ring depth)
-    int kps = env_int("COC_SLAB_KPS", boxes == 1 ? 4 : 2);
-    kps = kps >= 4 ? 4 : kps >= 2 ? 2 : 1;
+    int kps = kps0 >= 4 ? 4 : kps0 >= 2 ? 2 : 1;
     while (kps > 1 && kblocks % kps != 0) kps /= 2;
     const int64_t slabs = (n + 64 * boxes - 1) / (64 * boxes);
     const int64_t spu = static_cast<int64_t>(R) * (kblocks / kps);   // stages per slab
     int split = 1;
     // (each part finalises 64 boxes / split >= 32 columns and sums at least one stage)
-    const int max_split = boxes == 2 ? 4 : 2;
+    const int max_split = boxes == 1 ? 2 : 4;
     while (split < max_split && slabs * split * 2 <= sm_count && split * 2 <= spu) split *= 2;
     const int fs = env_int("COC_SLAB_SPLIT", 0);
     if ((fs == 1 || fs == 2 || fs == 4) && fs <= max_split && fs <= spu) split = fs;
-    if (forced != 1 && slabs * split * 2 < sm_count) return pl;
+    if (!forced && slabs * split * 2 < sm_count) return pl;
     // two stages at least must fit in shared memory (w8A16 also holds the
     // 16-bit ring): fewer k-blocks per stage where they do not
-    const bool w8 = (op == OP_W8);
     const int a_rows = static_cast<int>((m + 7) / 8 * 8);
     while (kps > 1 && slab_smem_bytes(2, a_rows, boxes, kps, split, w8) > kSlabSmemCap) kps /= 2;
     if (slab_smem_bytes(2, a_rows, boxes, kps, split, w8) > kSlabSmemCap) return pl;
@@ -366,6 +363,44 @@ SlabPlan slab_plan(int op, int R, int64_t m, int64_t n, int64_t ks, int sm_count
     pl.split = split;
     pl.kps = kps;
     return pl;
+}
+
+SlabPlan slab_plan(int op, int R, int64_t m, int64_t n, int64_t ks, int sm_count) {
+    SlabPlan pl;
+    if ((op != OP_AR && op != OP_RS && op != OP_W8) || ks <= 0 || m <= 0 || m > BM) return pl;
+    const int forced = env_int("COC_SLAB", -1);
+    if (forced == 0) return pl;
+    const int env_boxes = env_int("COC_SLAB_BOXES", 0);
+    const int env_kps = env_int("COC_SLAB_KPS", 0);
+    if (op == OP_W8 && env_boxes == 0) {
+        // w8A16: up to 32 rows 256-column slabs (their int8 rows are read as
+        // 256-byte segments; measured fastest from 1 to 32 rows, 30.4 against
+        // 32.5 us at m 1 with fewer bytes in flight), else the schedule with
+        // the most int8 weight bytes in flight (ties: 128 columns; at m 64
+        // 34.6 against 36.9 us for 256 columns split four ways).  Every
+        // candidate keeps 16 KiB int8 boxes: smaller ones stream far slower.
+        const int a_rows = static_cast<int>((m + 7) / 8 * 8);
+        long long best = 0;
+        for (const auto& c : {std::pair<int, int>{2, 2}, {4, 1}, {1, 4}}) {
+            const SlabPlan cand = slab_plan_for(op, R, m, n, ks, sm_count, c.first, c.second, forced == 1);
+            if (cand.boxes == 0 || cand.kps != c.second) continue;
+            const int st = slab_stages(a_rows, cand.boxes, cand.kps, cand.split, true);
+            const long long score = static_cast<long long>(st) * cand.kps * 64 * 64 * cand.boxes *
+                                    ((cand.boxes == 4 && a_rows <= 32) ? 2 : 1);
+            if (score > best) {
+                best = score;
+                pl = cand;
+            }
+        }
+        return pl;
+    }
+    // 128-column slabs (64 with COC_SLAB_BOXES=1; w8A16 also 256 with 4).
+    // k-blocks per stage: 4 for 64-column slabs, 2 for 128 (measured best; at
+    // m = 128 two stages of 2 k-blocks beat five of 1: fewer TMA operations
+    // in flight matter more than ring depth), 1 for 256
+    const int boxes = env_boxes == 1 ? 1 : (op == OP_W8 && env_boxes >= 4) ? 4 : 2;
+    const int kps = boxes == 4 ? 1 : (env_kps > 0 ? env_kps : boxes == 1 ? 4 : 2);
+    return slab_plan_for(op, R, m, n, ks, sm_count, boxes, kps, forced == 1);
 }
 
 // op OP_W8: the w8A16 AllReduce (int8 w, scales / zero points as for the

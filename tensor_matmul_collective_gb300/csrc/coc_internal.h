@@ -213,7 +213,7 @@ cudaError_t launch_split(int op, bool bf16, const KParams& p, int grid, int clus
 // for the persistent kernel; the kernel dequantises into kSlabW8BStages
 // 16-bit B stages.
 constexpr int kSlabMaxStages = 32;
-constexpr int kSlabW8BStages = 3;
+constexpr int kSlabW8BStages = 2;
 constexpr int kSlabSmemCap = 227 * 1024;                                // dynamic shared memory per CTA
 int slab_stages(int a_rows, int boxes, int kps, int split, bool w8);    // most stages that fit (at least 2)
 int slab_smem_bytes(int stages, int a_rows, int boxes, int kps, int split, bool w8);

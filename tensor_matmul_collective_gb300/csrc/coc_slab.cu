@@ -59,15 +59,15 @@ namespace coc {
 namespace {
 
 constexpr int SLAB_DQ_WARPS = 8;                  // w8A16: dequantisation warps
-// warps: producer, MMA, 4 epilogue; w8A16 adds the dequant warps and one X loader
-__host__ __device__ constexpr int slab_threads(bool w8) { return (6 + (w8 ? SLAB_DQ_WARPS + 1 : 0)) * 32; }
-constexpr int SLAB_XLOAD_WARP = 6 + SLAB_DQ_WARPS;   // w8A16: loads X into the A and B ring
+constexpr int SLAB_DQ_GW = SLAB_DQ_WARPS / 2;      // ... in two groups taking alternate stages
+// warps: producer, MMA, 4 epilogue; w8A16 adds the dequant warps
+__host__ __device__ constexpr int slab_threads(bool w8) { return (6 + (w8 ? SLAB_DQ_WARPS : 0)) * 32; }
 constexpr uint32_t kSlabBoxBytes = 64 * BK * 2;   // one 64 x 64 16-bit box
 constexpr uint32_t kSlabStageBar = 3;             // named barrier of the set-up phase
 static_assert(kSlabMaxStages <= 32, "the producer's fill masks hold one bit per stage");
 
 __host__ __device__ constexpr uint32_t slab_bar_bytes(int stages, bool w8) {
-    return static_cast<uint32_t>(8 * (2 * stages + (w8 ? 3 * kSlabW8BStages : 0) + 7) + 16);
+    return static_cast<uint32_t>(8 * (2 * stages + (w8 ? 2 * kSlabW8BStages : 0) + 7) + 16);
 }
 // Reception area of a slab split over `split` CTAs: per other part, per row
 // quadrant holding output rows (a_rows / 32 rounded up), 32 rows of the (64
@@ -76,11 +76,13 @@ __host__ __device__ constexpr uint32_t slab_recv_bytes(int boxes, int split, int
     return split > 1 ? static_cast<uint32_t>((split - 1) * ((a_rows + 31) / 32) * 32 * (64 * boxes / split) * 4) : 0u;
 }
 
-// w8A16: bytes of one int8 stage: the weight (kps k-blocks x 64 rows x 64
-// boxes columns) and its scale / zero-point table rows (kps rows of 64 boxes
-// 16-bit scales, then kps rows of int8 zero points), rounded to 1 KiB.
-__host__ __device__ constexpr int slab_raw_stage(int kps, int boxes) {
-    return (kps * 64 * 64 * boxes + kps * 64 * boxes * 3 + 1023) / 1024 * 1024;
+// w8A16: bytes of one stage of the producer's ring: X of the stage (kps
+// k-blocks x a_rows rows x 128 bytes, first: 1 KiB aligned for the swizzle),
+// the int8 weight (kps k-blocks x 64 rows x 64 boxes columns) and its scale /
+// zero-point table rows (kps rows of 64 boxes 16-bit scales, then kps rows of
+// int8 zero points), rounded to 1 KiB.
+__host__ __device__ constexpr int slab_raw_stage(int kps, int boxes, int a_rows) {
+    return kps * a_rows * 128 + (kps * 64 * 64 * boxes + kps * 64 * boxes * 3 + 1023) / 1024 * 1024;
 }
 
 template <int V>
@@ -92,7 +94,7 @@ struct IntC {
 // k-blocks: chunk cc (8 columns) of rows kr0, kr0 + R_STEP, ... of every
 // k-block, from the int8 stage `raw` (rows of 64 NB bytes) into the 16-bit B
 // stage (NB groups of KPS k-blocks x 64 rows x 128 bytes, 16-byte chunks
-// XOR-ed with row % 8).  All loads are issued before the first conversion.
+// XOR-ed with row % 8).  Up to 8 rows' loads are issued before their conversions.
 // The scale and zero points of this thread's 8 columns from table slot
 // `tab` of the stage (16-bit scales at tab, int8 zero points at ztab; zero
 // points 0 when there are none, scales 0 past n, as for the global tables).
@@ -119,19 +121,26 @@ template <bool BF16, int NB, int KPS>
 __device__ __forceinline__ void dequant_stage(const uint8_t* raw, uint8_t* bst, int kr0, int cc, int c16, Dq<BF16>& dq,
                                               const uint8_t* tab, const uint8_t* ztab, bool valid, bool per_group) {
     constexpr int W = 64 * NB;
-    constexpr int R_STEP = (SLAB_DQ_WARPS * 32) / (W / 8);
+    constexpr int R_STEP = (SLAB_DQ_GW * 32) / (W / 8);
     constexpr int RPK = BK / R_STEP;   // rows per k-block
     constexpr int ROWS = KPS * RPK;
-    uint2 q8[ROWS];
+    constexpr int RB = ROWS < 8 ? ROWS : 8;   // rows in flight (registers)
 #pragma unroll
-    for (int i = 0; i < ROWS; ++i)
-        q8[i] = *reinterpret_cast<const uint2*>(raw + ((i / RPK) * BK + kr0 + (i % RPK) * R_STEP) * W + cc * 8);
+    for (int b0 = 0; b0 < ROWS; b0 += RB) {
+        uint2 q8[RB];
 #pragma unroll
-    for (int i = 0; i < ROWS; ++i) {
-        if (per_group && i % RPK == 0)
-            dq_from_slot<BF16>(dq, tab + (i / RPK) * W * 2, ztab != nullptr ? ztab + (i / RPK) * W : nullptr, cc, valid);
-        const int kk = (i / RPK) * BK + kr0 + (i % RPK) * R_STEP;   // row of the stage
-        *reinterpret_cast<uint4*>(bst + kk * 128 + ((c16 ^ (kk & 7)) << 4)) = dq.convert(q8[i]);
+        for (int j = 0; j < RB; ++j) {
+            const int i = b0 + j;
+            q8[j] = *reinterpret_cast<const uint2*>(raw + ((i / RPK) * BK + kr0 + (i % RPK) * R_STEP) * W + cc * 8);
+        }
+#pragma unroll
+        for (int j = 0; j < RB; ++j) {
+            const int i = b0 + j;
+            if (per_group && i % RPK == 0)
+                dq_from_slot<BF16>(dq, tab + (i / RPK) * W * 2, ztab != nullptr ? ztab + (i / RPK) * W : nullptr, cc, valid);
+            const int kk = (i / RPK) * BK + kr0 + (i % RPK) * R_STEP;   // row of the stage
+            *reinterpret_cast<uint4*>(bst + kk * 128 + ((c16 ^ (kk & 7)) << 4)) = dq.convert(q8[j]);
+        }
     }
 }
 
@@ -160,26 +169,27 @@ __global__ void __launch_bounds__(slab_threads(W8), 1) coc_slab_kernel(const __g
     const uint32_t b_stage = static_cast<uint32_t>(nb) * b_group;
     const int W = nb * 64;                // slab width
     const int ow = W / csplit;            // columns this CTA finalises (split: its share of the slab)
-    const uint32_t raw_stage = W8 ? static_cast<uint32_t>(slab_raw_stage(kps, nb)) : 0u;   // w8A16: int8 stage
-    // w8A16: the producer's ring carries only the int8 W (freed by the dequant
-    // warps, so it runs as far ahead as it is deep); X and the 16-bit W share
-    // a second ring of SB stages (X loaded by the dequant warps, freed by the MMA)
+    // w8A16: the producer's ring carries X and the int8 W of each stage (one
+    // barrier; freed by the dequant warps and the MMA, so X runs as far ahead
+    // as the weight); the dequant warps write the 16-bit W into a second ring
+    // of SB stages, freed by the MMA
+    const uint32_t raw_stage = W8 ? static_cast<uint32_t>(slab_raw_stage(kps, nb, a_rows)) : 0u;
     constexpr int SB = W8 ? kSlabW8BStages : 0;
-    const int SAB = W8 ? SB : S;                               // stages of the A and B rings
 
-    // A ring first: the MMA reads 128 rows from a k-block's start, past the
-    // last A stage into the B ring (>= 16 KiB), never past the allocation
-    uint8_t* a_st = smem;                                      // SAB x a_stage
-    uint8_t* b_st = a_st + SAB * a_stage;                      // SAB x b_stage
-    uint8_t* raw_st = b_st + SAB * b_stage;                    // w8A16: S x raw_stage
-    uint8_t* stg = raw_st + S * raw_stage;                     // 4 epilogue warps x 4 KiB
+    // A first: the MMA reads 128 rows from a k-block's start, past the last
+    // stage's A into the B ring (>= 16 KiB), never past the allocation.
+    // bf16: S stages of A, then S of B; w8A16: S stages of (X, int8 W,
+    // tables), then the SB 16-bit B stages.
+    uint8_t* a_st = smem;                                      // bf16: S x a_stage
+    uint8_t* raw_st = smem;                                    // w8A16: S x raw_stage (X at the start)
+    uint8_t* b_st = W8 ? raw_st + S * raw_stage : a_st + S * a_stage;   // S (w8A16: SB) x b_stage
+    uint8_t* stg = b_st + (W8 ? SB : S) * b_stage;             // 4 epilogue warps x 4 KiB
     uint8_t* recv = stg + NUM_EPI_WARPS * EPI_BUF_BYTES;   // split: the other parts' sums of this CTA's columns
     uint64_t* full = reinterpret_cast<uint64_t*>(recv + slab_recv_bytes(nb, csplit, a_rows));   // [S]
-    uint64_t* empty = full + S;                    // [S]  (w8A16: int8 stage read by every dequant warp)
-    uint64_t* bfull = empty + S;                   // [SB] w8A16: 16-bit B stage written (every dequant warp)
-    uint64_t* bempty = bfull + SB;                 // [SB] w8A16: A and B stage consumed by the MMA
-    uint64_t* afull = bempty + SB;                 // [SB] w8A16: X of the stage landed
-    uint64_t* accf = afull + SB;                   // [2] accumulator ready for the epilogue
+    uint64_t* empty = full + S;                    // [S]  (w8A16: read by the stage's dequant warps and the MMA)
+    uint64_t* bfull = empty + S;                   // [SB] w8A16: 16-bit B stage written (its dequant warps)
+    uint64_t* bempty = bfull + SB;                 // [SB] w8A16: 16-bit B stage consumed by the MMA
+    uint64_t* accf = bempty + SB;                  // [2] accumulator ready for the epilogue
     uint64_t* acce = accf + 2;                     // [2] accumulator drained (4 epilogue warps)
     uint64_t* never = acce + 2;                    // [1] nothing arrives here (fault-injection test)
     uint64_t* drain = never + 1;                   // [1] MMA drain before TMEM release
@@ -196,12 +206,11 @@ __global__ void __launch_bounds__(slab_threads(W8), 1) coc_slab_kernel(const __g
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
-            mbar_init(smem_u32(&empty[s]), W8 ? SLAB_DQ_WARPS : 1);
+            mbar_init(smem_u32(&empty[s]), W8 ? SLAB_DQ_GW + 1 : 1);
         }
         for (int b = 0; b < SB; ++b) {
-            mbar_init(smem_u32(&bfull[b]), SLAB_DQ_WARPS);
+            mbar_init(smem_u32(&bfull[b]), SLAB_DQ_GW);
             mbar_init(smem_u32(&bempty[b]), 1);
-            mbar_init(smem_u32(&afull[b]), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&accf[b]), 1);
@@ -214,7 +223,7 @@ __global__ void __launch_bounds__(slab_threads(W8), 1) coc_slab_kernel(const __g
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         fence_proxy_async_smem();
     }
-    const uint32_t tmem_cols = nb == 1 ? 128u : 256u;   // two W-column accumulators
+    const uint32_t tmem_cols = static_cast<uint32_t>(2 * W);   // two W-column accumulators
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), tmem_cols);
         tmem_relinquish();
@@ -280,20 +289,19 @@ __global__ void __launch_bounds__(slab_threads(W8), 1) coc_slab_kernel(const __g
                     const int tab_cols = W8 ? min(W, n - col0) : 0;
                     const int tab_rows = (W8 && p.gran == COC_SCALE_GROUP) ? kps : 0;
                     const uint32_t tab_bytes = static_cast<uint32_t>(tab_rows * tab_cols * (p.has_zero ? 3 : 2));
-                    mbar_expect_tx(fb, W8 ? static_cast<uint32_t>(kps * 64 * W) + tab_bytes : a_stage + b_stage);
-                    if constexpr (!W8) {
-                        const uint32_t adst = smem_u32(a_st + stage * a_stage);
-                        if (a3d) {
-                            tma_load_3d_hint(adst, am, 0, 0, kb, fb, pol_a);
-                        } else {
-                            for (int t = 0; t < kps; ++t)
-                                tma_load_2d_hint(adst + t * a_kb, am, (kb + t) * BK, 0, fb, pol_a);
-                        }
+                    mbar_expect_tx(fb, a_stage + (W8 ? static_cast<uint32_t>(kps * 64 * W) + tab_bytes : b_stage));
+                    // X of the stage (w8A16: at the start of the int8 stage)
+                    const uint32_t adst = W8 ? smem_u32(raw_st + stage * raw_stage) : smem_u32(a_st + stage * a_stage);
+                    if (a3d) {
+                        tma_load_3d_hint(adst, am, 0, 0, kb, fb, pol_a);
+                    } else {
+                        for (int t = 0; t < kps; ++t)
+                            tma_load_2d_hint(adst + t * a_kb, am, (kb + t) * BK, 0, fb, pol_a);
                     }
                     const uint32_t bdst = smem_u32(b_st + stage * b_stage);
                     if constexpr (W8) {
-                        // the int8 W of the stage: W columns x kps k-blocks, one box
-                        uint8_t* rs = raw_st + stage * raw_stage;
+                        // the int8 W of the stage after its X: W columns x kps k-blocks, one box
+                        uint8_t* rs = raw_st + stage * raw_stage + a_stage;
                         tma_load_2d_hint(smem_u32(rs), bm, col0, kb * BK, fb, pol_b);
                         uint8_t* tab = rs + kps * 64 * W;   // scale rows, then zero-point rows
                         for (int t = 0; t < tab_rows; ++t) {
@@ -349,19 +357,17 @@ __global__ void __launch_bounds__(slab_threads(W8), 1) coc_slab_kernel(const __g
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * W);
             for (int i = 0; i < st_hi - st_lo; ++i) {
-                if constexpr (W8) {
-                    ok = warp_wait(smem_u32(&afull[bstage]), bphase, ctl, 0x590u + bstage);
-                    if (ok) ok = warp_wait(smem_u32(&bfull[bstage]), bphase, ctl, 0x598u + bstage);
-                } else {
-                    ok = warp_wait(smem_u32(&full[stage]), phase, ctl, 0x540u + stage);
-                }
+                // (w8A16: X landed with the int8 stage, the 16-bit W is in B stage bstage)
+                ok = warp_wait(smem_u32(&full[stage]), phase, ctl, 0x540u + stage);
+                if (W8 && ok) ok = warp_wait(smem_u32(&bfull[bstage]), bphase, ctl, 0x598u + bstage);
                 if (!ok) break;
                 tc_fence_after();
                 if (lane == 0) {
-                    const uint32_t bs = W8 ? bstage : stage;   // stage of the A and B rings
+                    const uint8_t* a_s = W8 ? raw_st + stage * raw_stage : a_st + stage * a_stage;
+                    const uint8_t* b_s = b_st + (W8 ? bstage : stage) * b_stage;
                     for (int t = 0; t < kps; ++t) {
-                        const uint64_t ad = make_sdesc(smem_u32(a_st + bs * a_stage + t * a_kb), 16u, 1024u);
-                        const uint64_t bd = make_sdesc(smem_u32(b_st + bs * b_stage + t * b_kb), b_lbo, 1024u);
+                        const uint64_t ad = make_sdesc(smem_u32(a_s + t * a_kb), 16u, 1024u);
+                        const uint64_t bd = make_sdesc(smem_u32(b_s + t * b_kb), b_lbo, 1024u);
 #pragma unroll
                         for (int kk = 0; kk < BK / UMMA_K; ++kk)
                             tc_mma_f16(d_tmem, ad + static_cast<uint64_t>(kk) * 2u,
@@ -369,10 +375,10 @@ __global__ void __launch_bounds__(slab_threads(W8), 1) coc_slab_kernel(const __g
                                        (i > 0 || t > 0 || kk > 0) ? 1u : 0u);
                     }
                     if (W8) tc_commit(smem_u32(&bempty[bstage]));
-                    else tc_commit(smem_u32(&empty[stage]));
+                    tc_commit(smem_u32(&empty[stage]));
                 }
                 __syncwarp();
-                if (!W8 && ++stage == static_cast<uint32_t>(S)) { stage = 0; phase ^= 1u; }
+                if (++stage == static_cast<uint32_t>(S)) { stage = 0; phase ^= 1u; }
                 if (W8 && ++bstage == static_cast<uint32_t>(SB)) { bstage = 0; bphase ^= 1u; }
             }
             if (!ok) break;
@@ -534,7 +540,7 @@ __global__ void __launch_bounds__(slab_threads(W8), 1) coc_slab_kernel(const __g
     }
 
     if constexpr (W8) {
-        if (warp >= 2 + NUM_EPI_WARPS && warp < SLAB_XLOAD_WARP) {
+        if (warp >= 2 + NUM_EPI_WARPS) {
             // ================================================= w8A16 dequant ===
             // Per stage: once the MMA has freed the A and B stage (bempty) and the
             // int8 stage has landed (full), thread tt, which owns 8 consecutive
@@ -543,19 +549,32 @@ __global__ void __launch_bounds__(slab_threads(W8), 1) coc_slab_kernel(const __g
             // kernel's and the pre-pass's conversion) and writes the 16-bit B
             // stage in the MMA's MN-major 128-byte-swizzled layout.  Every warp
             // then arrives on the B stage's `bfull` and the int8 stage's `empty`.
-            const int tt = (warp - 2 - NUM_EPI_WARPS) * 32 + lane;
+            // Two groups of SLAB_DQ_GW warps take alternate stages (group g the
+            // stages c with c % 2 == g, c counted over all units), so one group's
+            // waits, fence and arrivals overlap the other's conversion.  Any ring
+            // depth works: a slot is refilled (producer) or rewritten (16-bit
+            // ring) only after the group that used it and the MMA are done with
+            // it, so no wait can be two phases behind its barrier.
+            const int dw = warp - 2 - NUM_EPI_WARPS;
+            const int group = dw / SLAB_DQ_GW;
+            const int tt = (dw % SLAB_DQ_GW) * 32 + lane;
             const int chunks = W / 8;
             const int cc = tt % chunks;
             const int kr0 = tt / chunks;
             const W8Layout w8l{p.gran, p.group, p.n};
-            uint32_t stage = 0, phase = 0, bstage = 0, bphase = 0;
+            uint32_t stage = 0, phase = 0, bstage = 0, bphase = 0, cnt = 0;
             bool ok = true;
             for (int u = first_u; ok && u < units; u += u_step) {
                 const int j0 = u * W + cc * 8;   // this thread's first output column
                 int dq_ks = -1;
                 Dq<BF16> dq;
                 const bool valid = j0 + 8 <= n;   // this thread's columns lie inside the output
-                for (int s = st_lo; s < st_hi; ++s) {
+                for (int s = st_lo; s < st_hi; ++s, ++cnt) {
+                    if (static_cast<int>(cnt & 1u) != group) {   // the other group's stage
+                        if (++stage == static_cast<uint32_t>(S)) { stage = 0; phase ^= 1u; }
+                        if (++bstage == static_cast<uint32_t>(SB)) { bstage = 0; bphase ^= 1u; }
+                        continue;
+                    }
                     const int ks = s / spk;
                     // per-tensor / per-channel: the shard's constants from global memory
                     if (ks != dq_ks && p.gran != COC_SCALE_GROUP)
@@ -564,7 +583,7 @@ __global__ void __launch_bounds__(slab_threads(W8), 1) coc_slab_kernel(const __g
                     ok = warp_wait(smem_u32(&bempty[bstage]), bphase ^ 1u, ctl, 0x5C0u + bstage);
                     if (ok) ok = warp_wait(smem_u32(&full[stage]), phase, ctl, 0x5A0u + stage);
                     if (!ok) break;
-                    const uint8_t* raw = raw_st + stage * raw_stage;
+                    const uint8_t* raw = raw_st + stage * raw_stage + a_stage;   // after the stage's X
                     const uint8_t* tab = raw + kps * 64 * W;
                     const uint8_t* ztab = p.has_zero ? tab + kps * W * 2 : nullptr;
                     uint8_t* bst = b_st + bstage * b_stage + (cc >> 3) * b_group;
@@ -575,7 +594,9 @@ __global__ void __launch_bounds__(slab_threads(W8), 1) coc_slab_kernel(const __g
                         dequant_stage<BF16, decltype(nb_c)::value, decltype(kps_c)::value>(
                             raw, bst, kr0, cc, c16, dq, tab, ztab, valid, p.gran == COC_SCALE_GROUP);
                     };
-                    if (nb == 2) {
+                    if (nb == 4) {
+                        run(IntC<4>{}, IntC<1>{});   // (256-column slabs take one k-block per stage)
+                    } else if (nb == 2) {
                         if (kps == 4) run(IntC<2>{}, IntC<4>{});
                         else if (kps == 2) run(IntC<2>{}, IntC<2>{});
                         else run(IntC<2>{}, IntC<1>{});
@@ -596,48 +617,6 @@ __global__ void __launch_bounds__(slab_threads(W8), 1) coc_slab_kernel(const __g
             }
         }
     }
-    if constexpr (W8) {
-        if (warp == SLAB_XLOAD_WARP) {
-            // ================================================= w8A16 X loads ===
-            // once the MMA has freed an A and B stage (bempty), X of the stage it
-            // will hold next into its A part (afull); the int8 stream never waits
-            // behind these loads
-            const bool a3d = p.slab_a3d != 0;
-            const uint64_t pol_a = make_l2_policy(2);   // X: reused by every slab
-            uint32_t bstage = 0, bphase = 0, a_filled = 0, a_parity = 0;
-            bool ok = true;
-            for (int u = first_u; ok && u < units; u += u_step) {
-                for (int s = st_lo; s < st_hi; ++s) {
-                    const int ks = s / spk;
-                    const int kb = (s - ks * spk) * kps;
-                    ok = warp_wait(smem_u32(&bempty[bstage]), bphase ^ 1u, ctl, 0x5E0u + bstage);
-                    if (!ok) break;
-                    if (lane == 0) {
-                        const CUtensorMap* am = &p.tm_a[ks];
-                        const uint32_t ab = smem_u32(&afull[bstage]);
-                        const uint32_t adst = smem_u32(a_st + bstage * a_stage);
-                        mbar_expect_tx(ab, a_stage);
-                        if (a3d) {
-                            tma_load_3d_hint(adst, am, 0, 0, kb, ab, pol_a);
-                        } else {
-                            for (int t = 0; t < kps; ++t)
-                                tma_load_2d_hint(adst + t * a_kb, am, (kb + t) * BK, 0, ab, pol_a);
-                        }
-                        a_filled |= 1u << bstage;
-                        a_parity = (a_parity & ~(1u << bstage)) | (bphase << bstage);
-                    }
-                    __syncwarp();
-                    if (++bstage == static_cast<uint32_t>(SB)) { bstage = 0; bphase ^= 1u; }
-                }
-            }
-            if (!ok && lane == 0) {
-                // leave no X load in flight into shared memory
-                for (int b = 0; b < SB; ++b)
-                    if (a_filled & (1u << b)) drain_wait(smem_u32(&afull[b]), (a_parity >> b) & 1u, kDrainNs);
-            }
-        }
-    }
-
     if (csplit > 1) {
         // no CTA leaves while a part may still push into its shared memory
         if (warp == 0) cluster_wait();   // the set-up phase this warp only arrived at
@@ -719,9 +698,9 @@ int slab_stages(int a_rows, int boxes, int kps, int split, bool w8) {
 
 int slab_smem_bytes(int stages, int a_rows, int boxes, int kps, int split, bool w8) {
     const int b_stage = boxes * kps * static_cast<int>(kSlabBoxBytes);   // 16-bit B of a stage
-    const int raw_stage = slab_raw_stage(kps, boxes);                     // w8A16: int8 stage with its tables
+    const int raw_stage = slab_raw_stage(kps, boxes, a_rows);             // w8A16: X, int8 W and its tables
     const int a_stage = kps * a_rows * 128;
-    return 1024 + (w8 ? stages * raw_stage + kSlabW8BStages * (a_stage + b_stage) : stages * (a_stage + b_stage)) +
+    return 1024 + (w8 ? stages * raw_stage + kSlabW8BStages * b_stage : stages * (a_stage + b_stage)) +
            NUM_EPI_WARPS * EPI_BUF_BYTES + static_cast<int>(slab_recv_bytes(boxes, split, a_rows)) +
            static_cast<int>(slab_bar_bytes(stages, w8));
 }

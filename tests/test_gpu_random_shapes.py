@@ -125,7 +125,7 @@ def test_random_column_slab(seed, monkeypatch):
     if kind == "rs" and m % (8 * R) != 0:
         kind = "ar"
     n = 16 * rng.randint(1, 400)                     # up to 6400 columns
-    plan = (rng.choice([1, 2]), rng.choice([1, 2, 4]), rng.choice([1, 2, 4]))
+    plan = (rng.choice([1, 2, 4] if kind == "w8" else [1, 2]), rng.choice([1, 2, 4]), rng.choice([1, 2, 4]))
     for k, v in zip(("COC_SLAB", "COC_SLAB_BOXES", "COC_SLAB_SPLIT", "COC_SLAB_KPS", "COC_W8_PATH"),
                     (1,) + plan + ("slab",)):
         monkeypatch.setenv(k, str(v))

@@ -1,5 +1,5 @@
 """w8A16 MATMUL_ALL_REDUCE at decode-sized m through the column-slab kernel:
-the int8 weight streamed over all SMs in slabs of 64 or 128 columns, each
+the int8 weight streamed over all SMs in slabs of 64, 128 or 256 columns, each
 stage dequantised in shared memory by the kernel's own warps (the fused
 kernel's conversion), and, with the split, each slab's contraction shared by
 a cluster of 2 or 4 CTAs whose fp32 parts add in part order.
@@ -57,6 +57,10 @@ CASES = [
     (2, 100, 528, 128, 128, (1, 2, 2)),     # four row quadrants, 64-column slabs split in two
     (8, 128, 4096, 256, 256, (2, 1, 2)),    # unsplit, group 256
     (2, 33, 20000, 64, 64, (2, 1, 1)),      # several slabs per CTA
+    # 256-column slabs (one k-block per stage)
+    (8, 16, 4000, 128, 64, (4, 4, 1)),      # clusters of 4, the last slab 160 columns wide
+    (2, 100, 2064, 192, 64, (4, 2, 1)),     # clusters of 2, k_shard of three k-blocks, ragged m
+    (4, 33, 4352, 256, 128, (4, 1, 1)),     # unsplit, several slabs per CTA
 ]
 
 
@@ -78,9 +82,10 @@ def test_w8a16_slab_parity(monkeypatch, dt, zero, gran, R, m, n, ks, group, plan
         assert torch.equal(outs[r], outs[0])
 
 
+@pytest.mark.parametrize("plan", [(2, 1, 2), (4, 1, 1)], ids=["128col", "256col"])
 @pytest.mark.parametrize("dt", [torch.float16, torch.bfloat16], ids=["fp16", "bf16"])
 @pytest.mark.parametrize("gran", ["tensor", "channel", "group"])
-def test_unsplit_slab_gives_the_other_schedules_bits(monkeypatch, dt, gran):
+def test_unsplit_slab_gives_the_other_schedules_bits(monkeypatch, dt, gran, plan):
     """One CTA per slab: the same conversion and the same accumulation order
     (rank 0..R-1, k ascending, 16 k per MMA) as the fused, pre-pass and
     tensor-memory schedules, so the same bits."""
@@ -89,7 +94,7 @@ def test_unsplit_slab_gives_the_other_schedules_bits(monkeypatch, dt, gran):
     zs = shape.zeros(gran)
     args = (to_dev(xs), to_dev(wqs), to_dev(scales), gran, 64)
     kw = dict(zeros=to_dev(zs))
-    _slab(monkeypatch, (2, 1, 2))
+    _slab(monkeypatch, plan)
     a = [t.clone() for t in coc.matmul_all_reduce_w8a16(*args, **kw)]
     outs = {}
     for path in ("fused", "prepass", "ts"):
@@ -101,7 +106,7 @@ def test_unsplit_slab_gives_the_other_schedules_bits(monkeypatch, dt, gran):
             assert torch.equal(x, y), f"slab differs from the {path} schedule"
 
 
-@pytest.mark.parametrize("plan", [(2, 1, 2), (2, 2, 2), (1, 2, 4)])
+@pytest.mark.parametrize("plan", [(2, 1, 2), (2, 2, 2), (1, 2, 4), (4, 4, 1)])
 def test_w8a16_slab_dequant_bitwise(monkeypatch, plan):
     """One-hot activations (X_r = e_i rows of one rank, the others zero):
     output row i is the dequantised weight row i of that rank, bit for bit."""
@@ -125,11 +130,13 @@ def test_w8a16_slab_dequant_bitwise(monkeypatch, plan):
         assert np.array_equal(wl.bits16(got[i:i + 1])[0], wd[k]), f"row {i} (rank {r}, k {k})"
 
 
-def test_w8a16_decode_default_takes_the_slab(monkeypatch):
+@pytest.mark.parametrize("m", [1, 16, 64, 128])
+def test_w8a16_decode_default_takes_the_slab(monkeypatch, m):
     """The default schedule at the decode layer's shape gives the oracle's
-    values (on a 152-SM GB300 it is the slab kernel split in clusters)."""
+    values (on a 152-SM GB300 it is the slab kernel split in clusters, with
+    the slab width and stage depth the library picks for m)."""
     monkeypatch.delenv("COC_W8_PATH", raising=False)
-    shape = wl.W8A16(R=8, m=16, n=8192, k_shard=1024, group=128, seed=75, dtype=torch.float16)
+    shape = wl.W8A16(R=8, m=m, n=8192, k_shard=1024, group=128, seed=75 + m, dtype=torch.float16)
     xs, wqs, scales = shape.make("channel")
     outs = coc.matmul_all_reduce_w8a16(to_dev(xs), to_dev(wqs), to_dev(scales), "channel", 128)
     coc.sync_status()
