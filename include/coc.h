@@ -103,9 +103,10 @@
  *     column-slab kernel), COC_KSPLIT=<n> (rank-split part count, rounded
  *     down to a power of two dividing R), COC_SPLIT_PATH=scratch (rank split
  *     through global memory), COC_SLAB=0|1 (column-slab kernel off / for
- *     every m <= 128) with COC_SLAB_BOXES=1|2, COC_SLAB_SPLIT=1|2|4 and
- *     COC_SLAB_KPS=1|2|4 (its slab width in 64-column groups, CTAs per
- *     slab, k-blocks per stage).  Forcing one can change the last bit of
+ *     every m <= 128) with COC_SLAB_BOXES=1|2 (w8A16 also 4),
+ *     COC_SLAB_SPLIT=1|2|4 and COC_SLAB_KPS=1|2|4 (its slab width in
+ *     64-column groups, CTAs per slab, k-blocks per stage; 256-column slabs
+ *     take one k-block per stage).  Forcing one can change the last bit of
  *     results (a different summation grouping).
  */
 #ifndef COC_H_
