@@ -47,6 +47,7 @@
 // the CTA abort flag and the device status word, every role leaves its loop,
 // issued copies and MMAs are drained, TMEM is freed and the kernel returns.
 #include <atomic>
+#include <cstdlib>
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -242,6 +243,13 @@ __global__ void __launch_bounds__(slab_threads(W8), 1) coc_slab_kernel(const __g
         named_sync(kSlabStageBar, THREADS);
     }
     tc_fence_after();
+    // Everything above touches only this CTA's shared and tensor memory and
+    // the kernel parameters, so with a programmatic launch it overlaps the
+    // previous kernel in the stream; global memory is touched only after it
+    // has completed.  Every CTA of this grid is resident at once, so the next
+    // kernel may then start on the SMs this one leaves free.
+    grid_dependency_wait();
+    grid_dependents_launch();
     const uint32_t tmem_base = warp == 0 ? 0u : *tmem_slot;
     const bool probe = p.clock_slot >= 0 && blockIdx.x == 0 && threadIdx.x == 0;
     uint64_t probe_clk = 0, probe_ns = 0;
@@ -639,6 +647,16 @@ __global__ void __launch_bounds__(slab_threads(W8), 1) coc_slab_kernel(const __g
 
 constexpr int kMaxDevices = 64;
 
+// Programmatic dependent launches of the slab kernel (COC_PDL=0: plain
+// stream order).
+bool slab_pdl() {
+    static const bool on = [] {
+        const char* e = std::getenv("COC_PDL");
+        return e == nullptr || std::atoi(e) != 0;
+    }();
+    return on;
+}
+
 template <int OP, bool BF16, bool W8>
 cudaError_t launch_slab_t(const KParams& p, int grid, cudaStream_t stream) {
     auto kern = coc_slab_kernel<OP, BF16, W8>;
@@ -651,19 +669,26 @@ cudaError_t launch_slab_t(const KParams& p, int grid, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < kMaxDevices) smem_set[dev].store(1, std::memory_order_release);
     }
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
     cfg.blockDim = dim3(slab_threads(W8), 1, 1);
     cfg.dynamicSmemBytes = slab_smem_bytes(p.slab_stages, p.a_box_rows, p.slab_boxes, p.slab_kps, p.slab_split, W8);
     cfg.stream = stream;
+    cfg.attrs = attr;
     if (p.slab_split > 1) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = p.slab_split;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[cfg.numAttrs].id = cudaLaunchAttributeClusterDimension;
+        attr[cfg.numAttrs].val.clusterDim.x = p.slab_split;
+        attr[cfg.numAttrs].val.clusterDim.y = 1;
+        attr[cfg.numAttrs].val.clusterDim.z = 1;
+        ++cfg.numAttrs;
+    }
+    if (slab_pdl()) {
+        // may start its set-up while the previous kernel in the stream runs
+        // (the kernel waits for it before touching global memory)
+        attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+        ++cfg.numAttrs;
     }
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
