@@ -106,10 +106,10 @@
  *     every m <= 128) with COC_SLAB_BOXES=1|2 (w8A16 also 4),
  *     COC_SLAB_SPLIT=1|2|4 and COC_SLAB_KPS=1|2|4 (its slab width in
  *     64-column groups, CTAs per slab, k-blocks per stage; 256-column slabs
- *     take one k-block per stage), COC_PDL=0 (the column-slab kernel
- *     launched in plain stream order instead of as a programmatic
- *     dependent launch, which runs its set-up while the previous kernel in
- *     the stream finishes).  Forcing one can change the last bit of
+ *     take one k-block per stage), COC_PDL=0 (the kernels launched in
+ *     plain stream order instead of as programmatic dependent launches,
+ *     which run their set-up while the previous kernel in the stream
+ *     finishes).  Forcing one can change the last bit of
  *     results (a different summation grouping).
  */
 #ifndef COC_H_

@@ -331,6 +331,18 @@ int rank_split(int op, int R, int64_t ks, int64_t tiles, bool pair, int sm_count
 struct SlabPlan {
     int boxes = 0, split = 1, kps = 1;
 };
+}  // namespace
+
+bool pdl_launch() {
+    static const bool on = [] {
+        const char* e = std::getenv("COC_PDL");
+        return e == nullptr || std::atoi(e) != 0;
+    }();
+    return on;
+}
+
+namespace {
+
 int env_int(const char* name, int dflt) {
     const char* e = std::getenv(name);
     return e == nullptr ? dflt : std::atoi(e);

@@ -215,6 +215,10 @@ cudaError_t launch_split(int op, bool bf16, const KParams& p, int grid, int clus
 constexpr int kSlabMaxStages = 32;
 constexpr int kSlabW8BStages = 2;
 constexpr int kSlabSmemCap = 227 * 1024;                                // dynamic shared memory per CTA
+// Programmatic dependent launches (the persistent and column-slab kernels
+// start their set-up while the previous kernel in the stream finishes and
+// wait for it before touching global memory); COC_PDL=0: plain stream order.
+bool pdl_launch();
 int slab_stages(int a_rows, int boxes, int kps, int split, bool w8);    // most stages that fit (at least 2)
 int slab_smem_bytes(int stages, int a_rows, int boxes, int kps, int split, bool w8);
 cudaError_t launch_slab(int op, bool bf16, bool w8, const KParams& p, int grid, cudaStream_t stream);

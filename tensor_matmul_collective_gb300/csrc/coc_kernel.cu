@@ -298,6 +298,13 @@ __global__ void __launch_bounds__(Cfg<OP, PAIR>::THREADS, 1) coc_fused_kernel(co
         named_sync(kSetupBar, C::THREADS);
     }
     tc_fence_after();
+    // Everything above touches only this CTA's shared and tensor memory and
+    // the kernel parameters, so with a programmatic launch it overlaps the
+    // previous kernel in the stream; global memory is touched only after it
+    // has completed.  Every CTA of this grid is resident at once, so the next
+    // kernel may then start on the SMs this one leaves free.
+    grid_dependency_wait();
+    grid_dependents_launch();
     const uint32_t tmem_base = early_producer ? 0u : *tmem_slot;
     // clock probe: block 0 measures the SM cycles and nanoseconds it spends
     const bool probe = p.clock_slot >= 0 && blockIdx.x == 0 && threadIdx.x == 0;
@@ -945,21 +952,27 @@ cudaError_t launch_t(const KParams& p, int grid, cudaStream_t stream, int cluste
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < kMaxDevices) smem_set[dev].store(1, std::memory_order_release);
     }
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
     cfg.blockDim = dim3(C::THREADS, 1, 1);
     cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = stream;
-    cfg.attrs = nullptr;
+    cfg.attrs = attr;
     cfg.numAttrs = 0;
     if (PAIR || cluster > 1) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = PAIR ? 2 : cluster;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[cfg.numAttrs].id = cudaLaunchAttributeClusterDimension;
+        attr[cfg.numAttrs].val.clusterDim.x = PAIR ? 2 : cluster;
+        attr[cfg.numAttrs].val.clusterDim.y = 1;
+        attr[cfg.numAttrs].val.clusterDim.z = 1;
+        ++cfg.numAttrs;
+    }
+    if (pdl_launch()) {
+        // may start its set-up while the previous kernel in the stream runs
+        // (the kernel waits for it before touching global memory)
+        attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+        ++cfg.numAttrs;
     }
     return cudaLaunchKernelEx(&cfg, kern, p);
 }

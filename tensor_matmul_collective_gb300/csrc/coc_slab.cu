@@ -647,16 +647,6 @@ __global__ void __launch_bounds__(slab_threads(W8), 1) coc_slab_kernel(const __g
 
 constexpr int kMaxDevices = 64;
 
-// Programmatic dependent launches of the slab kernel (COC_PDL=0: plain
-// stream order).
-bool slab_pdl() {
-    static const bool on = [] {
-        const char* e = std::getenv("COC_PDL");
-        return e == nullptr || std::atoi(e) != 0;
-    }();
-    return on;
-}
-
 template <int OP, bool BF16, bool W8>
 cudaError_t launch_slab_t(const KParams& p, int grid, cudaStream_t stream) {
     auto kern = coc_slab_kernel<OP, BF16, W8>;
@@ -683,7 +673,7 @@ cudaError_t launch_slab_t(const KParams& p, int grid, cudaStream_t stream) {
         attr[cfg.numAttrs].val.clusterDim.z = 1;
         ++cfg.numAttrs;
     }
-    if (slab_pdl()) {
+    if (pdl_launch()) {
         // may start its set-up while the previous kernel in the stream runs
         // (the kernel waits for it before touching global memory)
         attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
