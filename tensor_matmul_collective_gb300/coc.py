@@ -121,8 +121,16 @@ def _ptrs(ts) -> ctypes.Array:
     return arr
 
 
+# The current stream's handle without building a torch.cuda.Stream object
+# (a few microseconds per call on the host); the public query where this
+# PyTorch lacks the raw one.
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(stream) -> int:
     if stream is None:
+        if _raw_stream is not None:
+            return _raw_stream(torch.cuda.current_device())
         return torch.cuda.current_stream().cuda_stream
     if isinstance(stream, torch.cuda.Stream):
         return stream.cuda_stream
@@ -140,6 +148,14 @@ def _dtype_code(dt: torch.dtype) -> int:
 def _check_list(ts, name, shape, dtype, device):
     if not isinstance(ts, (list, tuple)) or len(ts) == 0:
         raise ValueError(f"{name} must be a non-empty list of tensors")
+    # one combined test per tensor; the checks below only word the error
+    shape = tuple(shape)
+    for t in ts:
+        if (not isinstance(t, torch.Tensor) or t.dtype is not dtype or t.shape != shape or t.device != device
+                or not t.is_contiguous()):
+            break
+    else:
+        return
     for i, t in enumerate(ts):
         if not isinstance(t, torch.Tensor):
             raise TypeError(f"{name}[{i}] is not a tensor")
