@@ -68,7 +68,7 @@ constexpr uint32_t kSlabStageBar = 3;             // named barrier of the set-up
 static_assert(kSlabMaxStages <= 32, "the producer's fill masks hold one bit per stage");
 
 __host__ __device__ constexpr uint32_t slab_bar_bytes(int stages, bool w8) {
-    return static_cast<uint32_t>(8 * (2 * stages + (w8 ? 2 * kSlabW8BStages : 0) + 7) + 16);
+    return static_cast<uint32_t>(8 * (2 * stages + (w8 ? 2 * kSlabW8BStages : 0) + 8) + 16);
 }
 // Reception area of a slab split over `split` CTAs: per other part, per row
 // quadrant holding output rows (a_rows / 32 rounded up), 32 rows of the (64
@@ -76,6 +76,12 @@ __host__ __device__ constexpr uint32_t slab_bar_bytes(int stages, bool w8) {
 __host__ __device__ constexpr uint32_t slab_recv_bytes(int boxes, int split, int a_rows) {
     return split > 1 ? static_cast<uint32_t>((split - 1) * ((a_rows + 31) / 32) * 32 * (64 * boxes / split) * 4) : 0u;
 }
+// Above 32 rows the reception area lies over the rings, which are idle once
+// every part's last MMA has completed (the parts wait for that before they
+// push): its room goes to more stages.  Measured, from 64 rows: bf16 m 128
+// 36.1 -> 30.9 us, w8A16 m 128 44.8 -> 39.2 us; at m 16 the wait for the
+// slowest part's mainloop cost more (0.2-1.1 us) than the extra stage gave.
+__host__ __device__ constexpr bool slab_recv_over_rings(int split, int a_rows) { return split > 1 && a_rows > 32; }
 
 // w8A16: bytes of one stage of the producer's ring: X of the stage (kps
 // k-blocks x a_rows rows x 128 bytes, first: 1 KiB aligned for the swizzle),
@@ -184,9 +190,15 @@ __global__ void __launch_bounds__(slab_threads(W8), 1) coc_slab_kernel(const __g
     uint8_t* a_st = smem;                                      // bf16: S x a_stage
     uint8_t* raw_st = smem;                                    // w8A16: S x raw_stage (X at the start)
     uint8_t* b_st = W8 ? raw_st + S * raw_stage : a_st + S * a_stage;   // S (w8A16: SB) x b_stage
-    uint8_t* stg = b_st + (W8 ? SB : S) * b_stage;             // 4 epilogue warps x 4 KiB
-    uint8_t* recv = stg + NUM_EPI_WARPS * EPI_BUF_BYTES;   // split: the other parts' sums of this CTA's columns
-    uint64_t* full = reinterpret_cast<uint64_t*>(recv + slab_recv_bytes(nb, csplit, a_rows));   // [S]
+    // split: the other parts' fp32 sums of this CTA's columns, after the
+    // staging buffers, or (over 32 rows) at the start of shared memory over
+    // the rings, once every part's last MMA has completed (ring_free)
+    const bool over_rings = slab_recv_over_rings(csplit, a_rows);
+    const uint32_t ring_bytes = W8 ? S * raw_stage + SB * b_stage : S * (a_stage + b_stage);
+    const uint32_t recv_bytes = slab_recv_bytes(nb, csplit, a_rows);
+    uint8_t* stg = smem + (over_rings && recv_bytes > ring_bytes ? recv_bytes : ring_bytes);   // 4 warps x 4 KiB
+    uint8_t* recv = over_rings ? smem : stg + NUM_EPI_WARPS * EPI_BUF_BYTES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(stg + NUM_EPI_WARPS * EPI_BUF_BYTES + (over_rings ? 0u : recv_bytes));   // [S]
     uint64_t* empty = full + S;                    // [S]  (w8A16: read by the stage's dequant warps and the MMA)
     uint64_t* bfull = empty + S;                   // [SB] w8A16: 16-bit B stage written (its dequant warps)
     uint64_t* bempty = bfull + SB;                 // [SB] w8A16: 16-bit B stage consumed by the MMA
@@ -195,7 +207,8 @@ __global__ void __launch_bounds__(slab_threads(W8), 1) coc_slab_kernel(const __g
     uint64_t* never = acce + 2;                    // [1] nothing arrives here (fault-injection test)
     uint64_t* drain = never + 1;                   // [1] MMA drain before TMEM release
     uint64_t* red_full = drain + 1;                // [1] split: every other part pushed its sums here
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red_full + 1);
+    uint64_t* ring_free = red_full + 1;            // [1] split: every part's rings are idle
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ring_free + 1);
     uint32_t* abort_word = tmem_slot + 1;
     const Ctl ctl{abort_word, p.status};
     const int nq = min(NUM_EPI_WARPS, (m + 31) / 32);   // epilogue warps holding output rows
@@ -220,6 +233,7 @@ __global__ void __launch_bounds__(slab_threads(W8), 1) coc_slab_kernel(const __g
         mbar_init(smem_u32(never), 1);
         mbar_init(smem_u32(drain), 1);
         mbar_init(smem_u32(red_full), csplit > 1 ? (csplit - 1) * nq : 1);
+        mbar_init(smem_u32(ring_free), csplit > 1 ? csplit : 1);
         *abort_word = 0u;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         fence_proxy_async_smem();
@@ -470,6 +484,18 @@ __global__ void __launch_bounds__(slab_threads(W8), 1) coc_slab_kernel(const __g
             if (!ok) break;
             tc_fence_after();
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(row0) << 16) + static_cast<uint32_t>(buf * W);
+            if (over_rings) {
+                // this CTA's rings are idle (a split slab is its only unit, and its
+                // last MMA has completed): tell every part, and push only once
+                // every part's rings are idle
+                if (warp == 2 && lane == 0)
+                    for (int j = 0; j < csplit; ++j)
+                        mbar_arrive_cluster(map_to_rank(smem_u32(ring_free), static_cast<uint32_t>(j)));
+                if (active) {
+                    ok = warp_wait<true>(smem_u32(ring_free), 0, ctl, 0x590u);
+                    if (!ok) break;
+                }
+            }
             if (active && csplit > 1) {
                 // push this part's sums of every other part's columns into that
                 // part's reception area (16-byte chunk c of a row at c ^ (row % 8))
@@ -715,9 +741,10 @@ int slab_smem_bytes(int stages, int a_rows, int boxes, int kps, int split, bool 
     const int b_stage = boxes * kps * static_cast<int>(kSlabBoxBytes);   // 16-bit B of a stage
     const int raw_stage = slab_raw_stage(kps, boxes, a_rows);             // w8A16: X, int8 W and its tables
     const int a_stage = kps * a_rows * 128;
-    return 1024 + (w8 ? stages * raw_stage + kSlabW8BStages * b_stage : stages * (a_stage + b_stage)) +
-           NUM_EPI_WARPS * EPI_BUF_BYTES + static_cast<int>(slab_recv_bytes(boxes, split, a_rows)) +
-           static_cast<int>(slab_bar_bytes(stages, w8));
+    const int rings = w8 ? stages * raw_stage + kSlabW8BStages * b_stage : stages * (a_stage + b_stage);
+    const int recv = static_cast<int>(slab_recv_bytes(boxes, split, a_rows));
+    const int area = slab_recv_over_rings(split, a_rows) ? (rings > recv ? rings : recv) : rings + recv;
+    return 1024 + area + NUM_EPI_WARPS * EPI_BUF_BYTES + static_cast<int>(slab_bar_bytes(stages, w8));
 }
 
 cudaError_t launch_slab(int op, bool bf16, bool w8, const KParams& p, int grid, cudaStream_t stream) {
