@@ -514,7 +514,7 @@ int64_t coc_debug_alloc_count(void);
  * (%globaltimer) it ran for to that slot of the device status buffer; -1
  * stops it.  coc_debug_clock_read waits for the device, returns a slot's two
  * sums and clears them: cycles / ns is the SM clock the kernels actually ran
- * at, which the driver's sampled clock does not show on a power-capped GPU.
+ * at, which a clock sampled through NVML does not show on a power-capped GPU.
  * (The allocation-free entry point never records.)
  */
 coc_status_t coc_debug_clock_probe(int slot);

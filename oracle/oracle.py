@@ -238,9 +238,9 @@ def dequant_w8a16_ex(wq, scale_bits, gran: int, group: int = 0, k_offset: int = 
     """Extended w8A16 weight of one rank: bits (in `dtype`) of RNE((q - z) * s).
 
     The zero point `zero` (int8, laid out like the scale; None = symmetric)
-    and the bfloat16 activation type are this build's reading of the
-    "antiquant offset" and "bf16 activation" extensions; the scale is in
-    `dtype` too.  With zero=None and dtype=F16 this is dequant_w8a16.
+    and the bfloat16 activation type are the plain reading of the pages'
+    antiquant-offset and bf16-activation extensions; the scale is in `dtype`
+    too.  With zero=None and dtype=F16 this is dequant_w8a16.
     """
     q = np.ascontiguousarray(wq, dtype=np.int8)
     s = _c16(scale_bits)
