@@ -187,14 +187,18 @@ int chunk_m_tiles(int64_t m, int chunks, int tile_m) {
 }
 
 // The 2-SM variant (a CTA pair per 256-row tile) is used once the output has
-// more than one 128-row tile.  COC_PAIR=0/1 forces a variant (tuning only).
+// more than one 128-row tile; the AllReduce and ReduceScatter keep single-CTA
+// tiles up to two of them (twice the tiles over the same SMs: the 8-rank
+// layer with n 8192, K 8 x 1024 at m 129-256 measured 45-46 us against 50-52
+// with pairs; from 384 rows pairs are faster).  COC_PAIR=0/1 forces a
+// variant (tuning only).
 bool use_pair(int op, int64_t m) {
-    (void)op;
     static const int forced = [] {
         const char* e = std::getenv("COC_PAIR");
         return e == nullptr ? -1 : (std::atoi(e) != 0 ? 1 : 0);
     }();
     if (forced >= 0) return forced == 1;
+    if ((op == OP_AR || op == OP_RS) && m <= 2 * BM) return false;
     return m > BM;
 }
 
