@@ -442,20 +442,27 @@ coc_status_t slab_row_parallel(int op, int R, int64_t m, int64_t n, int64_t ks, 
     p.a_box_rows = static_cast<int>((m + 7) / 8 * 8);
     const int kps = pl.kps, boxes = pl.boxes;
     // A split slab takes one cluster for its whole life (the parts' reception
-    // areas are not reused), so every slab needs a resident cluster; else
-    // the slabs run unsplit.
-    int split = pl.split, clusters = 0;
-    if (split > 1) {
+    // areas are not reused), so every slab needs a resident cluster: where
+    // the clusters of `split` CTAs do not all fit at once, smaller ones are
+    // taken (measured, 8 ranks, n 4864, K 8 x 2048, m 16: 38 slabs in
+    // clusters of 4, of which only 32 fit at once, ran unsplit in 65.6 us;
+    // in clusters of 2 they take 36.9 us).
+    int split = pl.split;
+    while (split > 1) {
         const int smem =
             slab_smem_bytes(slab_stages(p.a_box_rows, boxes, kps, split, w8), p.a_box_rows, boxes, kps, split, w8);
         const long long key = (static_cast<long long>(w8) << 41) | (static_cast<long long>(dt == COC_BF16) << 40) |
                               (static_cast<long long>(split) << 32) | smem;
-        std::lock_guard<std::mutex> lk(g_mu);
-        auto it = ds->slab_clusters.find(key);
-        if (it == ds->slab_clusters.end())
-            it = ds->slab_clusters.emplace(key, slab_max_clusters(dt == COC_BF16, w8, split, smem)).first;
-        clusters = it->second;
-        if (clusters < p.units) split = 1;
+        int clusters = 0;
+        {
+            std::lock_guard<std::mutex> lk(g_mu);
+            auto it = ds->slab_clusters.find(key);
+            if (it == ds->slab_clusters.end())
+                it = ds->slab_clusters.emplace(key, slab_max_clusters(dt == COC_BF16, w8, split, smem)).first;
+            clusters = it->second;
+        }
+        if (clusters >= p.units) break;
+        split /= 2;
     }
     p.slab_boxes = boxes;
     p.slab_kps = kps;
