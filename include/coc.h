@@ -180,13 +180,13 @@ typedef struct CUstream_st* coc_stream_t;
  * Decode-sized m (this call, coc_matmul_reduce_scatter, coc_matmul,
  * coc_fused_matmul's AllReduce / ReduceScatter, and the w8A16 AllReduce):
  * for m <= 128 a column-slab kernel streams the weights over all SMs in
- * slabs of 128 output columns (all m rows), each summed over the whole
- * contraction by one CTA (the same bits as one accumulator) or, while the
- * slabs fill at most half of the SMs, by a cluster of 2 or 4 CTAs that each
- * sum a fixed contiguous range of it and add the ranges in order.  Shapes
- * with too few slabs to fill half of the SMs take the rank split instead.
+ * slabs of 128 output columns (all m rows; w8A16 also 64 or 256), each
+ * summed over the whole contraction by one CTA (the same bits as one
+ * accumulator) or, while the slabs fill at most half of the SMs, by a
+ * cluster of 2 or 4 CTAs that each sum a fixed contiguous range of it and
+ * add the ranges in order.
  *
- * Rank split (the same operators except w8A16): for m <= 128 with at most
+ * Rank split (the same operators except w8A16, with COC_SLAB=0): for m <= 128 with at most
  * half as many 128 x 256 output tiles as the GPU has SMs,
  * each tile's R shards are cut into ksplit parts (the largest power of two
  * dividing R that keeps tiles x ksplit within one wave), each a work unit of

@@ -325,11 +325,11 @@ int rank_split(int op, int R, int64_t ks, int64_t tiles, bool pair, int sm_count
 // 64 columns, whose 128-byte rows moved 30% less per SM), two k-blocks per
 // stage (one TMA operation per 64-column group and one for X), and, while the
 // slabs fill at most half of the SMs, each slab's contraction split over a
-// cluster of 2 or 4 CTAs.  No plan (boxes 0) when the CTAs would fill less
-// than half of the SMs: the persistent kernel's rank split takes those
-// shapes.  Measured (8 ranks, K 8 x 1024, bf16, CUDA graph): n 8192 at m 16 /
-// 64 / 96 / 128 takes 27.0 / 27.7 / 30.0 / 37.1 us against 34.1 / 34.4 /
-// 37.0 / 41.5 us for the rank split.  COC_SLAB=0 turns the kernel off;
+// cluster of 2 or 4 CTAs.  Taken for every m <= 128, even where the CTAs fill
+// few SMs.  Measured (8 ranks, K 8 x 1024, bf16, CUDA graph): n 8192 at m 16
+// / 64 / 96 / 128 takes 27.0 / 27.7 / 30.0 / 37.1 us against 34.1 / 34.4 /
+// 37.0 / 41.5 us for the persistent kernel's rank split, and n 1024 / 2048 at
+// m 16 13.5 / 13.6 against 33.9 / 33.8 us.  COC_SLAB=0 turns the kernel off;
 // COC_SLAB=1 takes it whenever m <= 128, with COC_SLAB_BOXES, COC_SLAB_KPS
 // and COC_SLAB_SPLIT overriding the plan (tests and tuning only).
 struct SlabPlan {
@@ -369,7 +369,8 @@ SlabPlan slab_plan_for(int op, int R, int64_t m, int64_t n, int64_t ks, int sm_c
     while (split < max_split && slabs * split * 2 <= sm_count && split * 2 <= spu) split *= 2;
     const int fs = env_int("COC_SLAB_SPLIT", 0);
     if ((fs == 1 || fs == 2 || fs == 4) && fs <= max_split && fs <= spu) split = fs;
-    if (!forced && slabs * split * 2 < sm_count) return pl;
+    (void)forced;   // (slabs that fill few SMs still beat the persistent kernel's rank split:
+                    // 8 ranks, K 8 x 1024, m 16, n 1024 / 2048: 13.4 / 13.6 against 33.9 / 33.8 us)
     // two stages at least must fit in shared memory (w8A16 also holds the
     // 16-bit ring): fewer k-blocks per stage where they do not
     const int a_rows = static_cast<int>((m + 7) / 8 * 8);
@@ -389,20 +390,25 @@ SlabPlan slab_plan(int op, int R, int64_t m, int64_t n, int64_t ks, int sm_count
     const int env_boxes = env_int("COC_SLAB_BOXES", 0);
     const int env_kps = env_int("COC_SLAB_KPS", 0);
     if (op == OP_W8 && env_boxes == 0) {
-        // w8A16: up to 32 rows 256-column slabs (their int8 rows are read as
-        // 256-byte segments; measured fastest from 1 to 32 rows, 30.4 against
-        // 32.5 us at m 1 with fewer bytes in flight), else the schedule with
-        // the most int8 weight bytes in flight (ties: 128 columns; at m 64
-        // 34.6 against 36.9 us for 256 columns split four ways).  Every
-        // candidate keeps 16 KiB int8 boxes: smaller ones stream far slower.
+        // w8A16: the schedule with the most int8 weight bytes in flight over
+        // all its CTAs (stages x int8 stage bytes x CTAs at once, per round;
+        // ties: 128 columns), 256-column slabs counted a quarter more up to
+        // 32 rows (their int8 rows are read as 256-byte segments; measured
+        // fastest from 1 to 32 rows at n 8192, 30.4 against 32.5 us at m 1
+        // with fewer bytes in flight per CTA; at m 64 128 columns, 34.6
+        // against 36.9 us).  Every candidate keeps 16 KiB int8 boxes:
+        // smaller ones stream far slower.
         const int a_rows = static_cast<int>((m + 7) / 8 * 8);
         long long best = 0;
         for (const auto& c : {std::pair<int, int>{2, 2}, {4, 1}, {1, 4}}) {
             const SlabPlan cand = slab_plan_for(op, R, m, n, ks, sm_count, c.first, c.second, forced == 1);
             if (cand.boxes == 0 || cand.kps != c.second) continue;
             const int st = slab_stages(a_rows, cand.boxes, cand.kps, cand.split, true);
-            const long long score = static_cast<long long>(st) * cand.kps * 64 * 64 * cand.boxes *
-                                    ((cand.boxes == 4 && a_rows <= 32) ? 2 : 1);
+            // CTAs working at once, averaged over the rounds the units take
+            const long long units = (n + 64 * cand.boxes - 1) / (64 * cand.boxes) * cand.split;
+            const long long ctas = units / ((units + sm_count - 1) / sm_count);
+            const long long score = static_cast<long long>(st) * cand.kps * 64 * 64 * cand.boxes * ctas *
+                                    ((cand.boxes == 4 && a_rows <= 32) ? 5 : 4);
             if (score > best) {
                 best = score;
                 pl = cand;
