@@ -730,6 +730,33 @@ def time_context(ops, dev, bus=None, index=0):
         g: {"us_per_call": round(1e3 * r[g]["median_ms"] / 20, 1),
             "hbm_gbs": round(byts[g] / (1e3 * r[g]["median_ms"] / 20) / 1e3, 0)} for g in graphs}
     del keep, graphs
+    # AllGather-V2 on the LLaMA2-70B layer (n_shard 7168, k 8192: 940 MB of
+    # weights) at decode-sized m_shard 8 and 16 (column-slab kernel); bytes:
+    # W, X, the R products and the R gathered copies
+    graphs, keep, byts = {}, [], {}
+    for ms in (8, 16):
+        ag_ = wl.ColumnParallelSP(R=8, m_shard=ms, n_shard=7168, k=8192, dtype=torch.bfloat16, x_dist="normal(0,1)",
+                                  w_dist="normal(0,0.02)", seed=2)
+        axs, aws = ag_.make()
+        dax, daw = [x.to(dev) for x in axs], [w.to(dev) for w in aws]
+        m_ = 8 * ms
+        dout = [torch.empty(m_, 7168, dtype=torch.bfloat16, device=dev) for _ in range(8)]
+        dg = [torch.empty(m_, 8192, dtype=torch.bfloat16, device=dev) for _ in range(8)]
+        call = lambda dax=dax, daw=daw, dout=dout, dg=dg: coc.all_gather_matmul_v2(dax, daw, dout, dg)  # noqa: E731
+        call()
+        torch.cuda.synchronize()
+        gd = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gd):
+            for _ in range(20):
+                call()
+        graphs[str(ms)] = gd.replay
+        keep.append((gd, dax, daw, dout, dg))
+        byts[str(ms)] = 2 * (8 * 8192 * 7168 + m_ * 8192 + 8 * m_ * 7168 + 8 * m_ * 8192)
+    r = interleaved(graphs, it=10)
+    out["decode_ag_v2_r8_ns7168_k8192_cuda_graph"] = {
+        ms: {"us_per_call": round(1e3 * r[ms]["median_ms"] / 20, 1),
+             "hbm_gbs": round(byts[ms] / (1e3 * r[ms]["median_ms"] / 20) / 1e3, 0)} for ms in graphs}
+    del keep, graphs
     # the whole suite step captured once into a CUDA graph and replayed,
     # against the same step launched eagerly (the host's launch cost)
     try:

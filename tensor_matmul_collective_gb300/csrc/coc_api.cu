@@ -361,8 +361,10 @@ SlabPlan slab_plan_for(int op, int R, int64_t m, int64_t n, int64_t ks, int sm_c
     const int64_t kblocks = (ks + BK - 1) / BK;
     int kps = kps0 >= 4 ? 4 : kps0 >= 2 ? 2 : 1;
     while (kps > 1 && kblocks % kps != 0) kps /= 2;
-    const int64_t slabs = (n + 64 * boxes - 1) / (64 * boxes);
-    const int64_t spu = static_cast<int64_t>(R) * (kblocks / kps);   // stages per slab
+    // AllGather: R rank outputs of n columns, each slab's contraction the
+    // whole k; otherwise one output, each slab summed over the R shards
+    const int64_t slabs = (op == OP_AG ? R : 1) * ((n + 64 * boxes - 1) / (64 * boxes));
+    const int64_t spu = static_cast<int64_t>(op == OP_AG ? 1 : R) * (kblocks / kps);   // stages per slab
     int split = 1;
     // (each part finalises 64 boxes / split >= 32 columns and sums at least one stage)
     const int max_split = boxes == 1 ? 2 : 4;
@@ -384,7 +386,7 @@ SlabPlan slab_plan_for(int op, int R, int64_t m, int64_t n, int64_t ks, int sm_c
 
 SlabPlan slab_plan(int op, int R, int64_t m, int64_t n, int64_t ks, int sm_count) {
     SlabPlan pl;
-    if ((op != OP_AR && op != OP_RS && op != OP_W8) || ks <= 0 || m <= 0 || m > BM) return pl;
+    if ((op != OP_AR && op != OP_RS && op != OP_W8 && op != OP_AG) || ks <= 0 || m <= 0 || m > BM) return pl;
     const int forced = env_int("COC_SLAB", -1);
     if (forced == 0) return pl;
     const int env_boxes = env_int("COC_SLAB_BOXES", 0);
@@ -425,6 +427,31 @@ SlabPlan slab_plan(int op, int R, int64_t m, int64_t n, int64_t ks, int sm_count
     return slab_plan_for(op, R, m, n, ks, sm_count, boxes, kps, forced == 1);
 }
 
+// A split slab takes one cluster for its whole life (the parts' reception
+// areas are not reused), so every slab needs a resident cluster: where the
+// clusters of `split` CTAs do not all fit at once, smaller ones are taken
+// (measured, 8 ranks, n 4864, K 8 x 2048, m 16: 38 slabs in clusters of 4,
+// of which only 32 fit at once, ran unsplit in 65.6 us; in clusters of 2
+// they take 36.9 us).
+int slab_resident_split(DeviceState* ds, bool bf16, bool w8, int boxes, int kps, int a_rows, int split, int units) {
+    while (split > 1) {
+        const int smem = slab_smem_bytes(slab_stages(a_rows, boxes, kps, split, w8), a_rows, boxes, kps, split, w8);
+        const long long key = (static_cast<long long>(w8) << 41) | (static_cast<long long>(bf16) << 40) |
+                              (static_cast<long long>(split) << 32) | smem;
+        int clusters = 0;
+        {
+            std::lock_guard<std::mutex> lk(g_mu);
+            auto it = ds->slab_clusters.find(key);
+            if (it == ds->slab_clusters.end())
+                it = ds->slab_clusters.emplace(key, slab_max_clusters(bf16, w8, split, smem)).first;
+            clusters = it->second;
+        }
+        if (clusters >= units) break;
+        split /= 2;
+    }
+    return split;
+}
+
 // op OP_W8: the w8A16 AllReduce (int8 w, scales / zero points as for the
 // persistent kernel).
 coc_status_t slab_row_parallel(int op, int R, int64_t m, int64_t n, int64_t ks, const void* const* x,
@@ -447,29 +474,7 @@ coc_status_t slab_row_parallel(int op, int R, int64_t m, int64_t n, int64_t ks, 
     p.rows_per_rank = static_cast<int>(m / R);
     p.a_box_rows = static_cast<int>((m + 7) / 8 * 8);
     const int kps = pl.kps, boxes = pl.boxes;
-    // A split slab takes one cluster for its whole life (the parts' reception
-    // areas are not reused), so every slab needs a resident cluster: where
-    // the clusters of `split` CTAs do not all fit at once, smaller ones are
-    // taken (measured, 8 ranks, n 4864, K 8 x 2048, m 16: 38 slabs in
-    // clusters of 4, of which only 32 fit at once, ran unsplit in 65.6 us;
-    // in clusters of 2 they take 36.9 us).
-    int split = pl.split;
-    while (split > 1) {
-        const int smem =
-            slab_smem_bytes(slab_stages(p.a_box_rows, boxes, kps, split, w8), p.a_box_rows, boxes, kps, split, w8);
-        const long long key = (static_cast<long long>(w8) << 41) | (static_cast<long long>(dt == COC_BF16) << 40) |
-                              (static_cast<long long>(split) << 32) | smem;
-        int clusters = 0;
-        {
-            std::lock_guard<std::mutex> lk(g_mu);
-            auto it = ds->slab_clusters.find(key);
-            if (it == ds->slab_clusters.end())
-                it = ds->slab_clusters.emplace(key, slab_max_clusters(dt == COC_BF16, w8, split, smem)).first;
-            clusters = it->second;
-        }
-        if (clusters >= p.units) break;
-        split /= 2;
-    }
+    const int split = slab_resident_split(ds, dt == COC_BF16, w8, boxes, kps, p.a_box_rows, pl.split, p.units);
     p.slab_boxes = boxes;
     p.slab_kps = kps;
     p.slab_split = split;
@@ -952,6 +957,93 @@ COC_API coc_status_t coc_matmul_all_reduce_w8a16(int R, int64_t m, int64_t n, in
 namespace coc {
 namespace {
 
+// ALL_GATHER_MATMUL(_V2) through the column-slab kernel (gathered m = R
+// m_shard <= 128): first the gather kernel stacks the R shards of X into the
+// first non-NULL gathered output (V2) or, with none, into the call's
+// scratch; then the slab kernel reads A from that one m x k buffer (3-D
+// boxes when k % 64 == 0) and B from each rank's W (k x n_s, or w_nk n_s x
+// k), one unit per column slab of one rank's output, and copies the buffer
+// into V2's other gathered outputs.
+coc_status_t slab_all_gather(int R, int64_t ms, int64_t ns, int64_t k, const void* const* x, const void* const* w,
+                             void* const* out, void* const* gathered, coc_dtype_t dt, const SlabPlan& pl,
+                             DeviceState* ds, cudaStream_t stream, bool w_nk) {
+    KParams p;
+    std::memset(&p, 0, sizeof p);
+    const int64_t m = static_cast<int64_t>(R) * ms;
+    const int boxes = pl.boxes, kps = pl.kps;
+    p.R = R;
+    p.n_out = R;
+    p.m = static_cast<int>(m);
+    p.n = static_cast<int>(ns);
+    p.k = static_cast<int>(k);
+    p.num_kshards = 1;
+    p.kblocks = static_cast<int>((k + BK - 1) / BK);
+    p.m_tiles = 1;
+    p.n_tiles = static_cast<int>((ns + 64 * boxes - 1) / (64 * boxes));   // slabs per rank output
+    p.units = R * p.n_tiles;
+    p.rows_per_rank = static_cast<int>(ms);
+    p.a_box_rows = static_cast<int>(m);   // m_shard % 8 == 0
+    const int split = slab_resident_split(ds, dt == COC_BF16, false, boxes, kps, p.a_box_rows, pl.split, p.units);
+    p.slab_boxes = boxes;
+    p.slab_kps = kps;
+    p.slab_split = split;
+    p.slab_stages = slab_stages(p.a_box_rows, boxes, kps, split, false);
+    if (slab_smem_bytes(p.slab_stages, p.a_box_rows, boxes, kps, split, false) > kSlabSmemCap)
+        return fail(COC_ERR_SHAPE, "column-slab schedule does not fit in shared memory (m = %lld)", (long long)m);
+    p.b_kmajor = w_nk ? 1 : 0;
+
+    // the gathered X the slab kernel reads: V2's first gathered output, else scratch
+    AgGatherParams g;
+    std::memset(&g, 0, sizeof g);
+    g.R = R;
+    g.shard_vecs = ms * k / 8;
+    for (int r = 0; r < R; ++r) {
+        g.src[r] = static_cast<const uint16_t*>(x[r]);
+        uint16_t* d = gathered != nullptr ? static_cast<uint16_t*>(gathered[r]) : nullptr;
+        if (d != nullptr && g.dst == nullptr) {
+            g.dst = d;   // stacked by the gather kernel
+        } else if (d != nullptr) {
+            p.gdst[r] = d;   // copied from it by the slab kernel
+            p.has_gather = 1;
+        }
+    }
+    coc_status_t st;
+    Scratch sc;
+    if (g.dst == nullptr) {
+        if ((st = scratch_acquire(ds, stream, static_cast<size_t>(m) * k * 2, &sc)) != COC_OK) return st;
+        g.dst = static_cast<uint16_t*>(sc.ptr);
+    }
+    const void* xg = g.dst;
+    p.gsrc[0] = g.dst;
+    const CUtensorMapDataType tdt = tma_dtype(dt);
+    // 3-D maps (one A box per stage; n x k B likewise) where the k-blocks tile k exactly
+    bool a3d = kps > 1 && k % BK == 0;
+    if (a3d) a3d = encode_blocked(&p.tm_a[0], tdt, xg, BK, m, k / BK, k * 2, BK, m, kps) == CUDA_SUCCESS;
+    for (int r = 0; a3d && w_nk && r < R; ++r)
+        a3d = encode_blocked(&p.tm_b[r], tdt, w[r], BK, ns, k / BK, k * 2, BK, 64 * boxes, kps) == CUDA_SUCCESS;
+    p.slab_a3d = a3d ? 1 : 0;
+    st = a3d ? COC_OK : encode(&p.tm_a[0], tdt, xg, k, m, k * 2, BK, m, CU_TENSOR_MAP_SWIZZLE_128B);
+    for (int r = 0; st == COC_OK && r < R; ++r) {
+        if (w_nk && !a3d) st = encode(&p.tm_b[r], tdt, w[r], k, ns, k * 2, BK, 64 * boxes, CU_TENSOR_MAP_SWIZZLE_128B);
+        else if (!w_nk) st = encode(&p.tm_b[r], tdt, w[r], ns, k, ns * 2, 64, BK * kps, CU_TENSOR_MAP_SWIZZLE_128B);
+        p.outp[r] = static_cast<uint16_t*>(out[r]);
+    }
+    if (st == COC_OK) {
+        p.status = ds->status;
+        p.inject_timeout = g_inject.load();
+        p.clock_slot = g_clock_slot.load();
+        const int grid = split > 1 ? split * p.units : (p.units < ds->sm_count ? p.units : ds->sm_count);
+        cudaError_t e = launch_ag_gather(g, ds->sm_count, stream);
+        if (e != cudaSuccess) {
+            st = cuda_fail(e, "kernel launch (AllGather copy)");
+        } else {
+            e = launch_slab(OP_AG, dt == COC_BF16, false, p, grid, stream);
+            if (e != cudaSuccess) st = cuda_fail(e, "kernel launch (column slabs)");
+        }
+    }
+    return scratch_release(stream, sc, st);
+}
+
 coc_status_t all_gather(int R, int64_t ms, int64_t ns, int64_t k, const void* const* x, const void* const* w,
                         void* const* out, void* const* gathered, bool v2, coc_dtype_t dt, int chunks, int det,
                         cudaStream_t stream, bool w_nk = false) {
@@ -974,6 +1066,12 @@ coc_status_t all_gather(int R, int64_t ms, int64_t ns, int64_t k, const void* co
     if (v2 && ns == 0 && ms > 0) return fail(COC_ERR_SHAPE, "ALL_GATHER_MATMUL_V2 needs n_shard > 0");
     if (empty) return COC_OK;
 
+    DeviceState* ds = nullptr;
+    if ((st = device_state(&ds)) != COC_OK) return st;
+    if (k > 0) {
+        const SlabPlan pl = slab_plan(OP_AG, R, m, ns, k, ds->sm_count);
+        if (pl.boxes > 0) return slab_all_gather(R, ms, ns, k, x, w, out, v2 ? gathered : nullptr, dt, pl, ds, stream, w_nk);
+    }
     KParams p;
     std::memset(&p, 0, sizeof p);
     p.R = R;
@@ -1002,8 +1100,6 @@ coc_status_t all_gather(int R, int64_t ms, int64_t ns, int64_t k, const void* co
     p.b_hint = 0;
     p.group_mt = l2_group(p.chunk_mt, static_cast<int64_t>(tile_m) * k * 2);
 
-    DeviceState* ds = nullptr;
-    if ((st = device_state(&ds)) != COC_OK) return st;
     const CUtensorMapDataType tdt = tma_dtype(dt);
     for (int r = 0; r < R; ++r) {
         if (k > 0) {

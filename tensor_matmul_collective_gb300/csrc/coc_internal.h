@@ -196,7 +196,7 @@ cudaError_t launch(int op, bool bf16, bool pair, const KParams& p, int grid, cud
 // clusters that can be co-resident.
 cudaError_t launch_split(int op, bool bf16, const KParams& p, int grid, int cluster, cudaStream_t stream);
 
-// Column-slab kernel (coc_slab.cu), AllReduce and ReduceScatter at
+// Column-slab kernel (coc_slab.cu), AllReduce, ReduceScatter and AllGather at
 // decode-sized m: one unit per slab of 64 x slab_boxes output columns, all m
 // rows (m <= 128), the whole contraction in one CTA.  Launched with grid =
 // min(units, SMs), slab_smem_bytes of dynamic shared memory.  128-byte
@@ -205,7 +205,11 @@ cudaError_t launch_split(int op, bool bf16, const KParams& p, int grid, int clus
 // k x n storage: 64 x (slab_kps BK) boxes; n x k storage (b_kmajor): BK x
 // 64 slab_boxes boxes (2-D) or dims (BK, n, kblocks) with boxes (BK, 64
 // slab_boxes, slab_kps) (3-D, slab_a3d).  outp holds the n_out outputs
-// (AllReduce) or the R rank outputs (ReduceScatter).  With slab_split > 1
+// (AllReduce) or the R rank outputs (ReduceScatter, AllGather).  AllGather
+// (op OP_AG): num_kshards 1, n = n_shard, n_tiles slabs per rank output and
+// units R n_tiles, tm_a[0] over the gathered X (m = R m_shard rows, written
+// by launch_ag_gather first), tm_b[r] over rank r's W; V2 (has_gather): the
+// kernel copies that X (gsrc[0]) into every non-NULL gdst.  With slab_split > 1
 // the grid is slab_split x the slabs run at once, in clusters of
 // slab_split CTAs.
 // w8A16 (AllReduce, w8 true): the B maps are the int8 weights, boxed 64
@@ -223,6 +227,16 @@ int slab_stages(int a_rows, int boxes, int kps, int split, bool w8);    // most 
 int slab_smem_bytes(int stages, int a_rows, int boxes, int kps, int split, bool w8);
 cudaError_t launch_slab(int op, bool bf16, bool w8, const KParams& p, int grid, cudaStream_t stream);
 int slab_max_clusters(bool bf16, bool w8, int split, int smem);         // clusters of `split` resident at once
+// AllGather ahead of the column-slab kernel: dst (m x k) = the R shards
+// src[i] (m_shard x k each) stacked in rank order; shard_vecs = m_shard k / 8
+// (k % 8 == 0).
+struct AgGatherParams {
+    const uint16_t* src[COC_MAX_RANKS];
+    uint16_t* dst;
+    int R;
+    long long shard_vecs;
+};
+cudaError_t launch_ag_gather(const AgGatherParams& g, int sm_count, cudaStream_t stream);
 int max_split_clusters(int op, bool bf16, int cluster);
 // Co-resident CTA pairs the 2-SM variant can have on the current device.
 int max_pairs(int op, bool bf16);

@@ -1,6 +1,7 @@
-// Column-slab kernel: MATMUL_ALL_REDUCE and MATMUL_REDUCE_SCATTER at
-// decode-sized m (CoC page, 融合算子实现: the same two operators as the
-// persistent kernel, for the few-row activations of token generation).
+// Column-slab kernel: MATMUL_ALL_REDUCE, MATMUL_REDUCE_SCATTER and
+// ALL_GATHER_MATMUL(_V2) at decode-sized m (CoC page, 融合算子实现: the same
+// operators as the persistent kernel, for the few-row activations of token
+// generation).
 //
 // At m <= 128 (one row tile) the operator reads the R weight shards (R x
 // k_shard x n) once and does little arithmetic per weight byte, so its time
@@ -29,6 +30,18 @@
 //                  64 columns x kps * 64 k; n x k storage (K-major): per
 //                  k-block SN rows x 64 k, as one 3-D box for the stage when
 //                  k_shard % 64 == 0.
+//   AllGather      m = R m_shard gathered rows; a unit is one column slab
+//                  of one rank's output (R x n_shard / SN units), its
+//                  contraction the full k (no shard loop).  A is the gathered
+//                  X, stacked beforehand by coc_ag_gather_kernel into one
+//                  m x k buffer (V2's first gathered output, else the call's
+//                  scratch) and loaded like one AllReduce shard; B comes from
+//                  the unit's rank's W, and the slab is stored to that rank's
+//                  output only.  V2's other gathered copies are written from
+//                  that buffer by the epilogue warps while the first slab's
+//                  mainloop runs.  (Loading A as one box per source rank and
+//                  k-block instead measured 1.9x slower at 8 ranks: a CTA's
+//                  stream is bound by its TMA operations, about 80 ns each.)
 //   stages         as many as fit in shared memory (up to kSlabMaxStages).
 //   accumulator    two TMEM buffers of SN fp32 columns, so a CTA with a
 //                  second unit overlaps its epilogue with the next mainloop.
@@ -151,6 +164,34 @@ __device__ __forceinline__ void dequant_stage(const uint8_t* raw, uint8_t* bst, 
     }
 }
 
+// AllGather-V2: the gathered X (m x k at gsrc[0], stacked before the kernel)
+// into every non-NULL gdst.  Its 16-byte vectors are cut into `ctas`
+// contiguous slices, one per CTA, shared by the CTA's epilogue warps (wi of
+// NUM_EPI_WARPS) while the first slab's mainloop runs.
+__device__ __forceinline__ void slab_copy_gathered(const KParams& p, int cta, int ctas, int wi, int lane) {
+    const long long total = static_cast<long long>(p.m) * (p.k / 8);   // k % 8 == 0
+    const long long lo = total * cta / ctas, hi = total * (cta + 1) / ctas;
+    const long long a = lo + (hi - lo) * wi / NUM_EPI_WARPS, b = lo + (hi - lo) * (wi + 1) / NUM_EPI_WARPS;
+    const uint4* src = reinterpret_cast<const uint4*>(p.gsrc[0]);
+    for (long long v0 = a; v0 < b; v0 += 32 * 4) {
+        uint4 d[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const long long v = v0 + j * 32 + lane;
+            d[j] = v < b ? src[v] : make_uint4(0u, 0u, 0u, 0u);
+        }
+        for (int r = 0; r < p.R; ++r) {
+            uint4* dst = reinterpret_cast<uint4*>(p.gdst[r]);
+            if (dst == nullptr) continue;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const long long v = v0 + j * 32 + lane;
+                if (v < b) dst[v] = d[j];
+            }
+        }
+    }
+}
+
 template <int OP, bool BF16, bool W8>
 __global__ void __launch_bounds__(slab_threads(W8), 1) coc_slab_kernel(const __grid_constant__ KParams p) {
     constexpr int THREADS = slab_threads(W8);
@@ -166,8 +207,9 @@ __global__ void __launch_bounds__(slab_threads(W8), 1) coc_slab_kernel(const __g
     const int kps = p.slab_kps;           // k-blocks per stage (divides kblocks)
     const int csplit = p.slab_split;      // CTAs (one cluster) per slab
     const int a_rows = p.a_box_rows;
-    const int R = p.num_kshards;
+    const int R = p.num_kshards;          // shards summed per slab (AllGather: 1)
     const int kblocks = p.kblocks;
+    const int spr = p.n_tiles;            // AllGather: slabs per rank output
     const int units = p.units;
     const int m = p.m, n = p.n;
     const uint32_t a_kb = static_cast<uint32_t>(a_rows) * 128u;                 // A bytes per k-block
@@ -213,8 +255,8 @@ __global__ void __launch_bounds__(slab_threads(W8), 1) coc_slab_kernel(const __g
     const Ctl ctl{abort_word, p.status};
     const int nq = min(NUM_EPI_WARPS, (m + 31) / 32);   // epilogue warps holding output rows
 
-    if (warp == 0 && lane < R && lane < COC_MAX_RANKS) {
-        prefetch_tmap(&p.tm_a[lane]);
+    if (warp == 0 && lane < p.R && lane < COC_MAX_RANKS) {
+        if (lane < R) prefetch_tmap(&p.tm_a[lane]);   // (AllGather: one A map)
         prefetch_tmap(&p.tm_b[lane]);
     }
     if (threadIdx.x == 0) {
@@ -292,7 +334,8 @@ __global__ void __launch_bounds__(slab_threads(W8), 1) coc_slab_kernel(const __g
         uint32_t stage = 0, phase = 0, filled = 0, fill_parity = 0;
         bool ok = true;
         for (int u = first_u; ok && u < units; u += u_step) {
-            const int col0 = u * W;
+            const int ur = OP == OP_AG ? u / spr : 0;   // AllGather: the rank whose W and output
+            const int col0 = (u - ur * spr) * W;
             for (int s = st_lo; s < st_hi; ++s) {
                 const int ks = s / spk;
                 const int kb = (s - ks * spk) * kps;
@@ -300,7 +343,7 @@ __global__ void __launch_bounds__(slab_threads(W8), 1) coc_slab_kernel(const __g
                 if (!ok) break;
                 if (lane == 0) {
                     const CUtensorMap* am = &p.tm_a[ks];
-                    const CUtensorMap* bm = &p.tm_b[ks];
+                    const CUtensorMap* bm = &p.tm_b[OP == OP_AG ? ur : ks];
                     const uint32_t fb = smem_u32(&full[stage]);
                     // w8A16 per-group: the int8 box plus the in-range columns of the
                     // scale and zero-point rows of the stage's k-blocks (measured:
@@ -427,7 +470,7 @@ __global__ void __launch_bounds__(slab_threads(W8), 1) coc_slab_kernel(const __g
         // chunk j at j ^ (row / 2 % 4)), read back so that lane l holds chunk
         // l % 4 of rows l / 4 + 8 i, then 16-byte stores to every rank output
         // (AllReduce) or to the rank owning the row (ReduceScatter).
-        auto emit32 = [&](int col, const uint32_t (&v)[32]) {
+        auto emit32 = [&](int col, int ur, const uint32_t (&v)[32]) {
             uint8_t* rowp = buf_s + lane * 64;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -459,7 +502,9 @@ __global__ void __launch_bounds__(slab_threads(W8), 1) coc_slab_kernel(const __g
                     }
                 }
             } else {
-                for (int o = 0; o < n_out; ++o) {
+                // AllReduce: every rank output; AllGather: rank ur's
+                const int o0 = OP == OP_AG ? ur : 0, o1 = OP == OP_AG ? ur + 1 : n_out;
+                for (int o = o0; o < o1; ++o) {
                     uint16_t* base = p.outp[o] + c;
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
@@ -477,6 +522,10 @@ __global__ void __launch_bounds__(slab_threads(W8), 1) coc_slab_kernel(const __g
         };
         int acc_i = 0;
         bool ok = true;
+        if constexpr (OP == OP_AG) {
+            // AllGather-V2: this CTA's slice of the other gathered copies
+            if (p.has_gather) slab_copy_gathered(p, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), warp - 2, lane);
+        }
         if (p.inject_timeout) ok = warp_wait(smem_u32(never), 0, ctl, 0x560u);
         for (int u = first_u; ok && u < units; u += u_step) {
             const int buf = acc_i & 1;
@@ -540,7 +589,8 @@ __global__ void __launch_bounds__(slab_threads(W8), 1) coc_slab_kernel(const __g
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_u32(&acce[buf]));
                 }
-                const int col = u * W + static_cast<int>(part) * ow + cc;
+                const int ur = OP == OP_AG ? u / spr : 0;
+                const int col = (u - ur * spr) * W + static_cast<int>(part) * ow + cc;
                 if (!active || col >= n) continue;
                 if (csplit > 1) {
                     uint32_t own[32];
@@ -567,7 +617,7 @@ __global__ void __launch_bounds__(slab_threads(W8), 1) coc_slab_kernel(const __g
                             v[i] = sp == 0 ? w[i] : __float_as_uint(__uint_as_float(v[i]) + __uint_as_float(w[i]));
                     }
                 }
-                emit32(col, v);
+                emit32(col, ur, v);
             }
             ++acc_i;
         }
@@ -671,6 +721,25 @@ __global__ void __launch_bounds__(slab_threads(W8), 1) coc_slab_kernel(const __g
     }
 }
 
+// AllGather ahead of the column-slab kernel: the R shards' m_shard rows of k
+// 16-bit values, stacked in rank order into dst (the slab kernel's A: V2's
+// first gathered output, or the call's scratch).  One 16-byte vector per
+// thread and grid-stride step.  A programmatic launch like the slab kernel:
+// it waits for the previous kernel before reading X, and lets the slab kernel
+// start its set-up at once (the slab kernel waits for this one to complete
+// before its first load).
+__global__ void __launch_bounds__(256) coc_ag_gather_kernel(const __grid_constant__ AgGatherParams g) {
+    grid_dependency_wait();
+    grid_dependents_launch();
+    const long long total = g.shard_vecs * g.R;
+    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+    uint4* dst = reinterpret_cast<uint4*>(g.dst);
+    for (long long v = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; v < total; v += stride) {
+        const long long sh = v / g.shard_vecs;   // the source rank of this row
+        dst[v] = __ldg(reinterpret_cast<const uint4*>(g.src[sh]) + (v - sh * g.shard_vecs));
+    }
+}
+
 constexpr int kMaxDevices = 64;
 
 template <int OP, bool BF16, bool W8>
@@ -759,8 +828,30 @@ cudaError_t launch_slab(int op, bool bf16, bool w8, const KParams& p, int grid, 
         case OP_RS:
             return bf16 ? launch_slab_t<OP_RS, true, false>(p, grid, stream)
                         : launch_slab_t<OP_RS, false, false>(p, grid, stream);
+        case OP_AG:
+            return bf16 ? launch_slab_t<OP_AG, true, false>(p, grid, stream)
+                        : launch_slab_t<OP_AG, false, false>(p, grid, stream);
         default: return cudaErrorInvalidValue;
     }
+}
+
+cudaError_t launch_ag_gather(const AgGatherParams& g, int sm_count, cudaStream_t stream) {
+    const long long total = g.shard_vecs * g.R;
+    long long blocks = (total + 255) / 256;
+    if (blocks > 8LL * sm_count) blocks = 8LL * sm_count;
+    if (blocks < 1) blocks = 1;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    if (pdl_launch()) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, coc_ag_gather_kernel, g);
 }
 
 int slab_max_clusters(bool bf16, bool w8, int split, int smem) {

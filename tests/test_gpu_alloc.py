@@ -2,9 +2,9 @@
 
 The operators own no per-call memory: the status block is created by the
 first call on a device, and the scratch some calls need (the rank-split fp32
-parts, the MoE routing tables, the w8A16 pre-pass weight) lives in a
-workspace the library keeps per stream, sized by the first call that needs
-it.  The library counts every device allocation it makes
+parts, the MoE routing tables, the w8A16 pre-pass weight, the stacked X of a
+decode-sized AllGather) lives in a workspace the library keeps per stream,
+sized by the first call that needs it.  The library counts every device allocation it makes
 (coc_debug_alloc_count); after one warm-up call of every operator, further
 calls of the same shapes on the same stream must leave the count unchanged,
 and so must replays of a CUDA graph that captured them."""
@@ -82,6 +82,14 @@ def _calls():
     agg = [torch.empty(256, 192, dtype=BF16, device=DEV) for _ in range(4)]
     calls["ag"] = lambda: coc.all_gather_matmul(ax, aw, ago)
     calls["ag_v2"] = lambda: coc.all_gather_matmul_v2(ax, aw, ago, agg)
+    # decode-sized AllGather (column-slab kernel): V1 stacks X in the stream's workspace
+    s8 = wl.ColumnParallelSP(R=8, m_shard=8, n_shard=1024, k=512, dtype=BF16, x_dist="uniform[-1,1]",
+                             w_dist="uniform[-1,1]", seed=6)
+    dx8, dw8 = map(to_dev, s8.make())
+    do8 = [torch.empty(64, 1024, dtype=BF16, device=DEV) for _ in range(8)]
+    dg8 = [torch.empty(64, 512, dtype=BF16, device=DEV) for _ in range(8)]
+    calls["ag_slab"] = lambda: coc.all_gather_matmul(dx8, dw8, do8)
+    calls["ag_slab_v2"] = lambda: coc.all_gather_matmul_v2(dx8, dw8, do8, dg8)
     dws = [torch.empty(264, 192, dtype=BF16, device=DEV) for _ in range(4)]
     calls["wgrad"] = lambda: coc.weight_grad(ago, agg, dws)
     # w8A16: the schedules without scratch (in-kernel dequantisation to shared
@@ -157,12 +165,14 @@ def test_graph_replays_allocate_nothing():
     calls = _calls()
     calls["ar_split"]()
     calls["w8_prepass"]()
+    calls["ag_slab"]()
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
         calls["ar_split"]()
         calls["w8_prepass"]()
         calls["moe"]()
+        calls["ag_slab"]()
     n0 = coc.alloc_count()
     for _ in range(5):
         g.replay()

@@ -3,8 +3,10 @@
 Every fused operator writes R rank buffers, and several of its store paths
 compute their addresses by hand instead of going through a bounds-clipped TMA
 store: the AllReduce replica stores, the rank-split slab stores, the
-column-slab kernel's stores, the ALL_GATHER_MATMUL_V2 gather copy, the MoE token permute and combine scatter,
-and the w8A16 and allocation-free AllReduce paths.  A store that runs past a
+column-slab kernel's stores (AllReduce, ReduceScatter and AllGather), the
+ALL_GATHER_MATMUL_V2 gather copies (persistent and column-slab kernels), the
+MoE token permute and combine scatter, and the w8A16 and allocation-free
+AllReduce paths.  A store that runs past a
 buffer would land in the next rank's buffer, which only an element-wise
 check of that row would notice.
 
@@ -221,6 +223,45 @@ def test_all_gather_v2_guards(R, ms, ns, k, dt, chunks):
         Slab.assert_written(outs[r], f"AG-V2 product rank {r}")
         assert np.array_equal(wl.bits16(gathered[r].cpu()), xg), f"gather copy rank {r}"
         assert_close(outs[r], orc.all_gather_matmul(CODE[dt], bx, bw, r), k, f"AG-V2 rank {r}")
+
+
+# The column-slab kernel's AllGather (gathered m <= 128): plain 16-byte stores
+# of each slab to its rank's output, the gathered copies from the epilogue
+# warps, ragged last slab and k, clusters of 2 and 4.
+AG_SLAB_CASES = [
+    # R, m_shard, n_shard, k, dtype, (boxes, split, kps)
+    (8, 8, 1000, 200, BF16, (2, 2, 1)),
+    (4, 24, 520, 128, F16, (1, 2, 2)),
+    (2, 64, 1104, 512, BF16, (2, 4, 1)),
+    (8, 16, 136, 72, F16, (2, 1, 1)),
+]
+
+
+@pytest.mark.parametrize("R,ms,ns,k,dt,plan", AG_SLAB_CASES)
+def test_all_gather_v2_column_slab_guards(R, ms, ns, k, dt, plan, monkeypatch):
+    b, sp, kps = plan
+    for key, v in (("COC_SLAB", 1), ("COC_SLAB_BOXES", b), ("COC_SLAB_SPLIT", sp), ("COC_SLAB_KPS", kps)):
+        monkeypatch.setenv(key, str(v))
+    s = wl.ColumnParallelSP(R=R, m_shard=ms, n_shard=ns, k=k, dtype=dt, x_dist="uniform[-1,1]",
+                            w_dist="uniform[-1,1]", seed=760 + ms)
+    xs, ws = s.make()
+    m = R * ms
+    slab = Slab([(m, ns)] * R + [(m, k)] * R, [dt] * (2 * R))
+    outs, gathered = slab.views[:R], slab.views[R:]
+    g = [t if r % 3 != 1 else None for r, t in enumerate(gathered)]   # some copies skipped
+    coc.all_gather_matmul_v2(to_dev(xs), to_dev(ws), outs, g)
+    coc.sync_status()
+    slab.check_guards("AllGather-V2 column slab")
+    bx, bw = bits(xs), bits(ws)
+    xg = orc.all_gather(bx)
+    for r in range(R):
+        Slab.assert_written(outs[r], f"AG-V2 column slab product rank {r}")
+        assert_close(outs[r], orc.all_gather_matmul(CODE[dt], bx, bw, r), k, f"AG-V2 column slab rank {r}")
+        raw = gathered[r].view(torch.int16).cpu().numpy().view(np.uint16)
+        if g[r] is None:
+            assert np.all(raw == CANARY), f"skipped gather buffer {r} was written"
+        else:
+            assert np.array_equal(raw, xg), f"gather copy rank {r}"
 
 
 def test_all_gather_v2_skipped_copies_leave_buffers_alone():
