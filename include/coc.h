@@ -103,7 +103,8 @@
  *     column-slab kernel), COC_KSPLIT=<n> (rank-split part count, rounded
  *     down to a power of two dividing R), COC_SPLIT_PATH=scratch (rank split
  *     through global memory), COC_SLAB=0|1 (column-slab kernel off / for
- *     every m <= 128) with COC_SLAB_BOXES=1|2 (w8A16 also 4),
+ *     every m <= 128; AllGather: gathered m) with COC_SLAB_BOXES=1|2
+ *     (w8A16 also 4),
  *     COC_SLAB_SPLIT=1|2|4 and COC_SLAB_KPS=1|2|4 (its slab width in
  *     64-column groups, CTAs per slab, k-blocks per stage; 256-column slabs
  *     take one k-block per stage), COC_PDL=0 (the kernels launched in
@@ -231,6 +232,14 @@ coc_status_t coc_matmul_reduce_scatter(int R, int64_t m, int64_t n, int64_t k_sh
  *          gathered rows.  k % 8 == 0, n_shard % 8 == 0.
  * `deterministic` is accepted; there is no cross-rank sum, so results are
  * always reproducible.
+ * Decode-sized m (R*m_shard <= 128, this call, the V2 call and
+ * coc_fused_matmul's AllGather forms): the column-slab kernel takes one unit
+ * per 128-column slab of one rank's output, after a copy kernel has stacked
+ * Xg once (into the first non-NULL gathered output for V2, else into the
+ * call's scratch: the stream's workspace, or a stream-ordered allocation
+ * while the stream is being captured).  Each slab is one accumulator over k
+ * (the persistent kernel's bits) or, in clusters of 2 or 4 CTAs, fixed
+ * contiguous k ranges added in order.
  */
 coc_status_t coc_all_gather_matmul(int R, int64_t m_shard, int64_t n_shard, int64_t k,
                                    const void* const* x, const void* const* w,
