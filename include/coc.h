@@ -45,7 +45,8 @@
  * so every tile's reduce/scatter/gather epilogue runs while the next tile's
  * mainloop runs.  The result never depends on `chunks`.
  *
- * Deterministic mode (same section: "及其确定性计算").  Every call is
+ * Deterministic mode (same section, which lists a deterministic form of the
+ * AllReduce and of the ReduceScatter operator).  Every call is
  * bitwise reproducible for identical inputs on the same GPU and library
  * build, across runs and across chunk counts: each output element is
  * accumulated in fp32 in the fixed order rank 0..R-1, k ascending, and
@@ -248,8 +249,8 @@ coc_status_t coc_all_gather_matmul(int R, int64_t m_shard, int64_t n_shard, int6
 
 /*
  * ALL_GATHER_MATMUL_V2 — as coc_all_gather_matmul, and the AllGather
- * intermediate is also returned (CoC page, 融合算子实现, third bullet: "V2
- * supports obtaining the ALL_GATHER intermediate result").
+ * intermediate is also returned (CoC page, 融合算子实现, third bullet: the V2
+ * form hands the gathered input back to the caller as well).
  *
  * gathered[r]  (R*m_shard) x k, row pitch k: receives a bit-exact copy of Xg.
  *              Entries may be NULL to skip that rank's copy; `gathered`
@@ -264,8 +265,8 @@ coc_status_t coc_all_gather_matmul_v2(int R, int64_t m_shard, int64_t n_shard, i
 
 /*
  * w8A16 MATMUL_ALL_REDUCE — fp16 activations, int8 weights dequantised in the
- * kernel (CoC page, 融合算子实现, last bullet: "pseudo-quantisation, fp16,
- * per tensor / per channel / per group").
+ * kernel (CoC page, 融合算子实现, last bullet: fake-quantised int8 weights
+ * with fp16 activations, scaled per tensor, per channel or per group).
  *
  *   Wd_r[t, j] = fp16_rne( float(Wq_r[t, j]) * s_r(t, j) )   (exact product, one rounding)
  *   Y = sum_r X_r @ Wd_r;  out[r] = fp16_rne(Y) for every r

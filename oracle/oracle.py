@@ -201,7 +201,7 @@ def all_gather_matmul(dtype: int, xs, ws, rank: int, rows=None, nthreads=None) -
 
 def all_gather_matmul_v2(dtype: int, xs, ws, rank: int, rows=None, nthreads=None):
     """ALL_GATHER_MATMUL_V2: as ALL_GATHER_MATMUL, and the AllGather result is
-    also returned ("supports obtaining the ALL_GATHER intermediate result").
+    also returned (the V2 form gives the caller the gathered input as well).
     Returns (out_rank[rows], gathered bits)."""
     return all_gather_matmul(dtype, xs, ws, rank, rows, nthreads), all_gather(xs)
 

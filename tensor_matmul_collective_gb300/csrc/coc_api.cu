@@ -1069,8 +1069,13 @@ coc_status_t all_gather(int R, int64_t ms, int64_t ns, int64_t k, const void* co
     DeviceState* ds = nullptr;
     if ((st = device_state(&ds)) != COC_OK) return st;
     if (k > 0) {
+        // (the stacked X goes to V2's first kept copy, else to scratch, which
+        // must fit under the workspace cap)
+        bool kept = false;
+        for (int r = 0; v2 && r < R; ++r) kept = kept || gathered[r] != nullptr;
         const SlabPlan pl = slab_plan(OP_AG, R, m, ns, k, ds->sm_count);
-        if (pl.boxes > 0) return slab_all_gather(R, ms, ns, k, x, w, out, v2 ? gathered : nullptr, dt, pl, ds, stream, w_nk);
+        if (pl.boxes > 0 && (kept || static_cast<size_t>(m) * static_cast<size_t>(k) * 2 <= kWorkspaceCap))
+            return slab_all_gather(R, ms, ns, k, x, w, out, v2 ? gathered : nullptr, dt, pl, ds, stream, w_nk);
     }
     KParams p;
     std::memset(&p, 0, sizeof p);

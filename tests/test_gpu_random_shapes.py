@@ -166,6 +166,44 @@ def test_random_column_slab(seed, monkeypatch):
         assert torch.equal(torch.cat(rs, 0), ar[0]), what + " concat(RS) != AR"
 
 
+@pytest.mark.parametrize("seed", range(24))
+def test_random_ag_column_slab(seed, monkeypatch):
+    """AllGather and AllGather-V2 at decode-sized gathered m through the
+    column-slab kernel with a random schedule: m_shard a multiple of 8 with
+    R m_shard <= 128, ragged n_shard and k, k x n or n x k weights, V2 with
+    random skipped copies (A then read from the first kept copy, or from
+    scratch when none is kept)."""
+    rng = random.Random(6000 + seed)
+    R = rng.choice([1, 2, 4, 8])
+    ms = 8 * rng.randint(1, 16 // R)
+    ns = 8 * rng.randint(1, 800)                     # up to 6400 columns
+    k = 8 * rng.randint(1, 256)                      # up to 2048
+    plan = (rng.choice([1, 2]), rng.choice([1, 2, 4]), rng.choice([1, 2, 4]))
+    for key, v in zip(("COC_SLAB", "COC_SLAB_BOXES", "COC_SLAB_SPLIT", "COC_SLAB_KPS"), (1,) + plan):
+        monkeypatch.setenv(key, str(v))
+    dt = rng.choice([F16, BF16])
+    nk = rng.random() < 0.3
+    v2 = rng.random() < 0.6
+    what = f"AG R={R} ms={ms} ns={ns} k={k} {dt} plan={plan} nk={nk} v2={v2}"
+    xs, ws = wl.ColumnParallelSP(R=R, m_shard=ms, n_shard=ns, k=k, dtype=dt, x_dist="normal(0,1)",
+                                 w_dist="normal(0,0.02)", seed=seed).make()
+    dx, dw = to_dev(xs), to_dev(ws)
+    m = R * ms
+    keep = [rng.random() < 0.6 for _ in range(R)]
+    gath = [torch.full((m, k), 5.0, dtype=dt, device=dx[0].device) if kk else None for kk in keep]
+    op = "all_gather_v2" if v2 else "all_gather"
+    wl_ = [w.t().contiguous() for w in dw] if nk else dw
+    res = coc.fused_matmul(op, dx, wl_, w_layout="nk" if nk else "kn", gathered=gath if v2 else None)
+    outs = res[0] if v2 else res
+    coc.sync_status()
+    bx, bw = bits(xs), bits(ws)
+    xg = orc.all_gather(bx)
+    for r in range(R):
+        assert_close(outs[r], orc.all_gather_matmul(CODE[dt], bx, bw, r), k, f"{what} rank {r}")
+        if v2 and keep[r]:
+            assert np.array_equal(wl.bits16(gath[r].cpu()), xg), f"{what} gathered copy {r}"
+
+
 @pytest.mark.parametrize("seed", range(16))
 def test_random_moe(seed):
     """MoE dispatch + GroupedMatMul + combine: top-1 through the fused combine,
