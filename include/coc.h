@@ -233,6 +233,9 @@ coc_status_t coc_matmul_reduce_scatter(int R, int64_t m, int64_t n, int64_t k_sh
  *          gathered rows.  k % 8 == 0, n_shard % 8 == 0.
  * `deterministic` is accepted; there is no cross-rank sum, so results are
  * always reproducible.
+ * Where m_shard is not a multiple of 128, Xg is first stacked by a copy
+ * kernel (into the first non-NULL gathered output for V2, else into the
+ * call's scratch, which the persistent kernel then reads as one operand).
  * Decode-sized m (R*m_shard <= 128, this call, the V2 call and
  * coc_fused_matmul's AllGather forms): the column-slab kernel takes one unit
  * per 128-column slab of one rank's output, after a copy kernel has stacked

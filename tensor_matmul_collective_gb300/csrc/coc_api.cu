@@ -199,6 +199,16 @@ bool use_pair(int op, int64_t m) {
     }();
     if (forced >= 0) return forced == 1;
     if ((op == OP_AR || op == OP_RS) && m <= 2 * BM) return false;
+    if (op == OP_AG && m > 2 * BM) {
+        // 256-row pair tiles run about 15% faster per tile than 128-row
+        // single-CTA tiles, but where the last pair tile is at most half full
+        // and there are few row tiles, the single-CTA tiles take clearly fewer
+        // rounds: m in (256, 384] and (512, 640].  Measured (8 ranks, n_shard
+        // 7168, k 8192): m 384 266 against 296 us, m 640 404 against 447; m
+        // 512 / 768 / 1280 take pairs (275 / 397 / 650 against 319 / 455 / 743).
+        const int64_t mt_pair = (m + 2 * BM - 1) / (2 * BM), mt_single = (m + BM - 1) / BM;
+        return 10 * mt_single >= 17 * mt_pair;
+    }
     return m > BM;
 }
 
@@ -1105,20 +1115,60 @@ coc_status_t all_gather(int R, int64_t ms, int64_t ns, int64_t k, const void* co
     p.b_hint = 0;
     p.group_mt = l2_group(p.chunk_mt, static_cast<int64_t>(tile_m) * k * 2);
 
+    // Shards that do not fill whole 128-row boxes would need several A boxes
+    // per tile and k-block (one per shard piece, down to 8 rows), and a CTA's
+    // operand stream is bound by its TMA operations: stack X once instead
+    // (into V2's first kept copy, else into scratch under the workspace cap)
+    // and read it as one shard of m rows (measured, 8 ranks, n_shard 7168, k
+    // 8192: m_shard 24 / 48 took 738 / 847 us with 8 / 16-row boxes).
     const CUtensorMapDataType tdt = tma_dtype(dt);
-    for (int r = 0; r < R; ++r) {
+    AgGatherParams g;
+    std::memset(&g, 0, sizeof g);
+    Scratch sc;
+    if (k > 0 && p.a_box_rows < BM) {
+        g.R = R;
+        g.shard_vecs = ms * k / 8;
+        for (int r = 0; r < R; ++r) {
+            g.src[r] = static_cast<const uint16_t*>(x[r]);
+            if (v2 && g.dst == nullptr && gathered[r] != nullptr) g.dst = static_cast<uint16_t*>(gathered[r]);
+        }
+        if (g.dst == nullptr && static_cast<size_t>(m) * static_cast<size_t>(k) * 2 <= kWorkspaceCap) {
+            if ((st = scratch_acquire(ds, stream, static_cast<size_t>(m) * k * 2, &sc)) != COC_OK) return st;
+            g.dst = static_cast<uint16_t*>(sc.ptr);
+        }
+    }
+    const bool stacked = g.dst != nullptr;
+    if (stacked) {
+        // one shard covering every tile's rows, so that the kernel's shard
+        // index (row / rows_per_rank) is 0 for all of them, also for the
+        // rows of a ragged last tile past m (zero-filled); every map entry
+        // holds the stacked map all the same
+        p.rows_per_rank = p.m_tiles * tile_m;
+        p.a_box_rows = BM;
+        st = encode(&p.tm_a[0], tdt, g.dst, k, m, k * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B);
+        for (int r = 1; r < R; ++r) p.tm_a[r] = p.tm_a[0];
+        p.gsrc[0] = g.dst;
+    }
+    for (int r = 0; st == COC_OK && r < R; ++r) {
         if (k > 0) {
-            if ((st = encode(&p.tm_a[r], tdt, x[r], k, ms, k * 2, BK, p.a_box_rows, CU_TENSOR_MAP_SWIZZLE_128B)) != COC_OK) return st;
+            if (!stacked && (st = encode(&p.tm_a[r], tdt, x[r], k, ms, k * 2, BK, p.a_box_rows, CU_TENSOR_MAP_SWIZZLE_128B)) != COC_OK)
+                break;
             st = w_nk ? encode(&p.tm_b[r], tdt, w[r], k, ns, k * 2, BK, pair ? BN / 2 : BN, CU_TENSOR_MAP_SWIZZLE_128B)
                       : encode(&p.tm_b[r], tdt, w[r], ns, k, ns * 2, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B);
-            if (st != COC_OK) return st;
+            if (st != COC_OK) break;
         }
         if ((st = encode(&p.tm_out[r], tdt, out[r], ns, m, ns * 2, EPI_COLS, p.store_rows, CU_TENSOR_MAP_SWIZZLE_128B)) != COC_OK)
-            return st;
-        p.gsrc[r] = static_cast<const uint16_t*>(x[r]);
-        p.gdst[r] = v2 ? static_cast<uint16_t*>(gathered[r]) : nullptr;
+            break;
+        if (!stacked) p.gsrc[r] = static_cast<const uint16_t*>(x[r]);
+        // (the stacking kernel already wrote the copy it stacked into)
+        p.gdst[r] = v2 && gathered[r] != g.dst ? static_cast<uint16_t*>(gathered[r]) : nullptr;
     }
-    return launch_checked(OP_AG, dt == COC_BF16, pair, p, ds, stream);
+    if (st == COC_OK && stacked) {
+        const cudaError_t e = launch_ag_gather(g, ds->sm_count, stream);
+        if (e != cudaSuccess) st = cuda_fail(e, "kernel launch (AllGather copy)");
+    }
+    if (st == COC_OK) st = launch_checked(OP_AG, dt == COC_BF16, pair, p, ds, stream);
+    return scratch_release(stream, sc, st);
 }
 
 }  // namespace

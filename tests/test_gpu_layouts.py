@@ -4,8 +4,9 @@ A Megatron linear layer keeps W as [out_features, in_features] (n x k), so
 its forward pass is X @ W^T (COC_W_NK) and its data-gradient pass multiplies
 by W itself (COC_W_KN with inner = out_features).  These tests check the n x k
 layout against the oracle and bitwise against the k x n call on the
-transposed weights, for both kernel variants (<= 128 rows: single CTA;
-more: CTA pair), and run the four TP pairings of the CoC page's layers."""
+transposed weights, for every kernel variant (single-CTA and CTA-pair
+tiles, the column-slab kernel at decode-sized AllGather rows), and run the
+four TP pairings of the CoC page's layers."""
 import numpy as np
 import pytest
 import torch
@@ -66,8 +67,10 @@ def test_row_parallel_nk_layout(op, R, m, n, ks, dt, chunks):
 
 AG_CASES = [
     # R, m_shard, n_shard, k, dtype
-    (2, 40, 136, 72, BF16),      # 80 gathered rows: single CTA, 8-row A boxes
-    (4, 64, 264, 136, F16),      # 256 rows: CTA pairs
+    (2, 40, 136, 72, BF16),      # 80 gathered rows: the column-slab kernel
+    (4, 64, 264, 136, F16),      # 256 rows: CTA pairs on the stacked X (64-row shards)
+    (2, 128, 264, 72, BF16),     # 256 rows of whole 128-row shards: CTA pairs, A straight from the shards
+    (4, 96, 136, 200, F16),      # 384 rows: single-CTA tiles on the stacked X
 ]
 
 
@@ -127,7 +130,8 @@ def test_megatron_column_parallel_sp_forward_backward():
 WG_CASES = [
     # R, tokens (inner), out_features (rows), in_features (cols), dtype
     (2, 200, 96, 136, BF16),      # <= 128 rows: single-CTA kernel, ragged tokens
-    (4, 256, 264, 72, F16),       # CTA pairs, ragged rows and cols
+    (4, 256, 264, 72, F16),       # 3 single-CTA row tiles (a last pair tile would be mostly empty), ragged
+    (2, 136, 776, 200, BF16),     # CTA pairs (4 row tiles), ragged rows, cols and tokens
 ]
 
 
