@@ -192,23 +192,17 @@ int chunk_m_tiles(int64_t m, int chunks, int tile_m) {
 // layer with n 8192, K 8 x 1024 at m 129-256 measured 45-46 us against 50-52
 // with pairs; from 384 rows pairs are faster).  COC_PAIR=0/1 forces a
 // variant (tuning only).
-bool use_pair(int op, int64_t m) {
+int pair_forced() {
     static const int forced = [] {
         const char* e = std::getenv("COC_PAIR");
         return e == nullptr ? -1 : (std::atoi(e) != 0 ? 1 : 0);
     }();
-    if (forced >= 0) return forced == 1;
+    return forced;
+}
+
+bool use_pair(int op, int64_t m) {
+    if (pair_forced() >= 0) return pair_forced() == 1;
     if ((op == OP_AR || op == OP_RS) && m <= 2 * BM) return false;
-    if (op == OP_AG && m > 2 * BM) {
-        // 256-row pair tiles run about 15% faster per tile than 128-row
-        // single-CTA tiles, but where the last pair tile is at most half full
-        // and there are few row tiles, the single-CTA tiles take clearly fewer
-        // rounds: m in (256, 384] and (512, 640].  Measured (8 ranks, n_shard
-        // 7168, k 8192): m 384 266 against 296 us, m 640 404 against 447; m
-        // 512 / 768 / 1280 take pairs (275 / 397 / 650 against 319 / 455 / 743).
-        const int64_t mt_pair = (m + 2 * BM - 1) / (2 * BM), mt_single = (m + BM - 1) / BM;
-        return 10 * mt_single >= 17 * mt_pair;
-    }
     return m > BM;
 }
 
@@ -251,6 +245,25 @@ int pairs_available(DeviceState* ds, int op, bool bf16) {
     int& v = ds->max_pairs[op][bf16 ? 1 : 0];
     if (v < 0) v = max_pairs(op, bf16);
     return v;
+}
+
+// ALL_GATHER_MATMUL's tile shape for m gathered rows and col_units (rank,
+// n-tile) columns: 256-row pair tiles run about 15% faster per tile than
+// 128-row single-CTA tiles, so pairs, unless the single-CTA tiles take
+// clearly fewer rounds (tiles / co-resident pairs or CTAs, at least one):
+// where a last pair tile would be at most half full among few row tiles.
+// Measured (8 ranks, n_shard 7168, k 8192, 224 columns): m 384 269 against
+// 296 us, m 640 413 against 447 single-CTA; m 512 / 768 / 1280 pairs (275 /
+// 397 / 650 against 319 / 455 / 743).  The AllReduce and ReduceScatter, with
+// 32 columns at n 8192, ran pairs faster at m 384 and 640 (56 / 98 against
+// 66 / 116 us): both shapes fit one round there.
+bool ag_use_pair(DeviceState* ds, int64_t m, int64_t col_units, bool bf16) {
+    if (pair_forced() >= 0 || m <= 2 * BM) return use_pair(OP_AG, m);
+    const int pairs = pairs_available(ds, OP_AG, bf16);
+    if (pairs <= 0 || ds->sm_count <= 0) return true;
+    const double rp = std::max(1.0, static_cast<double>((m + 2 * BM - 1) / (2 * BM)) * col_units / pairs);
+    const double rs = std::max(1.0, static_cast<double>((m + BM - 1) / BM) * col_units / ds->sm_count);
+    return !(rs < 0.85 * rp);
 }
 
 int largest_pow2_divisor_le(int64_t v, int cap) {
@@ -1095,7 +1108,7 @@ coc_status_t all_gather(int R, int64_t ms, int64_t ns, int64_t k, const void* co
     p.n = static_cast<int>(ns);
     p.k = static_cast<int>(k);
     p.num_kshards = 1;
-    const bool pair = use_pair(OP_AG, m);
+    const bool pair = ag_use_pair(ds, m, R * ((ns + BN - 1) / BN), dt == COC_BF16);
     const int tile_m = pair ? 2 * BM : BM;
     p.kblocks = static_cast<int>((k + BK - 1) / BK);
     p.m_tiles = static_cast<int>((m + tile_m - 1) / tile_m);

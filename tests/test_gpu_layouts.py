@@ -70,7 +70,7 @@ AG_CASES = [
     (2, 40, 136, 72, BF16),      # 80 gathered rows: the column-slab kernel
     (4, 64, 264, 136, F16),      # 256 rows: CTA pairs on the stacked X (64-row shards)
     (2, 128, 264, 72, BF16),     # 256 rows of whole 128-row shards: CTA pairs, A straight from the shards
-    (4, 96, 136, 200, F16),      # 384 rows: single-CTA tiles on the stacked X
+    (8, 48, 1400, 136, F16),     # 384 rows x 48 (rank, n-tile) columns: single-CTA tiles on the stacked X
 ]
 
 
@@ -130,8 +130,8 @@ def test_megatron_column_parallel_sp_forward_backward():
 WG_CASES = [
     # R, tokens (inner), out_features (rows), in_features (cols), dtype
     (2, 200, 96, 136, BF16),      # <= 128 rows: single-CTA kernel, ragged tokens
-    (4, 256, 264, 72, F16),       # 3 single-CTA row tiles (a last pair tile would be mostly empty), ragged
-    (2, 136, 776, 200, BF16),     # CTA pairs (4 row tiles), ragged rows, cols and tokens
+    (4, 256, 264, 72, F16),       # CTA pairs, ragged rows and cols
+    (2, 136, 776, 200, BF16),     # 4 pair row tiles, ragged rows, cols and tokens
 ]
 
 
