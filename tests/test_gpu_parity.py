@@ -177,10 +177,12 @@ def test_reduce_scatter_concat_equals_allreduce_bits():
 
 AG_CASES = [
     # R, m_shard, n_shard, k, dtype, chunks
-    (2, 40, 72, 136, BF16, 1),       # 8-row A boxes, tiles straddle shards
-    (4, 128, 264, 64, F16, 2),       # aligned shards, ragged n
-    (8, 24, 256, 72, BF16, 8),       # 192 gathered rows, 8 chunks
+    (2, 40, 72, 136, BF16, 1),       # 80 gathered rows: the column-slab kernel on the stacked X
+    (4, 128, 264, 64, F16, 2),       # aligned shards read in place, ragged n
+    (8, 24, 256, 72, BF16, 8),       # 192 gathered rows from 24-row shards (X stacked), 8 chunks
     (1, 136, 40, 200, BF16, 1),      # R = 1
+    (8, 136, 248, 136, BF16, 2),     # 1088 rows, X stacked: the last pair tile's second CTA starts past m
+    (4, 200, 136, 72, F16, 1),       # 800 rows of 200-row shards, ragged k
 ]
 
 
