@@ -980,6 +980,33 @@ COC_API coc_status_t coc_matmul_all_reduce_w8a16(int R, int64_t m, int64_t n, in
 namespace coc {
 namespace {
 
+// An AllGather call can stack X (the R shards in rank order, m x k) into
+// V2's first kept gathered output, or else into scratch under the workspace
+// cap.  `kept`: V2's gathered outputs (entries may be NULL), NULL for V1.
+bool ag_can_stack(int R, int64_t ms, int64_t k, void* const* kept) {
+    for (int r = 0; kept != nullptr && r < R; ++r)
+        if (kept[r] != nullptr) return true;
+    return static_cast<size_t>(R) * static_cast<size_t>(ms) * static_cast<size_t>(k) * 2 <= kWorkspaceCap;
+}
+
+// The copy that stacks X (for calls where ag_can_stack holds): g->src the
+// shards, g->dst the first kept gathered output or, with none, scratch taken
+// into *sc (released by the caller with scratch_release).
+coc_status_t ag_stack_target(DeviceState* ds, cudaStream_t stream, int R, int64_t ms, int64_t k, const void* const* x,
+                             void* const* kept, AgGatherParams* g, Scratch* sc) {
+    std::memset(g, 0, sizeof *g);
+    g->R = R;
+    g->shard_vecs = ms * k / 8;
+    for (int r = 0; r < R; ++r) {
+        g->src[r] = static_cast<const uint16_t*>(x[r]);
+        if (kept != nullptr && g->dst == nullptr && kept[r] != nullptr) g->dst = static_cast<uint16_t*>(kept[r]);
+    }
+    if (g->dst != nullptr) return COC_OK;
+    const coc_status_t st = scratch_acquire(ds, stream, static_cast<size_t>(R) * ms * k * 2, sc);
+    g->dst = static_cast<uint16_t*>(sc->ptr);
+    return st;
+}
+
 // ALL_GATHER_MATMUL(_V2) through the column-slab kernel (gathered m = R
 // m_shard <= 128): first the gather kernel stacks the R shards of X into the
 // first non-NULL gathered output (V2) or, with none, into the call's
@@ -1015,26 +1042,17 @@ coc_status_t slab_all_gather(int R, int64_t ms, int64_t ns, int64_t k, const voi
         return fail(COC_ERR_SHAPE, "column-slab schedule does not fit in shared memory (m = %lld)", (long long)m);
     p.b_kmajor = w_nk ? 1 : 0;
 
-    // the gathered X the slab kernel reads: V2's first gathered output, else scratch
+    // the gathered X the slab kernel reads (V2's first kept gathered output,
+    // else scratch); the slab kernel copies it into V2's other kept outputs
     AgGatherParams g;
-    std::memset(&g, 0, sizeof g);
-    g.R = R;
-    g.shard_vecs = ms * k / 8;
-    for (int r = 0; r < R; ++r) {
-        g.src[r] = static_cast<const uint16_t*>(x[r]);
-        uint16_t* d = gathered != nullptr ? static_cast<uint16_t*>(gathered[r]) : nullptr;
-        if (d != nullptr && g.dst == nullptr) {
-            g.dst = d;   // stacked by the gather kernel
-        } else if (d != nullptr) {
-            p.gdst[r] = d;   // copied from it by the slab kernel
+    Scratch sc;
+    coc_status_t st = ag_stack_target(ds, stream, R, ms, k, x, gathered, &g, &sc);
+    if (st != COC_OK) return scratch_release(stream, sc, st);
+    for (int r = 0; gathered != nullptr && r < R; ++r) {
+        if (gathered[r] != nullptr && gathered[r] != g.dst) {
+            p.gdst[r] = static_cast<uint16_t*>(gathered[r]);
             p.has_gather = 1;
         }
-    }
-    coc_status_t st;
-    Scratch sc;
-    if (g.dst == nullptr) {
-        if ((st = scratch_acquire(ds, stream, static_cast<size_t>(m) * k * 2, &sc)) != COC_OK) return st;
-        g.dst = static_cast<uint16_t*>(sc.ptr);
     }
     const void* xg = g.dst;
     p.gsrc[0] = g.dst;
@@ -1091,14 +1109,11 @@ coc_status_t all_gather(int R, int64_t ms, int64_t ns, int64_t k, const void* co
 
     DeviceState* ds = nullptr;
     if ((st = device_state(&ds)) != COC_OK) return st;
-    if (k > 0) {
-        // (the stacked X goes to V2's first kept copy, else to scratch, which
-        // must fit under the workspace cap)
-        bool kept = false;
-        for (int r = 0; v2 && r < R; ++r) kept = kept || gathered[r] != nullptr;
+    void* const* kept = v2 ? gathered : nullptr;
+    const bool can_stack = k > 0 && ag_can_stack(R, ms, k, kept);
+    if (can_stack) {
         const SlabPlan pl = slab_plan(OP_AG, R, m, ns, k, ds->sm_count);
-        if (pl.boxes > 0 && (kept || static_cast<size_t>(m) * static_cast<size_t>(k) * 2 <= kWorkspaceCap))
-            return slab_all_gather(R, ms, ns, k, x, w, out, v2 ? gathered : nullptr, dt, pl, ds, stream, w_nk);
+        if (pl.boxes > 0) return slab_all_gather(R, ms, ns, k, x, w, out, kept, dt, pl, ds, stream, w_nk);
     }
     KParams p;
     std::memset(&p, 0, sizeof p);
@@ -1138,18 +1153,8 @@ coc_status_t all_gather(int R, int64_t ms, int64_t ns, int64_t k, const void* co
     AgGatherParams g;
     std::memset(&g, 0, sizeof g);
     Scratch sc;
-    if (k > 0 && p.a_box_rows < BM) {
-        g.R = R;
-        g.shard_vecs = ms * k / 8;
-        for (int r = 0; r < R; ++r) {
-            g.src[r] = static_cast<const uint16_t*>(x[r]);
-            if (v2 && g.dst == nullptr && gathered[r] != nullptr) g.dst = static_cast<uint16_t*>(gathered[r]);
-        }
-        if (g.dst == nullptr && static_cast<size_t>(m) * static_cast<size_t>(k) * 2 <= kWorkspaceCap) {
-            if ((st = scratch_acquire(ds, stream, static_cast<size_t>(m) * k * 2, &sc)) != COC_OK) return st;
-            g.dst = static_cast<uint16_t*>(sc.ptr);
-        }
-    }
+    if (can_stack && p.a_box_rows < BM && (st = ag_stack_target(ds, stream, R, ms, k, x, kept, &g, &sc)) != COC_OK)
+        return scratch_release(stream, sc, st);
     const bool stacked = g.dst != nullptr;
     if (stacked) {
         // one shard covering every tile's rows, so that the kernel's shard
