@@ -68,7 +68,8 @@
  *   - Library-owned device memory.  The first call on a device allocates a
  *     small status buffer (a few words).  Calls that need scratch (the fp32
  *     parts of a rank-split AllReduce / ReduceScatter, the MoE routing
- *     tables, the w8A16 pre-pass's dequantised weight) take it from a
+ *     tables, the w8A16 pre-pass's dequantised weight, the stacked X of an
+ *     AllGather that keeps no gathered copy) take it from a
  *     workspace the library keeps per stream: allocated by the first such
  *     call on the stream and grown only when a later call needs more (the
  *     growing call waits for the earlier users of the old buffer first), so
